@@ -1,0 +1,145 @@
+"""fp64 CPU oracle for the selective scan -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, fp64, one loop per
+definition); this module only builds that file with gcc, loads it with ctypes
+and converts numpy arrays to contiguous float64.
+
+Every function here is pinned by tests outside of itself (see
+``tests/test_oracle_pins.py``): the LTI convolution view of "Mamba: How
+Selective State Spaces Achieve 5x Faster Inference Than Transformers"
+(section "State space models before Mamba: HiPPO and S4") and "Mamba
+Architecture Explained" (section "How State Space Models Work"), closed forms,
+the remember/forget limits of "State Space Models (SSMs) & Mamba" (section
+"The Magic of Selective Scan"), and finite differences for the backward.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_HDR = os.path.join(_HERE, "ssm_oracle.h")
+_LIB = os.path.join(_HERE, "libssmoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -O3 without -ffast-math: exp/log1p keep their libm semantics.  No
+# -march=native: the built library travels to hosts with other CPUs.
+CFLAGS = ["-O3", "-std=c11", "-fPIC", "-shared", "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into libssmoracle.so (in place) if stale."""
+    stale = force or not os.path.exists(_LIB) or any(
+        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+    if stale:
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int64
+            lib.oracle_softplus.argtypes = [ctypes.c_double]
+            lib.oracle_softplus.restype = ctypes.c_double
+            lib.oracle_silu.argtypes = [ctypes.c_double]
+            lib.oracle_silu.restype = ctypes.c_double
+            lib.oracle_scan_fwd.argtypes = [I, I, I, I] + [P] * 11
+            lib.oracle_scan_fwd.restype = None
+            lib.oracle_scan_step.argtypes = [I, I, I] + [P] * 10
+            lib.oracle_scan_step.restype = None
+            lib.oracle_scan_bwd.argtypes = [I, I, I, I] + [P] * 20
+            lib.oracle_scan_bwd.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def softplus(x: float) -> float:
+    return _load().oracle_softplus(float(x))
+
+
+def silu(x: float) -> float:
+    return _load().oracle_silu(float(x))
+
+
+def scan_fwd(u, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None, h0=None):
+    """Forward selective scan.  Shapes: u, delta_raw, z (Bt,D,L); Bm, Cm (Bt,N,L);
+    A (D,N); Dv, delta_bias (D); h0 (Bt,D,N).  Returns (y (Bt,D,L), hL (Bt,D,N))."""
+    u, delta_raw, A, Bm, Cm = map(_f64, (u, delta_raw, A, Bm, Cm))
+    Dv, z, delta_bias, h0 = map(_f64, (Dv, z, delta_bias, h0))
+    Bt, D, L = u.shape
+    N = A.shape[1]
+    assert delta_raw.shape == u.shape and A.shape == (D, N)
+    assert Bm.shape == (Bt, N, L) and Cm.shape == (Bt, N, L)
+    assert z is None or z.shape == u.shape
+    assert h0 is None or h0.shape == (Bt, D, N)
+    y = np.empty((Bt, D, L), np.float64)
+    hL = np.empty((Bt, D, N), np.float64)
+    _load().oracle_scan_fwd(Bt, D, N, L, _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(Bm),
+                            _ptr(Cm), _ptr(Dv), _ptr(z), _ptr(delta_bias), _ptr(h0),
+                            _ptr(y), _ptr(hL))
+    return y, hL
+
+
+def scan_step(u, delta_raw, A, Bm, Cm, state, Dv=None, z=None, delta_bias=None):
+    """One decode step.  u, delta_raw, z (Bt,D); Bm, Cm (Bt,N); state (Bt,D,N).
+    Returns (y (Bt,D), new_state (Bt,D,N)); the input state is not modified."""
+    u, delta_raw, A, Bm, Cm = map(_f64, (u, delta_raw, A, Bm, Cm))
+    Dv, z, delta_bias = map(_f64, (Dv, z, delta_bias))
+    st = np.array(state, dtype=np.float64, copy=True, order="C")
+    Bt, D = u.shape
+    N = A.shape[1]
+    assert st.shape == (Bt, D, N) and Bm.shape == (Bt, N) and Cm.shape == (Bt, N)
+    y = np.empty((Bt, D), np.float64)
+    _load().oracle_scan_step(Bt, D, N, _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(Bm),
+                             _ptr(Cm), _ptr(Dv), _ptr(z), _ptr(delta_bias), _ptr(st),
+                             _ptr(y))
+    return y, st
+
+
+def scan_bwd(u, delta_raw, A, Bm, Cm, dy, Dv=None, z=None, delta_bias=None, h0=None,
+             dhL=None):
+    """Reverse mode of scan_fwd.  Returns a dict with du, ddelta_raw, dA, dB, dC,
+    dD, dz, ddelta_bias, dh0 (all float64)."""
+    u, delta_raw, A, Bm, Cm, dy = map(_f64, (u, delta_raw, A, Bm, Cm, dy))
+    Dv, z, delta_bias, h0, dhL = map(_f64, (Dv, z, delta_bias, h0, dhL))
+    Bt, D, L = u.shape
+    N = A.shape[1]
+    out = {
+        "du": np.empty((Bt, D, L)), "ddelta_raw": np.empty((Bt, D, L)),
+        "dA": np.empty((D, N)), "dB": np.empty((Bt, N, L)), "dC": np.empty((Bt, N, L)),
+        "dD": np.empty((D,)), "dz": np.empty((Bt, D, L)), "ddelta_bias": np.empty((D,)),
+        "dh0": np.empty((Bt, D, N)),
+    }
+    _load().oracle_scan_bwd(Bt, D, N, L, _ptr(u), _ptr(delta_raw), _ptr(A), _ptr(Bm),
+                            _ptr(Cm), _ptr(Dv), _ptr(z), _ptr(delta_bias), _ptr(h0),
+                            _ptr(dy), _ptr(dhL), _ptr(out["du"]), _ptr(out["ddelta_raw"]),
+                            _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                            _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]),
+                            _ptr(out["dh0"]))
+    return out

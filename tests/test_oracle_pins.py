@@ -1,0 +1,336 @@
+"""Pins for the fp64 oracle, against facts fixed outside of the oracle itself.
+
+Each test names the passage or the mathematics that fixes the expected value:
+  * the LTI special case -- with Delta, B, C constant in time a state space
+    model is a causal convolution ("Mamba: How Selective State Spaces Achieve
+    5x Faster Inference Than Transformers", section "State space models before
+    Mamba: HiPPO and S4"; "Mamba Architecture Explained", section "How State
+    Space Models Work"), checked by brute force and by a library FFT;
+  * the materialised time-varying kernel y = M u (the scan unrolled), which
+    pins which token's B, C and Delta enter each term;
+  * closed forms (L = 1, geometric series), the remember / forget limits of
+    Delta ("State Space Models (SSMs) & Mamba", section "The Magic of
+    Selective Scan: Content-Aware Memory");
+  * library routines for softplus and the sigmoid;
+  * central finite differences and the adjoint identity for the backward.
+A plausible slip in the oracle (a dropped term, a sign, an off-by-one in t, B
+and C swapped, the gate applied before the D term) fails at least one of them.
+"""
+import numpy as np
+import pytest
+from scipy.signal import fftconvolve
+from scipy.special import expit
+
+import oracle
+from scan_inputs import make_inputs
+
+RTOL = 1e-12
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _softplus_lib(x):
+    return np.logaddexp(0.0, x)
+
+
+def _silu_lib(z):
+    return z * expit(z)
+
+
+def test_softplus_and_silu_match_library():
+    xs = np.concatenate([np.linspace(-60, 60, 241), [-745.0, -30.5, 0.0, 1e-8, 700.0]])
+    for x in xs:
+        assert oracle.softplus(x) == pytest.approx(_softplus_lib(x), rel=1e-14, abs=1e-300)
+        assert oracle.silu(x) == pytest.approx(_silu_lib(x), rel=1e-14, abs=1e-300)
+
+
+def _lti_problem(rng, Bt, D, N, L, with_h0):
+    """Delta, B, C constant in t (per channel / batch), u and z varying."""
+    u = rng.standard_normal((Bt, D, L))
+    z = rng.standard_normal((Bt, D, L))
+    draw = np.repeat(rng.standard_normal((Bt, D, 1)), L, axis=2)
+    bias = rng.uniform(-4, 0, D)
+    A = -rng.uniform(0.1, 3.0, (D, N))
+    Bc = rng.standard_normal((Bt, N))
+    Cc = rng.standard_normal((Bt, N))
+    Bm = np.repeat(Bc[:, :, None], L, axis=2)
+    Cm = np.repeat(Cc[:, :, None], L, axis=2)
+    Dv = rng.standard_normal(D)
+    h0 = rng.standard_normal((Bt, D, N)) if with_h0 else None
+    return u, z, draw, bias, A, Bc, Cc, Bm, Cm, Dv, h0
+
+
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_lti_equals_bruteforce_causal_convolution(with_h0):
+    """Constant Delta, B, C: y = (K * u + D u) silu(z), K_k = sum_n C_n e^{delta A_n k} delta B_n,
+    plus the free response sum_n C_n e^{delta A_n (t+1)} h0_n."""
+    rng = _rng(11)
+    Bt, D, N, L = 2, 3, 4, 37
+    u, z, draw, bias, A, Bc, Cc, Bm, Cm, Dv, h0 = _lti_problem(rng, Bt, D, N, L, with_h0)
+    y, hL = oracle.scan_fwd(u, draw, A, Bm, Cm, Dv=Dv, z=z, delta_bias=bias, h0=h0)
+    for b in range(Bt):
+        for d in range(D):
+            delta = _softplus_lib(draw[b, d, 0] + bias[d])
+            lam = np.exp(delta * A[d])                     # (N,)
+            k = np.arange(L)
+            K = (Cc[b] * delta * Bc[b] * lam[None, :] ** k[:, None]).sum(1)
+            ys = np.array([sum(K[j] * u[b, d, t - j] for j in range(t + 1)) for t in range(L)])
+            if with_h0:
+                ys += (Cc[b] * h0[b, d] * lam[None, :] ** (k[:, None] + 1)).sum(1)
+            ys += Dv[d] * u[b, d]
+            np.testing.assert_allclose(y[b, d], ys * _silu_lib(z[b, d]), rtol=1e-11, atol=1e-12)
+            # final state: h_L = sum_s lam^{L-1-s} delta B u_s (+ lam^L h0)
+            hexp = (lam[None, :] ** (L - 1 - k)[:, None] * delta * Bc[b] * u[b, d][:, None]).sum(0)
+            if with_h0:
+                hexp += lam ** L * h0[b, d]
+            np.testing.assert_allclose(hL[b, d], hexp, rtol=1e-11, atol=1e-12)
+
+
+def test_lti_long_sequence_equals_fft_convolution():
+    """Same view at L = 4096 through a library FFT convolution (no gate, no D)."""
+    rng = _rng(12)
+    Bt, D, N, L = 1, 2, 16, 4096
+    u, z, draw, bias, A, Bc, Cc, Bm, Cm, Dv, _ = _lti_problem(rng, Bt, D, N, L, False)
+    y, _ = oracle.scan_fwd(u, draw, A, Bm, Cm, delta_bias=bias)
+    for d in range(D):
+        delta = _softplus_lib(draw[0, d, 0] + bias[d])
+        lam = np.exp(delta * A[d])
+        k = np.arange(L)
+        K = (Cc[0] * delta * Bc[0] * np.exp(np.outer(k, np.log(lam)))).sum(1)
+        ref = fftconvolve(u[0, d], K)[:L]
+        scale = np.sqrt(np.mean(ref ** 2))
+        np.testing.assert_allclose(y[0, d], ref, rtol=0, atol=1e-9 * scale)
+
+
+def test_time_varying_kernel_materialised():
+    """The scan unrolled: ys_t = sum_{s<=t} sum_n C_t[n] exp(A_n (S_t - S_s)) delta_s B_s[n] u_s
+    + D u_t with S_t = sum_{r<=t} delta_r.  Pins which token's B, C and Delta enter."""
+    rng = _rng(13)
+    Bt, D, N, L = 1, 2, 3, 24
+    u = rng.standard_normal((Bt, D, L))
+    z = rng.standard_normal((Bt, D, L))
+    draw = rng.standard_normal((Bt, D, L))
+    bias = rng.uniform(-3, 0, D)
+    A = -rng.uniform(0.2, 2.0, (D, N))
+    Bm = rng.standard_normal((Bt, N, L))
+    Cm = rng.standard_normal((Bt, N, L))
+    Dv = rng.standard_normal(D)
+    y, _ = oracle.scan_fwd(u, draw, A, Bm, Cm, Dv=Dv, z=z, delta_bias=bias)
+    for d in range(D):
+        delta = _softplus_lib(draw[0, d] + bias[d])
+        S = np.cumsum(delta)
+        M = np.zeros((L, L))
+        for t in range(L):
+            for s in range(t + 1):
+                M[t, s] = np.sum(Cm[0, :, t] * np.exp(A[d] * (S[t] - S[s])) * delta[s] * Bm[0, :, s])
+        ys = M @ u[0, d] + Dv[d] * u[0, d]
+        np.testing.assert_allclose(y[0, d], ys * _silu_lib(z[0, d]), rtol=1e-10, atol=1e-12)
+
+
+def test_single_token_closed_form():
+    """L = 1: h_1 = e^{delta A} h0 + delta B u, y = (C.h_1 + D u) silu(z)."""
+    rng = _rng(14)
+    D, N = 5, 4
+    u, draw, z = rng.standard_normal((3, 1, D, 1))
+    A = -rng.uniform(0.5, 4, (D, N))
+    Bm, Cm = rng.standard_normal((2, 1, N, 1))
+    Dv, bias = rng.standard_normal(D), rng.uniform(-5, 1, D)
+    h0 = rng.standard_normal((1, D, N))
+    y, hL = oracle.scan_fwd(u, draw, A, Bm, Cm, Dv=Dv, z=z, delta_bias=bias, h0=h0)
+    delta = np.logaddexp(0.0, draw[0, :, 0] + bias)
+    h1 = np.exp(delta[:, None] * A) * h0[0] + delta[:, None] * Bm[0, :, 0] * u[0, :, 0][:, None]
+    ref = (h1 @ Cm[0, :, 0] + Dv * u[0, :, 0]) * _silu_lib(z[0, :, 0])
+    np.testing.assert_allclose(y[0, :, 0], ref, rtol=1e-13)
+    np.testing.assert_allclose(hL[0], h1, rtol=1e-13)
+
+
+def test_constant_input_geometric_series():
+    """N = 1, u = 1, constant delta, B, C, h0 = 0: h_t = delta B (1 - a^{t+1}) / (1 - a)."""
+    L = 200
+    a_coef, Bv, Cv, draw = -0.7, 1.3, -0.4, 0.25
+    u = np.ones((1, 1, L))
+    y, hL = oracle.scan_fwd(u, np.full((1, 1, L), draw), np.array([[a_coef]]),
+                            np.full((1, 1, L), Bv), np.full((1, 1, L), Cv))
+    delta = np.log1p(np.exp(draw))
+    a = np.exp(delta * a_coef)
+    t = np.arange(L)
+    h = delta * Bv * (1 - a ** (t + 1)) / (1 - a)
+    np.testing.assert_allclose(y[0, 0], Cv * h, rtol=1e-12)
+    np.testing.assert_allclose(hL[0, 0, 0], h[-1], rtol=1e-12)
+
+
+def test_delta_to_zero_remembers_state():
+    """Delta_raw + bias = -200: delta ~ e^-200, the state is kept ("selectively
+    remember") and y_t = (C_t . h0 + D u_t) silu(z_t)."""
+    rng = _rng(15)
+    Bt, D, N, L = 1, 3, 4, 50
+    u, z = rng.standard_normal((2, Bt, D, L))
+    draw = np.full((Bt, D, L), -200.0)
+    A = -rng.uniform(0.5, 16, (D, N))
+    Bm, Cm = rng.standard_normal((2, Bt, N, L))
+    Dv = rng.standard_normal(D)
+    h0 = rng.standard_normal((Bt, D, N))
+    y, hL = oracle.scan_fwd(u, draw, A, Bm, Cm, Dv=Dv, z=z, delta_bias=np.zeros(D), h0=h0)
+    np.testing.assert_allclose(hL, h0, rtol=1e-80, atol=0)
+    ref = (np.einsum("dn,nt->dt", h0[0], Cm[0]) + Dv[:, None] * u[0]) * _silu_lib(z[0])
+    np.testing.assert_allclose(y[0], ref, rtol=1e-12)
+
+
+def test_large_delta_forgets_state():
+    """delta |A| >> 1: the past decays away ("selectively forget") and
+    h_t = delta_t B_t u_t exactly to double precision."""
+    rng = _rng(16)
+    Bt, D, N, L = 1, 2, 3, 30
+    u = rng.standard_normal((Bt, D, L))
+    draw = 60.0 + rng.uniform(0, 1, (Bt, D, L))
+    A = -rng.uniform(1.0, 5.0, (D, N))
+    Bm, Cm = rng.standard_normal((2, Bt, N, L))
+    h0 = rng.standard_normal((Bt, D, N))
+    y, hL = oracle.scan_fwd(u, draw, A, Bm, Cm, h0=h0)
+    delta = draw[0]                                   # softplus(x) = x + O(e^-60)
+    ref = np.einsum("nt,nt->t", Cm[0], Bm[0])[None, :] * delta * u[0]
+    np.testing.assert_allclose(y[0], ref, rtol=1e-12)
+    np.testing.assert_allclose(hL[0], delta[:, -1:] * Bm[0, :, -1][None, :] * u[0, :, -1:],
+                               rtol=1e-12)
+
+
+def _small_random(seed, Bt=2, D=3, N=4, L=40, h0=True):
+    x = make_inputs(Bt, D, N, L, seed=seed, in_dtype="f32", h0=h0, dy=True)
+    return x
+
+
+def test_split_and_carry_reproduces_unsplit():
+    x = _small_random(3)
+    y, hL = oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    for L1 in (1, 17, 39):
+        ya, ha = oracle.scan_fwd(x.u[..., :L1], x.delta_raw[..., :L1], x.A, x.Bm[..., :L1],
+                                 x.Cm[..., :L1], x.Dv, x.z[..., :L1], x.delta_bias, x.h0)
+        yb, hb = oracle.scan_fwd(x.u[..., L1:], x.delta_raw[..., L1:], x.A, x.Bm[..., L1:],
+                                 x.Cm[..., L1:], x.Dv, x.z[..., L1:], x.delta_bias, ha)
+        np.testing.assert_allclose(np.concatenate([ya, yb], -1), y, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(hb, hL, rtol=1e-12, atol=1e-14)
+
+
+def test_linear_in_u_and_causal():
+    x = _small_random(4, h0=False)
+    rng = _rng(17)
+    u2 = rng.standard_normal(x.u.shape)
+    f = lambda uu: oracle.scan_fwd(uu, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias)[0]
+    np.testing.assert_allclose(f(2.0 * x.u - 3.0 * u2), 2.0 * f(x.u) - 3.0 * f(u2),
+                               rtol=1e-10, atol=1e-12)
+    t0 = 23
+    up = x.u.copy()
+    up[..., t0] += 5.0
+    y0, y1 = f(x.u), f(up)
+    np.testing.assert_array_equal(y0[..., :t0], y1[..., :t0])
+    assert np.all(np.abs(y0[..., t0] - y1[..., t0]) > 0)
+
+
+def test_channels_are_independent():
+    x = _small_random(5)
+    y, hL = oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    d = 1
+    y1, h1 = oracle.scan_fwd(x.u[:, d:d + 1], x.delta_raw[:, d:d + 1], x.A[d:d + 1], x.Bm,
+                             x.Cm, x.Dv[d:d + 1], x.z[:, d:d + 1], x.delta_bias[d:d + 1],
+                             x.h0[:, d:d + 1])
+    np.testing.assert_array_equal(y1[:, 0], y[:, d])
+    np.testing.assert_array_equal(h1[:, 0], hL[:, d])
+
+
+def test_decode_steps_reproduce_forward():
+    """Recurrent inference ("State Space Models (SSMs) & Mamba", section "The Payoff"):
+    L single-token steps from h0 equal the forward scan over L tokens."""
+    x = _small_random(6, L=12)
+    y, hL = oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    st = x.h0.copy()
+    for t in range(x.u.shape[-1]):
+        yt, st = oracle.scan_step(x.u[..., t], x.delta_raw[..., t], x.A, x.Bm[..., t],
+                                  x.Cm[..., t], st, x.Dv, x.z[..., t], x.delta_bias)
+        np.testing.assert_allclose(yt, y[..., t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(st, hL, rtol=1e-13)
+
+
+def test_decode_step_closed_form():
+    rng = _rng(18)
+    Bt, D, N = 3, 4, 5
+    u, draw, z = rng.standard_normal((3, Bt, D))
+    A = -rng.uniform(0.5, 4, (D, N))
+    Bm, Cm = rng.standard_normal((2, Bt, N))
+    Dv, bias = rng.standard_normal(D), rng.uniform(-5, 1, D)
+    st = rng.standard_normal((Bt, D, N))
+    y, st2 = oracle.scan_step(u, draw, A, Bm, Cm, st, Dv, z, bias)
+    delta = np.logaddexp(0.0, draw + bias[None, :])
+    h = np.exp(delta[..., None] * A[None]) * st + delta[..., None] * Bm[:, None, :] * u[..., None]
+    np.testing.assert_allclose(st2, h, rtol=1e-13)
+    ref = (np.einsum("bdn,bn->bd", h, Cm) + Dv[None] * u) * _silu_lib(z)
+    np.testing.assert_allclose(y, ref, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- backward ---
+
+def _loss(x, dy, dhL, **over):
+    args = dict(u=x.u, delta_raw=x.delta_raw, A=x.A, Bm=x.Bm, Cm=x.Cm, Dv=x.Dv, z=x.z,
+                delta_bias=x.delta_bias, h0=x.h0)
+    args.update(over)
+    y, hL = oracle.scan_fwd(**args)
+    return float(np.sum(dy * y) + np.sum(dhL * hL))
+
+
+_BWD_NAMES = [("u", "du"), ("delta_raw", "ddelta_raw"), ("A", "dA"), ("Bm", "dB"),
+              ("Cm", "dC"), ("Dv", "dD"), ("z", "dz"), ("delta_bias", "ddelta_bias"),
+              ("h0", "dh0")]
+
+
+def test_backward_matches_central_finite_differences():
+    x = make_inputs(1, 2, 2, 5, seed=7, in_dtype="f32", h0=True, dy=True)
+    for k in ("u", "delta_raw", "A", "Bm", "Cm", "Dv", "z", "delta_bias", "h0", "dy"):
+        setattr(x, k, getattr(x, k).astype(np.float64))
+    rng = _rng(19)
+    dy = x.dy
+    dhL = rng.standard_normal(x.h0.shape)
+    g = oracle.scan_bwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, dy, Dv=x.Dv, z=x.z,
+                        delta_bias=x.delta_bias, h0=x.h0, dhL=dhL)
+    eps = 1e-6
+    for name, gname in _BWD_NAMES:
+        base = getattr(x, name)
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            p = base.copy(); p[idx] += eps
+            m = base.copy(); m[idx] -= eps
+            fd[idx] = (_loss(x, dy, dhL, **{name: p}) - _loss(x, dy, dhL, **{name: m})) / (2 * eps)
+        np.testing.assert_allclose(g[gname], fd, rtol=2e-6, atol=2e-8, err_msg=gname)
+
+
+def test_backward_adjoint_identity():
+    """<dy, J v> = <J^T dy, v> for a random direction v over all inputs (J by
+    a central difference along v)."""
+    x = make_inputs(2, 3, 4, 16, seed=8, in_dtype="f32", h0=True, dy=True)
+    rng = _rng(20)
+    names = [n for n, _ in _BWD_NAMES]
+    base = {n: getattr(x, n).astype(np.float64) for n in names}
+    v = {n: rng.standard_normal(base[n].shape) for n in names}
+    dy = x.dy.astype(np.float64)
+    dhL = np.zeros(x.h0.shape)
+    g = oracle.scan_bwd(base["u"], base["delta_raw"], base["A"], base["Bm"], base["Cm"], dy,
+                        Dv=base["Dv"], z=base["z"], delta_bias=base["delta_bias"],
+                        h0=base["h0"], dhL=dhL)
+    eps = 1e-5
+    plus = {n: base[n] + eps * v[n] for n in names}
+    minus = {n: base[n] - eps * v[n] for n in names}
+    yp, _ = oracle.scan_fwd(**plus)
+    ym, _ = oracle.scan_fwd(**minus)
+    lhs = np.sum(dy * (yp - ym)) / (2 * eps)
+    rhs = sum(np.sum(g[gn] * v[n]) for n, gn in _BWD_NAMES)
+    assert lhs == pytest.approx(rhs, rel=1e-7)
+
+
+def test_backward_closed_form_dD():
+    """dD = sum_{b,t} dy silu(z) u, a direct consequence of y = (... + D u) silu(z)."""
+    x = make_inputs(2, 3, 4, 16, seed=9, in_dtype="f32", h0=False, dy=True)
+    g = oracle.scan_bwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, Dv=x.Dv, z=x.z,
+                        delta_bias=x.delta_bias)
+    z = x.z.astype(np.float64)
+    ref = np.sum(x.dy.astype(np.float64) * _silu_lib(z) * x.u, axis=(0, 2))
+    np.testing.assert_allclose(g["dD"], ref, rtol=1e-12)
