@@ -1,0 +1,164 @@
+/*
+ * ssm_scan.h -- C ABI of libssmscan.so: the selective scan of the Mamba
+ * selective state space model on one B300 GPU (sm_103a).
+ *
+ * What is computed (per batch b, channel d, state n, token t):
+ *
+ *   delta_t = softplus(delta_raw[b,d,t] + delta_bias[d])
+ *   h_t[n]  = exp(delta_t * A[d,n]) * h_{t-1}[n] + delta_t * B[b,n,t] * u[b,d,t]
+ *   y[b,d,t] = (sum_n C[b,n,t] h_t[n] + D[d] u[b,d,t]) * silu(z[b,d,t])
+ *   hL[b,d,n] = h_L[n],   h_0 = h0[b,d,n] (or 0)
+ *
+ * Sources (page title, section):
+ *  - "State Space Models (SSMs) & Mamba" (aidatadrop): section "State-Space
+ *    Models (SSMs): A Resurgent Paradigm for Sequence Modeling" gives the
+ *    continuous system h' = A h + B u, y = C h + D u; section "The Magic of
+ *    Selective Scan: Content-Aware Memory" makes B, C and the step Delta
+ *    functions of the input token while A stays fixed; section "The Payoff:
+ *    Linear Scaling and Lightning-Fast Inference" gives the constant-memory
+ *    recurrent step.
+ *  - "Mamba: How Selective State Spaces Achieve 5x Faster Inference Than
+ *    Transformers", section "The selective mechanism: input-dependent SSM
+ *    parameters": B, C and Delta are computed per token; training runs the
+ *    recurrence as a parallel prefix scan; inference is a pure recurrence.
+ *  - "The convolution trick is gone -- what now?" (Mamba lesson 2): the scan
+ *    keeps the recurrence on chip and writes back only the final state.
+ *  - "Mamba Architecture Explained", section "The Architecture in Practice":
+ *    the SSM output is gated by SiLU of a second branch (z here).
+ *  The pages do not print the discretisation; this library reads it as
+ *  dA = exp(Delta A) with input term Delta B u, the gate applied after the
+ *  D skip term.
+ *
+ * Layouts: row-major, contiguous, token axis fastest.
+ *   u, delta_raw, z, y, dy, du, ddelta_raw, dz : (batch, dim, seqlen)
+ *   B, C, dB, dC                               : (batch, dstate, seqlen), shared by all channels
+ *   A, dA                                      : (dim, dstate)   fp32
+ *   D, delta_bias, dD, ddelta_bias             : (dim)           fp32
+ *   h0, hL, dhL, dh0, decode state             : (batch, dim, dstate) fp32
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers except the shape struct, and must be
+ *    16-byte aligned.  The caller owns and allocates every buffer, including
+ *    the workspace; the library never allocates, frees or synchronises
+ *    (except ssm_get_status, which synchronises the stream it is given).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  Argument errors are detected on the
+ *    host before anything is enqueued and returned synchronously.  Errors
+ *    detected on the device (a bounded wait that expired) are written to the
+ *    status word in the workspace and read with ssm_get_status.
+ *  - Gradient outputs are overwritten, never accumulated into.
+ *  - Return value: SSM_OK (0) or one of the negative SSM_ERR_* codes.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* ssm_stream_t; /* a cudaStream_t */
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef struct {
+    int64_t batch;     /* Bt >= 0 */
+    int64_t dim;       /* D  >= 0 channels */
+    int64_t dstate;    /* N, 1 <= N <= 64 */
+    int64_t seqlen;    /* L >= 0 */
+    int32_t in_dtype;  /* ssm_dtype of u, delta_raw, z, B, C (and dy in backward) */
+    int32_t out_dtype; /* ssm_dtype of y (and du, ddelta_raw, dz in backward) */
+} ssm_shape;
+
+enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = -1,        /* a required pointer is NULL */
+    SSM_ERR_SHAPE = -2,       /* negative size, dstate outside 1..64, or size overflow */
+    SSM_ERR_DTYPE = -3,       /* in_dtype / out_dtype not an ssm_dtype */
+    SSM_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+    SSM_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than ssm_scan_workspace_bytes */
+    SSM_ERR_CUDA = -6,        /* a CUDA runtime call failed (launch, attribute query) */
+    SSM_ERR_TIMEOUT = -7,     /* device side: a bounded wait expired; outputs undefined */
+    SSM_ERR_UNSUPPORTED = -8  /* valid request this build does not implement */
+};
+
+/* Bytes of device workspace the call needs for this shape on the current
+ * device: for_backward = 0 for ssm_scan_fwd, 1 for ssm_scan_bwd.  Always at
+ * least 256 (the status word lives at offset 0).  Returns 0 for an invalid
+ * shape. */
+SSM_API size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward);
+
+/* Forward selective scan over the whole sequence.
+ *   u, delta_raw, B, C : in_dtype, required.     A : fp32 (dim, dstate), required.
+ *   D, z, delta_bias, h0 : nullable (absent term / no gate / zero bias / zero state).
+ *   y  : out_dtype (batch, dim, seqlen), required.
+ *   hL : fp32 (batch, dim, dstate), nullable (final state not written).
+ *   workspace : >= ssm_scan_workspace_bytes(shape, 0) bytes of device memory.
+ * Long sequences with few channels are split into segments whose carried
+ * state is combined between two passes ("write back only the final state
+ * per tile", Mamba lesson 2); the result is the same recurrence. */
+SSM_API int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw,
+                 const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* delta_bias, const float* h0,
+                 void* y, float* hL, void* workspace, size_t ws_bytes,
+                 ssm_stream_t stream);
+
+/* Reverse mode of ssm_scan_fwd (the pages give no backward; it is the exact
+ * derivative of the recurrence above).  Inputs are the forward inputs plus
+ *   dy  : in_dtype (batch, dim, seqlen), required;   dhL : fp32, nullable (= 0).
+ * Outputs (overwritten):
+ *   du, ddelta_raw : out_dtype, required.   dz : out_dtype, nullable.
+ *   dA (dim,dstate), dB, dC (batch,dstate,seqlen) : fp32, required
+ *     (dB and dC are sums over all channels).
+ *   dD, ddelta_bias (dim), dh0 (batch,dim,dstate) : fp32, nullable.
+ *   ddelta_raw is the derivative with respect to delta_raw (before softplus).
+ * workspace : >= ssm_scan_workspace_bytes(shape, 1) bytes. */
+SSM_API int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw,
+                 const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* delta_bias, const float* h0,
+                 const void* dy, const float* dhL,
+                 void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
+                 float* dD, void* dz, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/* One recurrent (decode) step for a single token per sequence, with the
+ * state updated in place ("Mamba: How Selective State Spaces ...", section
+ * "The selective mechanism": constant memory per generated token).
+ *   u, delta_raw, z, y : (batch, dim);  B, C : (batch, dstate);  in_dtype / out_dtype.
+ *   A : fp32 (dim, dstate), required.  D, z, delta_bias : nullable.
+ *   state : fp32 (batch, dim, dstate), read and overwritten with the new state.
+ * Needs no workspace. */
+SSM_API int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype,
+                  int32_t out_dtype, const void* u, const void* delta_raw,
+                  const float* A, const void* B, const void* C, const float* D,
+                  const void* z, const float* delta_bias, float* state, void* y,
+                  ssm_stream_t stream);
+
+/* Synchronise `stream`, then return the device status word held in
+ * `workspace` (SSM_OK or SSM_ERR_TIMEOUT) and reset it to SSM_OK.  Returns
+ * SSM_ERR_CUDA if the synchronisation itself fails, SSM_ERR_NULL for a NULL
+ * workspace. */
+SSM_API int ssm_get_status(void* workspace, ssm_stream_t stream);
+
+/* Human-readable text of a status code (static storage, never NULL). */
+SSM_API const char* ssm_strerror(int code);
+
+/* Failure-detection self test: launches one block that waits on a device
+ * flag nothing ever sets, giving up after `spin_limit` polls; the expired
+ * wait is reported through the workspace status word (SSM_ERR_TIMEOUT, read
+ * with ssm_get_status).  No copy is in flight while it waits. */
+SSM_API int ssm_debug_expired_wait(void* workspace, size_t ws_bytes, int64_t spin_limit,
+                           ssm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSM_SCAN_H */

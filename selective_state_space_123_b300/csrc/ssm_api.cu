@@ -1,0 +1,357 @@
+// ssm_api.cu -- the C ABI of libssmscan.so (declared in include/ssm_scan.h):
+// argument validation, planning of the forward launch, TMA descriptors,
+// workspace layout, status word.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ssm_scan.h"
+#include "ssm_internal.h"
+
+using namespace ssm;
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;   // status word at offset 0
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int dtype_bytes(int32_t t) { return t == SSM_BF16 ? 2 : 4; }
+
+bool valid_dtype(int32_t t) { return t == SSM_F32 || t == SSM_BF16; }
+
+// multiply with overflow check (all operands >= 0)
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+int padded_state(int64_t N) {
+    if (N <= 4) return 4;
+    if (N <= 8) return 8;
+    if (N <= 16) return 16;
+    if (N <= 32) return 32;
+    return 64;
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::atoi(v);
+}
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 148; }
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 148;
+    }
+    return sms > 0 ? sms : 148;
+}
+
+int shape_check(const ssm_shape* s) {
+    if (!s) return SSM_ERR_NULL;
+    if (s->batch < 0 || s->dim < 0 || s->seqlen < 0) return SSM_ERR_SHAPE;
+    if (s->dstate < 1 || s->dstate > 64) return SSM_ERR_SHAPE;
+    if (!valid_dtype(s->in_dtype) || !valid_dtype(s->out_dtype)) return SSM_ERR_DTYPE;
+    int64_t bd, bdl, bl;
+    if (!mul_ok(s->batch, s->dim, &bd) || !mul_ok(bd, s->seqlen, &bdl) ||
+        !mul_ok(s->batch, s->seqlen, &bl))
+        return SSM_ERR_SHAPE;
+    int64_t tmp;
+    if (!mul_ok(bdl, 8, &tmp) || !mul_ok(bd, 64 * 8, &tmp) || !mul_ok(bl, 128 * 4, &tmp))
+        return SSM_ERR_SHAPE;
+    // TMA coordinates are 32-bit: rows of (batch*dim) and (batch*seqlen);
+    // the batch index is a grid dimension (at most 65535)
+    if (bd >= (int64_t(1) << 31) || bl >= (int64_t(1) << 31)) return SSM_ERR_UNSUPPORTED;
+    if (s->batch > 65535) return SSM_ERR_UNSUPPORTED;
+    return SSM_OK;
+}
+
+struct FwdPlan {
+    int NP = 16, NT = 2, CH = 64;
+    int nseg = 1;
+    int64_t nchunks = 0, seg_chunks = 0;
+    bool tma_raw = false;
+    size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, bytes = 0;
+};
+
+FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
+    FwdPlan pl;
+    pl.NP = padded_state(s.dstate);
+    int nts[4];
+    const int cnt = fwd_supported_nt(pl.NP, nts, 4);
+    pl.NT = nts[0];
+    const int want = env_int("SSM_FWD_NT", 0);
+    for (int i = 0; i < cnt; ++i)
+        if (nts[i] == want) pl.NT = want;
+    pl.CH = kConsumers / pl.NT;
+    pl.nchunks = (s.seqlen + kT - 1) / kT;
+    pl.tma_raw = (s.seqlen * dtype_bytes(s.in_dtype)) % 16 == 0;
+    // Too few channel tiles to fill the GPU: cut the sequence into segments
+    // (two passes and a carry; about 1.6x the arithmetic, many more CTAs).
+    const int64_t ctas = s.batch * ((s.dim + pl.CH - 1) / pl.CH);
+    int64_t nseg = 1;
+    if (ctas > 0 && ctas * 2 < sm_count && pl.nchunks >= 16)
+        nseg = (6 * (int64_t)sm_count + ctas - 1) / ctas;
+    const int forced = env_int("SSM_FWD_NSEG", 0);
+    if (forced > 0) nseg = forced;
+    if (nseg > pl.nchunks / 4) nseg = pl.nchunks / 4;
+    if (nseg < 1) nseg = 1;
+    pl.seg_chunks = (pl.nchunks + nseg - 1) / nseg;
+    if (pl.seg_chunks < 1) pl.seg_chunks = 1;
+    pl.nseg = (int)((pl.nchunks + pl.seg_chunks - 1) / pl.seg_chunks);
+    if (pl.nseg < 1) pl.nseg = 1;
+
+    size_t off = kHeaderBytes;
+    pl.off_bc = off;
+    off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
+    if (pl.nseg > 1) {
+        const size_t st = (size_t)pl.nseg * s.batch * s.dim;
+        pl.off_hin = off;
+        off += align256(st * pl.NP * 4);
+        pl.off_hloc = off;
+        off += align256(st * pl.NP * 4);
+        pl.off_sumd = off;
+        off += align256(st * 4);
+    }
+    pl.bytes = off;
+    return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D row-major tensor (rows x cols elements), tile box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * (cuuint64_t)esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_fwd(int NP, int NT, int tin, int tout, bool summary, bool tma,
+                       const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NP) {
+        case 4: return launch_fwd_np4(NT, tin, tout, summary, tma, p, m, grid, st);
+        case 8: return launch_fwd_np8(NT, tin, tout, summary, tma, p, m, grid, st);
+        case 16: return launch_fwd_np16(NT, tin, tout, summary, tma, p, m, grid, st);
+        case 32: return launch_fwd_np32(NT, tin, tout, summary, tma, p, m, grid, st);
+        default: return launch_fwd_np64(NT, tin, tout, summary, tma, p, m, grid, st);
+    }
+}
+
+}  // namespace
+
+namespace ssm {
+int fwd_supported_nt(int NP, int* out, int cap) {
+    static const int t4[] = {1}, t8[] = {2, 1}, t16[] = {2, 1, 4}, t32[] = {4, 2}, t64[] = {4};
+    const int* t = t16;
+    int n = 3;
+    switch (NP) {
+        case 4: t = t4; n = 1; break;
+        case 8: t = t8; n = 2; break;
+        case 16: t = t16; n = 3; break;
+        case 32: t = t32; n = 2; break;
+        default: t = t64; n = 1; break;
+    }
+    for (int i = 0; i < n && i < cap; ++i) out[i] = t[i];
+    return n < cap ? n : cap;
+}
+}  // namespace ssm
+
+extern "C" {
+
+const char* ssm_strerror(int code) {
+    switch (code) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_NULL: return "a required pointer is NULL";
+        case SSM_ERR_SHAPE: return "invalid shape (negative size, dstate outside 1..64, or overflow)";
+        case SSM_ERR_DTYPE: return "invalid dtype";
+        case SSM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case SSM_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSM_ERR_CUDA: return "a CUDA runtime call failed";
+        case SSM_ERR_TIMEOUT: return "device-side bounded wait expired";
+        case SSM_ERR_UNSUPPORTED: return "unsupported request";
+        default: return "unknown status";
+    }
+}
+
+size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
+    if (shape_check(shape) != SSM_OK) return 0;
+    const FwdPlan pl = plan_fwd(*shape, device_sm_count());
+    size_t bytes = pl.bytes;
+    (void)for_backward;
+    return bytes < kHeaderBytes ? kHeaderBytes : bytes;
+}
+
+int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, void* y, float* hL, void* workspace,
+                 size_t ws_bytes, ssm_stream_t stream) {
+    const int sc = shape_check(shape);
+    if (sc != SSM_OK) return sc;
+    const ssm_shape s = *shape;
+    const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    const bool any_work = Bt > 0 && Dm > 0;
+    if (!any_work) return SSM_OK;
+    if (!A || !workspace) return !A ? SSM_ERR_NULL : SSM_ERR_WORKSPACE;
+    if (L > 0 && (!u || !delta_raw || !B || !C || !y)) return SSM_ERR_NULL;
+    const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, hL, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const FwdPlan pl = plan_fwd(s, device_sm_count());
+    if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+
+    if (L == 0) {
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (hL) {
+            const size_t bytes = (size_t)(Bt * Dm * N) * sizeof(float);
+            cudaError_t e = h0 ? cudaMemcpyAsync(hL, h0, bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(hL, 0, bytes, st);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+
+    float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
+    if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+
+    const int eb = dtype_bytes(s.in_dtype);
+    const CUtensorMapDataType tdt =
+        s.in_dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!make_map(&maps.bc, bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT,
+                  false))
+        return SSM_ERR_CUDA;
+    if (pl.tma_raw) {
+        const uint32_t box_t = 128 / eb;
+        if (!make_map(&maps.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+            !make_map(&maps.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+            (z && !make_map(&maps.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)))
+            return SSM_ERR_CUDA;
+    }
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Bt = Bt; p.D = Dm; p.L = L; p.N = (int)N;
+    p.u = u; p.dr = delta_raw; p.z = z; p.A = A; p.Dv = D; p.bias = delta_bias; p.h0 = h0;
+    p.bc = bc; p.y = y; p.hL = hL;
+    p.seg_chunks = pl.seg_chunks;
+    p.nseg = pl.nseg;
+    p.status = status;
+    p.timeout_ns = kDefaultTimeoutNs;
+    const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
+
+    if (pl.nseg > 1) {
+        p.hin = reinterpret_cast<float*>(ws + pl.off_hin);
+        p.hloc = reinterpret_cast<float*>(ws + pl.off_hloc);
+        p.sumd = reinterpret_cast<float*>(ws + pl.off_sumd);
+        // pass 1: summaries of every segment but the last
+        FwdParams p1 = p;
+        p1.hin = nullptr;
+        if (launch_fwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, true, pl.tma_raw, p1, maps,
+                       dim3(gx, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, p.hloc, p.sumd, p.hin, st) !=
+            cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (launch_fwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, false, pl.tma_raw, p, maps,
+                   dim3(gx, (unsigned)Bt, (unsigned)pl.nseg), st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
+}
+
+int ssm_scan_bwd(const ssm_shape* shape, const void*, const void*, const float*, const void*,
+                 const void*, const float*, const void*, const float*, const float*, const void*,
+                 const float*, void*, void*, float*, float*, float*, float*, void*, float*, float*,
+                 void*, size_t, ssm_stream_t) {
+    const int sc = shape_check(shape);
+    if (sc != SSM_OK) return sc;
+    return SSM_ERR_UNSUPPORTED;
+}
+
+int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, int32_t out_dtype,
+                  const void* u, const void* delta_raw, const float* A, const void* B,
+                  const void* C, const float* D, const void* z, const float* delta_bias,
+                  float* state, void* y, ssm_stream_t stream) {
+    if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64) return SSM_ERR_SHAPE;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
+    int64_t bd, tmp;
+    if (!mul_ok(batch, dim, &bd) || !mul_ok(bd, dstate * 16, &tmp)) return SSM_ERR_SHAPE;
+    if (bd == 0) return SSM_OK;
+    if (!u || !delta_raw || !A || !B || !C || !state || !y) return SSM_ERR_NULL;
+    const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, state, y};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    StepParams p;
+    p.Bt = batch; p.D = dim; p.N = (int)dstate;
+    p.u = u; p.dr = delta_raw; p.z = z; p.A = A; p.Dv = D; p.bias = delta_bias;
+    p.B = B; p.C = C; p.state = state; p.y = y;
+    if (launch_step(in_dtype, out_dtype, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
+}
+
+int ssm_get_status(void* workspace, ssm_stream_t stream) {
+    if (!workspace) return SSM_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (v != SSM_OK) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    return v;
+}
+
+int ssm_debug_expired_wait(void* workspace, size_t ws_bytes, int64_t spin_limit,
+                           ssm_stream_t stream) {
+    if (!workspace) return SSM_ERR_NULL;
+    if (ws_bytes < kHeaderBytes) return SSM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SSM_ERR_ALIGN;
+    if (spin_limit < 1) return SSM_ERR_SHAPE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = static_cast<int*>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (launch_expired_wait(status, spin_limit, st) != cudaSuccess) return SSM_ERR_CUDA;
+    return SSM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// ssm_common.cuh -- device helpers shared by the selective-scan kernels
+// (inline PTX for sm_103a: packed f32x2 arithmetic, MUFU exp2/log2/rcp,
+// mbarrier waits with a time limit, TMA tile loads).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/ssm_scan.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "this library targets sm_103a (Blackwell) only"
+#endif
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ----------------------------------------------------------------- MUFU ---
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// --------------------------------------------------- packed f32x2 math ---
+// A pair of fp32 values in one 64-bit register; one instruction does both.
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 pk(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk(f2 r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// exp2 of both halves (two MUFU operations)
+__device__ __forceinline__ f2 ex2x2(f2 x) {
+    float lo, hi;
+    upk(x, lo, hi);
+    return pk(ex2(lo), ex2(hi));
+}
+
+// 2^x to about one fp32 ulp, on the FMA pipe, for the fp32-input path where
+// the MUFU's ~2^-22 relative error would compound over long decay products.
+// Range reduction x = n + f with n = round(x), |f| <= 1/2 (exact in fp32),
+// then 2^f = sum_k (f ln 2)^k / k! to k = 7 (truncation < 6e-9 relative),
+// then n is added to the exponent field.  x is clamped to [-125, 127]; below
+// -125 the true value is under 2^-125 and the result stays a normal number.
+__device__ __forceinline__ float exp2_accurate(float x) {
+    x = fminf(fmaxf(x, -125.0f), 127.0f);
+    const int n = __float2int_rn(x);
+    const float f = x - (float)n;
+    float p = 1.5252733804059840e-05f;            // ln2^7 / 7!
+    p = fmaf(p, f, 1.5403530393381606e-04f);      // ln2^6 / 6!
+    p = fmaf(p, f, 1.3333558146428443e-03f);      // ln2^5 / 5!
+    p = fmaf(p, f, 9.6181291076284770e-03f);      // ln2^4 / 4!
+    p = fmaf(p, f, 5.5504108664821580e-02f);      // ln2^3 / 3!
+    p = fmaf(p, f, 2.4022650695910070e-01f);      // ln2^2 / 2!
+    p = fmaf(p, f, 6.9314718055994530e-01f);      // ln2
+    p = fmaf(p, f, 1.0f);
+    return __int_as_float(__float_as_int(p) + (n << 23));
+}
+__device__ __forceinline__ f2 exp2_accurate_x2(f2 x) {
+    float lo, hi;
+    upk(x, lo, hi);
+    return pk(exp2_accurate(lo), exp2_accurate(hi));
+}
+
+// ------------------------------------------------------- element types ---
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kBytes = 4;
+    __device__ __forceinline__ static float to_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+};
+
+// two bf16 packed in a 32-bit word -> two floats (exact widening)
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// two floats -> packed bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ----------------------------------------------------------- time base ---
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Record a device-side error in the status word (first error wins).
+__device__ __forceinline__ void set_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------ mbarrier ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// nanoseconds or `spin_limit` polls, whichever comes first (spin_limit 0 means
+// the default cap of 2^28 polls, so the wait ends even if the clock stalls).
+// Returns false on timeout; the caller records SSM_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                          int64_t spin_limit = 0) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const int64_t cap = spin_limit > 0 ? spin_limit : (int64_t(1) << 28);
+    const uint64_t t0 = globaltimer_ns();
+    for (int64_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= cap) return false;
+        if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ----------------------------------------------------------------- TMA ---
+// 2-D tiled load of box {x, y} into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Byte offset of element (row r, column byte cb) inside a tile whose rows are
+// 128 bytes long and were written by TMA with the 128-byte swizzle: the
+// 16-byte chunk index is XORed with the row index modulo 8 (tile base
+// 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t cb) {
+    return r * 128u + ((((cb >> 4) ^ r) & 7u) << 4) + (cb & 15u);
+}
+
+}  // namespace ssm

@@ -1,0 +1,447 @@
+// ssm_fwd.cuh -- forward selective-scan kernel (templated; instantiated in
+// the ssm_fwd_*.cu translation units) plus the small helper kernels of the
+// forward path.
+//
+// What one CTA does (sources: "The convolution trick is gone -- what now?",
+// Mamba lesson 2: keep the recurrence on chip, write back only the final
+// state; "State Space Models (SSMs) & Mamba", section "Hardware-Aware
+// Parallelism": the recurrence is a scan over the sequence):
+//   * it owns CH = 128/NT channels of one batch row for a whole segment of
+//     the sequence (normally the whole sequence);
+//   * a producer warp streams 64-token chunks of u, delta_raw, z (TMA, 128-B
+//     swizzle) and of the prepared B/C tile into a multi-stage shared-memory
+//     ring guarded by mbarriers;
+//   * each of the 128 compute threads keeps G = NP/NT states of one channel
+//     in registers; the NT threads of a channel split the per-token work
+//     (softplus, gate, D skip) and exchange it with warp shuffles;
+//   * per token and state: dA = 2^(delta2 * A) on the MUFU (delta2 = delta /
+//     ln 2, so no extra scaling), h = dA h + delta u B, y += C h, in packed
+//     f32x2 arithmetic.  With fp32 inputs the exp2 is the FMA-pipe series
+//     (exp2_accurate) so that long sequences keep fp32-level agreement.
+// SUMMARY = true is pass 1 of the segmented plan for very long sequences: no
+// read-out, the kernel records each segment's end state from a zero start and
+// the segment's sum of delta2 (the decay of the carried state over the
+// segment is 2^(A * sum)).
+#pragma once
+
+#include "ssm_common.cuh"
+#include "ssm_kernels.cuh"
+
+namespace ssm {
+
+template <int NT, int EB>
+struct FwdCfg {
+    static constexpr int CH = kConsumers / NT;       // channels per CTA
+    static constexpr int SB = 8 * NT;                // tokens per super-block
+    static constexpr int RAW = CH * kT * EB;         // bytes of one raw tile
+    static constexpr int BOXES = kT * EB / 128;      // 128-byte TMA boxes per tile row
+    static constexpr int BOX_T = 128 / EB;           // tokens per box
+};
+
+template <int NP>
+constexpr int bc_tile_bytes() { return kT * 2 * NP * 4; }
+
+template <int NT, int EB, int NP, bool SUMMARY>
+constexpr int fwd_stage_bytes() {
+    return (SUMMARY ? 2 : 3) * FwdCfg<NT, EB>::RAW + bc_tile_bytes<NP>();
+}
+
+template <int NT, int EB, int NP, bool SUMMARY>
+constexpr int fwd_stages() {
+    // as many stages as fit in ~100 KB (two CTAs per SM), at least 2
+    return (100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>()) < 2
+               ? 2
+               : ((100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>()) > 4
+                      ? 4
+                      : 100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>());
+}
+
+template <int NT, int EB, int NP, bool SUMMARY>
+constexpr int fwd_smem_bytes() {
+    return fwd_stages<NT, EB, NP, SUMMARY>() * fwd_stage_bytes<NT, EB, NP, SUMMARY>() + 1024;
+}
+
+// softplus in log2 units: for x = (delta_raw + bias) * log2(e) return
+// log2(1 + 2^x) = delta / ln 2.
+//  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), where for 2^-|x| <
+//  1/16 the logarithm is its Taylor series to the fifth power (relative
+//  truncation error < 2e-7) instead of the MUFU lg2, whose absolute error
+//  near 1 would dominate small results.
+//  fast (bf16 inputs): max(x, lg2(1 + 2^min(x, 64))); the absolute error of
+//  lg2 near 1 (~1e-7) is far below the bf16 tolerance.
+template <bool ACCURATE>
+__device__ __forceinline__ float softplus2(float x) {
+    if (ACCURATE) {
+        const float e = ex2(-fabsf(x));
+        float p = fmaf(e, 0.2f, -0.25f);
+        p = fmaf(e, p, 0.33333334f);
+        p = fmaf(e, p, -0.5f);
+        p = fmaf(e, p, 1.0f);
+        const float series = e * p * kLog2e;
+        const float direct = lg2(1.0f + e);
+        return fmaxf(x, 0.0f) + (e < 0.0625f ? series : direct);
+    } else {
+        return fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
+    }
+}
+
+// 8 consecutive tokens [tb, tb+8) of local channel c from a raw tile.
+template <typename TIN, int CH>
+__device__ __forceinline__ void load_raw8(const uint8_t* tile, int c, int tb, float (&v)[8]) {
+    if constexpr (sizeof(TIN) == 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + swz128(c, tb * 2));
+        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+        v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+    } else {
+        const uint8_t* box = tile + (tb / 32) * (CH * 128);
+        const int cb = (tb % 32) * 4;
+        const float4 a = *reinterpret_cast<const float4*>(box + swz128(c, cb));
+        const float4 b = *reinterpret_cast<const float4*>(box + swz128(c, cb + 16));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// Store 8 consecutive outputs of one row; `nv` of them are inside the row.
+template <typename TOUT>
+__device__ __forceinline__ void store_out8(void* y, int64_t off, const float (&v)[8], int nv,
+                                           bool vec_ok) {
+    if (nv <= 0) return;
+    if constexpr (sizeof(TOUT) == 2) {
+        __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(y) + off;
+        if (vec_ok && nv >= 8) {
+            uint4 w;
+            w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
+            w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(yp) = w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < nv) yp[q] = __float2bfloat16_rn(v[q]);
+        }
+    } else {
+        float* yp = reinterpret_cast<float*>(y) + off;
+        if (vec_ok && nv >= 8) {
+            reinterpret_cast<float4*>(yp)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4*>(yp)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < nv) yp[q] = v[q];
+        }
+    }
+}
+
+// Plain (non-TMA) fill of one raw tile, used when rows are not 16-byte
+// aligned (seqlen * element size not a multiple of 16).  Same swizzled layout.
+template <typename TIN, int CH>
+__device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, int64_t row0,
+                                              int64_t rows_valid, int64_t L, int64_t t0,
+                                              int lane) {
+    const TIN* s = reinterpret_cast<const TIN*>(src);
+    for (int idx = lane; idx < CH * kT; idx += 32) {
+        const int c = idx / kT, t = idx % kT;
+        TIN v = TIN(0.0f);
+        if (c < rows_valid && t0 + t < L) v = s[(row0 + c) * L + t0 + t];
+        uint8_t* dst;
+        if constexpr (sizeof(TIN) == 2) {
+            dst = tile + swz128(c, t * 2);
+        } else {
+            dst = tile + (t / 32) * (CH * 128) + swz128(c, (t % 32) * 4);
+        }
+        *reinterpret_cast<TIN*>(dst) = v;
+    }
+}
+
+template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW>
+__global__ void __launch_bounds__(kThreads, 2)
+fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
+           const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
+           const __grid_constant__ CUtensorMap tm_bc) {
+    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
+    constexpr int G = NP / NT;
+    constexpr int CH = Cfg::CH;
+    constexpr int SB = Cfg::SB;
+    constexpr int RAW = Cfg::RAW;
+    constexpr int NRAW = SUMMARY ? 2 : 3;
+    constexpr int BCB = bc_tile_bytes<NP>();
+    constexpr int STAGE = fwd_stage_bytes<NT, (int)sizeof(TIN), NP, SUMMARY>();
+    constexpr int STAGES = fwd_stages<NT, (int)sizeof(TIN), NP, SUMMARY>();
+    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    static_assert(G == 4 || G == 8 || G == 16, "states per thread");
+    static_assert(NT == 1 || NT == 2 || NT == 4, "threads per channel");
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int seg = blockIdx.z;
+    const int64_t L = p.L;
+    const int64_t nchunks = (L + kT - 1) / kT;
+    const int64_t k_begin = (int64_t)seg * p.seg_chunks;
+    const int64_t k_end = min(nchunks, k_begin + p.seg_chunks);
+    const bool has_z = !SUMMARY && p.z != nullptr;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------ producer warp
+    if (tid >= kConsumers) {
+        const int lane = tid - kConsumers;
+        if (lane == 0) {
+            prefetch_tmap(&tm_bc);
+            if (TMA_RAW) {
+                prefetch_tmap(&tm_u);
+                prefetch_tmap(&tm_dr);
+                if (has_z) prefetch_tmap(&tm_z);
+            }
+        }
+        const int64_t row0 = b * p.D + d0;
+        const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const int64_t i = k - k_begin;
+            const int s = (int)(i % STAGES);
+            if (i >= STAGES) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&empty_bar[s], (uint32_t)(((i / STAGES) - 1) & 1), p.timeout_ns);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                    return;
+                }
+            }
+            uint8_t* st = smem + s * STAGE;
+            const int32_t t0 = (int32_t)(k * kT);
+            if (TMA_RAW) {
+                if (lane == 0) {
+                    const uint32_t bytes = (has_z ? 3 : 2) * RAW + BCB;
+                    mbar_arrive_expect_tx(&full_bar[s], bytes);
+#pragma unroll
+                    for (int bx = 0; bx < Cfg::BOXES; ++bx) {
+                        const int32_t x = t0 + bx * Cfg::BOX_T;
+                        tma_load_2d(st + bx * CH * 128, &tm_u, &full_bar[s], x, (int32_t)row0);
+                        tma_load_2d(st + RAW + bx * CH * 128, &tm_dr, &full_bar[s], x, (int32_t)row0);
+                        if (has_z)
+                            tma_load_2d(st + 2 * RAW + bx * CH * 128, &tm_z, &full_bar[s], x,
+                                        (int32_t)row0);
+                    }
+                    tma_load_2d(st + NRAW * RAW, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
+                }
+            } else {
+                fill_raw_tile<TIN, CH>(st, p.u, row0, rows_valid, L, t0, lane);
+                fill_raw_tile<TIN, CH>(st + RAW, p.dr, row0, rows_valid, L, t0, lane);
+                if (has_z) fill_raw_tile<TIN, CH>(st + 2 * RAW, p.z, row0, rows_valid, L, t0, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full_bar[s], BCB);
+                    tma_load_2d(st + NRAW * RAW, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- compute threads
+    const int lane = tid & 31;
+    const int c = tid / NT;
+    const int g = tid % NT;
+    const int64_t d = d0 + c;
+    const bool ch_ok = d < p.D;
+    const int64_t row = b * p.D + d;
+    const int N = p.N;
+
+    f2 Ap[G / 2], h[G / 2];
+#pragma unroll
+    for (int j = 0; j < G / 2; ++j) {
+        const int n0 = g * G + 2 * j, n1 = n0 + 1;
+        const float a0 = (ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f;
+        const float a1 = (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f;
+        Ap[j] = pk(a0, a1);
+        float h0v = 0.0f, h1v = 0.0f;
+        if (!SUMMARY && ch_ok) {
+            if (p.hin) {
+                const float* hs = p.hin + ((int64_t)seg * p.Bt * p.D + row) * NP;
+                h0v = hs[n0];
+                h1v = hs[n1];
+            } else if (p.h0) {
+                if (n0 < N) h0v = p.h0[row * N + n0];
+                if (n1 < N) h1v = p.h0[row * N + n1];
+            }
+        }
+        h[j] = pk(h0v, h1v);
+    }
+    const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
+    const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
+    const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
+    double sum_d2 = 0.0;
+    const int src_base = lane & ~(NT - 1);
+
+    for (int64_t k = k_begin; k < k_end; ++k) {
+        const int64_t i = k - k_begin;
+        const int s = (int)(i % STAGES);
+        if (!mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns)) {
+            set_status(p.status, SSM_ERR_TIMEOUT);
+            return;
+        }
+        const uint8_t* st = smem + s * STAGE;
+        const float* bct = reinterpret_cast<const float*>(st + NRAW * RAW);
+        const int nvalid = (int)min((int64_t)kT, L - k * kT);
+
+#pragma unroll 1
+        for (int sb = 0; sb < kT / SB; ++sb) {
+            if (sb * SB >= nvalid) break;
+            const int tb = sb * SB + g * 8;  // this thread's 8 tokens within the chunk
+
+            // per-token work for this thread's 8 tokens
+            float uv[8], dv[8], zv[8];
+            load_raw8<TIN, CH>(st, c, tb, uv);
+            load_raw8<TIN, CH>(st + RAW, c, tb, dv);
+            if (has_z) load_raw8<TIN, CH>(st + 2 * RAW, c, tb, zv);
+            float d2[8], du[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                d2[q] = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+                du[q] = d2[q] * uv[q];
+            }
+            if (nvalid < kT) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (tb + q >= nvalid) { d2[q] = 0.0f; du[q] = 0.0f; }
+            }
+            if (SUMMARY) {
+                float s8 = ((d2[0] + d2[1]) + (d2[2] + d2[3])) + ((d2[4] + d2[5]) + (d2[6] + d2[7]));
+                sum_d2 += (double)s8;
+            }
+
+            // every thread of the channel needs delta2 and delta2*u of all SB tokens
+            float D2[SB], DU[SB];
+#pragma unroll
+            for (int tt = 0; tt < SB; ++tt) {
+                if (NT == 1) {
+                    D2[tt] = d2[tt];
+                    DU[tt] = du[tt];
+                } else {
+                    D2[tt] = __shfl_sync(0xffffffffu, d2[tt % 8], src_base + tt / 8);
+                    DU[tt] = __shfl_sync(0xffffffffu, du[tt % 8], src_base + tt / 8);
+                }
+            }
+
+            // the recurrence over SB tokens for this thread's G states
+            float yp[SB];
+#pragma unroll
+            for (int tt = 0; tt < SB; ++tt) {
+                const float* bcrow = bct + (sb * SB + tt) * (2 * NP) + g * G;
+                const f2 d2p = pk(D2[tt], D2[tt]);
+                const f2 dup = pk(DU[tt], DU[tt]);
+                f2 acc0 = pk(0.0f, 0.0f), acc1 = pk(0.0f, 0.0f);
+#pragma unroll
+                for (int q4 = 0; q4 < G / 4; ++q4) {
+                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+                    const f2 a0 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4]))
+                                           : ex2x2(mul2(d2p, Ap[2 * q4]));
+                    const f2 a1 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4 + 1]))
+                                           : ex2x2(mul2(d2p, Ap[2 * q4 + 1]));
+                    h[2 * q4] = fma2(a0, h[2 * q4], mul2(dup, Bq.x));
+                    h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
+                    if (!SUMMARY) {
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+                        acc0 = fma2(Cq.x, h[2 * q4], acc0);
+                        acc1 = fma2(Cq.y, h[2 * q4 + 1], acc1);
+                    }
+                }
+                if (!SUMMARY) {
+                    float lo, hi;
+                    upk(add2(acc0, acc1), lo, hi);
+                    yp[tt] = lo + hi;
+                }
+            }
+
+            if (!SUMMARY) {
+                // sum the partial read-outs of the NT threads; thread g keeps its 8 tokens
+                float yt[8];
+                if (NT == 1) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) yt[q] = yp[q];
+                } else if (NT == 2) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float keep = g ? yp[8 + q] : yp[q];
+                        const float send = g ? yp[q] : yp[8 + q];
+                        yt[q] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                } else {
+                    float r1[16];
+                    const bool hb = (g & 2) != 0;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float keep = hb ? yp[16 + q] : yp[q];
+                        const float send = hb ? yp[q] : yp[16 + q];
+                        r1[q] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    }
+                    const bool lb = (g & 1) != 0;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float keep = lb ? r1[8 + q] : r1[q];
+                        const float send = lb ? r1[q] : r1[8 + q];
+                        yt[q] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                }
+                // D skip and SiLU gate for this thread's tokens
+                float out[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float v = fmaf(Dd, uv[q], yt[q]);
+                    if (has_z) {
+                        const float zq = zv[q];
+                        v *= zq * rcp(1.0f + ex2(-kLog2e * zq));
+                    }
+                    out[q] = v;
+                }
+                if (ch_ok)
+                    store_out8<TOUT>(p.y, row * L + k * kT + tb, out, nvalid - tb, vec_out);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+
+    if (SUMMARY) {
+        // one thread per channel records the segment's sum of delta2
+        double tot = sum_d2;
+#pragma unroll
+        for (int o = 1; o < NT; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (ch_ok) {
+            float* hl = p.hloc + ((int64_t)seg * p.Bt * p.D + row) * NP + g * G;
+#pragma unroll
+            for (int j = 0; j < G / 2; ++j) {
+                float lo, hi;
+                upk(h[j], lo, hi);
+                hl[2 * j] = lo;
+                hl[2 * j + 1] = hi;
+            }
+            if (g == 0) p.sumd[(int64_t)seg * p.Bt * p.D + row] = (float)tot;
+        }
+    } else if (k_end == nchunks && p.hL && ch_ok) {
+#pragma unroll
+        for (int j = 0; j < G / 2; ++j) {
+            float lo, hi;
+            upk(h[j], lo, hi);
+            const int n0 = g * G + 2 * j;
+            if (n0 < N) p.hL[row * N + n0] = lo;
+            if (n0 + 1 < N) p.hL[row * N + n0 + 1] = hi;
+        }
+    }
+}
+
+}  // namespace ssm

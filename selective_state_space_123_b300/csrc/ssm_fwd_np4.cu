@@ -1,0 +1,14 @@
+// ssm_fwd_np4.cu -- forward-kernel instantiations for padded state size 4.
+#include "ssm_fwd_launch.cuh"
+
+namespace ssm {
+
+cudaError_t launch_fwd_np4(int NT, int tin, int tout, bool summary, bool tma_raw,
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NT) {
+        case 1: return launch_fwd_nt<4, 1>(tin, tout, summary, tma_raw, p, m, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ssm

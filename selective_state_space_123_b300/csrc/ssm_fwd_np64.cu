@@ -1,0 +1,14 @@
+// ssm_fwd_np64.cu -- forward-kernel instantiations for padded state size 64.
+#include "ssm_fwd_launch.cuh"
+
+namespace ssm {
+
+cudaError_t launch_fwd_np64(int NT, int tin, int tout, bool summary, bool tma_raw,
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NT) {
+        case 4: return launch_fwd_nt<64, 4>(tin, tout, summary, tma_raw, p, m, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ssm

@@ -1,0 +1,15 @@
+// ssm_fwd_np8.cu -- forward-kernel instantiations for padded state size 8.
+#include "ssm_fwd_launch.cuh"
+
+namespace ssm {
+
+cudaError_t launch_fwd_np8(int NT, int tin, int tout, bool summary, bool tma_raw,
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NT) {
+        case 2: return launch_fwd_nt<8, 2>(tin, tout, summary, tma_raw, p, m, grid, st);
+        case 1: return launch_fwd_nt<8, 1>(tin, tout, summary, tma_raw, p, m, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ssm

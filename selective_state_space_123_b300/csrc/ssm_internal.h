@@ -1,0 +1,43 @@
+// ssm_internal.h -- launchers shared between the C-ABI layer and the kernel
+// translation units.  Internal to libssmscan.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ssm_kernels.cuh"
+
+namespace ssm {
+
+// Tensor maps of one forward launch: raw tiles of u, delta_raw, z (unused
+// entries zeroed) and the prepared B/C tile.
+struct FwdMaps {
+    CUtensorMap u, dr, z, bc;
+};
+
+// Forward kernel launch for padded state size NP (4, 8, 16, 32, 64) and NT
+// threads per channel.  tin/tout are ssm_dtype values.
+cudaError_t launch_fwd_np4(int NT, int tin, int tout, bool summary, bool tma_raw,
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_np8(int NT, int tin, int tout, bool summary, bool tma_raw,
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_np16(int NT, int tin, int tout, bool summary, bool tma_raw,
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_np64(int NT, int tin, int tout, bool summary, bool tma_raw,
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+
+// The NT values each NP supports (first entry = default).
+int fwd_supported_nt(int NP, int* out, int cap);
+
+cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
+                           const void* C, float* out, int* status, cudaStream_t st);
+cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
+                         const float* h0, const float* hloc, const float* sumd, float* hin,
+                         cudaStream_t st);
+cudaError_t launch_step(int tin, int tout, const StepParams& p, cudaStream_t st);
+cudaError_t launch_expired_wait(int* status, int64_t spin_limit, cudaStream_t st);
+
+}  // namespace ssm

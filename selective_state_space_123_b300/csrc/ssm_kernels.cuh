@@ -1,0 +1,59 @@
+// ssm_kernels.cuh -- launch parameters shared between the host dispatcher
+// (ssm_api.cu) and the kernels.  Internal to libssmscan.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+constexpr int kT = 64;              // tokens per chunk (one TMA tile along L)
+constexpr int kConsumers = 128;     // compute threads per CTA (4 warps)
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded waits: 2 s
+
+// Forward scan parameters.  Layouts are the public ones (see ssm_scan.h);
+// `bc` is the prepared copy of B and C: (batch, seqlen, 2*NP) fp32 with
+// [0, NP) = ln2 * B[b, n, t] and [NP, 2NP) = C[b, n, t], zero for n >= N.
+struct FwdParams {
+    int64_t Bt, D, L;
+    int N;
+    const void* u;
+    const void* dr;
+    const void* z;          // nullable
+    const float* A;
+    const float* Dv;        // nullable
+    const float* bias;      // nullable
+    const float* h0;        // nullable
+    const float* bc;
+    void* y;
+    float* hL;              // nullable
+    // segmented plan (nseg > 1): the sequence is cut into nseg segments of
+    // seg_chunks chunks; pass 1 writes per-segment summaries, the carry
+    // kernel turns them into per-segment initial states, pass 2 writes y.
+    int64_t seg_chunks;
+    int nseg;
+    float* hin;             // (nseg, Bt, D, NP) initial state of each segment (pass 2)
+    float* hloc;            // (nseg, Bt, D, NP) end state from a zero start (pass 1)
+    float* sumd;            // (nseg, Bt, D) sum of delta/ln2 over the segment (pass 1)
+    int* status;
+    uint64_t timeout_ns;
+};
+
+struct StepParams {
+    int64_t Bt, D;
+    int N;
+    const void* u;
+    const void* dr;
+    const void* z;
+    const float* A;
+    const float* Dv;
+    const float* bias;
+    const void* B;
+    const void* C;
+    float* state;
+    void* y;
+};
+
+}  // namespace ssm

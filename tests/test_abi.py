@@ -1,0 +1,113 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments before touching the GPU (no compute call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    from tests.buildlib import ensure_built
+    ensure_built()
+    import selective_state_space_123_b300 as m
+    return m
+
+
+def _declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "ssm_scan.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", hdr)))
+
+
+def test_exports_every_declared_symbol(pkg):
+    declared = _declared_symbols()
+    assert set(declared) == set(pkg.EXPORTS), declared
+    raw = ctypes.CDLL(pkg.LIB_PATH)
+    for name in declared:
+        assert hasattr(raw, name), name
+
+
+def test_strerror_covers_codes(pkg):
+    for code in range(-8, 1):
+        s = pkg.ssm_strerror(code)
+        assert s and s != "unknown status"
+    assert pkg.ssm_strerror(-99) == "unknown status"
+
+
+def _call_fwd(pkg, shape, ptrs=None, ws_bytes=1 << 20, ws=0x10000):
+    p = dict(u=0x1000, dr=0x2000, A=0x3000, B=0x4000, C=0x5000, D=None, z=None, bias=None,
+             h0=None, y=0x6000, hL=None)
+    if ptrs:
+        p.update(ptrs)
+    V = lambda x: None if x is None else ctypes.c_void_p(x)
+    return pkg.lib.ssm_scan_fwd(ctypes.byref(shape) if shape is not None else None,
+                                V(p["u"]), V(p["dr"]), V(p["A"]), V(p["B"]), V(p["C"]),
+                                V(p["D"]), V(p["z"]), V(p["bias"]), V(p["h0"]), V(p["y"]),
+                                V(p["hL"]), V(ws), ws_bytes, None)
+
+
+def test_fwd_argument_errors(pkg):
+    S = lambda **k: pkg.make_shape(k.get("b", 2), k.get("d", 8), k.get("n", 16), k.get("l", 64),
+                                   k.get("ti", 1), k.get("to", 0))
+    assert _call_fwd(pkg, None) == pkg.SSM_ERR_NULL
+    assert _call_fwd(pkg, S(n=0)) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd(pkg, S(n=65)) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd(pkg, S(b=-1)) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd(pkg, S(l=-5)) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd(pkg, S(ti=7)) == pkg.SSM_ERR_DTYPE
+    assert _call_fwd(pkg, S(to=-1)) == pkg.SSM_ERR_DTYPE
+    assert _call_fwd(pkg, S(b=1 << 40, d=1 << 40)) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd(pkg, S(), {"u": None}) == pkg.SSM_ERR_NULL
+    assert _call_fwd(pkg, S(), {"A": None}) == pkg.SSM_ERR_NULL
+    assert _call_fwd(pkg, S(), {"y": None}) == pkg.SSM_ERR_NULL
+    assert _call_fwd(pkg, S(), {"B": 0x4008}) == pkg.SSM_ERR_ALIGN
+    assert _call_fwd(pkg, S(), {"hL": 0x7004}) == pkg.SSM_ERR_ALIGN
+    assert _call_fwd(pkg, S(), ws=None) == pkg.SSM_ERR_WORKSPACE
+    assert _call_fwd(pkg, S(), ws_bytes=16) == pkg.SSM_ERR_WORKSPACE
+    # nothing to do: empty batch or no channels succeed without touching the GPU
+    assert _call_fwd(pkg, S(b=0), {"u": None, "y": None}) == pkg.SSM_OK
+    assert _call_fwd(pkg, S(d=0), {"u": None, "y": None}) == pkg.SSM_OK
+
+
+def test_workspace_query(pkg):
+    ok = pkg.make_shape(4, 4096, 16, 4096, 1, 1)
+    n = pkg.ssm_scan_workspace_bytes(ok)
+    # header + prepared B/C (batch * L * 2 * 16 fp32)
+    assert n >= 256 + 4 * 4096 * 32 * 4
+    assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 1, 0, 1, 1, 1)) == 0
+    assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 1, 4, 1, 5, 1)) == 0
+    # a million-length sequence with few channels takes the segmented plan
+    long = pkg.make_shape(1, 1536, 16, 1 << 20, 1, 1)
+    assert pkg.ssm_scan_workspace_bytes(long) > 256 + (1 << 20) * 32 * 4
+
+
+def test_step_argument_errors(pkg):
+    V = ctypes.c_void_p
+    f = pkg.lib.ssm_scan_step
+    args = [V(0x1000), V(0x2000), V(0x3000), V(0x4000), V(0x5000), None, None, None, V(0x6000),
+            V(0x7000), None]
+    assert f(2, 8, 0, 1, 1, *args) == pkg.SSM_ERR_SHAPE
+    assert f(2, 8, 16, 3, 1, *args) == pkg.SSM_ERR_DTYPE
+    assert f(0, 8, 16, 1, 1, *args) == pkg.SSM_OK
+    bad = list(args); bad[0] = None
+    assert f(2, 8, 16, 1, 1, *bad) == pkg.SSM_ERR_NULL
+    bad = list(args); bad[8] = V(0x6004)
+    assert f(2, 8, 16, 1, 1, *bad) == pkg.SSM_ERR_ALIGN
+
+
+def test_status_and_debug_argument_errors(pkg):
+    assert pkg.lib.ssm_get_status(None, None) == pkg.SSM_ERR_NULL
+    assert pkg.lib.ssm_debug_expired_wait(None, 256, 10, None) == pkg.SSM_ERR_NULL
+    assert pkg.lib.ssm_debug_expired_wait(ctypes.c_void_p(0x1000), 8, 10, None) == pkg.SSM_ERR_WORKSPACE
+    assert pkg.lib.ssm_debug_expired_wait(ctypes.c_void_p(0x1008), 256, 10, None) == pkg.SSM_ERR_ALIGN
+
+
+def test_binding_refuses_cpu_tensors(pkg):
+    import torch
+    u = torch.zeros(1, 2, 8)
+    with pytest.raises(ValueError):
+        pkg.ssm_scan_fwd(u, u, torch.zeros(2, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
