@@ -151,6 +151,32 @@ SSM_API int ssm_get_status(void* workspace, ssm_stream_t stream);
 /* Human-readable text of a status code (static storage, never NULL). */
 SSM_API const char* ssm_strerror(int code);
 
+/* ssm_scan_fwd for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this entry point; it exists for callers that are handed
+ * only their input and output buffers and may not allocate on the device
+ * themselves (a plug-in inside a host engine whose allocator owns all device
+ * memory, or a latency-bound loop that must not call cudaMalloc after
+ * start-up, since it can synchronise the device and take unbounded time).
+ * Arguments are those of ssm_scan_fwd without the workspace; nothing is
+ * allocated or freed.
+ *  - The scratch is a fixed 32 MiB array inside the library, held on every GPU
+ *    that loads it until the process exits.  A shape whose
+ *    ssm_scan_workspace_bytes(shape, 0) exceeds 32 MiB is rejected with
+ *    SSM_ERR_WORKSPACE before anything is enqueued (at 16 states that is about
+ *    262,000 tokens summed over the batch).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU
+ *    (different streams, or several host threads) race and corrupt each
+ *    other's results; issue them in order on one stream.  Each call rewrites
+ *    all the scratch it reads, so earlier contents do not matter.
+ *  - The device status word lives in that scratch and is not reachable by the
+ *    caller; an expired device-side wait leaves y and hL undefined. */
+SSM_API int ssm_scan_fwd_noalloc(const ssm_shape* shape, const void* u, const void* delta_raw,
+                 const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* delta_bias, const float* h0,
+                 void* y, float* hL, ssm_stream_t stream);
+
 /* Failure-detection self test: launches one block that waits on a device
  * flag nothing ever sets, giving up after `spin_limit` polls; the expired
  * wait is reported through the workspace status word (SSM_ERR_TIMEOUT, read

@@ -41,7 +41,7 @@ SSM_ERR_WORKSPACE, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_UNSUPPORTED = -5, -6, 
 
 # Every symbol include/ssm_scan.h declares.
 EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
-           "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait")
+           "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait", "ssm_scan_fwd_noalloc")
 
 
 class ssm_shape(ctypes.Structure):
@@ -66,6 +66,10 @@ lib.ssm_strerror.argtypes = [ctypes.c_int]
 lib.ssm_strerror.restype = ctypes.c_char_p
 lib.ssm_debug_expired_wait.argtypes = [_P, ctypes.c_size_t, _I64, _P]
 lib.ssm_debug_expired_wait.restype = ctypes.c_int
+# scratch-free forward (no workspace argument; see include/ssm_scan.h)
+lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 12
+lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class SSMError(RuntimeError):
