@@ -126,6 +126,36 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
     return pl;
 }
 
+// Backward plan: the two sweeps need the prepared B/C (state size padded to
+// at least 8), one fp32 number per (batch, channel, token), the final state
+// and the state at the end of every 64-token chunk.
+struct BwdPlan {
+    int NP = 16, NT = 2, CH = 64;
+    bool tma_raw = false;
+    size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, bytes = 0;
+};
+
+BwdPlan plan_bwd(const ssm_shape& s) {
+    BwdPlan pl;
+    pl.NP = padded_state(s.dstate);
+    if (pl.NP < 8) pl.NP = 8;
+    pl.NT = pl.NP <= 16 ? 2 : 4;
+    if (pl.NP == 16 && env_int("SSM_BWD_NT", 0) == 4) pl.NT = 4;
+    pl.CH = kConsumers / pl.NT;
+    pl.tma_raw = (s.seqlen * dtype_bytes(s.in_dtype)) % 16 == 0;
+    size_t off = kHeaderBytes;
+    pl.off_bc = off;
+    off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
+    pl.off_phi = off;
+    off += align256((size_t)s.batch * s.dim * s.seqlen * 4);
+    pl.off_hfin = off;
+    off += align256((size_t)s.batch * s.dim * pl.NP * 4);
+    pl.off_hck = off;
+    off += align256((size_t)s.batch * s.dim * ((s.seqlen + kT - 1) / kT) * pl.NP * 4);
+    pl.bytes = off;
+    return pl;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -168,6 +198,16 @@ cudaError_t launch_fwd(int NP, int NT, int tin, int tout, bool summary, bool tma
     }
 }
 
+cudaError_t launch_bwd(int NP, int NT, int tin, int tout, bool tma, const BwdParams& p,
+                       const BwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NP) {
+        case 8: return launch_bwd_np8(NT, tin, tout, tma, p, m, grid, st);
+        case 16: return launch_bwd_np16(NT, tin, tout, tma, p, m, grid, st);
+        case 32: return launch_bwd_np32(NT, tin, tout, tma, p, m, grid, st);
+        default: return launch_bwd_np64(NT, tin, tout, tma, p, m, grid, st);
+    }
+}
+
 }  // namespace
 
 namespace ssm {
@@ -206,9 +246,8 @@ const char* ssm_strerror(int code) {
 
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     if (shape_check(shape) != SSM_OK) return 0;
-    const FwdPlan pl = plan_fwd(*shape, device_sm_count());
-    size_t bytes = pl.bytes;
-    (void)for_backward;
+    const size_t bytes = for_backward ? plan_bwd(*shape).bytes
+                                      : plan_fwd(*shape, device_sm_count()).bytes;
     return bytes < kHeaderBytes ? kHeaderBytes : bytes;
 }
 
@@ -296,13 +335,108 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     return SSM_OK;
 }
 
-int ssm_scan_bwd(const ssm_shape* shape, const void*, const void*, const float*, const void*,
-                 const void*, const float*, const void*, const float*, const float*, const void*,
-                 const float*, void*, void*, float*, float*, float*, float*, void*, float*, float*,
-                 void*, size_t, ssm_stream_t) {
+int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, const void* dy, const float* dhL,
+                 void* du, void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                 void* dz, float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
+                 ssm_stream_t stream) {
     const int sc = shape_check(shape);
     if (sc != SSM_OK) return sc;
-    return SSM_ERR_UNSUPPORTED;
+    const ssm_shape s = *shape;
+    const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    if (Dm > 0 && !A) return SSM_ERR_NULL;
+    if (Dm > 0 && !dA) return SSM_ERR_NULL;
+    if (Bt == 0 || Dm == 0) {
+        // nothing flows; gradients of the per-channel parameters are zero
+        cudaStream_t st0 = static_cast<cudaStream_t>(stream);
+        const void* ptrs0[] = {A, dA, dD, ddelta_bias};
+        for (const void* q : ptrs0)
+            if (q && !aligned16(q)) return SSM_ERR_ALIGN;
+        if (dA && cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st0) != cudaSuccess) return SSM_ERR_CUDA;
+        if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st0) != cudaSuccess) return SSM_ERR_CUDA;
+        if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dm * 4, st0) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (Bt > 0 && L > 0 && dB && dC) {
+            if (cudaMemsetAsync(dB, 0, (size_t)(Bt * N * L) * 4, st0) != cudaSuccess ||
+                cudaMemsetAsync(dC, 0, (size_t)(Bt * N * L) * 4, st0) != cudaSuccess)
+                return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    if (!workspace) return SSM_ERR_WORKSPACE;
+    if (L > 0 && (!u || !delta_raw || !B || !C || !dy || !du || !ddelta_raw || !dB || !dC))
+        return SSM_ERR_NULL;
+    const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL, du, ddelta_raw,
+                          dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SSM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const BwdPlan pl = plan_bwd(s);
+    if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+
+    // outputs summed with atomics start at zero
+    if (cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dm * 4, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (L == 0) {
+        // an empty sequence passes dhL straight through to dh0
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (dh0) {
+            const size_t bytes = (size_t)(Bt * Dm * N) * 4;
+            cudaError_t e = dhL ? cudaMemcpyAsync(dh0, dhL, bytes, cudaMemcpyDeviceToDevice, st)
+                                : cudaMemsetAsync(dh0, 0, bytes, st);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    if (cudaMemsetAsync(dB, 0, (size_t)(Bt * N * L) * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(dC, 0, (size_t)(Bt * N * L) * 4, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+
+    float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
+    if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+
+    const int eb = dtype_bytes(s.in_dtype);
+    const CUtensorMapDataType tdt =
+        s.in_dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    float* phi = reinterpret_cast<float*>(ws + pl.off_phi);
+    BwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!make_map(&maps.bc, bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT,
+                  false))
+        return SSM_ERR_CUDA;
+    if (pl.tma_raw) {
+        const uint32_t box_t = 128 / eb;
+        if (!make_map(&maps.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+            !make_map(&maps.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+            (z && !make_map(&maps.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)) ||
+            !make_map(&maps.dy, dy, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+            !make_map(&maps.phi, phi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, Bt * Dm, 32, pl.CH,
+                      true))
+            return SSM_ERR_CUDA;
+    }
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Bt = Bt; p.D = Dm; p.L = L; p.N = (int)N;
+    p.u = u; p.dr = delta_raw; p.z = z; p.dy = dy; p.A = A; p.Dv = D; p.bias = delta_bias;
+    p.h0 = h0; p.dhL = dhL; p.bc = bc; p.phi = phi;
+    p.hfin = reinterpret_cast<float*>(ws + pl.off_hfin);
+    p.hck = reinterpret_cast<float*>(ws + pl.off_hck);
+    p.du = du; p.ddr = ddelta_raw; p.dz = dz;
+    p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dbias = ddelta_bias; p.dh0 = dh0;
+    p.status = status;
+    p.timeout_ns = kDefaultTimeoutNs;
+    const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
+    if (launch_bwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, pl.tma_raw, p, maps, dim3(gx, (unsigned)Bt),
+                   st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
 }
 
 int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, int32_t out_dtype,

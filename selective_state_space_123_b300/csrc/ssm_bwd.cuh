@@ -1,0 +1,775 @@
+// ssm_bwd.cuh -- reverse mode of the selective scan (templated; instantiated
+// in the ssm_bwd_*.cu translation units).
+//
+// The pages give no backward pass; this is the exact derivative of the
+// recurrence of "State Space Models (SSMs) & Mamba" (sections "State-Space
+// Models (SSMs): A Resurgent Paradigm" and "The Magic of Selective Scan"),
+// in natural units:
+//   g_t      = dy_t silu(z_t)                     (dy_t if there is no gate)
+//   lambda_t = g_t C_t + a_{t+1} lambda_{t+1},     lambda_L = g_L C_L + dhL
+//   du_t     = g_t D + delta_t sum_n lambda_t B_t
+//   ddelta_t = sum_n lambda_t (A a_t h_{t-1} + B_t u_t)
+//   dB_t     = sum_d lambda_t delta_t u_t,   dC_t = sum_d g_t h_t
+//   dA       = sum_{b,t} lambda_t delta_t a_t h_{t-1},   dh0 = a_1 lambda_1
+//   dz_t     = dy_t (sum_n C_t h_t + D u_t) silu'(z_t)
+//
+// Two streaming sweeps per channel tile, neither of which keeps per-token
+// states:
+//  * bwd_fwd_kernel runs the recurrence forward from h0 and, beside h, the
+//    tangent m = dh/dA (m_t = a_t m_{t-1} + delta_t a_t h_{t-1}), so that
+//    dA = sum_t g_t C_t m_t + dhL m_L needs no reverse pass.  It also emits
+//    dz, dC (reduced over the tile's channels, then added to global memory),
+//    the final state, and one fp32 number per token,
+//        phi_t = g_t sum_n A_n C_t[n] a_t[n] h_{t-1}[n].
+//  * bwd_rev_kernel walks the sequence backwards carrying lambda.  The one
+//    term of ddelta that needs h, Q_t = sum_n A_n lambda_t a_t h_{t-1}, is
+//    rebuilt from per-token scalars: substituting the two recurrences gives
+//    Q_t = Q_{t+1} + phi_t - rho_t with
+//        rho_t = delta_t u_t sum_n A_n a_{t+1}[n] lambda_{t+1}[n] B_t[n]
+//    and Q after the last token = psi = sum_n A_n dhL[n] h_L[n], hence
+//        ddelta_t = psi + sum_{s>=t} (phi_s - rho_s) + u_t sum_n lambda_t B_t.
+//    Both increments shrink with the decay a, so states that forget quickly
+//    add no large, cancelling terms to the fp32 suffix sum.  The sum runs
+//    over scalars per (channel, token); at every chunk boundary it is reset
+//    to its exact value, computed from lambda and the state at the end of the
+//    previous chunk (stored by the forward sweep, N floats per 64 tokens), so
+//    rounding never accumulates over more than one chunk.
+// Units: as in the forward kernel, delta2 = delta / ln2 and the prepared B
+// is ln2 * B, so delta * B * u = delta2 * u * B'.  Gradients are written in
+// natural units.
+#pragma once
+
+#include "ssm_fwd.cuh"
+
+namespace ssm {
+
+// tokens per batch of the cross-channel reduction of dB / dC: enough that a
+// lane's batch holds one value per channel lane of the warp
+template <int NP>
+constexpr int red_tokens() { return NP >= 32 ? 1 : 32 / NP; }
+
+template <int NT, int EB, int NP, bool REV>
+constexpr int bwd_stage_bytes() {
+    // raw tiles u, delta_raw, z, dy (+ the fp32 phi tile in the reverse sweep) + B/C
+    return 4 * FwdCfg<NT, EB>::RAW + (REV ? FwdCfg<NT, 4>::RAW : 0) + bc_tile_bytes<NP>();
+}
+
+// per-warp partial sums of dB or dC for one chunk: [4 warps][NP][kT] fp32
+template <int NP>
+constexpr int red_buf_bytes() { return (kConsumers / 32) * NP * kT * 4; }
+
+template <int NT, int EB, int NP, bool REV>
+constexpr int bwd_stages() {
+    return (200 * 1024 - red_buf_bytes<NP>()) / bwd_stage_bytes<NT, EB, NP, REV>() >= 3 &&
+                   3 * bwd_stage_bytes<NT, EB, NP, REV>() + red_buf_bytes<NP>() <= 110 * 1024
+               ? 3
+               : 2;
+}
+
+template <int NT, int EB, int NP, bool REV>
+constexpr int bwd_smem_bytes() {
+    return bwd_stages<NT, EB, NP, REV>() * bwd_stage_bytes<NT, EB, NP, REV>() +
+           red_buf_bytes<NP>() + 1024;
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Named barrier over the compute warps only (the producer warp never joins).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Reduce-scatter over the lanes that differ in the bits top_mask,
+// top_mask/2, ... (LEVELS of them): on return v[0, V >> LEVELS) of lane l
+// holds the sums of the entries whose index has as its top LEVELS bits the
+// lane bits (top_mask, top_mask/2, ...) of l, most significant first.
+template <int V, int LEVELS>
+__device__ __forceinline__ void reduce_scatter(float (&v)[V], int lane, int top_mask) {
+#pragma unroll
+    for (int l = 0; l < LEVELS; ++l) {
+        const int mask = top_mask >> l;
+        const int half = V >> (l + 1);
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = upper ? v[i + half] : v[i];
+            const float send = upper ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+}
+
+// Sum the four warps' partials of one chunk and add them to out[(b*N + n)*L
+// + t0 + t] for n < N, t < nvalid, scaled by `scale`.
+template <int NP>
+__device__ __forceinline__ void flush_red(const float* red, float* out, int64_t b, int N,
+                                          int64_t L, int64_t t0, int nvalid, float scale,
+                                          int tid) {
+    constexpr int W = kConsumers / 32;
+    const bool vec = (L % 4) == 0;
+    for (int idx = tid; idx < NP * (kT / 4); idx += kConsumers) {
+        const int n = idx / (kT / 4);
+        const int t = (idx % (kT / 4)) * 4;
+        if (n >= N || t >= nvalid) continue;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float4 v = *reinterpret_cast<const float4*>(red + (w * NP + n) * kT + t);
+            s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
+        }
+        float* o = out + (b * N + n) * L + t0 + t;
+        if (vec && t + 4 <= nvalid) {
+            red_add_v4(o, s[0] * scale, s[1] * scale, s[2] * scale, s[3] * scale);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (t + q < nvalid) atomicAdd(o + q, s[q] * scale);
+        }
+    }
+}
+
+// Issue the loads of one stage (producer warp).  Raw tiles at slots 0..3
+// (u, delta_raw, z, dy), then the optional fp32 tile, then the B/C tile.
+template <typename TIN, int NT, int NP, bool REV, bool TMA_RAW>
+__device__ __forceinline__ void bwd_load_stage(
+    uint8_t* st, uint64_t* bar, const BwdParams& p, const CUtensorMap* tm_u,
+    const CUtensorMap* tm_dr, const CUtensorMap* tm_z, const CUtensorMap* tm_dy,
+    const CUtensorMap* tm_phi, const CUtensorMap* tm_bc, int64_t b, int64_t row0,
+    int64_t rows_valid, int64_t k, bool has_z, int lane) {
+    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
+    using CfgF = FwdCfg<NT, 4>;
+    constexpr int CH = Cfg::CH;
+    constexpr int RAW = Cfg::RAW;
+    constexpr int BCB = bc_tile_bytes<NP>();
+    const int64_t L = p.L;
+    const int32_t t0 = (int32_t)(k * kT);
+    uint8_t* phi_dst = st + 4 * RAW;
+    uint8_t* bc_dst = st + 4 * RAW + (REV ? CfgF::RAW : 0);
+    if (TMA_RAW) {
+        if (lane == 0) {
+            const uint32_t bytes = (has_z ? 4 : 3) * RAW + (REV ? CfgF::RAW : 0) + BCB;
+            mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+            for (int bx = 0; bx < Cfg::BOXES; ++bx) {
+                const int32_t x = t0 + bx * Cfg::BOX_T;
+                tma_load_2d(st + bx * CH * 128, tm_u, bar, x, (int32_t)row0);
+                tma_load_2d(st + RAW + bx * CH * 128, tm_dr, bar, x, (int32_t)row0);
+                if (has_z) tma_load_2d(st + 2 * RAW + bx * CH * 128, tm_z, bar, x, (int32_t)row0);
+                tma_load_2d(st + 3 * RAW + bx * CH * 128, tm_dy, bar, x, (int32_t)row0);
+            }
+            if (REV) {
+#pragma unroll
+                for (int bx = 0; bx < CfgF::BOXES; ++bx)
+                    tma_load_2d(phi_dst + bx * CH * 128, tm_phi, bar, t0 + bx * CfgF::BOX_T,
+                                (int32_t)row0);
+            }
+            tma_load_2d(bc_dst, tm_bc, bar, 0, (int32_t)(b * L + t0));
+        }
+    } else {
+        fill_raw_tile<TIN, CH>(st, p.u, row0, rows_valid, L, t0, lane);
+        fill_raw_tile<TIN, CH>(st + RAW, p.dr, row0, rows_valid, L, t0, lane);
+        if (has_z) fill_raw_tile<TIN, CH>(st + 2 * RAW, p.z, row0, rows_valid, L, t0, lane);
+        fill_raw_tile<TIN, CH>(st + 3 * RAW, p.dy, row0, rows_valid, L, t0, lane);
+        if (REV) fill_raw_tile<float, CH>(phi_dst, p.phi, row0, rows_valid, L, t0, lane);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, BCB);
+            tma_load_2d(bc_dst, tm_bc, bar, 0, (int32_t)(b * L + t0));
+        }
+    }
+}
+
+// Producer warp: stream the chunks (forward or reverse order) through the
+// ring.  Returns false if a bounded wait expired (status already set).
+template <typename TIN, int NT, int NP, bool REV, bool TMA_RAW, int STAGES, int STAGE>
+__device__ __forceinline__ void bwd_producer(uint8_t* smem, uint64_t* full_bar, uint64_t* empty_bar,
+                                             const BwdParams& p, const CUtensorMap* tm_u,
+                                             const CUtensorMap* tm_dr, const CUtensorMap* tm_z,
+                                             const CUtensorMap* tm_dy, const CUtensorMap* tm_phi,
+                                             const CUtensorMap* tm_bc, int64_t b, int64_t d0,
+                                             bool has_z, int lane) {
+    constexpr int CH = FwdCfg<NT, (int)sizeof(TIN)>::CH;
+    if (lane == 0) {
+        prefetch_tmap(tm_bc);
+        if (TMA_RAW) {
+            prefetch_tmap(tm_u);
+            prefetch_tmap(tm_dr);
+            if (has_z) prefetch_tmap(tm_z);
+            prefetch_tmap(tm_dy);
+            if (REV) prefetch_tmap(tm_phi);
+        }
+    }
+    const int64_t nchunks = (p.L + kT - 1) / kT;
+    const int64_t row0 = b * p.D + d0;
+    const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int64_t k = REV ? nchunks - 1 - i : i;
+        const int s = (int)(i % STAGES);
+        if (i >= STAGES) {
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait(&empty_bar[s], (uint32_t)(((i / STAGES) - 1) & 1), p.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                return;
+            }
+        }
+        bwd_load_stage<TIN, NT, NP, REV, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr,
+                                                  tm_z, tm_dy, tm_phi, tm_bc, b, row0,
+                                                  rows_valid, k, has_z, lane);
+    }
+}
+
+// Per-token quantities of this lane's 8 tokens.
+// Per-token quantities the chain loop needs for this lane's 8 tokens:
+// delta2 = delta / ln2, delta2 * u and g = dy * silu(z) (dy without a gate).
+// Tokens past the end, and channels past D (whose tile rows belong to the
+// next batch row), get zeros and so contribute nothing.
+template <typename TIN, int CH, bool ACCURATE>
+__device__ __forceinline__ void token_prep(const uint8_t* st, int c, int tb, int nvalid,
+                                           bool has_z, bool ch_ok, float bias2, float (&d2)[8],
+                                           float (&du)[8], float (&gq)[8]) {
+    constexpr int RAW = CH * kT * (int)sizeof(TIN);
+    float uv[8], dv[8], gy[8];
+    load_raw8<TIN, CH>(st, c, tb, uv);
+    load_raw8<TIN, CH>(st + RAW, c, tb, dv);
+    load_raw8<TIN, CH>(st + 3 * RAW, c, tb, gy);
+    float zv[8];
+    if (has_z) load_raw8<TIN, CH>(st + 2 * RAW, c, tb, zv);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        d2[q] = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+        du[q] = d2[q] * uv[q];
+        gq[q] = has_z ? gy[q] * zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q])) : gy[q];
+        if (tb + q >= nvalid || !ch_ok) {
+            d2[q] = 0.0f;
+            du[q] = 0.0f;
+            gq[q] = 0.0f;
+        }
+    }
+}
+
+// Sum over the NT lanes of a channel (every lane gets the sum).
+template <int NT, int V>
+__device__ __forceinline__ void allreduce_nt(float (&v)[V]) {
+#pragma unroll
+    for (int o = 1; o < NT; o <<= 1)
+#pragma unroll
+        for (int q = 0; q < V; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+}
+
+// Cross-channel reduction of one batch of TB tokens (partials rb[tok * G +
+// s] of this lane's G states) into the warp's slice of the chunk buffer.
+template <int NP, int NT, int G, int TB>
+__device__ __forceinline__ void reduce_batch_to_smem(float (&rb)[TB * G], float* red, int warp,
+                                                     int lane, int g, int t_first) {
+    constexpr int RV = TB * G;
+    constexpr int CL = 32 / NT;
+    constexpr int LV = (CL == 32 ? 5 : CL == 16 ? 4 : CL == 8 ? 3 : CL == 4 ? 2 : CL == 2 ? 1 : 0);
+    static_assert(RV >= CL, "reduction batch");
+    reduce_scatter<RV, LV>(rb, lane, 16);
+    const int cw = lane / NT;
+#pragma unroll
+    for (int r = 0; r < RV / CL; ++r) {
+        const int idx = cw * (RV / CL) + r;
+        red[(warp * NP + g * G + idx % G) * kT + t_first + idx / G] = rb[r];
+    }
+}
+
+// ===================================================== forward sweep ===
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
+               const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_bc) {
+    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
+    constexpr int G = NP / NT;
+    constexpr int CH = Cfg::CH;
+    constexpr int SB = Cfg::SB;
+    constexpr int RAW = Cfg::RAW;
+    constexpr int STAGE = bwd_stage_bytes<NT, (int)sizeof(TIN), NP, false>();
+    constexpr int STAGES = bwd_stages<NT, (int)sizeof(TIN), NP, false>();
+    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    constexpr int TB = red_tokens<NP>();          // tokens per dC reduction batch
+    static_assert(G % 4 == 0 && G <= 16, "states per thread");
+    static_assert(8 % TB == 0, "reduction batches within a token group");
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int64_t L = p.L;
+    const int64_t nchunks = (L + kT - 1) / kT;
+    const bool has_z = p.z != nullptr;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (tid >= kConsumers) {
+        bwd_producer<TIN, NT, NP, false, TMA_RAW, STAGES, STAGE>(
+            smem, full_bar, empty_bar, p, &tm_u, &tm_dr, &tm_z, &tm_dy, nullptr, &tm_bc, b, d0,
+            has_z, tid - kConsumers);
+        return;
+    }
+
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int c = tid / NT;
+    const int g = tid % NT;
+    const int64_t d = d0 + c;
+    const bool ch_ok = d < p.D;
+    const int64_t row = b * p.D + d;
+    const int N = p.N;
+
+    f2 Ap[G / 2], h[G / 2], m[G / 2], dAc[G / 2];
+#pragma unroll
+    for (int j = 0; j < G / 2; ++j) {
+        const int n0 = g * G + 2 * j, n1 = n0 + 1;
+        Ap[j] = pk((ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f,
+                   (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f);
+        float h0v = 0.0f, h1v = 0.0f;
+        if (ch_ok && p.h0) {
+            if (n0 < N) h0v = p.h0[row * N + n0];
+            if (n1 < N) h1v = p.h0[row * N + n1];
+        }
+        h[j] = pk(h0v, h1v);
+        m[j] = pk(0.0f, 0.0f);
+        dAc[j] = pk(0.0f, 0.0f);
+    }
+    const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
+    const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
+    const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
+    const bool vec_phi = (L % 4) == 0;
+    const int src_base = lane & ~(NT - 1);
+
+    // A warp whose bounded wait expires records the error and stops working,
+    // but keeps joining the named barriers so the other warps never hang.
+    bool dead = false;
+    for (int64_t k = 0; k < nchunks; ++k) {
+        const int s = (int)(k % STAGES);
+        if (!dead) {
+            const bool ok = __all_sync(
+                0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((k / STAGES) & 1), p.timeout_ns));
+            if (!ok) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        const uint8_t* st = smem + s * STAGE;
+        const float* bct = reinterpret_cast<const float*>(st + 4 * RAW);
+        const int nvalid = (int)min((int64_t)kT, L - k * kT);
+
+#pragma unroll 1
+        for (int sb = 0; sb < kT / SB; ++sb) {
+            if (dead || sb * SB >= nvalid) break;
+            const int tb = sb * SB + g * 8;    // this lane's 8 tokens
+            float d2[8], du[8], gq[8];
+            token_prep<TIN, CH, ACCURATE>(st, c, tb, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+
+            float ys_own[8], ph_own[8];        // sums over n of this lane's tokens
+#pragma unroll 1
+            for (int j = 0; j < NT; ++j) {     // token group of lane j of the channel
+                const int src = src_base + j;
+                float D2[8], DU[8], GQ[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    D2[q] = NT == 1 ? d2[q] : __shfl_sync(0xffffffffu, d2[q], src);
+                    DU[q] = NT == 1 ? du[q] : __shfl_sync(0xffffffffu, du[q], src);
+                    GQ[q] = NT == 1 ? gq[q] : __shfl_sync(0xffffffffu, gq[q], src);
+                }
+                const int t_grp = sb * SB + j * 8;
+                float yp[8], pp[8];
+                float rb[TB * G];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
+                    const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
+                    f2 accy = pk(0.0f, 0.0f), accp = pk(0.0f, 0.0f);
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int jj = 2 * q4 + e;
+                            const f2 Bj = e ? Bq.y : Bq.x;
+                            const f2 Cj = e ? Cq.y : Cq.x;
+                            const f2 arg = mul2(d2p, Ap[jj]);
+                            const f2 a = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
+                            const f2 qv = mul2(a, h[jj]);            // a_t h_{t-1}
+                            h[jj] = fma2(dup, Bj, qv);
+                            m[jj] = fma2(a, m[jj], mul2(d2p, qv));   // dh/dA / ln2
+                            accy = fma2(Cj, h[jj], accy);
+                            accp = fma2(Ap[jj], mul2(Cj, qv), accp);
+                            dAc[jj] = fma2(mul2(gqp, Cj), m[jj], dAc[jj]);
+                            float lo, hi;
+                            upk(mul2(gqp, h[jj]), lo, hi);           // g_t h_t: dC partial
+                            rb[(q % TB) * G + 2 * jj] = lo;
+                            rb[(q % TB) * G + 2 * jj + 1] = hi;
+                        }
+                    }
+                    float lo, hi;
+                    upk(accy, lo, hi);
+                    yp[q] = lo + hi;
+                    upk(accp, lo, hi);
+                    pp[q] = lo + hi;
+                    if ((q % TB) == TB - 1)
+                        reduce_batch_to_smem<NP, NT, G, TB>(rb, red, warp, lane, g,
+                                                            t_grp + q - (TB - 1));
+                }
+                allreduce_nt<NT, 8>(yp);
+                allreduce_nt<NT, 8>(pp);
+                if (j == g) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        ys_own[q] = yp[q];
+                        ph_own[q] = pp[q];
+                    }
+                }
+            }
+
+            // this lane's tokens: dz and phi
+            constexpr int RAWB = CH * kT * (int)sizeof(TIN);
+            float uv[8], gy[8], zv[8];
+            load_raw8<TIN, CH>(st, c, tb, uv);
+            load_raw8<TIN, CH>(st + 3 * RAWB, c, tb, gy);
+            if (has_z) load_raw8<TIN, CH>(st + 2 * RAWB, c, tb, zv);
+            float dzv[8], phv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (has_z) {
+                    const float sz = rcp(1.0f + ex2(-kLog2e * zv[q]));
+                    const float pre = fmaf(Dd, uv[q], ys_own[q]);
+                    dzv[q] = gy[q] * pre * sz * fmaf(zv[q], 1.0f - sz, 1.0f);
+                } else {
+                    dzv[q] = 0.0f;
+                }
+                phv[q] = gq[q] * ph_own[q];
+            }
+            if (ch_ok) {
+                const int64_t off = row * L + k * kT + tb;
+                if (p.dz) store_out8<TOUT>(p.dz, off, dzv, nvalid - tb, vec_out);
+                store_out8<float>(p.phi, off, phv, nvalid - tb, vec_phi);
+            }
+        }
+        if (!dead && ch_ok && k + 1 < nchunks) {
+            // state at the end of this chunk: the reverse sweep re-anchors its
+            // suffix sum with it
+            float4* hc = reinterpret_cast<float4*>(p.hck + (row * nchunks + k) * NP + g * G);
+#pragma unroll
+            for (int j = 0; j < G / 4; ++j) {
+                float x0, x1, x2, x3;
+                upk(h[2 * j], x0, x1);
+                upk(h[2 * j + 1], x2, x3);
+                hc[j] = make_float4(x0, x1, x2, x3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
+        consumers_sync();
+        if (!dead) flush_red<NP>(red, p.dC, b, N, L, k * kT, nvalid, 1.0f, tid);
+        consumers_sync();
+    }
+
+    if (ch_ok && !dead) {
+#pragma unroll
+        for (int j = 0; j < G / 2; ++j) {
+            const int n0 = g * G + 2 * j;
+            float hl0, hl1, m0, m1, a0, a1;
+            upk(h[j], hl0, hl1);
+            upk(m[j], m0, m1);
+            upk(dAc[j], a0, a1);
+            p.hfin[row * NP + n0] = hl0;
+            p.hfin[row * NP + n0 + 1] = hl1;
+            const float g0 = (p.dhL && n0 < N) ? p.dhL[row * N + n0] : 0.0f;
+            const float g1 = (p.dhL && n0 + 1 < N) ? p.dhL[row * N + n0 + 1] : 0.0f;
+            if (n0 < N) atomicAdd(p.dA + d * N + n0, kLn2 * fmaf(g0, m0, a0));
+            if (n0 + 1 < N) atomicAdd(p.dA + d * N + n0 + 1, kLn2 * fmaf(g1, m1, a1));
+        }
+    }
+}
+
+// ===================================================== reverse sweep ===
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
+               const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_phi,
+               const __grid_constant__ CUtensorMap tm_bc) {
+    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
+    using CfgF = FwdCfg<NT, 4>;
+    constexpr int G = NP / NT;
+    constexpr int CH = Cfg::CH;
+    constexpr int SB = Cfg::SB;
+    constexpr int RAW = Cfg::RAW;
+    constexpr int STAGE = bwd_stage_bytes<NT, (int)sizeof(TIN), NP, true>();
+    constexpr int STAGES = bwd_stages<NT, (int)sizeof(TIN), NP, true>();
+    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    constexpr int TB = red_tokens<NP>();
+    static_assert(G % 4 == 0 && G <= 16, "states per thread");
+    static_assert(8 % TB == 0, "reduction batches within a token group");
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int64_t L = p.L;
+    const int64_t nchunks = (L + kT - 1) / kT;
+    const bool has_z = p.z != nullptr;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (tid >= kConsumers) {
+        bwd_producer<TIN, NT, NP, true, TMA_RAW, STAGES, STAGE>(
+            smem, full_bar, empty_bar, p, &tm_u, &tm_dr, &tm_z, &tm_dy, &tm_phi, &tm_bc, b, d0,
+            has_z, tid - kConsumers);
+        return;
+    }
+
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int c = tid / NT;
+    const int g = tid % NT;
+    const int64_t d = d0 + c;
+    const bool ch_ok = d < p.D;
+    const int64_t row = b * p.D + d;
+    const int N = p.N;
+
+    // lambda starts at dhL, the decay "after the last token" is 1, and
+    // psi = sum_n A dhL h_L starts the suffix sum
+    f2 Ap[G / 2], lam[G / 2], anext[G / 2];
+    float psi = 0.0f;
+#pragma unroll
+    for (int j = 0; j < G / 2; ++j) {
+        const int n0 = g * G + 2 * j, n1 = n0 + 1;
+        const float a0 = (ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f;
+        const float a1 = (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f;
+        Ap[j] = pk(a0, a1);
+        float l0 = 0.0f, l1 = 0.0f;
+        if (ch_ok && p.dhL) {
+            if (n0 < N) l0 = p.dhL[row * N + n0];
+            if (n1 < N) l1 = p.dhL[row * N + n1];
+        }
+        lam[j] = pk(l0, l1);
+        anext[j] = pk(1.0f, 1.0f);
+        if (ch_ok) psi += a0 * l0 * p.hfin[row * NP + n0] + a1 * l1 * p.hfin[row * NP + n1];
+    }
+#pragma unroll
+    for (int o = 1; o < NT; o <<= 1) psi += __shfl_xor_sync(0xffffffffu, psi, o);
+    float carry = psi;                 // psi + sum of (phi - rho) over the later tokens
+    const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
+    const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
+    const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
+    const int src_base = lane & ~(NT - 1);
+    float dD_acc = 0.0f, db_acc = 0.0f;
+    bool dead = false;   // see the forward sweep
+
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int64_t k = nchunks - 1 - i;
+        const int s = (int)(i % STAGES);
+        if (!dead) {
+            const bool ok = __all_sync(
+                0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns));
+            if (!ok) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        const uint8_t* st = smem + s * STAGE;
+        const uint8_t* phit = st + 4 * RAW;
+        const float* bct = reinterpret_cast<const float*>(st + 4 * RAW + CfgF::RAW);
+        const int nvalid = (int)min((int64_t)kT, L - k * kT);
+
+#pragma unroll 1
+        for (int sb = kT / SB - 1; sb >= 0; --sb) {
+            if (dead) break;
+            if (sb * SB >= nvalid) continue;
+            const int tb = sb * SB + g * 8;
+            float d2[8], du[8], gq[8];
+            token_prep<TIN, CH, ACCURATE>(st, c, tb, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+
+            float sb_own[8], sab_own[8];       // sum_n lambda B', sum_n A a_{t+1} lambda_{t+1} B'
+#pragma unroll 1
+            for (int j = NT - 1; j >= 0; --j) {
+                const int src = src_base + j;
+                float D2[8], DU[8], GQ[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    D2[q] = NT == 1 ? d2[q] : __shfl_sync(0xffffffffu, d2[q], src);
+                    DU[q] = NT == 1 ? du[q] : __shfl_sync(0xffffffffu, du[q], src);
+                    GQ[q] = NT == 1 ? gq[q] : __shfl_sync(0xffffffffu, gq[q], src);
+                }
+                const int t_grp = sb * SB + j * 8;
+                float bp[8], abp[8];
+                float rb[TB * G];
+#pragma unroll
+                for (int q = 7; q >= 0; --q) {
+                    const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
+                    const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
+                    f2 accb = pk(0.0f, 0.0f), accab = pk(0.0f, 0.0f);
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int jj = 2 * q4 + e;
+                            const f2 Bj = e ? Bq.y : Bq.x;
+                            const f2 Cj = e ? Cq.y : Cq.x;
+                            const f2 al = mul2(anext[jj], lam[jj]);   // a_{t+1} lambda_{t+1}
+                            lam[jj] = fma2(anext[jj], lam[jj], mul2(gqp, Cj));
+                            accb = add2(accb, mul2(lam[jj], Bj));
+                            accab = fma2(Ap[jj], mul2(al, Bj), accab);
+                            float lo, hi;
+                            upk(mul2(lam[jj], dup), lo, hi);         // dB partial / ln2
+                            rb[(q % TB) * G + 2 * jj] = lo;
+                            rb[(q % TB) * G + 2 * jj + 1] = hi;
+                            const f2 arg = mul2(d2p, Ap[jj]);
+                            anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
+                        }
+                    }
+                    float lo, hi;
+                    upk(accb, lo, hi);
+                    bp[q] = lo + hi;
+                    upk(accab, lo, hi);
+                    abp[q] = lo + hi;
+                    if ((q % TB) == 0)
+                        reduce_batch_to_smem<NP, NT, G, TB>(rb, red, warp, lane, g, t_grp + q);
+                }
+                allreduce_nt<NT, 8>(bp);
+                allreduce_nt<NT, 8>(abp);
+                if (j == g) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        sb_own[q] = bp[q];
+                        sab_own[q] = abp[q];
+                    }
+                }
+            }
+
+            // suffix sums of w = phi - rho over this lane's tokens, then over
+            // the later lanes of the channel, then the later super-blocks
+            constexpr int RAWB = CH * kT * (int)sizeof(TIN);
+            float phv[8], uv[8], dv[8];
+            load_raw8<float, CH>(phit, c, tb, phv);
+            load_raw8<TIN, CH>(st, c, tb, uv);
+            load_raw8<TIN, CH>(st + RAWB, c, tb, dv);
+            float suf[8];
+            float run = 0.0f;
+#pragma unroll
+            for (int q = 7; q >= 0; --q) {
+                run += phv[q] - du[q] * sab_own[q];
+                suf[q] = run;
+            }
+            float incl = run;
+#pragma unroll
+            for (int o = 1; o < NT; o <<= 1) {
+                const float v = __shfl_down_sync(0xffffffffu, incl, o, NT);
+                if (g + o < NT) incl += v;
+            }
+            const float excl = incl - run;
+            const float total = __shfl_sync(0xffffffffu, incl, src_base);
+            float duv[8], ddv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float dd = carry + excl + suf[q] + uv[q] * sb_own[q] * kLog2e;
+                const float sx = rcp(1.0f + ex2(-fmaf(dv[q], kLog2e, bias2)));  // d softplus / dx
+                ddv[q] = dd * sx;
+                duv[q] = fmaf(gq[q], Dd, d2[q] * sb_own[q]);
+                if (tb + q < nvalid) {
+                    dD_acc = fmaf(gq[q], uv[q], dD_acc);
+                    db_acc += ddv[q];
+                }
+            }
+            carry += total;
+            if (ch_ok) {
+                const int64_t off = row * L + k * kT + tb;
+                store_out8<TOUT>(p.du, off, duv, nvalid - tb, vec_out);
+                store_out8<TOUT>(p.ddr, off, ddv, nvalid - tb, vec_out);
+            }
+        }
+        if (k > 0) {
+            // Re-anchor: the suffix sum equals sum_n A a_t lambda_t h_{t-1} at
+            // this chunk's first token t, with h_{t-1} the state at the end of
+            // the previous chunk.  Rounding in the running sum is thereby
+            // confined to one chunk instead of random-walking over the sequence.
+            float part = 0.0f;
+            if (ch_ok && !dead) {
+                const float4* hc =
+                    reinterpret_cast<const float4*>(p.hck + (row * nchunks + k - 1) * NP + g * G);
+#pragma unroll
+                for (int j = 0; j < G / 4; ++j) {
+                    const float4 hv = hc[j];
+                    float l0, l1, l2, l3;
+                    upk(mul2(mul2(Ap[2 * j], anext[2 * j]), lam[2 * j]), l0, l1);
+                    upk(mul2(mul2(Ap[2 * j + 1], anext[2 * j + 1]), lam[2 * j + 1]), l2, l3);
+                    part = fmaf(l0, hv.x, part);
+                    part = fmaf(l1, hv.y, part);
+                    part = fmaf(l2, hv.z, part);
+                    part = fmaf(l3, hv.w, part);
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < NT; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            carry = part;
+        }
+        __syncwarp();
+        if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
+        consumers_sync();
+        if (!dead) flush_red<NP>(red, p.dB, b, N, L, k * kT, nvalid, kLn2, tid);
+        consumers_sync();
+    }
+
+#pragma unroll
+    for (int o = 1; o < NT; o <<= 1) {
+        dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
+        db_acc += __shfl_xor_sync(0xffffffffu, db_acc, o);
+    }
+    if (ch_ok && !dead) {
+        if (g == 0) {
+            if (p.dD) atomicAdd(p.dD + d, dD_acc);
+            if (p.dbias) atomicAdd(p.dbias + d, db_acc);
+        }
+        if (p.dh0) {
+#pragma unroll
+            for (int j = 0; j < G / 2; ++j) {
+                const int n0 = g * G + 2 * j;
+                float v0, v1;
+                upk(mul2(anext[j], lam[j]), v0, v1);
+                if (n0 < N) p.dh0[row * N + n0] = v0;
+                if (n0 + 1 < N) p.dh0[row * N + n0 + 1] = v1;
+            }
+        }
+    }
+}
+
+}  // namespace ssm

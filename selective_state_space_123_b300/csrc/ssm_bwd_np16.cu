@@ -1,0 +1,15 @@
+// ssm_bwd_np16.cu -- backward instantiations for padded state size 16.
+#include "ssm_bwd_launch.cuh"
+
+namespace ssm {
+
+cudaError_t launch_bwd_np16(int NT, int tin, int tout, bool tma, const BwdParams& p,
+                             const BwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (NT) {
+        case 2: return launch_bwd_nt<16, 2>(tin, tout, tma, p, m, grid, st);
+        case 4: return launch_bwd_nt<16, 4>(tin, tout, tma, p, m, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ssm

@@ -29,6 +29,23 @@ cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_ra
 cudaError_t launch_fwd_np64(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
 
+// Tensor maps of one backward call: raw tiles of u, delta_raw, z, dy, the
+// fp32 per-token tile written by the forward sweep, and the B/C tile.
+struct BwdMaps {
+    CUtensorMap u, dr, z, dy, phi, bc;
+};
+
+// Backward (forward sweep, then reverse sweep) for padded state size NP
+// (8, 16, 32, 64) and NT threads per channel.
+cudaError_t launch_bwd_np8(int NT, int tin, int tout, bool tma, const BwdParams& p,
+                           const BwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_np16(int NT, int tin, int tout, bool tma, const BwdParams& p,
+                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_np32(int NT, int tin, int tout, bool tma, const BwdParams& p,
+                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
+                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+
 // The NT values each NP supports (first entry = default).
 int fwd_supported_nt(int NP, int* out, int cap);
 

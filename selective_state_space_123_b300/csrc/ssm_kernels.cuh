@@ -41,6 +41,36 @@ struct FwdParams {
     uint64_t timeout_ns;
 };
 
+// Backward parameters (both sweeps).
+struct BwdParams {
+    int64_t Bt, D, L;
+    int N;
+    const void* u;
+    const void* dr;
+    const void* z;          // nullable
+    const void* dy;
+    const float* A;
+    const float* Dv;        // nullable
+    const float* bias;      // nullable
+    const float* h0;        // nullable
+    const float* dhL;       // nullable
+    const float* bc;        // prepared B/C (see FwdParams)
+    float* phi;             // (Bt*D, L) fp32 workspace, written by the forward sweep
+    float* hfin;            // (Bt*D, NP) fp32 workspace: final state
+    float* hck;             // (Bt*D, nchunks, NP) fp32 workspace: state at the end of each chunk
+    void* du;
+    void* ddr;
+    void* dz;               // nullable
+    float* dA;              // accumulated with atomics (zeroed by the host)
+    float* dB;              // accumulated with atomics (zeroed by the host)
+    float* dC;              // accumulated with atomics (zeroed by the host)
+    float* dD;              // nullable, accumulated (zeroed by the host)
+    float* dbias;           // nullable, accumulated (zeroed by the host)
+    float* dh0;             // nullable
+    int* status;
+    uint64_t timeout_ns;
+};
+
 struct StepParams {
     int64_t Bt, D;
     int N;

@@ -49,3 +49,10 @@ def rows_to_host(t, b_idx, d_idx):
     """Gather rows [b, d, :] of a device tensor to a float32 numpy array (Bsel, Dsel, ...)."""
     sub = t[b_idx][:, d_idx]
     return sub.float().cpu().numpy()
+
+
+def oracle_bwd_chunk(args):
+    """Worker for chunked oracle runs (spawned process): the reverse mode on a
+    subset of channels.  Returns the oracle's outputs for those channels."""
+    (u, dr, A, Bm, Cm, dy, Dv, z, bias) = args
+    return oracle.scan_bwd(u, dr, A, Bm, Cm, dy, Dv, z, bias, None, None)

@@ -111,3 +111,41 @@ def test_binding_refuses_cpu_tensors(pkg):
     u = torch.zeros(1, 2, 8)
     with pytest.raises(ValueError):
         pkg.ssm_scan_fwd(u, u, torch.zeros(2, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+
+
+def _call_bwd(pkg, shape, ptrs=None, ws_bytes=1 << 30, ws=0x10000):
+    p = dict(u=0x1000, dr=0x2000, A=0x3000, B=0x4000, C=0x5000, D=None, z=None, bias=None,
+             h0=None, dy=0x6000, dhL=None, du=0x7000, ddr=0x8000, dA=0x9000, dB=0xa000,
+             dC=0xb000, dD=None, dz=None, dbias=None, dh0=None)
+    if ptrs:
+        p.update(ptrs)
+    V = lambda x: None if x is None else ctypes.c_void_p(x)
+    order = ("u", "dr", "A", "B", "C", "D", "z", "bias", "h0", "dy", "dhL", "du", "ddr", "dA",
+             "dB", "dC", "dD", "dz", "dbias", "dh0")
+    return pkg.lib.ssm_scan_bwd(ctypes.byref(shape) if shape is not None else None,
+                                *[V(p[k]) for k in order], V(ws), ws_bytes, None)
+
+
+def test_bwd_argument_errors(pkg):
+    S = lambda **k: pkg.make_shape(k.get("b", 2), k.get("d", 8), k.get("n", 16), k.get("l", 64),
+                                   k.get("ti", 1), k.get("to", 0))
+    assert _call_bwd(pkg, None) == pkg.SSM_ERR_NULL
+    assert _call_bwd(pkg, S(n=0)) == pkg.SSM_ERR_SHAPE
+    assert _call_bwd(pkg, S(n=65)) == pkg.SSM_ERR_SHAPE
+    assert _call_bwd(pkg, S(ti=2)) == pkg.SSM_ERR_DTYPE
+    for name in ("u", "dr", "A", "B", "C", "dy", "du", "ddr", "dA", "dB", "dC"):
+        assert _call_bwd(pkg, S(), {name: None}) == pkg.SSM_ERR_NULL, name
+    for name in ("u", "dy", "dB", "dz", "dh0", "dhL"):
+        assert _call_bwd(pkg, S(), {name: 0x20004}) == pkg.SSM_ERR_ALIGN, name
+    assert _call_bwd(pkg, S(), ws=None) == pkg.SSM_ERR_WORKSPACE
+    assert _call_bwd(pkg, S(), ws_bytes=1024) == pkg.SSM_ERR_WORKSPACE
+
+
+def test_bwd_workspace_query(pkg):
+    s = pkg.make_shape(2, 5120, 16, 8192, 1, 1)
+    n = pkg.ssm_scan_workspace_bytes(s, True)
+    # header + prepared B/C + one fp32 number per (batch, channel, token) + final state
+    assert n >= 256 + 2 * 8192 * 32 * 4 + 2 * 5120 * 8192 * 4 + 2 * 5120 * 16 * 4
+    # small state sizes are padded to 8 in the backward
+    assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 4, 4, 64, 0, 0), True) >= \
+        256 + 64 * 16 * 4 + 4 * 64 * 4
