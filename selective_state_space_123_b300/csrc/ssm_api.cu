@@ -2,6 +2,7 @@
 // argument validation, planning of the forward launch, TMA descriptors,
 // workspace layout, status word.
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <cuda.h>
@@ -40,6 +41,13 @@ int padded_state(int64_t N) {
     return 64;
 }
 
+// A CUDA call failed: clear the (non-sticky) error state so the caller's next
+// CUDA call does not see it, and report SSM_ERR_CUDA.
+int cuda_fail() {
+    cudaGetLastError();
+    return SSM_ERR_CUDA;
+}
+
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -76,39 +84,113 @@ int shape_check(const ssm_shape* s) {
 }
 
 struct FwdPlan {
-    int NP = 16, NT = 2, CH = 64;
+    int NP = 16, NT = 2, W = 4, CH = 64, stages = 2;
+    size_t smem = 0;
     int nseg = 1;
     int64_t nchunks = 0, seg_chunks = 0;
     bool tma_raw = false;
     size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, bytes = 0;
 };
 
+// Per-NT constants of the forward kernel, on the host.
+int fwd_xy_bytes(int NT) {
+    return 4 * (NT == 4 ? FwdLayout<4>::XY_FLOATS : NT == 2 ? FwdLayout<2>::XY_FLOATS
+                                                           : FwdLayout<1>::XY_FLOATS);
+}
+int fwd_max_warps(int NT) { return NT == 4 ? FwdLayout<4>::kMaxWarps : FwdLayout<2>::kMaxWarps; }
+int fwd_min_blocks(int NT) { return NT == 4 ? FwdLayout<4>::kMinBlocks : FwdLayout<2>::kMinBlocks; }
+// registers per thread the launch bounds allow (65536 / (threads * min blocks))
+int fwd_reg_cap(int NT) {
+    const int threads = 32 * (fwd_max_warps(NT) + 1);
+    int r = 65536 / (threads * fwd_min_blocks(NT));
+    r = r > 255 ? 255 : r;
+    return r & ~7;
+}
+
+// Relative cost of one state update per NT (instructions per update of the
+// kernel body: more lanes per channel means more per-token exchange).
+double fwd_nt_cost(int NT) { return NT == 4 ? 1.15 : NT == 1 ? 1.05 : 1.0; }
+
+// Time model of one launch: `ctas` CTAs of W compute warps, each doing `work`
+// units; an SM runs up to `cps` CTAs at once and reaches full throughput
+// with about 6 compute warps.
+double fwd_launch_cost(int64_t ctas, int sms, int cps, int W, double work) {
+    if (ctas <= 0) return 0.0;
+    const int64_t k = (ctas + sms - 1) / sms;          // CTAs on the busiest SM
+    const int64_t res = k < cps ? k : cps;            // resident together
+    const int64_t waves = (k + res - 1) / res;
+    double sat = (double)(res * W) / 6.0;
+    if (sat > 1.0) sat = 1.0;
+    return (double)waves * (double)res * work / sat;
+}
+
 FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
     FwdPlan pl;
     pl.NP = padded_state(s.dstate);
+    const int eb = dtype_bytes(s.in_dtype);
+    pl.nchunks = (s.seqlen + kT - 1) / kT;
+    pl.tma_raw = (s.seqlen * eb) % 16 == 0;
     int nts[4];
     const int cnt = fwd_supported_nt(pl.NP, nts, 4);
-    pl.NT = nts[0];
-    const int want = env_int("SSM_FWD_NT", 0);
-    for (int i = 0; i < cnt; ++i)
-        if (nts[i] == want) pl.NT = want;
-    pl.CH = kConsumers / pl.NT;
-    pl.nchunks = (s.seqlen + kT - 1) / kT;
-    pl.tma_raw = (s.seqlen * dtype_bytes(s.in_dtype)) % 16 == 0;
-    // Too few channel tiles to fill the GPU: cut the sequence into segments
-    // (two passes and a carry; about 1.6x the arithmetic, many more CTAs).
-    const int64_t ctas = s.batch * ((s.dim + pl.CH - 1) / pl.CH);
-    int64_t nseg = 1;
-    if (ctas > 0 && ctas * 2 < sm_count && pl.nchunks >= 16)
-        nseg = (6 * (int64_t)sm_count + ctas - 1) / ctas;
-    const int forced = env_int("SSM_FWD_NSEG", 0);
-    if (forced > 0) nseg = forced;
-    if (nseg > pl.nchunks / 4) nseg = pl.nchunks / 4;
-    if (nseg < 1) nseg = 1;
-    pl.seg_chunks = (pl.nchunks + nseg - 1) / nseg;
-    if (pl.seg_chunks < 1) pl.seg_chunks = 1;
-    pl.nseg = (int)((pl.nchunks + pl.seg_chunks - 1) / pl.seg_chunks);
-    if (pl.nseg < 1) pl.nseg = 1;
+    const int want_nt = env_int("SSM_FWD_NT", 0);
+    const int want_w = env_int("SSM_FWD_W", 0);
+    const int want_seg = env_int("SSM_FWD_NSEG", 0);
+    double best = -1.0;
+    for (int ci = 0; ci < cnt; ++ci) {
+        const int NT = nts[ci];
+        if (want_nt > 0 && NT != want_nt) continue;
+        for (int W = 1; W <= fwd_max_warps(NT); ++W) {
+            if (want_w > 0 && W != want_w) continue;
+            const int CH = W * 32 / NT;
+            const int64_t tiles = (s.dim + CH - 1) / CH;
+            const size_t stage = (size_t)3 * CH * kT * eb + (size_t)kT * 2 * pl.NP * 4;
+            const size_t xy = (size_t)W * fwd_xy_bytes(NT);
+            // CTAs per SM: threads, registers, then shared memory with >= 2 stages
+            int cps = 2048 / (32 * (W + 1));
+            const int by_regs = 65536 / (fwd_reg_cap(NT) * 32 * (W + 1));
+            if (by_regs < cps) cps = by_regs;
+            while (cps > 1 && 2 * stage + xy + 2048 > (size_t)(228 * 1024) / cps) --cps;
+            if (cps < 1 || 2 * stage + xy + 2048 > (size_t)kMaxSmemPerCta) continue;
+            size_t avail = (size_t)(228 * 1024) / cps - 2048;
+            if (avail > (size_t)kMaxSmemPerCta - 1024) avail = (size_t)kMaxSmemPerCta - 1024;
+            int stages = (int)((avail - xy) / stage);
+            if (stages > 4) stages = 4;
+            if (stages < 2) stages = 2;
+            // segments of the sequence (two passes and a carry) when there
+            // are too few channel tiles to fill the GPU
+            int seg_lo = 1, seg_hi = 1;
+            if (want_seg > 0) seg_lo = seg_hi = want_seg;
+            else if (pl.nchunks >= 16 && s.batch * tiles * 2 <= (int64_t)sm_count * cps)
+                seg_hi = 64;
+            const int64_t nch = pl.nchunks > 0 ? pl.nchunks : 1;   // L = 0: no chunk at all
+            for (int nseg0 = seg_lo; nseg0 <= seg_hi; ++nseg0) {
+                int64_t nseg = nseg0;
+                if (nseg > nch / 4 && want_seg <= 0) nseg = nch / 4;
+                if (nseg > nch) nseg = nch;
+                if (nseg < 1) nseg = 1;
+                const int64_t seg_chunks = (nch + nseg - 1) / nseg;
+                nseg = (nch + seg_chunks - 1) / seg_chunks;
+                const double work = (double)CH * (double)seg_chunks * fwd_nt_cost(NT);
+                const int64_t ctas = s.batch * tiles;
+                double cost = fwd_launch_cost(ctas * nseg, sm_count, cps, W, work);
+                if (nseg > 1) cost += 0.6 * fwd_launch_cost(ctas * (nseg - 1), sm_count, cps, W, work);
+                if (best < 0.0 || cost < best * 0.999) {
+                    best = cost;
+                    pl.NT = NT; pl.W = W; pl.CH = CH; pl.stages = stages;
+                    pl.smem = (size_t)stages * stage + xy + 1024;
+                    pl.seg_chunks = seg_chunks > 0 ? seg_chunks : 1;
+                    pl.nseg = (int)nseg;
+                }
+            }
+        }
+    }
+    if (best < 0.0) {   // nothing fitted the overrides: the smallest configuration
+        pl.NT = nts[0]; pl.W = 1; pl.CH = 32 / pl.NT; pl.stages = 2;
+        pl.smem = 2 * ((size_t)3 * pl.CH * kT * eb + (size_t)kT * 2 * pl.NP * 4) +
+                  fwd_xy_bytes(pl.NT) + 1024;
+        pl.seg_chunks = pl.nchunks > 0 ? pl.nchunks : 1;
+        pl.nseg = 1;
+    }
 
     size_t off = kHeaderBytes;
     pl.off_bc = off;
@@ -123,6 +205,9 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
         off += align256(st * 4);
     }
     pl.bytes = off;
+    if (env_int("SSM_DEBUG_PLAN", 0))
+        std::fprintf(stderr, "ssm fwd plan: NP=%d NT=%d W=%d CH=%d stages=%d smem=%zu nseg=%d seg_chunks=%lld\n",
+                     pl.NP, pl.NT, pl.W, pl.CH, pl.stages, pl.smem, pl.nseg, (long long)pl.seg_chunks);
     return pl;
 }
 
@@ -187,14 +272,14 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
     return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_fwd(int NP, int NT, int tin, int tout, bool summary, bool tma,
-                       const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
-    switch (NP) {
-        case 4: return launch_fwd_np4(NT, tin, tout, summary, tma, p, m, grid, st);
-        case 8: return launch_fwd_np8(NT, tin, tout, summary, tma, p, m, grid, st);
-        case 16: return launch_fwd_np16(NT, tin, tout, summary, tma, p, m, grid, st);
-        case 32: return launch_fwd_np32(NT, tin, tout, summary, tma, p, m, grid, st);
-        default: return launch_fwd_np64(NT, tin, tout, summary, tma, p, m, grid, st);
+cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, const FwdParams& p,
+                       const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    switch (pl.NP) {
+        case 4: return launch_fwd_np4(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
+        case 8: return launch_fwd_np8(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
+        case 16: return launch_fwd_np16(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
+        case 32: return launch_fwd_np32(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
+        default: return launch_fwd_np64(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
     }
 }
 
@@ -212,7 +297,7 @@ cudaError_t launch_bwd(int NP, int NT, int tin, int tout, bool tma, const BwdPar
 
 namespace ssm {
 int fwd_supported_nt(int NP, int* out, int cap) {
-    static const int t4[] = {1}, t8[] = {2, 1}, t16[] = {2, 1, 4}, t32[] = {4, 2}, t64[] = {4};
+    static const int t4[] = {1}, t8[] = {2, 1}, t16[] = {2, 4, 1}, t32[] = {4, 2}, t64[] = {4};
     const int* t = t16;
     int n = 3;
     switch (NP) {
@@ -274,19 +359,19 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     int* status = reinterpret_cast<int*>(ws);
 
     if (L == 0) {
-        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
         if (hL) {
             const size_t bytes = (size_t)(Bt * Dm * N) * sizeof(float);
             cudaError_t e = h0 ? cudaMemcpyAsync(hL, h0, bytes, cudaMemcpyDeviceToDevice, st)
                                : cudaMemsetAsync(hL, 0, bytes, st);
-            if (e != cudaSuccess) return SSM_ERR_CUDA;
+            if (e != cudaSuccess) return cuda_fail();
         }
         return SSM_OK;
     }
 
     float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
     if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
 
     const int eb = dtype_bytes(s.in_dtype);
     const CUtensorMapDataType tdt =
@@ -295,13 +380,13 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     std::memset(&maps, 0, sizeof(maps));
     if (!make_map(&maps.bc, bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT,
                   false))
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     if (pl.tma_raw) {
         const uint32_t box_t = 128 / eb;
         if (!make_map(&maps.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
             !make_map(&maps.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
             (z && !make_map(&maps.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)))
-            return SSM_ERR_CUDA;
+            return cuda_fail();
     }
 
     FwdParams p;
@@ -311,6 +396,7 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     p.bc = bc; p.y = y; p.hL = hL;
     p.seg_chunks = pl.seg_chunks;
     p.nseg = pl.nseg;
+    p.stages = pl.stages;
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
@@ -322,16 +408,16 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
         // pass 1: summaries of every segment but the last
         FwdParams p1 = p;
         p1.hin = nullptr;
-        if (launch_fwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, true, pl.tma_raw, p1, maps,
+        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, p1, maps,
                        dim3(gx, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess)
-            return SSM_ERR_CUDA;
+            return cuda_fail();
         if (launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, p.hloc, p.sumd, p.hin, st) !=
             cudaSuccess)
-            return SSM_ERR_CUDA;
+            return cuda_fail();
     }
-    if (launch_fwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, false, pl.tma_raw, p, maps,
+    if (launch_fwd(pl, s.in_dtype, s.out_dtype, false, p, maps,
                    dim3(gx, (unsigned)Bt, (unsigned)pl.nseg), st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     return SSM_OK;
 }
 
@@ -353,14 +439,14 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
         const void* ptrs0[] = {A, dA, dD, ddelta_bias};
         for (const void* q : ptrs0)
             if (q && !aligned16(q)) return SSM_ERR_ALIGN;
-        if (dA && cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st0) != cudaSuccess) return SSM_ERR_CUDA;
-        if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st0) != cudaSuccess) return SSM_ERR_CUDA;
+        if (dA && cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st0) != cudaSuccess) return cuda_fail();
+        if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st0) != cudaSuccess) return cuda_fail();
         if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dm * 4, st0) != cudaSuccess)
-            return SSM_ERR_CUDA;
+            return cuda_fail();
         if (Bt > 0 && L > 0 && dB && dC) {
             if (cudaMemsetAsync(dB, 0, (size_t)(Bt * N * L) * 4, st0) != cudaSuccess ||
                 cudaMemsetAsync(dC, 0, (size_t)(Bt * N * L) * 4, st0) != cudaSuccess)
-                return SSM_ERR_CUDA;
+                return cuda_fail();
         }
         return SSM_OK;
     }
@@ -378,28 +464,28 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     int* status = reinterpret_cast<int*>(ws);
 
     // outputs summed with atomics start at zero
-    if (cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
-    if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st) != cudaSuccess) return cuda_fail();
+    if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st) != cudaSuccess) return cuda_fail();
     if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dm * 4, st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     if (L == 0) {
         // an empty sequence passes dhL straight through to dh0
-        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
         if (dh0) {
             const size_t bytes = (size_t)(Bt * Dm * N) * 4;
             cudaError_t e = dhL ? cudaMemcpyAsync(dh0, dhL, bytes, cudaMemcpyDeviceToDevice, st)
                                 : cudaMemsetAsync(dh0, 0, bytes, st);
-            if (e != cudaSuccess) return SSM_ERR_CUDA;
+            if (e != cudaSuccess) return cuda_fail();
         }
         return SSM_OK;
     }
     if (cudaMemsetAsync(dB, 0, (size_t)(Bt * N * L) * 4, st) != cudaSuccess ||
         cudaMemsetAsync(dC, 0, (size_t)(Bt * N * L) * 4, st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
 
     float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
     if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
 
     const int eb = dtype_bytes(s.in_dtype);
     const CUtensorMapDataType tdt =
@@ -409,7 +495,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     std::memset(&maps, 0, sizeof(maps));
     if (!make_map(&maps.bc, bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT,
                   false))
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     if (pl.tma_raw) {
         const uint32_t box_t = 128 / eb;
         if (!make_map(&maps.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
@@ -418,7 +504,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
             !make_map(&maps.dy, dy, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
             !make_map(&maps.phi, phi, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, Bt * Dm, 32, pl.CH,
                       true))
-            return SSM_ERR_CUDA;
+            return cuda_fail();
     }
 
     BwdParams p;
@@ -435,7 +521,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
     if (launch_bwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, pl.tma_raw, p, maps, dim3(gx, (unsigned)Bt),
                    st) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     return SSM_OK;
 }
 
@@ -457,7 +543,7 @@ int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, 
     p.u = u; p.dr = delta_raw; p.z = z; p.A = A; p.Dv = D; p.bias = delta_bias;
     p.B = B; p.C = C; p.state = state; p.y = y;
     if (launch_step(in_dtype, out_dtype, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SSM_ERR_CUDA;
+        return cuda_fail();
     return SSM_OK;
 }
 
@@ -466,11 +552,11 @@ int ssm_get_status(void* workspace, ssm_stream_t stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int v = 0;
     if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return SSM_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+        return cuda_fail();
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_fail();
     if (v != SSM_OK) {
-        if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
-        if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+        if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_fail();
     }
     return v;
 }
@@ -483,8 +569,8 @@ int ssm_debug_expired_wait(void* workspace, size_t ws_bytes, int64_t spin_limit,
     if (spin_limit < 1) return SSM_ERR_SHAPE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int* status = static_cast<int*>(workspace);
-    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SSM_ERR_CUDA;
-    if (launch_expired_wait(status, spin_limit, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+    if (launch_expired_wait(status, spin_limit, st) != cudaSuccess) return cuda_fail();
     return SSM_OK;
 }
 

@@ -299,8 +299,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     static_assert(8 % TB == 0, "reduction batches within a token group");
 
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -526,8 +525,7 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     static_assert(8 % TB == 0, "reduction batches within a token group");
 
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];

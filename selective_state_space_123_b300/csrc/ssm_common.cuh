@@ -185,6 +185,14 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// First 1024-byte aligned address of the dynamic shared-memory window (the
+// 128-byte TMA swizzle repeats every 1024 bytes).  The offset is added to the
+// __shared__ array itself so that the compiler keeps shared-memory
+// addressing for every access derived from the result.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* smem_dyn) {
+    return smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+}
+
 // Byte offset of element (row r, column byte cb) inside a tile whose rows are
 // 128 bytes long and were written by TMA with the 128-byte swizzle: the
 // 16-byte chunk index is XORed with the row index modulo 8 (tile base

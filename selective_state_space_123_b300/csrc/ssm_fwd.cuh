@@ -41,26 +41,6 @@ struct FwdCfg {
 template <int NP>
 constexpr int bc_tile_bytes() { return kT * 2 * NP * 4; }
 
-template <int NT, int EB, int NP, bool SUMMARY>
-constexpr int fwd_stage_bytes() {
-    return (SUMMARY ? 2 : 3) * FwdCfg<NT, EB>::RAW + bc_tile_bytes<NP>();
-}
-
-template <int NT, int EB, int NP, bool SUMMARY>
-constexpr int fwd_stages() {
-    // as many stages as fit in ~100 KB (two CTAs per SM), at least 2
-    return (100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>()) < 2
-               ? 2
-               : ((100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>()) > 4
-                      ? 4
-                      : 100 * 1024 / fwd_stage_bytes<NT, EB, NP, SUMMARY>());
-}
-
-template <int NT, int EB, int NP, bool SUMMARY>
-constexpr int fwd_smem_bytes() {
-    return fwd_stages<NT, EB, NP, SUMMARY>() * fwd_stage_bytes<NT, EB, NP, SUMMARY>() + 1024;
-}
-
 // softplus in log2 units: for x = (delta_raw + bias) * log2(e) return
 // log2(1 + 2^x) = delta / ln 2.
 //  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), where for 2^-|x| <
@@ -85,21 +65,28 @@ __device__ __forceinline__ float softplus2(float x) {
     }
 }
 
-// 8 consecutive tokens [tb, tb+8) of local channel c from a raw tile.
-template <typename TIN, int CH>
-__device__ __forceinline__ void load_raw8(const uint8_t* tile, int c, int tb, float (&v)[8]) {
+// 8 consecutive tokens [tb, tb+8) of local channel c from a raw tile of
+// `ch` channel rows (TMA 128-byte swizzle; fp32 tiles are two boxes of 32
+// tokens, each ch x 128 bytes).
+template <typename TIN>
+__device__ __forceinline__ void load_raw8r(const uint8_t* tile, int ch, int c, int tb,
+                                           float (&v)[8]) {
     if constexpr (sizeof(TIN) == 2) {
         const uint4 w = *reinterpret_cast<const uint4*>(tile + swz128(c, tb * 2));
         v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
         v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
     } else {
-        const uint8_t* box = tile + (tb / 32) * (CH * 128);
+        const uint8_t* box = tile + (tb / 32) * (ch * 128);
         const int cb = (tb % 32) * 4;
         const float4 a = *reinterpret_cast<const float4*>(box + swz128(c, cb));
         const float4 b = *reinterpret_cast<const float4*>(box + swz128(c, cb + 16));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
+}
+template <typename TIN, int CH>
+__device__ __forceinline__ void load_raw8(const uint8_t* tile, int c, int tb, float (&v)[8]) {
+    load_raw8r<TIN>(tile, CH, c, tb, v);
 }
 
 // Store 8 consecutive outputs of one row; `nv` of them are inside the row.
@@ -132,14 +119,15 @@ __device__ __forceinline__ void store_out8(void* y, int64_t off, const float (&v
     }
 }
 
-// Plain (non-TMA) fill of one raw tile, used when rows are not 16-byte
-// aligned (seqlen * element size not a multiple of 16).  Same swizzled layout.
-template <typename TIN, int CH>
-__device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, int64_t row0,
-                                              int64_t rows_valid, int64_t L, int64_t t0,
-                                              int lane) {
+// Plain (non-TMA) fill of one raw tile of `ch` rows, used when rows are not
+// 16-byte aligned (seqlen * element size not a multiple of 16).  Same
+// swizzled layout as the TMA tiles.
+template <typename TIN>
+__device__ __forceinline__ void fill_raw_tile_r(uint8_t* tile, int ch, const void* src,
+                                                int64_t row0, int64_t rows_valid, int64_t L,
+                                                int64_t t0, int lane) {
     const TIN* s = reinterpret_cast<const TIN*>(src);
-    for (int idx = lane; idx < CH * kT; idx += 32) {
+    for (int idx = lane; idx < ch * kT; idx += 32) {
         const int c = idx / kT, t = idx % kT;
         TIN v = TIN(0.0f);
         if (c < rows_valid && t0 + t < L) v = s[(row0 + c) * L + t0 + t];
@@ -147,37 +135,58 @@ __device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, in
         if constexpr (sizeof(TIN) == 2) {
             dst = tile + swz128(c, t * 2);
         } else {
-            dst = tile + (t / 32) * (CH * 128) + swz128(c, (t % 32) * 4);
+            dst = tile + (t / 32) * (ch * 128) + swz128(c, (t % 32) * 4);
         }
         *reinterpret_cast<TIN*>(dst) = v;
     }
 }
+template <typename TIN, int CH>
+__device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, int64_t row0,
+                                              int64_t rows_valid, int64_t L, int64_t t0,
+                                              int lane) {
+    fill_raw_tile_r<TIN>(tile, CH, src, row0, rows_valid, L, t0, lane);
+}
 
+// Forward kernel.  blockDim.x = 32 * (W + 1): W compute warps and one
+// producer warp (the last).  A CTA owns CH = W * 32 / NT channels of one
+// batch row for one segment of the sequence.  Per super-block of SB = 8 * NT
+// tokens each lane first prepares its own 8 tokens (softplus, delta * u) into
+// the warp's exchange buffer, then all lanes run the recurrence over the SB
+// tokens for their G = NP / NT states, then the per-token partial read-outs
+// go back through the same buffer and each lane finishes its own 8 tokens
+// (sum over the NT lanes, D skip, SiLU gate, store).  All exchange stays
+// inside the warp.
 template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
            const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
            const __grid_constant__ CUtensorMap tm_bc) {
-    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
+    using Lay = FwdLayout<NT>;
     constexpr int G = NP / NT;
-    constexpr int CH = Cfg::CH;
-    constexpr int SB = Cfg::SB;
-    constexpr int RAW = Cfg::RAW;
+    constexpr int CW = Lay::CW;
+    constexpr int SB = Lay::SB;
+    constexpr int EB = (int)sizeof(TIN);
     constexpr int NRAW = SUMMARY ? 2 : 3;
     constexpr int BCB = bc_tile_bytes<NP>();
-    constexpr int STAGE = fwd_stage_bytes<NT, (int)sizeof(TIN), NP, SUMMARY>();
-    constexpr int STAGES = fwd_stages<NT, (int)sizeof(TIN), NP, SUMMARY>();
-    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    constexpr bool ACCURATE = EB == 4;
     static_assert(G == 4 || G == 8 || G == 16, "states per thread");
     static_assert(NT == 1 || NT == 2 || NT == 4, "threads per channel");
 
+    const int W = (int)(blockDim.x / 32) - 1;
+    const int CH = W * CW;
+    const int RAW = CH * kT * EB;
+    const int STAGE = NRAW * RAW + BCB;
+    const int STAGES = p.stages;
+
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    uint8_t* smem = align_smem_1024(smem_dyn);
+    float* xy_all = reinterpret_cast<float*>(smem + STAGES * STAGE);
+    __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CH;
     const int seg = blockIdx.z;
@@ -190,15 +199,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], kConsumers / 32);
+            mbar_init(&empty_bar[s], W);
         }
         fence_mbar_init();
     }
     __syncthreads();
 
     // ------------------------------------------------------ producer warp
-    if (tid >= kConsumers) {
-        const int lane = tid - kConsumers;
+    if (warp == W) {
         if (lane == 0) {
             prefetch_tmap(&tm_bc);
             if (TMA_RAW) {
@@ -207,6 +215,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 if (has_z) prefetch_tmap(&tm_z);
             }
         }
+        constexpr int BOXES = kT * EB / 128;   // 128-byte TMA boxes per tile row
+        constexpr int BOX_T = 128 / EB;        // tokens per box
         const int64_t row0 = b * p.D + d0;
         const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
         for (int64_t k = k_begin; k < k_end; ++k) {
@@ -214,7 +224,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int s = (int)(i % STAGES);
             if (i >= STAGES) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(&empty_bar[s], (uint32_t)(((i / STAGES) - 1) & 1), p.timeout_ns);
+                if (lane == 0)
+                    ok = mbar_wait(&empty_bar[s], (uint32_t)(((i / STAGES) - 1) & 1), p.timeout_ns);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) {
                     if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
@@ -225,11 +236,10 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int32_t t0 = (int32_t)(k * kT);
             if (TMA_RAW) {
                 if (lane == 0) {
-                    const uint32_t bytes = (has_z ? 3 : 2) * RAW + BCB;
-                    mbar_arrive_expect_tx(&full_bar[s], bytes);
+                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)((has_z ? 3 : 2) * RAW + BCB));
 #pragma unroll
-                    for (int bx = 0; bx < Cfg::BOXES; ++bx) {
-                        const int32_t x = t0 + bx * Cfg::BOX_T;
+                    for (int bx = 0; bx < BOXES; ++bx) {
+                        const int32_t x = t0 + bx * BOX_T;
                         tma_load_2d(st + bx * CH * 128, &tm_u, &full_bar[s], x, (int32_t)row0);
                         tma_load_2d(st + RAW + bx * CH * 128, &tm_dr, &full_bar[s], x, (int32_t)row0);
                         if (has_z)
@@ -239,9 +249,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     tma_load_2d(st + NRAW * RAW, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
                 }
             } else {
-                fill_raw_tile<TIN, CH>(st, p.u, row0, rows_valid, L, t0, lane);
-                fill_raw_tile<TIN, CH>(st + RAW, p.dr, row0, rows_valid, L, t0, lane);
-                if (has_z) fill_raw_tile<TIN, CH>(st + 2 * RAW, p.z, row0, rows_valid, L, t0, lane);
+                fill_raw_tile_r<TIN>(st, CH, p.u, row0, rows_valid, L, t0, lane);
+                fill_raw_tile_r<TIN>(st + RAW, CH, p.dr, row0, rows_valid, L, t0, lane);
+                if (has_z) fill_raw_tile_r<TIN>(st + 2 * RAW, CH, p.z, row0, rows_valid, L, t0, lane);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full_bar[s], BCB);
@@ -252,14 +262,15 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
         return;
     }
 
-    // ---------------------------------------------------- compute threads
-    const int lane = tid & 31;
-    const int c = tid / NT;
-    const int g = tid % NT;
+    // ---------------------------------------------------- compute warps
+    const int cw = lane / NT;          // channel within the warp
+    const int g = lane % NT;           // state group
+    const int c = warp * CW + cw;      // channel within the CTA
     const int64_t d = d0 + c;
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
+    float* xy = xy_all + warp * Lay::XY_FLOATS;   // this warp's exchange buffer
 
     f2 Ap[G / 2], h[G / 2];
 #pragma unroll
@@ -285,14 +296,17 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
     const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
     double sum_d2 = 0.0;
-    const int src_base = lane & ~(NT - 1);
+    bool dead = false;   // a bounded wait expired: stop working (warp-uniform)
 
-    for (int64_t k = k_begin; k < k_end; ++k) {
+    for (int64_t k = k_begin; k < k_end && !dead; ++k) {
         const int64_t i = k - k_begin;
         const int s = (int)(i % STAGES);
-        if (!mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns)) {
-            set_status(p.status, SSM_ERR_TIMEOUT);
-            return;
+        const bool ok = __all_sync(
+            0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns));
+        if (!ok) {
+            if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+            dead = true;
+            break;
         }
         const uint8_t* st = smem + s * STAGE;
         const float* bct = reinterpret_cast<const float*>(st + NRAW * RAW);
@@ -301,50 +315,36 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll 1
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (sb * SB >= nvalid) break;
-            const int tb = sb * SB + g * 8;  // this thread's 8 tokens within the chunk
+            const int tb = sb * SB + g * 8;   // this lane's own 8 tokens
 
-            // per-token work for this thread's 8 tokens
-            float uv[8], dv[8], zv[8];
-            load_raw8<TIN, CH>(st, c, tb, uv);
-            load_raw8<TIN, CH>(st + RAW, c, tb, dv);
-            if (has_z) load_raw8<TIN, CH>(st + 2 * RAW, c, tb, zv);
-            float d2[8], du[8];
+            // 1. prepare the own tokens: (delta2, delta2, delta2*u, delta2*u)
+            float uv[8];
+            {
+                float dv[8];
+                load_raw8r<TIN>(st, CH, c, tb, uv);
+                load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
+                float s8 = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                d2[q] = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
-                du[q] = d2[q] * uv[q];
-            }
-            if (nvalid < kT) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (tb + q >= nvalid) { d2[q] = 0.0f; du[q] = 0.0f; }
-            }
-            if (SUMMARY) {
-                float s8 = ((d2[0] + d2[1]) + (d2[2] + d2[3])) + ((d2[4] + d2[5]) + (d2[6] + d2[7]));
-                sum_d2 += (double)s8;
-            }
-
-            // every thread of the channel needs delta2 and delta2*u of all SB tokens
-            float D2[SB], DU[SB];
-#pragma unroll
-            for (int tt = 0; tt < SB; ++tt) {
-                if (NT == 1) {
-                    D2[tt] = d2[tt];
-                    DU[tt] = du[tt];
-                } else {
-                    D2[tt] = __shfl_sync(0xffffffffu, d2[tt % 8], src_base + tt / 8);
-                    DU[tt] = __shfl_sync(0xffffffffu, du[tt % 8], src_base + tt / 8);
+                for (int q = 0; q < 8; ++q) {
+                    float d2 = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+                    if (tb + q >= nvalid) d2 = 0.0f;
+                    const float du = d2 * uv[q];
+                    s8 += d2;
+                    *reinterpret_cast<float4*>(xy + cw * Lay::XROW + (g * 8 + q) * 4) =
+                        make_float4(d2, d2, du, du);
                 }
+                if (SUMMARY) sum_d2 += (double)s8;
             }
+            __syncwarp();
 
-            // the recurrence over SB tokens for this thread's G states
+            // 2. the recurrence over the SB tokens for this lane's G states
             float yp[SB];
 #pragma unroll
             for (int tt = 0; tt < SB; ++tt) {
+                const ulonglong2 xd = *reinterpret_cast<const ulonglong2*>(xy + cw * Lay::XROW + tt * 4);
+                const f2 d2p = xd.x, dup = xd.y;
                 const float* bcrow = bct + (sb * SB + tt) * (2 * NP) + g * G;
-                const f2 d2p = pk(D2[tt], D2[tt]);
-                const f2 dup = pk(DU[tt], DU[tt]);
-                f2 acc0 = pk(0.0f, 0.0f), acc1 = pk(0.0f, 0.0f);
+                f2 acc = pk(0.0f, 0.0f);
 #pragma unroll
                 for (int q4 = 0; q4 < G / 4; ++q4) {
                     const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
@@ -356,65 +356,50 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
                     if (!SUMMARY) {
                         const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
-                        acc0 = fma2(Cq.x, h[2 * q4], acc0);
-                        acc1 = fma2(Cq.y, h[2 * q4 + 1], acc1);
+                        acc = fma2(Cq.x, h[2 * q4], acc);
+                        acc = fma2(Cq.y, h[2 * q4 + 1], acc);
                     }
                 }
                 if (!SUMMARY) {
                     float lo, hi;
-                    upk(add2(acc0, acc1), lo, hi);
+                    upk(acc, lo, hi);
                     yp[tt] = lo + hi;
                 }
             }
+            __syncwarp();   // every lane is done with the token buffer
 
             if (!SUMMARY) {
-                // sum the partial read-outs of the NT threads; thread g keeps its 8 tokens
-                float yt[8];
-                if (NT == 1) {
+                // 3. partial read-outs through the buffer; finish the own 8 tokens
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) yt[q] = yp[q];
-                } else if (NT == 2) {
+                for (int q = 0; q < SB; q += 4)
+                    *reinterpret_cast<float4*>(xy + cw * Lay::YROW + g * SB + q) =
+                        make_float4(yp[q], yp[q + 1], yp[q + 2], yp[q + 3]);
+                __syncwarp();
+                float yt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float keep = g ? yp[8 + q] : yp[q];
-                        const float send = g ? yp[q] : yp[8 + q];
-                        yt[q] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-                    }
-                } else {
-                    float r1[16];
-                    const bool hb = (g & 2) != 0;
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float keep = hb ? yp[16 + q] : yp[q];
-                        const float send = hb ? yp[q] : yp[16 + q];
-                        r1[q] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-                    }
-                    const bool lb = (g & 1) != 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float keep = lb ? r1[8 + q] : r1[q];
-                        const float send = lb ? r1[q] : r1[8 + q];
-                        yt[q] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-                    }
+                for (int gg = 0; gg < NT; ++gg) {
+                    const float4 a = *reinterpret_cast<const float4*>(xy + cw * Lay::YROW + gg * SB + g * 8);
+                    const float4 bq = *reinterpret_cast<const float4*>(xy + cw * Lay::YROW + gg * SB + g * 8 + 4);
+                    yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
+                    yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
                 }
-                // D skip and SiLU gate for this thread's tokens
+                float zv[8];
+                if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb, zv);
                 float out[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float v = fmaf(Dd, uv[q], yt[q]);
-                    if (has_z) {
-                        const float zq = zv[q];
-                        v *= zq * rcp(1.0f + ex2(-kLog2e * zq));
-                    }
+                    if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
                     out[q] = v;
                 }
-                if (ch_ok)
-                    store_out8<TOUT>(p.y, row * L + k * kT + tb, out, nvalid - tb, vec_out);
+                if (ch_ok) store_out8<TOUT>(p.y, row * L + k * kT + tb, out, nvalid - tb, vec_out);
+                __syncwarp();   // before the next super-block overwrites the buffer
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
+    if (dead) return;
 
     if (SUMMARY) {
         // one thread per channel records the segment's sum of delta2

@@ -4,9 +4,10 @@
 namespace ssm {
 
 cudaError_t launch_fwd_np64(int NT, int tin, int tout, bool summary, bool tma_raw,
-                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                             size_t smem, cudaStream_t st) {
     switch (NT) {
-        case 4: return launch_fwd_nt<64, 4>(tin, tout, summary, tma_raw, p, m, grid, st);
+        case 4: return launch_fwd_nt<64, 4>(tin, tout, summary, tma_raw, p, m, grid, warps, smem, st);
         default: return cudaErrorInvalidValue;
     }
 }

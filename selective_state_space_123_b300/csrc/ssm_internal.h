@@ -16,18 +16,27 @@ struct FwdMaps {
     CUtensorMap u, dr, z, bc;
 };
 
-// Forward kernel launch for padded state size NP (4, 8, 16, 32, 64) and NT
-// threads per channel.  tin/tout are ssm_dtype values.
+// Forward kernel launch for padded state size NP (4, 8, 16, 32, 64), NT
+// threads per channel and `warps` compute warps per CTA, with `smem` bytes of
+// dynamic shared memory.  tin/tout are ssm_dtype values.
 cudaError_t launch_fwd_np4(int NT, int tin, int tout, bool summary, bool tma_raw,
-                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                           size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np8(int NT, int tin, int tout, bool summary, bool tma_raw,
-                           const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+                           const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                           size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np16(int NT, int tin, int tout, bool summary, bool tma_raw,
-                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                            size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
-                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                            size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np64(int NT, int tin, int tout, bool summary, bool tma_raw,
-                            const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st);
+                            const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                            size_t smem, cudaStream_t st);
+
+// The NT values each NP supports.
+int fwd_supported_nt(int NP, int* out, int cap);
 
 // Tensor maps of one backward call: raw tiles of u, delta_raw, z, dy, the
 // fp32 per-token tile written by the forward sweep, and the B/C tile.
@@ -45,9 +54,6 @@ cudaError_t launch_bwd_np32(int NT, int tin, int tout, bool tma, const BwdParams
                             const BwdMaps& m, dim3 grid, cudaStream_t st);
 cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
                             const BwdMaps& m, dim3 grid, cudaStream_t st);
-
-// The NT values each NP supports (first entry = default).
-int fwd_supported_nt(int NP, int* out, int cap);
 
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);

@@ -13,6 +13,24 @@ constexpr int kConsumers = 128;     // compute threads per CTA (4 warps)
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
+// Forward-kernel layout per NT (threads per channel).  Per compute warp an
+// exchange buffer holds, per channel, the (delta2, delta2, delta2*u,
+// delta2*u) quadruples of one super-block and later the NT partial
+// read-outs; rows are padded by 16 bytes so the lanes' 16-byte accesses
+// spread over all banks.
+template <int NT>
+struct FwdLayout {
+    static constexpr int CW = 32 / NT;             // channels per compute warp
+    static constexpr int SB = 8 * NT;              // tokens per super-block
+    static constexpr int XROW = SB * 4 + 4;        // floats per channel row (token quadruples)
+    static constexpr int YROW = NT * SB + 4;       // floats per channel row (partial read-outs)
+    static constexpr int XY_FLOATS = CW * (XROW > YROW ? XROW : YROW);
+    static constexpr int kMaxWarps = 7;    // compute warps per CTA at most (+ the producer: 256 threads)
+    static constexpr int kMinBlocks = 1;   // launch bound: up to 255 registers, no spills
+};
+constexpr int kFwdMaxStages = 6;
+constexpr int kMaxSmemPerCta = 226 * 1024;   // dynamic shared memory per CTA (227 KB on sm_103a, less the static part)
+
 // Forward scan parameters.  Layouts are the public ones (see ssm_scan.h);
 // `bc` is the prepared copy of B and C: (batch, seqlen, 2*NP) fp32 with
 // [0, NP) = ln2 * B[b, n, t] and [NP, 2NP) = C[b, n, t], zero for n >= N.
@@ -37,6 +55,7 @@ struct FwdParams {
     float* hin;             // (nseg, Bt, D, NP) initial state of each segment (pass 2)
     float* hloc;            // (nseg, Bt, D, NP) end state from a zero start (pass 1)
     float* sumd;            // (nseg, Bt, D) sum of delta/ln2 over the segment (pass 1)
+    int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
     int* status;
     uint64_t timeout_ns;
 };

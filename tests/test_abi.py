@@ -149,3 +149,21 @@ def test_bwd_workspace_query(pkg):
     # small state sizes are padded to 8 in the backward
     assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 4, 4, 64, 0, 0), True) >= \
         256 + 64 * 16 * 4 + 4 * 64 * 4
+
+
+@pytest.mark.parametrize("for_backward", [False, True])
+def test_workspace_query_edge_shapes(pkg, for_backward):
+    """The host planner handles every edge shape (no GPU involved)."""
+    for sh in [(1, 8, 16, 0), (0, 8, 16, 64), (2, 0, 16, 64), (1, 1, 1, 1), (1, 1, 64, 1),
+               (3, 1000, 5, 63), (1, 7, 16, 1 << 20), (1, 1536, 16, 1 << 20),
+               (65535, 1, 16, 8), (1, 100000, 16, 64)]:
+        for ti in (0, 1):
+            n = pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, ti, ti), for_backward)
+            assert n >= 256, sh
+    for forced in ("1", "2", "3", "7", "1000"):
+        os.environ["SSM_FWD_NSEG"] = forced
+        try:
+            for sh in [(1, 8, 16, 0), (1, 8, 16, 1), (2, 40, 16, 64 * 29 + 13)]:
+                assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), for_backward) >= 256
+        finally:
+            del os.environ["SSM_FWD_NSEG"]
