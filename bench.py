@@ -1,22 +1,29 @@
 """Benchmark of the selective scan on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
 
-A step is one forward selective scan (softplus of delta, discretisation, the
-recurrence, read-out, D skip, SiLU gate, final state) over one batch of the
-Mamba-1.4B layer shape: batch 4, D=4096 channels, N=16 states, L=4096 tokens,
-bf16 u/delta/z/B/C, fp32 A/D/bias, fp32 arithmetic, bf16 y, fp32 final state.
+Default workload (the headline): one forward selective scan -- softplus of
+delta, discretisation, the recurrence, read-out, D skip, SiLU gate, final
+state -- over one batch of the Mamba-1.4B layer shape: batch 4, D=4096
+channels, N=16 states, L=4096 tokens, bf16 u/delta/z/B/C, fp32 A/D/bias,
+fp32 arithmetic, bf16 y, fp32 final state.  Other workloads:
+  mamba130m_fwd     forward, batch 8, D 1536, N 16, L 2048
+  mamba2p8b_fwd     forward, batch 2, D 5120, N 16, L 8192
+  mamba2p8b_fwdbwd  forward then backward (all gradients), same shape
+  million_fwd       forward, batch 1, D 1536, N 16, L 1,048,576
+  decode_step       one recurrent step, batch 256, D 5120, N 16, state in place
 Inputs are synthetic (seeded, drawn on the device) and resident in HBM before
-the timed region; they are larger than L2 (539 MB vs 126 MB), so no flush is
-needed between steps.
+the timed region; every workload's inputs exceed L2 (126 MB) except where the
+JSON line says otherwise, in which case L2 is flushed between steps.
 
 The JSON line (rank 0) reports B*D*L*N state updates per second for the whole
 job (N GPUs run independent replicas: the channels of different sequences
 never interact, so the work shards with no collective), the roofline of the
 dominant kernel, clocks sampled during the timed region, the end-to-end rate
 through the C ABI with host buffers (pinned host -> device copies of every
-input and the device -> host read of y and h_L inside the timed region), and
-the fp64 CPU oracle timed on a bounded sample as the CPU baseline.
+input and the device -> host read of every output inside the timed region),
+and the fp64 CPU oracle timed on a bounded sample as the CPU baseline.
 `--impl reference` times that oracle alone (this method has no runnable
 reference implementation; the oracle is the reference arm).
 """
@@ -24,7 +31,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import multiprocessing as mp
 import os
 import statistics
@@ -38,18 +44,27 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    "mamba1p4b_fwd": dict(name="mamba1p4b_fwd", Bt=4, D=4096, N=16, L=4096, seed=2),
-    "mamba130m_fwd": dict(name="mamba130m_fwd", Bt=8, D=1536, N=16, L=2048, seed=1),
-    "mamba2p8b_fwd": dict(name="mamba2p8b_fwd", Bt=2, D=5120, N=16, L=8192, seed=3),
-    "million_fwd": dict(name="million_fwd", Bt=1, D=1536, N=16, L=1 << 20, seed=4),
+    "mamba1p4b_fwd": dict(mode="fwd", Bt=4, D=4096, N=16, L=4096, seed=2,
+                          title="Mamba-1.4B layer forward"),
+    "mamba130m_fwd": dict(mode="fwd", Bt=8, D=1536, N=16, L=2048, seed=1,
+                          title="Mamba-130M layer forward"),
+    "mamba2p8b_fwd": dict(mode="fwd", Bt=2, D=5120, N=16, L=8192, seed=3,
+                          title="Mamba-2.8B layer forward"),
+    "mamba2p8b_fwdbwd": dict(mode="fwdbwd", Bt=2, D=5120, N=16, L=8192, seed=3,
+                             title="Mamba-2.8B layer forward + backward"),
+    "million_fwd": dict(mode="fwd", Bt=1, D=1536, N=16, L=1 << 20, seed=4,
+                        title="million-length forward"),
+    "decode_step": dict(mode="step", Bt=256, D=5120, N=16, L=1, seed=4,
+                        title="single-token decode step"),
 }
 WORKLOAD = WORKLOADS["mamba1p4b_fwd"]
 METRIC = "selective scan: achieved HBM GB/s (% of roofline) and B*D*L*N state updates/s"
 UNIT = "state updates/s"
-# measured on this machine's B300 with a register-only probe: MUFU ex2 results
-# per clock per SM ("Rooflines")
+# MUFU ex2 results per clock per SM on this machine's B300, measured with a
+# register-only probe ("Kernels and rooflines")
 SFU_EX2_PER_CLK_SM = 32
 SMS = 148
+L2_BYTES = 126 * 1024 * 1024
 
 
 def load_peaks():
@@ -64,6 +79,22 @@ def fwd_bytes(Bt, D, N, L, ein=2, eout=2):
     (Bt,N,L), A (D,N), D and bias (D) once; write y (Bt,D,L) and h_L (Bt,D,N)."""
     return (3 * Bt * D * L * ein + 2 * Bt * N * L * ein + D * N * 4 + 2 * D * 4
             + Bt * D * L * eout + Bt * D * N * 4)
+
+
+def bwd_bytes(Bt, D, N, L, ein=2, eout=2):
+    """Algorithmic bytes of one backward: read u, delta_raw, z, dy (Bt,D,L), B,
+    C (Bt,N,L), A, D, bias once; write du, ddelta_raw, dz (Bt,D,L), dB, dC
+    (Bt,N,L) fp32, dA (D,N), dD, ddelta_bias (D), dh0 (Bt,D,N)."""
+    return (4 * Bt * D * L * ein + 2 * Bt * N * L * ein + D * N * 4 + 2 * D * 4
+            + 3 * Bt * D * L * eout + 2 * Bt * N * L * 4 + D * N * 4 + 2 * D * 4
+            + Bt * D * N * 4)
+
+
+def step_bytes(Bt, D, N, ein=2, eout=2):
+    """Algorithmic bytes of one decode step: state read and written, u,
+    delta_raw, z (Bt,D), B, C (Bt,N), A, D, bias read, y (Bt,D) written."""
+    return 2 * Bt * D * N * 4 + 3 * Bt * D * ein + 2 * Bt * N * ein + D * N * 4 + 2 * D * 4 \
+        + Bt * D * eout
 
 
 # --------------------------------------------------------------- clocks ---
@@ -126,20 +157,32 @@ _INPUT_CACHE = {}
 def _oracle_worker(args):
     """Run the oracle on a slice of channels; returns (updates, seconds of the
     oracle call alone -- drawing the inputs is not timed, and is cached)."""
-    seed, Bt, D, N, L, chans = args
+    mode, seed, Bt, D, N, L, chans = args
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
     import oracle
-    from scan_inputs import make_inputs
-    key = (seed, Bt, D, N, L, tuple(chans))
+    from scan_inputs import make_inputs, make_step_inputs
+    key = (mode, seed, Bt, D, N, L, tuple(chans))
     x = _INPUT_CACHE.get(key)
     if x is None:
         if len(_INPUT_CACHE) > 64:
             _INPUT_CACHE.clear()
-        x = _INPUT_CACHE[key] = make_inputs(Bt, D, N, L, seed=seed, in_dtype="bf16",
-                                            channels=chans)
+        if mode == "step":
+            x = make_step_inputs(Bt, D, N, seed=seed, in_dtype="bf16", channels=chans)
+        else:
+            x = make_inputs(Bt, D, N, L, seed=seed, in_dtype="bf16", channels=chans,
+                            dy=(mode == "fwdbwd"))
+        _INPUT_CACHE[key] = x
     t0 = time.perf_counter()
-    oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    if mode == "fwd":
+        oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    elif mode == "fwdbwd":
+        oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+        oracle.scan_bwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, x.Dv, x.z, x.delta_bias,
+                        x.h0, None)
+    else:
+        oracle.scan_step(x["u"], x["delta_raw"], x["A"], x["Bm"], x["Cm"], x["state"],
+                         x["Dv"], x["z"], x["delta_bias"])
     return Bt * len(chans) * N * L, time.perf_counter() - t0
 
 
@@ -154,8 +197,14 @@ class OracleTimer:
         self.cores = cores or os.cpu_count() or 1
         self.pool = mp.get_context("spawn").Pool(self.cores)
         w = WORKLOAD
-        self.pool.map(_oracle_worker, [(w["seed"], 1, w["D"], w["N"], 64, [0])] * self.cores)
-        _, self.t_channel = _oracle_worker((w["seed"], 1, w["D"], w["N"], w["L"], [0]))
+        self.bt = w["Bt"] if w["mode"] == "step" else 1   # decode: all sequences of a channel
+        warm_L = min(64, w["L"])
+        self.pool.map(_oracle_worker, [(w["mode"], w["seed"], self.bt, w["D"], w["N"], warm_L,
+                                        [0])] * self.cores)
+        probe = 16 if w["mode"] == "step" else 1
+        _, t = _oracle_worker((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
+                               list(range(probe))))
+        self.t_channel = t / probe
         self.next = 0
 
     def measure(self, seconds_per_core, fixed=False):
@@ -163,21 +212,23 @@ class OracleTimer:
         fixed=True reuses the same channel sample every call (the reference
         arm's steps); otherwise the sample advances through the channels."""
         w = WORKLOAD
-        per = max(1, int(seconds_per_core / max(self.t_channel, 1e-6)))
+        per = max(1, min(w["D"], int(seconds_per_core / max(self.t_channel, 1e-7))))
         jobs = []
         start = 0 if fixed else self.next
         for i in range(self.cores):
-            jobs.append((w["seed"], 1, w["D"], w["N"], w["L"],
+            jobs.append((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
                          [(start + i * per + j) % w["D"] for j in range(per)]))
         if not fixed:
             self.next = (start + per * self.cores) % w["D"]
         res = self.pool.map(_oracle_worker, jobs)
         upd = sum(r[0] for r in res)
         busy = max(r[1] for r in res)
+        what = {"fwd": "forward", "fwdbwd": "forward + backward", "step": "decode step"}[w["mode"]]
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
-                "sample": "%d channels x %d tokens x %d states of the %s workload (batch row "
-                          "0), one spawned process per core; slowest process %.2f s" %
-                          (per * self.cores, w["L"], w["N"], w["name"], busy)}
+                "sample": "%s of %d channels x %d batch rows x %d tokens x %d states of the %s "
+                          "workload, one spawned process per core (%d channels each); slowest "
+                          "process %.2f s" % (what, per * self.cores, self.bt, w["L"], w["N"],
+                                              w["name"], per, busy)}
 
     def close(self):
         self.pool.close()
@@ -193,6 +244,74 @@ def cpu_oracle_rate(target_seconds=12.0):
 
 
 # ------------------------------------------------------------------ GPU ---
+class Workload:
+    """Device buffers and the step of one workload (inputs drawn on the device)."""
+
+    def __init__(self, ssm, w, rank):
+        import torch
+        from scan_inputs import device_inputs
+        self.ssm, self.w = ssm, w
+        Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
+        self.mode = w["mode"]
+        bf = torch.bfloat16
+        if self.mode == "step":
+            a = device_inputs(Bt, D, N, 1, seed=w["seed"] + 1000 * rank, in_dtype="bf16", h0=True)
+            self.inp = {"u": a["u"][:, :, 0].contiguous(), "delta_raw": a["delta_raw"][:, :, 0].contiguous(),
+                        "z": a["z"][:, :, 0].contiguous(), "Bm": a["Bm"][:, :, 0].contiguous(),
+                        "Cm": a["Cm"][:, :, 0].contiguous(), "A": a["A"], "Dv": a["Dv"],
+                        "delta_bias": a["delta_bias"]}
+            self.state = a["h0"]
+            self.y = torch.empty(Bt, D, dtype=bf, device="cuda")
+            self.ws = None
+            self.bytes = step_bytes(Bt, D, N)
+            self.exps = Bt * D * N
+            self.launches = 1
+            self.outs = [self.y, self.state]
+        else:
+            a = device_inputs(Bt, D, N, L, seed=w["seed"] + 1000 * rank, in_dtype="bf16",
+                              dy=(self.mode == "fwdbwd"))
+            self.inp = {k: v for k, v in a.items() if v is not None}
+            self.y = torch.empty(Bt, D, L, dtype=bf, device="cuda")
+            self.hL = torch.empty(Bt, D, N, dtype=torch.float32, device="cuda")
+            shape = ssm.make_shape(Bt, D, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
+            nb = ssm.ssm_scan_workspace_bytes(shape, self.mode == "fwdbwd")
+            nb = max(nb, ssm.ssm_scan_workspace_bytes(shape, False))
+            self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            self.bytes = fwd_bytes(Bt, D, N, L)
+            self.exps = Bt * D * L * N
+            # B/C preparation + scan; the million-length sequence takes the
+            # segmented plan (preparation, summary pass, carry, scan)
+            self.launches = 4 if L >= (1 << 18) and Bt * D <= 4096 else 2
+            self.outs = [self.y, self.hL]
+            self.grads = None
+            if self.mode == "fwdbwd":
+                self.bytes += bwd_bytes(Bt, D, N, L)
+                self.exps *= 3     # forward, and the backward's two sweeps
+                self.launches += 3
+        self.updates = Bt * D * L * N
+
+    def step(self, inp=None):
+        ssm, a = self.ssm, (inp or self.inp)
+        import torch
+        if self.mode == "step":
+            ssm.ssm_scan_step(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], self.state,
+                              a["Dv"], a["z"], a["delta_bias"], out_dtype=torch.bfloat16, y=self.y)
+            return
+        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
+                         a["delta_bias"], None, out_dtype=torch.bfloat16, y=self.y, hL=self.hL,
+                         workspace=self.ws)
+        if self.mode == "fwdbwd":
+            self.grads = ssm.ssm_scan_bwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["dy"],
+                                          a["Dv"], a["z"], a["delta_bias"], None, None,
+                                          out_dtype=torch.bfloat16, workspace=self.ws)
+
+    def results(self):
+        outs = list(self.outs)
+        if self.mode == "fwdbwd" and self.grads is not None:
+            outs += [v for v in self.grads.values() if v is not None]
+        return outs
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -210,27 +329,44 @@ def run_ours(args):
         cpu = cpu_oracle_rate(args.cpu_seconds)
 
     import selective_state_space_123_b300 as ssm
-    from scan_inputs import device_inputs
 
     w = WORKLOAD
+    wl = Workload(ssm, w, rank)
     Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
-    a = device_inputs(Bt, D, N, L, seed=w["seed"] + 1000 * rank, in_dtype="bf16")
-    y = torch.empty(Bt, D, L, dtype=torch.bfloat16, device="cuda")
-    hL = torch.empty(Bt, D, N, dtype=torch.float32, device="cuda")
-    shape = ssm.make_shape(Bt, D, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
-    ws = torch.empty(ssm.ssm_scan_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    in_bytes = sum(v.numel() * v.element_size() for v in wl.inp.values())
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    def step():
-        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
-                         a["delta_bias"], None, out_dtype=torch.bfloat16, y=y, hL=hL,
-                         workspace=ws)
+    flush_sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def do_flush():
+        # read (not write) a buffer twice the size of L2: the lines left in L2
+        # are clean, so the timed step pays no write-back of the flush
+        torch.sum(flush, dim=0, out=flush_sink)
+
+    def timed_step():
+        if flush is not None:
+            do_flush()
+        wl.step()
 
     for _ in range(args.warmup):
-        step()
+        timed_step()
     torch.cuda.synchronize()
-    if ssm.ssm_get_status(ws) != ssm.SSM_OK:
+    if wl.ws is not None and ssm.ssm_get_status(wl.ws) != ssm.SSM_OK:
         raise RuntimeError("device status not ok after warm-up")
+
+    # the flush (when needed) is timed separately and subtracted
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    if flush is not None:
+        e0.record(stream)
+        for _ in range(args.steps):
+            do_flush()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        flush_ms = e0.elapsed_time(e1)
 
     clocks = ClockSampler(local)
     if world > 1:
@@ -238,49 +374,49 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        timed_step()
     e1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if ssm.ssm_get_status(ws) != ssm.SSM_OK:
+    ms = e0.elapsed_time(e1) - flush_ms
+    if wl.ws is not None and ssm.ssm_get_status(wl.ws) != ssm.SSM_OK:
         raise RuntimeError("device status not ok after the timed region")
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     ms_step = ms / args.steps
-    updates = Bt * D * L * N
-    value = world * updates / (ms_step * 1e-3)
+    value = world * wl.updates / (ms_step * 1e-3)
 
     # ---- end to end through the C ABI with host buffers
-    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in a.items()} \
-        if not args.no_e2e else {}
-    dev = {k: (torch.empty_like(v, device="cuda") if v is not None else None)
-           for k, v in host.items()}
-    y_host = torch.empty(Bt, D, L, dtype=torch.bfloat16, pin_memory=not args.no_e2e)
-    h_host = torch.empty(Bt, D, N, dtype=torch.float32, pin_memory=not args.no_e2e)
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = y_host.numel() * 2 + h_host.numel() * 4
-
-    def e2e_step():
-        for k, v in host.items():
-            if v is not None:
-                dev[k].copy_(v, non_blocking=True)
-        ssm.ssm_scan_fwd(dev["u"], dev["delta_raw"], dev["A"], dev["Bm"], dev["Cm"], dev["Dv"],
-                         dev["z"], dev["delta_bias"], None, out_dtype=torch.bfloat16, y=y,
-                         hL=hL, workspace=ws)
-        y_host.copy_(y, non_blocking=True)
-        h_host.copy_(hL, non_blocking=True)
-
-    e2e_steps = max(3, min(args.steps // 20, 50))
-    e2e_ms = float("nan")
+    e2e = None
     if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in wl.inp.items()}
+        dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+        if wl.mode == "step":
+            state_host = wl.state.cpu().pin_memory()
+        wl.step(dev)
+        outs_dev = wl.results()
+        outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs_dev]
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        if wl.mode == "step":
+            h2d += state_host.numel() * 4
+        d2h = sum(o.numel() * o.element_size() for o in outs_host)
+
+        def e2e_step():
+            for k, v in host.items():
+                dev[k].copy_(v, non_blocking=True)
+            if wl.mode == "step":
+                wl.state.copy_(state_host, non_blocking=True)
+            wl.step(dev)
+            for oh, od in zip(outs_host, wl.results()):
+                oh.copy_(od, non_blocking=True)
+
+        e2e_steps = max(3, min(args.steps // 20, 50))
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
@@ -290,56 +426,65 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * wl.updates / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    # ---- roofline of the dominant kernel (the forward scan kernel; the
-    # call also runs the tiny B/C preparation kernel, included in the time)
+    # ---- roofline of the step: the slower of its algorithmic bytes at the
+    # measured HBM bandwidth and its exps at the MUFU ex2 rate
     peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6400.0)
+    hbm_basis = "MEASURED_PEAKS.json hbm_gbs (of measured)" if "hbm_gbs" in peaks else \
+        "fallback 6400 GB/s (of fallback)"
     sm_mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
     sfu_peak = SFU_EX2_PER_CLK_SM * SMS * sm_mhz * 1e6
-    exps_per_s = updates / (ms_step * 1e-3)
-    bytes_alg = fwd_bytes(Bt, D, N, L)
-    gbs = bytes_alg / (ms_step * 1e-3) / 1e9
-    t_hbm = bytes_alg / (hbm_peak * 1e9)
-    t_sfu = updates / sfu_peak
+    t_s = ms_step * 1e-3
+    gbs = wl.bytes / t_s / 1e9
+    t_hbm = wl.bytes / (hbm_peak * 1e9)
+    t_sfu = wl.exps / sfu_peak
     bound = "alu" if t_sfu >= t_hbm else "hbm"
+    kernel = {"fwd": "fwd_kernel", "fwdbwd": "fwd_kernel + bwd_fwd_kernel + bwd_rev_kernel",
+              "step": "step_kernel"}[wl.mode]
+    roof = {
+        "bound": bound,
+        "kernel": kernel,
+        "achieved": wl.exps / t_s / 1e12 if bound == "alu" else gbs,
+        "peak": sfu_peak / 1e12 if bound == "alu" else hbm_peak,
+        "unit": "Texp2/s" if bound == "alu" else "GB/s",
+        "frac": (wl.exps / t_s / sfu_peak) if bound == "alu" else gbs / hbm_peak,
+        "peak_basis": ("MUFU ex2 32/clk/SM x 148 SMs x median SM clock %.0f MHz sampled in the "
+                       "timed region (probe-measured rate)" % sm_mhz) if bound == "alu" else hbm_basis,
+        "roofline_time_us": max(t_hbm, t_sfu) * 1e6,
+        "frac_of_roofline_time": max(t_hbm, t_sfu) / t_s,
+        "algorithmic_bytes": wl.bytes,
+        "exps": wl.exps,
+        "traffic": None,
+        "timing_note": "achieved uses the whole step's CUDA-event time, which includes the small "
+                       "B/C preparation kernel",
+    }
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "%s: batch %d, D %d, N %d, L %d (forward scan)"
-                               % (w["name"], Bt, D, N, L),
-                   "io_dtype": "bf16 u/delta/z/B/C/y, fp32 A/D/bias/h_L",
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"},
+        "config": {"workload": "%s: %s, batch %d, D %d, N %d, L %d"
+                               % (w["name"], w["title"], Bt, D, N, L),
+                   "io_dtype": "bf16 u/delta/z/B/C/dy and outputs, fp32 A/D/bias/states",
+                   "l2": ("flushed between steps (a 2x L2 buffer read, its time subtracted)" if flush is not None
+                          else "inputs larger than L2 (no flush)"),
+                   "parallelism": "replicas"},
         "hbm_gbs": gbs,
         "hbm_frac_of_measured": gbs / hbm_peak,
-        "roofline": {
-            "bound": bound,
-            "achieved": exps_per_s / 1e12 if bound == "alu" else gbs,
-            "peak": sfu_peak / 1e12 if bound == "alu" else hbm_peak,
-            "unit": "Texp2/s" if bound == "alu" else "GB/s",
-            "frac": (exps_per_s / sfu_peak) if bound == "alu" else gbs / hbm_peak,
-            "peak_basis": ("MUFU ex2 32/clk/SM x 148 SMs x median SM clock %.0f MHz "
-                           "(probe-measured rate)" % sm_mhz) if bound == "alu" else
-                          "MEASURED_PEAKS.json hbm_gbs",
-            "roofline_time_us": max(t_hbm, t_sfu) * 1e6,
-            "frac_of_roofline_time": max(t_hbm, t_sfu) / (ms_step * 1e-3),
-            "traffic": None,
-        },
+        "roofline": roof,
         "clocks": clk,
-        "e2e": {"value": world * updates / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": wl.launches * args.steps,
     }
+    if e2e is not None:
+        line["e2e"] = e2e
     if cpu is not None:
         line["cpu_baseline"] = cpu
-    if args.no_e2e:
-        del line["e2e"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -368,8 +513,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": w["Bt"] * w["D"] * w["L"] * w["N"] / val * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": "%s: batch %d, D %d, N %d, L %d (Mamba-1.4B layer forward)"
-                               % (w["name"], w["Bt"], w["D"], w["N"], w["L"]),
+        "config": {"workload": "%s: %s, batch %d, D %d, N %d, L %d"
+                               % (w["name"], w["title"], w["Bt"], w["D"], w["N"], w["L"]),
                    "parallelism": "host cores"},
         "cpu_baseline": dict(rates[-1], value=val),
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -390,7 +535,7 @@ def main():
     ap.add_argument("--workload", default="mamba1p4b_fwd", choices=sorted(WORKLOADS))
     args = ap.parse_args()
     global WORKLOAD
-    WORKLOAD = WORKLOADS[args.workload]
+    WORKLOAD = dict(WORKLOADS[args.workload], name=args.workload)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

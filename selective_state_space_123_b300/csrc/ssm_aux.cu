@@ -90,10 +90,22 @@ cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const f
 }
 
 // ---------------------------------------------------------------- step ---
-// One thread per (b, d, group of 4 states); GT threads per channel (power of
-// two, GT * 4 >= N).  Reads the state once and writes it once: the step is
-// bound by the state's HBM traffic.
-template <typename TIN, typename TOUT, int GT>
+// One thread per (b, d, group of S states); GT = ceil(N / S) threads per
+// channel.  The step reads the state once and writes it once, so it is bound
+// by the state's HBM traffic: each thread keeps S * 4 bytes of state loads in
+// flight (S = 16 at N = 16, 64 bytes), issued before any arithmetic.
+template <typename TIN>
+__device__ __forceinline__ void load_vec4_in(const TIN* p, float (&v)[4]) {
+    if constexpr (sizeof(TIN) == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    } else {
+        const float4 w = *reinterpret_cast<const float4*>(p);
+        v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    }
+}
+
+template <typename TIN, typename TOUT, int S, int GT>
 __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = gid / GT;   // b * D + d
@@ -102,11 +114,43 @@ __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     const int64_t r = ok ? row : 0;
     const int64_t b = r / p.D, d = r % p.D;
     const int N = p.N;
+    const int n0 = g * S;
     const TIN* u = static_cast<const TIN*>(p.u);
     const TIN* dr = static_cast<const TIN*>(p.dr);
-    const TIN* Bv = static_cast<const TIN*>(p.B);
-    const TIN* Cv = static_cast<const TIN*>(p.C);
+    const TIN* Bv = static_cast<const TIN*>(p.B) + b * N;
+    const TIN* Cv = static_cast<const TIN*>(p.C) + b * N;
+    const float* Ad = p.A + d * N;
+    float* st = p.state + r * N;
+    // vector loads need 16-byte (state, A) and 8/16-byte (B, C) aligned rows
+    const bool vec = (N % 4) == 0 && n0 + S <= N;
 
+    float hv[S], av[S], bv[S], cv[S];
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 h4 = *reinterpret_cast<const float4*>(st + n0 + q);
+            hv[q] = h4.x; hv[q + 1] = h4.y; hv[q + 2] = h4.z; hv[q + 3] = h4.w;
+        }
+#pragma unroll
+        for (int q = 0; q < S; q += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(Ad + n0 + q);
+            av[q] = a4.x; av[q + 1] = a4.y; av[q + 2] = a4.z; av[q + 3] = a4.w;
+            float t4[4];
+            load_vec4_in<TIN>(Bv + n0 + q, t4);
+            bv[q] = t4[0]; bv[q + 1] = t4[1]; bv[q + 2] = t4[2]; bv[q + 3] = t4[3];
+            load_vec4_in<TIN>(Cv + n0 + q, t4);
+            cv[q] = t4[0]; cv[q + 1] = t4[1]; cv[q + 2] = t4[2]; cv[q + 3] = t4[3];
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < S; ++q) {
+            const bool in = ok && n0 + q < N;
+            hv[q] = in ? st[n0 + q] : 0.0f;
+            av[q] = in ? Ad[n0 + q] : 0.0f;
+            bv[q] = in ? Elem<TIN>::to_f(Bv[n0 + q]) : 0.0f;
+            cv[q] = in ? Elem<TIN>::to_f(Cv[n0 + q]) : 0.0f;
+        }
+    }
     const float uu = Elem<TIN>::to_f(u[r]);
     const float x = fmaf(Elem<TIN>::to_f(dr[r]), kLog2e, p.bias ? p.bias[d] * kLog2e : 0.0f);
     float d2;
@@ -122,35 +166,24 @@ __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     }
     const float du = d2 * uu * kLn2;   // delta * u
 
-    const int n0 = g * 4;
-    float* st = p.state + r * N;
-    float hv[4];
-    const bool vec = ok && (N % 4 == 0) && (n0 + 4 <= N);
-    if (vec) {
-        const float4 v = *reinterpret_cast<const float4*>(st + n0);
-        hv[0] = v.x; hv[1] = v.y; hv[2] = v.z; hv[3] = v.w;
-    } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) hv[q] = (ok && n0 + q < N) ? st[n0 + q] : 0.0f;
-    }
     float acc = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int n = n0 + q;
-        if (n < N) {
-            const float a = ex2(d2 * p.A[d * N + n]);
-            const float Bn = Elem<TIN>::to_f(Bv[b * N + n]);
-            const float Cn = Elem<TIN>::to_f(Cv[b * N + n]);
-            hv[q] = fmaf(a, hv[q], du * Bn);
-            acc = fmaf(Cn, hv[q], acc);
-        }
+    for (int q = 0; q < S; ++q) {
+        const float a = sizeof(TIN) == 4 ? exp2_accurate(d2 * av[q]) : ex2(d2 * av[q]);
+        hv[q] = fmaf(a, hv[q], du * bv[q]);
+        acc = fmaf(cv[q], hv[q], acc);
     }
-    if (vec) {
-        *reinterpret_cast<float4*>(st + n0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-    } else if (ok) {
+    if (ok) {
+        if (vec) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (n0 + q < N) st[n0 + q] = hv[q];
+            for (int q = 0; q < S; q += 4)
+                *reinterpret_cast<float4*>(st + n0 + q) =
+                    make_float4(hv[q], hv[q + 1], hv[q + 2], hv[q + 3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < S; ++q)
+                if (n0 + q < N) st[n0 + q] = hv[q];
+        }
     }
 #pragma unroll
     for (int o = 1; o < GT; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -167,21 +200,23 @@ __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     }
 }
 
-template <typename TIN, typename TOUT>
-static cudaError_t launch_step_t(const StepParams& p, cudaStream_t st) {
-    const int groups = (p.N + 3) / 4;
-    int GT = 1;
-    while (GT < groups) GT <<= 1;
+template <typename TIN, typename TOUT, int S, int GT>
+static cudaError_t launch_step_s(const StepParams& p, cudaStream_t st) {
     const int64_t threads = p.Bt * p.D * GT;
     const unsigned blocks = (unsigned)((threads + 255) / 256);
-    switch (GT) {
-        case 1: step_kernel<TIN, TOUT, 1><<<blocks, 256, 0, st>>>(p); break;
-        case 2: step_kernel<TIN, TOUT, 2><<<blocks, 256, 0, st>>>(p); break;
-        case 4: step_kernel<TIN, TOUT, 4><<<blocks, 256, 0, st>>>(p); break;
-        case 8: step_kernel<TIN, TOUT, 8><<<blocks, 256, 0, st>>>(p); break;
-        default: step_kernel<TIN, TOUT, 16><<<blocks, 256, 0, st>>>(p); break;
-    }
+    step_kernel<TIN, TOUT, S, GT><<<blocks, 256, 0, st>>>(p);
     return cudaGetLastError();
+}
+
+template <typename TIN, typename TOUT>
+static cudaError_t launch_step_t(const StepParams& p, cudaStream_t st) {
+    // S states per thread (a multiple of 4 when N allows vector loads), GT
+    // threads per channel (a power of two, for the shuffle reduction)
+    if (p.N <= 4) return launch_step_s<TIN, TOUT, 4, 1>(p, st);
+    if (p.N <= 8) return launch_step_s<TIN, TOUT, 8, 1>(p, st);
+    if (p.N <= 16) return launch_step_s<TIN, TOUT, 16, 1>(p, st);
+    if (p.N <= 32) return launch_step_s<TIN, TOUT, 16, 2>(p, st);
+    return launch_step_s<TIN, TOUT, 16, 4>(p, st);
 }
 
 cudaError_t launch_step(int tin, int tout, const StepParams& p, cudaStream_t st) {

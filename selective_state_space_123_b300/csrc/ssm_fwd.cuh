@@ -147,15 +147,50 @@ __device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, in
     fill_raw_tile_r<TIN>(tile, CH, src, row0, rows_valid, L, t0, lane);
 }
 
+// The recurrence over one super-block of SB tokens for one lane's G states.
+//   d2, du: delta/ln2 and delta2*u of the SB tokens (registers)
+//   bcb:    prepared B/C row of the super-block's first token at this lane's states
+template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE>
+__device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&du)[SB],
+                                          const float* bcb, const f2 (&Ap)[G / 2],
+                                          f2 (&h)[G / 2], float (&yp)[SB]) {
+    constexpr int Q = G / 4;
+#pragma unroll
+    for (int tt = 0; tt < SB; ++tt) {
+        const f2 d2p = pk(d2[tt], d2[tt]), dup = pk(du[tt], du[tt]);
+        const float* bcrow = bcb + tt * (2 * NP);
+        f2 acc = pk(0.0f, 0.0f);
+#pragma unroll
+        for (int q4 = 0; q4 < Q; ++q4) {
+            const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+            const f2 a0 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4]))
+                                   : ex2x2(mul2(d2p, Ap[2 * q4]));
+            const f2 a1 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4 + 1]))
+                                   : ex2x2(mul2(d2p, Ap[2 * q4 + 1]));
+            h[2 * q4] = fma2(a0, h[2 * q4], mul2(dup, Bq.x));
+            h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
+            if (!SUMMARY) {
+                const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+                acc = fma2(Cq.x, h[2 * q4], acc);
+                acc = fma2(Cq.y, h[2 * q4 + 1], acc);
+            }
+        }
+        if (!SUMMARY) {
+            float lo, hi;
+            upk(acc, lo, hi);
+            yp[tt] = lo + hi;
+        }
+    }
+}
+
 // Forward kernel.  blockDim.x = 32 * (W + 1): W compute warps and one
 // producer warp (the last).  A CTA owns CH = W * 32 / NT channels of one
 // batch row for one segment of the sequence.  Per super-block of SB = 8 * NT
-// tokens each lane first prepares its own 8 tokens (softplus, delta * u) into
-// the warp's exchange buffer, then all lanes run the recurrence over the SB
-// tokens for their G = NP / NT states, then the per-token partial read-outs
-// go back through the same buffer and each lane finishes its own 8 tokens
-// (sum over the NT lanes, D skip, SiLU gate, store).  All exchange stays
-// inside the warp.
+// tokens each lane computes softplus and delta * u of all SB tokens of its
+// channel, runs the recurrence over them for its G = NP / NT states, writes
+// its per-token partial read-outs to the warp's exchange buffer, and then
+// finishes its own 8 tokens (sum over the NT lanes, D skip, SiLU gate,
+// store).  All exchange stays inside the warp.
 template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW>
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
@@ -165,6 +200,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     constexpr int G = NP / NT;
     constexpr int CW = Lay::CW;
     constexpr int SB = Lay::SB;
+    constexpr int TPL = Lay::TPL;     // tokens each lane finishes per super-block
     constexpr int EB = (int)sizeof(TIN);
     constexpr int NRAW = SUMMARY ? 2 : 3;
     constexpr int BCB = bc_tile_bytes<NP>();
@@ -315,84 +351,70 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll 1
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (sb * SB >= nvalid) break;
-            const int tb = sb * SB + g * 8;   // this lane's own 8 tokens
 
-            // 1. prepare the own tokens: (delta2, delta2, delta2*u, delta2*u)
-            float uv[8];
-            {
-                float dv[8];
-                load_raw8r<TIN>(st, CH, c, tb, uv);
-                load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
-                float s8 = 0.0f;
+            // 1. every lane of the channel computes delta2 = softplus / ln2 and
+            //    delta2 * u for all SB tokens itself: the recurrence then reads
+            //    them from registers (recomputing is cheaper than an exchange
+            //    through shared memory at the head of every token)
+            float d2[SB], du[SB];
+#pragma unroll
+            for (int k8 = 0; k8 < SB / 8; ++k8) {
+                float dv[8], u8[8];
+                load_raw8r<TIN>(st, CH, c, sb * SB + 8 * k8, u8);
+                load_raw8r<TIN>(st + RAW, CH, c, sb * SB + 8 * k8, dv);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    float d2 = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
-                    if (tb + q >= nvalid) d2 = 0.0f;
-                    const float du = d2 * uv[q];
-                    s8 += d2;
-                    *reinterpret_cast<float4*>(xy + cw * Lay::XROW + (g * 8 + q) * 4) =
-                        make_float4(d2, d2, du, du);
+                    float dd = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+                    if (sb * SB + 8 * k8 + q >= nvalid) dd = 0.0f;
+                    d2[8 * k8 + q] = dd;
+                    du[8 * k8 + q] = dd * u8[q];
                 }
-                if (SUMMARY) sum_d2 += (double)s8;
             }
-            __syncwarp();
+            if (SUMMARY) {
+                float s8 = 0.0f;   // every lane of the channel sums all SB tokens
+#pragma unroll
+                for (int q = 0; q < SB; ++q) s8 += d2[q];
+                sum_d2 += (double)s8;
+            }
 
             // 2. the recurrence over the SB tokens for this lane's G states
             float yp[SB];
-#pragma unroll
-            for (int tt = 0; tt < SB; ++tt) {
-                const ulonglong2 xd = *reinterpret_cast<const ulonglong2*>(xy + cw * Lay::XROW + tt * 4);
-                const f2 d2p = xd.x, dup = xd.y;
-                const float* bcrow = bct + (sb * SB + tt) * (2 * NP) + g * G;
-                f2 acc = pk(0.0f, 0.0f);
-#pragma unroll
-                for (int q4 = 0; q4 < G / 4; ++q4) {
-                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
-                    const f2 a0 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4]))
-                                           : ex2x2(mul2(d2p, Ap[2 * q4]));
-                    const f2 a1 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4 + 1]))
-                                           : ex2x2(mul2(d2p, Ap[2 * q4 + 1]));
-                    h[2 * q4] = fma2(a0, h[2 * q4], mul2(dup, Bq.x));
-                    h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
-                    if (!SUMMARY) {
-                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
-                        acc = fma2(Cq.x, h[2 * q4], acc);
-                        acc = fma2(Cq.y, h[2 * q4 + 1], acc);
-                    }
-                }
-                if (!SUMMARY) {
-                    float lo, hi;
-                    upk(acc, lo, hi);
-                    yp[tt] = lo + hi;
-                }
-            }
-            __syncwarp();   // every lane is done with the token buffer
+            fwd_chain<NP, G, SB, SUMMARY, ACCURATE>(d2, du, bct + sb * SB * (2 * NP) + g * G, Ap,
+                                                    h, yp);
 
             if (!SUMMARY) {
-                // 3. partial read-outs through the buffer; finish the own 8 tokens
+                // 3. partial read-outs through the buffer; finish the own tokens
+                const int tb = sb * SB + g * TPL;
+                float* yb = xy + cw * Lay::YROW;
 #pragma unroll
                 for (int q = 0; q < SB; q += 4)
-                    *reinterpret_cast<float4*>(xy + cw * Lay::YROW + g * SB + q) =
+                    *reinterpret_cast<float4*>(yb + g * SB + q) =
                         make_float4(yp[q], yp[q + 1], yp[q + 2], yp[q + 3]);
                 __syncwarp();
-                float yt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int gg = 0; gg < NT; ++gg) {
-                    const float4 a = *reinterpret_cast<const float4*>(xy + cw * Lay::YROW + gg * SB + g * 8);
-                    const float4 bq = *reinterpret_cast<const float4*>(xy + cw * Lay::YROW + gg * SB + g * 8 + 4);
-                    yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
-                    yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
-                }
-                float zv[8];
-                if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb, zv);
-                float out[8];
+                for (int k8 = 0; k8 < TPL / 8; ++k8) {
+                    float yt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float v = fmaf(Dd, uv[q], yt[q]);
-                    if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
-                    out[q] = v;
+                    for (int gg = 0; gg < NT; ++gg) {
+                        const float4 a = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8);
+                        const float4 bq = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8 + 4);
+                        yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
+                        yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
+                    }
+                    float zv[8], u8[8];
+                    load_raw8r<TIN>(st, CH, c, tb + 8 * k8, u8);
+                    if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb + 8 * k8, zv);
+                    float out[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float v = fmaf(Dd, u8[q], yt[q]);
+                        if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
+                        out[q] = v;
+                    }
+                    if (ch_ok)
+                        store_out8<TOUT>(p.y, row * L + k * kT + tb + 8 * k8, out,
+                                         nvalid - (tb + 8 * k8), vec_out);
                 }
-                if (ch_ok) store_out8<TOUT>(p.y, row * L + k * kT + tb, out, nvalid - tb, vec_out);
                 __syncwarp();   // before the next super-block overwrites the buffer
             }
         }
@@ -402,10 +424,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (dead) return;
 
     if (SUMMARY) {
-        // one thread per channel records the segment's sum of delta2
-        double tot = sum_d2;
-#pragma unroll
-        for (int o = 1; o < NT; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        // one thread per channel records the segment's sum of delta2 (every
+        // lane of the channel holds the whole sum)
+        const double tot = sum_d2;
         if (ch_ok) {
             float* hl = p.hloc + ((int64_t)seg * p.Bt * p.D + row) * NP + g * G;
 #pragma unroll

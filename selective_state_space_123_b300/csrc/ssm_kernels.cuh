@@ -14,17 +14,16 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
 // Forward-kernel layout per NT (threads per channel).  Per compute warp an
-// exchange buffer holds, per channel, the (delta2, delta2, delta2*u,
-// delta2*u) quadruples of one super-block and later the NT partial
-// read-outs; rows are padded by 16 bytes so the lanes' 16-byte accesses
+// exchange buffer holds, per channel, the NT partial read-outs of one
+// super-block; rows are padded by 16 bytes so the lanes' 16-byte accesses
 // spread over all banks.
 template <int NT>
 struct FwdLayout {
     static constexpr int CW = 32 / NT;             // channels per compute warp
-    static constexpr int SB = 8 * NT;              // tokens per super-block
-    static constexpr int XROW = SB * 4 + 4;        // floats per channel row (token quadruples)
+    static constexpr int TPL = 8;                  // tokens each lane finishes per super-block
+    static constexpr int SB = TPL * NT;            // tokens per super-block
     static constexpr int YROW = NT * SB + 4;       // floats per channel row (partial read-outs)
-    static constexpr int XY_FLOATS = CW * (XROW > YROW ? XROW : YROW);
+    static constexpr int XY_FLOATS = CW * YROW;
     static constexpr int kMaxWarps = 7;    // compute warps per CTA at most (+ the producer: 256 threads)
     static constexpr int kMinBlocks = 1;   // launch bound: up to 255 registers, no spills
 };
