@@ -213,21 +213,59 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
 
 // Backward plan: the two sweeps need the prepared B/C (state size padded to
 // at least 8), one fp32 number per (batch, channel, token), the final state
-// and the state at the end of every 64-token chunk.
+// and the state at the end of every 64-token chunk.  Channel tiles of W
+// compute warps, one CTA per SM, chosen like the forward's.
 struct BwdPlan {
-    int NP = 16, NT = 2, CH = 64;
+    int NP = 16, NT = 2, W = 4, CH = 32;
+    int stages_f = 2, stages_r = 2;
+    size_t smem_f = 0, smem_r = 0;
     bool tma_raw = false;
     size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, bytes = 0;
 };
 
-BwdPlan plan_bwd(const ssm_shape& s) {
+int bwd_tbuf_floats(int NT, int NP) {
+    const int CW = 32 / NT;
+    return 8 * (CW * NP + 4);
+}
+
+BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
     BwdPlan pl;
     pl.NP = padded_state(s.dstate);
     if (pl.NP < 8) pl.NP = 8;
-    pl.NT = pl.NP <= 16 ? 2 : 4;
-    if (pl.NP == 16 && env_int("SSM_BWD_NT", 0) == 4) pl.NT = 4;
-    pl.CH = kConsumers / pl.NT;
-    pl.tma_raw = (s.seqlen * dtype_bytes(s.in_dtype)) % 16 == 0;
+    const int eb = dtype_bytes(s.in_dtype);
+    pl.tma_raw = (s.seqlen * eb) % 16 == 0;
+    const int nts_all[2] = {2, 4};
+    const int want_nt = env_int("SSM_BWD_NT", 0);
+    const int want_w = env_int("SSM_BWD_W", 0);
+    double best = -1.0;
+    for (int ni = 0; ni < 2; ++ni) {
+        const int NT = nts_all[ni];
+        if (pl.NP == 8 && NT != 2) continue;       // G = NP / NT must be 4, 8 or 16
+        if (pl.NP >= 32 && NT != 4) continue;
+        if (want_nt > 0 && NT != want_nt) continue;
+        for (int W = 1; W <= BwdLayout<2, 16>::kMaxWarps; ++W) {
+            if (want_w > 0 && W != want_w) continue;
+            const int CH = W * 32 / NT;
+            const size_t raw = (size_t)CH * kT * eb, rawf = (size_t)CH * kT * 4;
+            const size_t bcb = (size_t)kT * 2 * pl.NP * 4;
+            const size_t fixed = (size_t)W * pl.NP * kT * 4 + (size_t)W * bwd_tbuf_floats(NT, pl.NP) * 4 + 1024;
+            const size_t stf = 4 * raw + bcb, str = 4 * raw + rawf + bcb;
+            if (2 * str + fixed > (size_t)kMaxSmemPerCta) continue;
+            const int64_t tiles = (s.dim + CH - 1) / CH;
+            const double work = (double)CH * (NT == 4 ? 1.15 : 1.0);
+            const double cost = fwd_launch_cost(s.batch * tiles, sm_count, 1, W, work);
+            if (best < 0.0 || cost < best * 0.999) {
+                best = cost;
+                pl.NT = NT; pl.W = W; pl.CH = CH;
+                int sf = (int)(((size_t)kMaxSmemPerCta - fixed) / stf);
+                int sr = (int)(((size_t)kMaxSmemPerCta - fixed) / str);
+                pl.stages_f = sf > 4 ? 4 : sf;
+                pl.stages_r = sr > 4 ? 4 : sr;
+                pl.smem_f = (size_t)pl.stages_f * stf + fixed;
+                pl.smem_r = (size_t)pl.stages_r * str + fixed;
+            }
+        }
+    }
     size_t off = kHeaderBytes;
     pl.off_bc = off;
     off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
@@ -238,6 +276,9 @@ BwdPlan plan_bwd(const ssm_shape& s) {
     pl.off_hck = off;
     off += align256((size_t)s.batch * s.dim * ((s.seqlen + kT - 1) / kT) * pl.NP * 4);
     pl.bytes = off;
+    if (env_int("SSM_DEBUG_PLAN", 0))
+        std::fprintf(stderr, "ssm bwd plan: NP=%d NT=%d W=%d CH=%d stages=%d/%d smem=%zu/%zu\n",
+                     pl.NP, pl.NT, pl.W, pl.CH, pl.stages_f, pl.stages_r, pl.smem_f, pl.smem_r);
     return pl;
 }
 
@@ -283,13 +324,20 @@ cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, const
     }
 }
 
-cudaError_t launch_bwd(int NP, int NT, int tin, int tout, bool tma, const BwdParams& p,
-                       const BwdMaps& m, dim3 grid, cudaStream_t st) {
-    switch (NP) {
-        case 8: return launch_bwd_np8(NT, tin, tout, tma, p, m, grid, st);
-        case 16: return launch_bwd_np16(NT, tin, tout, tma, p, m, grid, st);
-        case 32: return launch_bwd_np32(NT, tin, tout, tma, p, m, grid, st);
-        default: return launch_bwd_np64(NT, tin, tout, tma, p, m, grid, st);
+cudaError_t launch_bwd(const BwdPlan& pl, int tin, int tout, const BwdParams& p, const BwdMaps& m,
+                       dim3 grid, cudaStream_t st) {
+    BwdLaunch lc;
+    lc.grid = grid;
+    lc.warps = pl.W;
+    lc.stages_f = pl.stages_f;
+    lc.stages_r = pl.stages_r;
+    lc.smem_f = pl.smem_f;
+    lc.smem_r = pl.smem_r;
+    switch (pl.NP) {
+        case 8: return launch_bwd_np8(pl.NT, tin, tout, pl.tma_raw, p, m, lc, st);
+        case 16: return launch_bwd_np16(pl.NT, tin, tout, pl.tma_raw, p, m, lc, st);
+        case 32: return launch_bwd_np32(pl.NT, tin, tout, pl.tma_raw, p, m, lc, st);
+        default: return launch_bwd_np64(pl.NT, tin, tout, pl.tma_raw, p, m, lc, st);
     }
 }
 
@@ -331,7 +379,7 @@ const char* ssm_strerror(int code) {
 
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     if (shape_check(shape) != SSM_OK) return 0;
-    const size_t bytes = for_backward ? plan_bwd(*shape).bytes
+    const size_t bytes = for_backward ? plan_bwd(*shape, device_sm_count()).bytes
                                       : plan_fwd(*shape, device_sm_count()).bytes;
     return bytes < kHeaderBytes ? kHeaderBytes : bytes;
 }
@@ -458,7 +506,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const BwdPlan pl = plan_bwd(s);
+    const BwdPlan pl = plan_bwd(s, device_sm_count());
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
@@ -519,8 +567,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
-    if (launch_bwd(pl.NP, pl.NT, s.in_dtype, s.out_dtype, pl.tma_raw, p, maps, dim3(gx, (unsigned)Bt),
-                   st) != cudaSuccess)
+    if (launch_bwd(pl, s.in_dtype, s.out_dtype, p, maps, dim3(gx, (unsigned)Bt), st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
 }

@@ -43,79 +43,28 @@
 
 namespace ssm {
 
-// tokens per batch of the cross-channel reduction of dB / dC: enough that a
-// lane's batch holds one value per channel lane of the warp
-template <int NP>
-constexpr int red_tokens() { return NP >= 32 ? 1 : 32 / NP; }
-
-template <int NT, int EB, int NP, bool REV>
-constexpr int bwd_stage_bytes() {
-    // raw tiles u, delta_raw, z, dy (+ the fp32 phi tile in the reverse sweep) + B/C
-    return 4 * FwdCfg<NT, EB>::RAW + (REV ? FwdCfg<NT, 4>::RAW : 0) + bc_tile_bytes<NP>();
-}
-
-// per-warp partial sums of dB or dC for one chunk: [4 warps][NP][kT] fp32
-template <int NP>
-constexpr int red_buf_bytes() { return (kConsumers / 32) * NP * kT * 4; }
-
-template <int NT, int EB, int NP, bool REV>
-constexpr int bwd_stages() {
-    return (200 * 1024 - red_buf_bytes<NP>()) / bwd_stage_bytes<NT, EB, NP, REV>() >= 3 &&
-                   3 * bwd_stage_bytes<NT, EB, NP, REV>() + red_buf_bytes<NP>() <= 110 * 1024
-               ? 3
-               : 2;
-}
-
-template <int NT, int EB, int NP, bool REV>
-constexpr int bwd_smem_bytes() {
-    return bwd_stages<NT, EB, NP, REV>() * bwd_stage_bytes<NT, EB, NP, REV>() +
-           red_buf_bytes<NP>() + 1024;
-}
-
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                  ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // Named barrier over the compute warps only (the producer warp never joins).
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+__device__ __forceinline__ void consumers_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Reduce-scatter over the lanes that differ in the bits top_mask,
-// top_mask/2, ... (LEVELS of them): on return v[0, V >> LEVELS) of lane l
-// holds the sums of the entries whose index has as its top LEVELS bits the
-// lane bits (top_mask, top_mask/2, ...) of l, most significant first.
-template <int V, int LEVELS>
-__device__ __forceinline__ void reduce_scatter(float (&v)[V], int lane, int top_mask) {
-#pragma unroll
-    for (int l = 0; l < LEVELS; ++l) {
-        const int mask = top_mask >> l;
-        const int half = V >> (l + 1);
-        const bool upper = (lane & mask) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float keep = upper ? v[i + half] : v[i];
-            const float send = upper ? v[i] : v[i + half];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-    }
-}
-
-// Sum the four warps' partials of one chunk and add them to out[(b*N + n)*L
-// + t0 + t] for n < N, t < nvalid, scaled by `scale`.
+// Sum the W warps' partials of one chunk (red[w][n][t]) and add them to
+// out[(b*N + n)*L + t0 + t] for n < N, t < nvalid, scaled by `scale`.
 template <int NP>
-__device__ __forceinline__ void flush_red(const float* red, float* out, int64_t b, int N,
+__device__ __forceinline__ void flush_red(const float* red, int W, float* out, int64_t b, int N,
                                           int64_t L, int64_t t0, int nvalid, float scale,
-                                          int tid) {
-    constexpr int W = kConsumers / 32;
+                                          int tid, int nthreads) {
     const bool vec = (L % 4) == 0;
-    for (int idx = tid; idx < NP * (kT / 4); idx += kConsumers) {
+    for (int idx = tid; idx < NP * (kT / 4); idx += nthreads) {
         const int n = idx / (kT / 4);
         const int t = (idx % (kT / 4)) * 4;
         if (n >= N || t >= nvalid) continue;
         float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
         for (int w = 0; w < W; ++w) {
             const float4 v = *reinterpret_cast<const float4*>(red + (w * NP + n) * kT + t);
             s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
@@ -131,30 +80,61 @@ __device__ __forceinline__ void flush_red(const float* red, float* out, int64_t 
     }
 }
 
+// Cross-channel sum of one group of 8 tokens through the warp's transpose
+// buffer tb[token][channel][state] (rows padded by 16 bytes): lane tasks are
+// (token, group of 4 states); each sums the CW channels' float4s and writes
+// the 4 sums to the warp's chunk buffer redw[n][t].
+template <int NP, int CW>
+__device__ __forceinline__ void transpose_reduce(const float* tb, float* redw, int t_first, int lane) {
+    constexpr int TROW = BwdLayout<32 / CW, NP>::TROW;
+    constexpr int TASKS = 8 * NP / 4;
+    for (int task = lane; task < TASKS; task += 32) {
+        const int t = task / (NP / 4);
+        const int q = task % (NP / 4);
+        const float* src = tb + t * TROW + q * 4;
+        f2 s01 = pk(0.0f, 0.0f), s23 = pk(0.0f, 0.0f);
+#pragma unroll
+        for (int c = 0; c < CW; ++c) {
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + c * NP);
+            s01 = add2(s01, v.x);
+            s23 = add2(s23, v.y);
+        }
+        float a0, a1, a2, a3;
+        upk(s01, a0, a1);
+        upk(s23, a2, a3);
+        float* o = redw + (q * 4) * kT + t_first + t;
+        o[0] = a0;
+        o[kT] = a1;
+        o[2 * kT] = a2;
+        o[3 * kT] = a3;
+    }
+}
+
 // Issue the loads of one stage (producer warp).  Raw tiles at slots 0..3
-// (u, delta_raw, z, dy), then the optional fp32 tile, then the B/C tile.
-template <typename TIN, int NT, int NP, bool REV, bool TMA_RAW>
+// (u, delta_raw, z, dy) of RAW bytes each, then (reverse sweep) the fp32
+// per-token tile of RAWF bytes, then the B/C tile.
+template <typename TIN, int NP, bool REV, bool TMA_RAW>
 __device__ __forceinline__ void bwd_load_stage(
     uint8_t* st, uint64_t* bar, const BwdParams& p, const CUtensorMap* tm_u,
     const CUtensorMap* tm_dr, const CUtensorMap* tm_z, const CUtensorMap* tm_dy,
     const CUtensorMap* tm_phi, const CUtensorMap* tm_bc, int64_t b, int64_t row0,
-    int64_t rows_valid, int64_t k, bool has_z, int lane) {
-    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
-    using CfgF = FwdCfg<NT, 4>;
-    constexpr int CH = Cfg::CH;
-    constexpr int RAW = Cfg::RAW;
+    int64_t rows_valid, int64_t k, bool has_z, int lane, int CH) {
+    constexpr int EB = (int)sizeof(TIN);
+    constexpr int BOXES = kT * EB / 128, BOX_T = 128 / EB;
+    const int RAW = CH * kT * EB;
+    const int RAWF = CH * kT * 4;
     constexpr int BCB = bc_tile_bytes<NP>();
     const int64_t L = p.L;
     const int32_t t0 = (int32_t)(k * kT);
     uint8_t* phi_dst = st + 4 * RAW;
-    uint8_t* bc_dst = st + 4 * RAW + (REV ? CfgF::RAW : 0);
+    uint8_t* bc_dst = st + 4 * RAW + (REV ? RAWF : 0);
     if (TMA_RAW) {
         if (lane == 0) {
-            const uint32_t bytes = (has_z ? 4 : 3) * RAW + (REV ? CfgF::RAW : 0) + BCB;
+            const uint32_t bytes = (has_z ? 4 : 3) * RAW + (REV ? RAWF : 0) + BCB;
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-            for (int bx = 0; bx < Cfg::BOXES; ++bx) {
-                const int32_t x = t0 + bx * Cfg::BOX_T;
+            for (int bx = 0; bx < BOXES; ++bx) {
+                const int32_t x = t0 + bx * BOX_T;
                 tma_load_2d(st + bx * CH * 128, tm_u, bar, x, (int32_t)row0);
                 tma_load_2d(st + RAW + bx * CH * 128, tm_dr, bar, x, (int32_t)row0);
                 if (has_z) tma_load_2d(st + 2 * RAW + bx * CH * 128, tm_z, bar, x, (int32_t)row0);
@@ -162,18 +142,17 @@ __device__ __forceinline__ void bwd_load_stage(
             }
             if (REV) {
 #pragma unroll
-                for (int bx = 0; bx < CfgF::BOXES; ++bx)
-                    tma_load_2d(phi_dst + bx * CH * 128, tm_phi, bar, t0 + bx * CfgF::BOX_T,
-                                (int32_t)row0);
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_2d(phi_dst + bx * CH * 128, tm_phi, bar, t0 + bx * 32, (int32_t)row0);
             }
             tma_load_2d(bc_dst, tm_bc, bar, 0, (int32_t)(b * L + t0));
         }
     } else {
-        fill_raw_tile<TIN, CH>(st, p.u, row0, rows_valid, L, t0, lane);
-        fill_raw_tile<TIN, CH>(st + RAW, p.dr, row0, rows_valid, L, t0, lane);
-        if (has_z) fill_raw_tile<TIN, CH>(st + 2 * RAW, p.z, row0, rows_valid, L, t0, lane);
-        fill_raw_tile<TIN, CH>(st + 3 * RAW, p.dy, row0, rows_valid, L, t0, lane);
-        if (REV) fill_raw_tile<float, CH>(phi_dst, p.phi, row0, rows_valid, L, t0, lane);
+        fill_raw_tile_r<TIN>(st, CH, p.u, row0, rows_valid, L, t0, lane);
+        fill_raw_tile_r<TIN>(st + RAW, CH, p.dr, row0, rows_valid, L, t0, lane);
+        if (has_z) fill_raw_tile_r<TIN>(st + 2 * RAW, CH, p.z, row0, rows_valid, L, t0, lane);
+        fill_raw_tile_r<TIN>(st + 3 * RAW, CH, p.dy, row0, rows_valid, L, t0, lane);
+        if (REV) fill_raw_tile_r<float>(phi_dst, CH, p.phi, row0, rows_valid, L, t0, lane);
         __syncwarp();
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, BCB);
@@ -183,15 +162,15 @@ __device__ __forceinline__ void bwd_load_stage(
 }
 
 // Producer warp: stream the chunks (forward or reverse order) through the
-// ring.  Returns false if a bounded wait expired (status already set).
-template <typename TIN, int NT, int NP, bool REV, bool TMA_RAW, int STAGES, int STAGE>
-__device__ __forceinline__ void bwd_producer(uint8_t* smem, uint64_t* full_bar, uint64_t* empty_bar,
+// ring.  Gives up (status set) if a bounded wait expires.
+template <typename TIN, int NP, bool REV, bool TMA_RAW>
+__device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAGE,
+                                             uint64_t* full_bar, uint64_t* empty_bar,
                                              const BwdParams& p, const CUtensorMap* tm_u,
                                              const CUtensorMap* tm_dr, const CUtensorMap* tm_z,
                                              const CUtensorMap* tm_dy, const CUtensorMap* tm_phi,
                                              const CUtensorMap* tm_bc, int64_t b, int64_t d0,
-                                             bool has_z, int lane) {
-    constexpr int CH = FwdCfg<NT, (int)sizeof(TIN)>::CH;
+                                             bool has_z, int lane, int CH) {
     if (lane == 0) {
         prefetch_tmap(tm_bc);
         if (TMA_RAW) {
@@ -218,28 +197,27 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, uint64_t* full_bar, 
                 return;
             }
         }
-        bwd_load_stage<TIN, NT, NP, REV, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr,
-                                                  tm_z, tm_dy, tm_phi, tm_bc, b, row0,
-                                                  rows_valid, k, has_z, lane);
+        bwd_load_stage<TIN, NP, REV, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr, tm_z,
+                                              tm_dy, tm_phi, tm_bc, b, row0, rows_valid, k, has_z,
+                                              lane, CH);
     }
 }
 
-// Per-token quantities of this lane's 8 tokens.
 // Per-token quantities the chain loop needs for this lane's 8 tokens:
 // delta2 = delta / ln2, delta2 * u and g = dy * silu(z) (dy without a gate).
 // Tokens past the end, and channels past D (whose tile rows belong to the
 // next batch row), get zeros and so contribute nothing.
-template <typename TIN, int CH, bool ACCURATE>
-__device__ __forceinline__ void token_prep(const uint8_t* st, int c, int tb, int nvalid,
+template <typename TIN, bool ACCURATE>
+__device__ __forceinline__ void token_prep(const uint8_t* st, int CH, int c, int tb, int nvalid,
                                            bool has_z, bool ch_ok, float bias2, float (&d2)[8],
                                            float (&du)[8], float (&gq)[8]) {
-    constexpr int RAW = CH * kT * (int)sizeof(TIN);
+    const int RAW = CH * kT * (int)sizeof(TIN);
     float uv[8], dv[8], gy[8];
-    load_raw8<TIN, CH>(st, c, tb, uv);
-    load_raw8<TIN, CH>(st + RAW, c, tb, dv);
-    load_raw8<TIN, CH>(st + 3 * RAW, c, tb, gy);
+    load_raw8r<TIN>(st, CH, c, tb, uv);
+    load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
+    load_raw8r<TIN>(st + 3 * RAW, CH, c, tb, gy);
     float zv[8];
-    if (has_z) load_raw8<TIN, CH>(st + 2 * RAW, c, tb, zv);
+    if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb, zv);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         d2[q] = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
@@ -262,49 +240,51 @@ __device__ __forceinline__ void allreduce_nt(float (&v)[V]) {
         for (int q = 0; q < V; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
 }
 
-// Cross-channel reduction of one batch of TB tokens (partials rb[tok * G +
-// s] of this lane's G states) into the warp's slice of the chunk buffer.
-template <int NP, int NT, int G, int TB>
-__device__ __forceinline__ void reduce_batch_to_smem(float (&rb)[TB * G], float* red, int warp,
-                                                     int lane, int g, int t_first) {
-    constexpr int RV = TB * G;
-    constexpr int CL = 32 / NT;
-    constexpr int LV = (CL == 32 ? 5 : CL == 16 ? 4 : CL == 8 ? 3 : CL == 4 ? 2 : CL == 2 ? 1 : 0);
-    static_assert(RV >= CL, "reduction batch");
-    reduce_scatter<RV, LV>(rb, lane, 16);
-    const int cw = lane / NT;
+// Store the G partials of one token into the transpose buffer slot.
+template <int G>
+__device__ __forceinline__ void put_tr(float* slot, const f2 (&v)[G / 2]) {
 #pragma unroll
-    for (int r = 0; r < RV / CL; ++r) {
-        const int idx = cw * (RV / CL) + r;
-        red[(warp * NP + g * G + idx % G) * kT + t_first + idx / G] = rb[r];
+    for (int j = 0; j < G / 4; ++j) {
+        float a, bb, cc, dd;
+        upk(v[2 * j], a, bb);
+        upk(v[2 * j + 1], cc, dd);
+        *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(a, bb, cc, dd);
     }
 }
 
 // ===================================================== forward sweep ===
+// blockDim.x = 32 * (W + 1): W compute warps and one producer warp (the last).
 template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
                const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_bc) {
-    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
-    constexpr int G = NP / NT;
-    constexpr int CH = Cfg::CH;
-    constexpr int SB = Cfg::SB;
-    constexpr int RAW = Cfg::RAW;
-    constexpr int STAGE = bwd_stage_bytes<NT, (int)sizeof(TIN), NP, false>();
-    constexpr int STAGES = bwd_stages<NT, (int)sizeof(TIN), NP, false>();
-    constexpr bool ACCURATE = sizeof(TIN) == 4;
-    constexpr int TB = red_tokens<NP>();          // tokens per dC reduction batch
+    using Lay = BwdLayout<NT, NP>;
+    constexpr int G = Lay::G;
+    constexpr int CW = Lay::CW;
+    constexpr int SB = Lay::SB;
+    constexpr int EB = (int)sizeof(TIN);
+    constexpr int BCB = bc_tile_bytes<NP>();
+    constexpr bool ACCURATE = EB == 4;
     static_assert(G % 4 == 0 && G <= 16, "states per thread");
-    static_assert(8 % TB == 0, "reduction batches within a token group");
+
+    const int W = (int)(blockDim.x / 32) - 1;
+    const int CH = W * CW;
+    const int RAW = CH * kT * EB;
+    const int STAGE = 4 * RAW + BCB;
+    const int STAGES = p.stages;
+    const int NTH = 32 * W;
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    float* trb = red + W * NP * kT;
+    __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CH;
     const int64_t L = p.L;
@@ -314,27 +294,28 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], kConsumers / 32);
+            mbar_init(&empty_bar[s], W);
         }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (tid >= kConsumers) {
-        bwd_producer<TIN, NT, NP, false, TMA_RAW, STAGES, STAGE>(
-            smem, full_bar, empty_bar, p, &tm_u, &tm_dr, &tm_z, &tm_dy, nullptr, &tm_bc, b, d0,
-            has_z, tid - kConsumers);
+    if (warp == W) {
+        bwd_producer<TIN, NP, false, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, p, &tm_u,
+                                              &tm_dr, &tm_z, &tm_dy, nullptr, &tm_bc, b, d0, has_z,
+                                              lane, CH);
         return;
     }
 
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int c = tid / NT;
-    const int g = tid % NT;
+    const int cw = lane / NT;
+    const int g = lane % NT;
+    const int c = warp * CW + cw;
     const int64_t d = d0 + c;
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
+    float* redw = red + warp * NP * kT;
+    float* tb = trb + warp * Lay::TBUF;
 
     f2 Ap[G / 2], h[G / 2], m[G / 2], dAc[G / 2];
 #pragma unroll
@@ -377,9 +358,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll 1
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (dead || sb * SB >= nvalid) break;
-            const int tb = sb * SB + g * 8;    // this lane's 8 tokens
+            const int tbk = sb * SB + g * 8;   // this lane's 8 tokens
             float d2[8], du[8], gq[8];
-            token_prep<TIN, CH, ACCURATE>(st, c, tb, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
 
             float ys_own[8], ph_own[8];        // sums over n of this lane's tokens
 #pragma unroll 1
@@ -394,12 +375,12 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
                 const int t_grp = sb * SB + j * 8;
                 float yp[8], pp[8];
-                float rb[TB * G];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
                     const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
                     f2 accy = pk(0.0f, 0.0f), accp = pk(0.0f, 0.0f);
+                    f2 gh[G / 2];
 #pragma unroll
                     for (int q4 = 0; q4 < G / 4; ++q4) {
                         const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
@@ -417,21 +398,18 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             accy = fma2(Cj, h[jj], accy);
                             accp = fma2(Ap[jj], mul2(Cj, qv), accp);
                             dAc[jj] = fma2(mul2(gqp, Cj), m[jj], dAc[jj]);
-                            float lo, hi;
-                            upk(mul2(gqp, h[jj]), lo, hi);           // g_t h_t: dC partial
-                            rb[(q % TB) * G + 2 * jj] = lo;
-                            rb[(q % TB) * G + 2 * jj + 1] = hi;
+                            gh[jj] = mul2(gqp, h[jj]);               // g_t h_t: dC partial
                         }
                     }
+                    put_tr<G>(tb + q * Lay::TROW + cw * NP + g * G, gh);
                     float lo, hi;
                     upk(accy, lo, hi);
                     yp[q] = lo + hi;
                     upk(accp, lo, hi);
                     pp[q] = lo + hi;
-                    if ((q % TB) == TB - 1)
-                        reduce_batch_to_smem<NP, NT, G, TB>(rb, red, warp, lane, g,
-                                                            t_grp + q - (TB - 1));
                 }
+                __syncwarp();
+                transpose_reduce<NP, CW>(tb, redw, t_grp, lane);
                 allreduce_nt<NT, 8>(yp);
                 allreduce_nt<NT, 8>(pp);
                 if (j == g) {
@@ -441,14 +419,14 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                         ph_own[q] = pp[q];
                     }
                 }
+                __syncwarp();   // the transpose buffer is reused by the next group
             }
 
             // this lane's tokens: dz and phi
-            constexpr int RAWB = CH * kT * (int)sizeof(TIN);
             float uv[8], gy[8], zv[8];
-            load_raw8<TIN, CH>(st, c, tb, uv);
-            load_raw8<TIN, CH>(st + 3 * RAWB, c, tb, gy);
-            if (has_z) load_raw8<TIN, CH>(st + 2 * RAWB, c, tb, zv);
+            load_raw8r<TIN>(st, CH, c, tbk, uv);
+            load_raw8r<TIN>(st + 3 * RAW, CH, c, tbk, gy);
+            if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tbk, zv);
             float dzv[8], phv[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -462,9 +440,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 phv[q] = gq[q] * ph_own[q];
             }
             if (ch_ok) {
-                const int64_t off = row * L + k * kT + tb;
-                if (p.dz) store_out8<TOUT>(p.dz, off, dzv, nvalid - tb, vec_out);
-                store_out8<float>(p.phi, off, phv, nvalid - tb, vec_phi);
+                const int64_t off = row * L + k * kT + tbk;
+                if (p.dz) store_out8<TOUT>(p.dz, off, dzv, nvalid - tbk, vec_out);
+                store_out8<float>(p.phi, off, phv, nvalid - tbk, vec_phi);
             }
         }
         if (!dead && ch_ok && k + 1 < nchunks) {
@@ -481,9 +459,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         }
         __syncwarp();
         if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
-        consumers_sync();
-        if (!dead) flush_red<NP>(red, p.dC, b, N, L, k * kT, nvalid, 1.0f, tid);
-        consumers_sync();
+        consumers_sync(NTH);
+        if (!dead) flush_red<NP>(red, W, p.dC, b, N, L, k * kT, nvalid, 1.0f, tid, NTH);
+        consumers_sync(NTH);
     }
 
     if (ch_ok && !dead) {
@@ -506,31 +484,38 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 
 // ===================================================== reverse sweep ===
 template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
                const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_phi,
                const __grid_constant__ CUtensorMap tm_bc) {
-    using Cfg = FwdCfg<NT, (int)sizeof(TIN)>;
-    using CfgF = FwdCfg<NT, 4>;
-    constexpr int G = NP / NT;
-    constexpr int CH = Cfg::CH;
-    constexpr int SB = Cfg::SB;
-    constexpr int RAW = Cfg::RAW;
-    constexpr int STAGE = bwd_stage_bytes<NT, (int)sizeof(TIN), NP, true>();
-    constexpr int STAGES = bwd_stages<NT, (int)sizeof(TIN), NP, true>();
-    constexpr bool ACCURATE = sizeof(TIN) == 4;
-    constexpr int TB = red_tokens<NP>();
+    using Lay = BwdLayout<NT, NP>;
+    constexpr int G = Lay::G;
+    constexpr int CW = Lay::CW;
+    constexpr int SB = Lay::SB;
+    constexpr int EB = (int)sizeof(TIN);
+    constexpr int BCB = bc_tile_bytes<NP>();
+    constexpr bool ACCURATE = EB == 4;
     static_assert(G % 4 == 0 && G <= 16, "states per thread");
-    static_assert(8 % TB == 0, "reduction batches within a token group");
+
+    const int W = (int)(blockDim.x / 32) - 1;
+    const int CH = W * CW;
+    const int RAW = CH * kT * EB;
+    const int RAWF = CH * kT * 4;
+    const int STAGE = 4 * RAW + RAWF + BCB;
+    const int STAGES = p.stages;
+    const int NTH = 32 * W;
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    float* trb = red + W * NP * kT;
+    __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CH;
     const int64_t L = p.L;
@@ -540,27 +525,28 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], kConsumers / 32);
+            mbar_init(&empty_bar[s], W);
         }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (tid >= kConsumers) {
-        bwd_producer<TIN, NT, NP, true, TMA_RAW, STAGES, STAGE>(
-            smem, full_bar, empty_bar, p, &tm_u, &tm_dr, &tm_z, &tm_dy, &tm_phi, &tm_bc, b, d0,
-            has_z, tid - kConsumers);
+    if (warp == W) {
+        bwd_producer<TIN, NP, true, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, p, &tm_u,
+                                             &tm_dr, &tm_z, &tm_dy, &tm_phi, &tm_bc, b, d0, has_z,
+                                             lane, CH);
         return;
     }
 
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int c = tid / NT;
-    const int g = tid % NT;
+    const int cw = lane / NT;
+    const int g = lane % NT;
+    const int c = warp * CW + cw;
     const int64_t d = d0 + c;
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
+    float* redw = red + warp * NP * kT;
+    float* tb = trb + warp * Lay::TBUF;
 
     // lambda starts at dhL, the decay "after the last token" is 1, and
     // psi = sum_n A dhL h_L starts the suffix sum
@@ -604,16 +590,16 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         }
         const uint8_t* st = smem + s * STAGE;
         const uint8_t* phit = st + 4 * RAW;
-        const float* bct = reinterpret_cast<const float*>(st + 4 * RAW + CfgF::RAW);
+        const float* bct = reinterpret_cast<const float*>(st + 4 * RAW + RAWF);
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
 
 #pragma unroll 1
         for (int sb = kT / SB - 1; sb >= 0; --sb) {
             if (dead) break;
             if (sb * SB >= nvalid) continue;
-            const int tb = sb * SB + g * 8;
+            const int tbk = sb * SB + g * 8;
             float d2[8], du[8], gq[8];
-            token_prep<TIN, CH, ACCURATE>(st, c, tb, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
 
             float sb_own[8], sab_own[8];       // sum_n lambda B', sum_n A a_{t+1} lambda_{t+1} B'
 #pragma unroll 1
@@ -628,12 +614,12 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
                 const int t_grp = sb * SB + j * 8;
                 float bp[8], abp[8];
-                float rb[TB * G];
 #pragma unroll
                 for (int q = 7; q >= 0; --q) {
                     const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
                     const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
                     f2 accb = pk(0.0f, 0.0f), accab = pk(0.0f, 0.0f);
+                    f2 ld[G / 2];
 #pragma unroll
                     for (int q4 = 0; q4 < G / 4; ++q4) {
                         const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
@@ -647,22 +633,20 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             lam[jj] = fma2(anext[jj], lam[jj], mul2(gqp, Cj));
                             accb = add2(accb, mul2(lam[jj], Bj));
                             accab = fma2(Ap[jj], mul2(al, Bj), accab);
-                            float lo, hi;
-                            upk(mul2(lam[jj], dup), lo, hi);         // dB partial / ln2
-                            rb[(q % TB) * G + 2 * jj] = lo;
-                            rb[(q % TB) * G + 2 * jj + 1] = hi;
+                            ld[jj] = mul2(lam[jj], dup);              // dB partial / ln2
                             const f2 arg = mul2(d2p, Ap[jj]);
                             anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
                         }
                     }
+                    put_tr<G>(tb + q * Lay::TROW + cw * NP + g * G, ld);
                     float lo, hi;
                     upk(accb, lo, hi);
                     bp[q] = lo + hi;
                     upk(accab, lo, hi);
                     abp[q] = lo + hi;
-                    if ((q % TB) == 0)
-                        reduce_batch_to_smem<NP, NT, G, TB>(rb, red, warp, lane, g, t_grp + q);
                 }
+                __syncwarp();
+                transpose_reduce<NP, CW>(tb, redw, t_grp, lane);
                 allreduce_nt<NT, 8>(bp);
                 allreduce_nt<NT, 8>(abp);
                 if (j == g) {
@@ -672,15 +656,16 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                         sab_own[q] = abp[q];
                     }
                 }
+                __syncwarp();   // the transpose buffer is reused by the next group
             }
 
             // suffix sums of w = phi - rho over this lane's tokens, then over
             // the later lanes of the channel, then the later super-blocks
-            constexpr int RAWB = CH * kT * (int)sizeof(TIN);
+            const int RAWB = RAW;
             float phv[8], uv[8], dv[8];
-            load_raw8<float, CH>(phit, c, tb, phv);
-            load_raw8<TIN, CH>(st, c, tb, uv);
-            load_raw8<TIN, CH>(st + RAWB, c, tb, dv);
+            load_raw8r<float>(phit, CH, c, tbk, phv);
+            load_raw8r<TIN>(st, CH, c, tbk, uv);
+            load_raw8r<TIN>(st + RAWB, CH, c, tbk, dv);
             float suf[8];
             float run = 0.0f;
 #pragma unroll
@@ -703,16 +688,16 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 const float sx = rcp(1.0f + ex2(-fmaf(dv[q], kLog2e, bias2)));  // d softplus / dx
                 ddv[q] = dd * sx;
                 duv[q] = fmaf(gq[q], Dd, d2[q] * sb_own[q]);
-                if (tb + q < nvalid) {
+                if (tbk + q < nvalid) {
                     dD_acc = fmaf(gq[q], uv[q], dD_acc);
                     db_acc += ddv[q];
                 }
             }
             carry += total;
             if (ch_ok) {
-                const int64_t off = row * L + k * kT + tb;
-                store_out8<TOUT>(p.du, off, duv, nvalid - tb, vec_out);
-                store_out8<TOUT>(p.ddr, off, ddv, nvalid - tb, vec_out);
+                const int64_t off = row * L + k * kT + tbk;
+                store_out8<TOUT>(p.du, off, duv, nvalid - tbk, vec_out);
+                store_out8<TOUT>(p.ddr, off, ddv, nvalid - tbk, vec_out);
             }
         }
         if (k > 0) {
@@ -742,9 +727,9 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         }
         __syncwarp();
         if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
-        consumers_sync();
-        if (!dead) flush_red<NP>(red, p.dB, b, N, L, k * kT, nvalid, kLn2, tid);
-        consumers_sync();
+        consumers_sync(NTH);
+        if (!dead) flush_red<NP>(red, W, p.dB, b, N, L, k * kT, nvalid, kLn2, tid, NTH);
+        consumers_sync(NTH);
     }
 
 #pragma unroll

@@ -4,9 +4,9 @@
 namespace ssm {
 
 cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
-                             const BwdMaps& m, dim3 grid, cudaStream_t st) {
+                             const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st) {
     switch (NT) {
-        case 4: return launch_bwd_nt<64, 4>(tin, tout, tma, p, m, grid, st);
+        case 4: return launch_bwd_nt<64, 4>(tin, tout, tma, p, m, lc, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -29,15 +29,6 @@
 
 namespace ssm {
 
-template <int NT, int EB>
-struct FwdCfg {
-    static constexpr int CH = kConsumers / NT;       // channels per CTA
-    static constexpr int SB = 8 * NT;                // tokens per super-block
-    static constexpr int RAW = CH * kT * EB;         // bytes of one raw tile
-    static constexpr int BOXES = kT * EB / 128;      // 128-byte TMA boxes per tile row
-    static constexpr int BOX_T = 128 / EB;           // tokens per box
-};
-
 template <int NP>
 constexpr int bc_tile_bytes() { return kT * 2 * NP * 4; }
 

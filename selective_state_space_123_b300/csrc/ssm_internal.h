@@ -44,16 +44,25 @@ struct BwdMaps {
     CUtensorMap u, dr, z, dy, phi, bc;
 };
 
+// Launch shape of one backward call: grid, compute warps per CTA, ring
+// depths and dynamic shared memory of the two sweeps.
+struct BwdLaunch {
+    dim3 grid;
+    int warps;
+    int stages_f, stages_r;
+    size_t smem_f, smem_r;
+};
+
 // Backward (forward sweep, then reverse sweep) for padded state size NP
 // (8, 16, 32, 64) and NT threads per channel.
 cudaError_t launch_bwd_np8(int NT, int tin, int tout, bool tma, const BwdParams& p,
-                           const BwdMaps& m, dim3 grid, cudaStream_t st);
+                           const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 cudaError_t launch_bwd_np16(int NT, int tin, int tout, bool tma, const BwdParams& p,
-                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+                            const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 cudaError_t launch_bwd_np32(int NT, int tin, int tout, bool tma, const BwdParams& p,
-                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+                            const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
-                            const BwdMaps& m, dim3 grid, cudaStream_t st);
+                            const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);

@@ -9,8 +9,6 @@
 namespace ssm {
 
 constexpr int kT = 64;              // tokens per chunk (one TMA tile along L)
-constexpr int kConsumers = 128;     // compute threads per CTA (4 warps)
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
 // Forward-kernel layout per NT (threads per channel).  Per compute warp an
@@ -59,6 +57,19 @@ struct FwdParams {
     uint64_t timeout_ns;
 };
 
+// Backward-kernel layout per (NT, NP): per compute warp a transpose buffer
+// of 8 tokens x CW channels x NP states (token rows padded by 16 bytes) for
+// the cross-channel sums of dB and dC.
+template <int NT, int NP>
+struct BwdLayout {
+    static constexpr int CW = 32 / NT;             // channels per compute warp
+    static constexpr int G = NP / NT;              // states per lane
+    static constexpr int SB = 8 * NT;              // tokens per super-block
+    static constexpr int TROW = CW * NP + 4;       // floats per token row of the transpose buffer
+    static constexpr int TBUF = 8 * TROW;          // floats per warp
+    static constexpr int kMaxWarps = 7;            // compute warps per CTA at most
+};
+
 // Backward parameters (both sweeps).
 struct BwdParams {
     int64_t Bt, D, L;
@@ -85,6 +96,7 @@ struct BwdParams {
     float* dD;              // nullable, accumulated (zeroed by the host)
     float* dbias;           // nullable, accumulated (zeroed by the host)
     float* dh0;             // nullable
+    int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
     int* status;
     uint64_t timeout_ns;
 };
