@@ -248,7 +248,7 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
             const int CH = W * 32 / NT;
             const size_t raw = (size_t)CH * kT * eb, rawf = (size_t)CH * kT * 4;
             const size_t bcb = (size_t)kT * 2 * pl.NP * 4;
-            const size_t fixed = (size_t)W * pl.NP * kT * 4 + (size_t)W * bwd_tbuf_floats(NT, pl.NP) * 4 + 1024;
+            const size_t fixed = (size_t)2 * W * pl.NP * kT * 4 + (size_t)W * bwd_tbuf_floats(NT, pl.NP) * 4 + 1024;
             const size_t stf = 4 * raw + bcb, str = 4 * raw + rawf + bcb;
             if (2 * str + fixed > (size_t)kMaxSmemPerCta) continue;
             const int64_t tiles = (s.dim + CH - 1) / CH;

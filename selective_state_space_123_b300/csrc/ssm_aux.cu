@@ -200,6 +200,324 @@ __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     }
 }
 
+// Pipelined step for state sizes that are a multiple of 4 (the usual case):
+// each of the 256 threads owns one 16-byte quad of states of one channel per
+// tile of 256 / (N/4) channels; tiles are taken grid-stride and the states of
+// the next kStepDepth tiles are already on their way into shared memory
+// (cp.async, 16 bytes per thread, no registers held), so each SM keeps
+// ~kStepDepth * 4 KB * CTAs of state loads in flight.  The per-channel inputs
+// of the next tile are loaded one tile ahead into registers.
+constexpr int kStepDepth = 6;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory"); }
+
+template <typename TIN, typename TOUT, int QPR>
+__global__ void __launch_bounds__(256) step_pipe_kernel(const StepParams p) {
+    constexpr int RPT = 256 / QPR;                    // channels (rows) per tile
+    __shared__ __align__(16) float4 ring[kStepDepth][256];
+    const int tid = threadIdx.x;
+    const int N = p.N;                                // = 4 * QPR
+    const int64_t rows = p.Bt * p.D;
+    const int64_t ntiles = (rows + RPT - 1) / RPT;
+    const int k = tid % QPR;                          // this thread's quad of the row
+    const int lr = tid / QPR;                         // row within the tile
+    const TIN* u = static_cast<const TIN*>(p.u);
+    const TIN* dr = static_cast<const TIN*>(p.dr);
+    const TIN* zz = static_cast<const TIN*>(p.z);
+    const TIN* Bv = static_cast<const TIN*>(p.B);
+    const TIN* Cv = static_cast<const TIN*>(p.C);
+
+    auto issue = [&](int64_t tile, int slot) {
+        const int64_t r = tile * RPT + lr;
+        const bool valid = tile < ntiles && r < rows;
+        cp_async16(smem_u32(&ring[slot][tid]), p.state + (valid ? r : 0) * N + 4 * k, valid);
+        // the tile's per-channel inputs (u, delta_raw, z: one line each) are
+        // pulled into L2 as far ahead as its states
+        if (tid < 3 && tile < ntiles) {
+            const TIN* src = tid == 0 ? u : tid == 1 ? dr : zz;
+            if (src) prefetch_l2(src + tile * RPT);
+        }
+    };
+    // per-row inputs of one tile, loaded into registers one tile ahead
+    struct Row {
+        float u, x2, z, a[4], b[4], c[4], dd, bias;
+    };
+    auto load_row = [&](int64_t tile, Row& w) {
+        const int64_t r0 = tile * RPT + lr;
+        const bool valid = tile < ntiles && r0 < rows;
+        const int64_t r = valid ? r0 : 0;
+        const int64_t b = r / p.D, d = r % p.D;
+        w.u = Elem<TIN>::to_f(u[r]);
+        w.bias = p.bias ? p.bias[d] : 0.0f;
+        w.x2 = Elem<TIN>::to_f(dr[r]);
+        w.z = zz ? Elem<TIN>::to_f(zz[r]) : 0.0f;
+        w.dd = p.Dv ? p.Dv[d] : 0.0f;
+        const float4 a4 = *reinterpret_cast<const float4*>(p.A + d * N + 4 * k);
+        w.a[0] = a4.x; w.a[1] = a4.y; w.a[2] = a4.z; w.a[3] = a4.w;
+        load_vec4_in<TIN>(Bv + b * N + 4 * k, w.b);
+        load_vec4_in<TIN>(Cv + b * N + 4 * k, w.c);
+    };
+
+    int64_t tile = blockIdx.x;
+#pragma unroll
+    for (int j = 0; j < kStepDepth; ++j) {
+        issue(tile + (int64_t)j * gridDim.x, j);
+        cp_async_commit();
+    }
+    Row cur, nxt;
+    load_row(tile, cur);
+    for (int jt = 0; tile < ntiles; ++jt, tile += gridDim.x) {
+        const int slot = jt % kStepDepth;
+        // refill the slot read in the previous iteration (long complete) with
+        // the tile kStepDepth - 1 ahead; one commit per iteration keeps the
+        // group count regular, so waiting for all but the newest
+        // kStepDepth - 1 groups guarantees this tile has landed
+        if (jt > 0)
+            issue(tile + (int64_t)(kStepDepth - 1) * gridDim.x, (jt - 1) % kStepDepth);
+        cp_async_commit();
+        load_row(tile + gridDim.x, nxt);
+        cp_async_wait<kStepDepth - 1>();
+        const float4 h4 = ring[slot][tid];            // this thread's own 16 bytes
+
+        const int64_t r = tile * RPT + lr;
+        const bool ok = r < rows;
+        const float x = fmaf(cur.x2, kLog2e, cur.bias * kLog2e);
+        float d2;
+        if (sizeof(TIN) == 4) {
+            const float e = ex2(-fabsf(x));
+            float q = fmaf(e, 0.2f, -0.25f);
+            q = fmaf(e, q, 0.33333334f);
+            q = fmaf(e, q, -0.5f);
+            q = fmaf(e, q, 1.0f);
+            d2 = fmaxf(x, 0.0f) + (e < 0.0625f ? e * q * kLog2e : lg2(1.0f + e));
+        } else {
+            d2 = fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
+        }
+        const float du = d2 * cur.u * kLn2;   // delta * u
+        float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+        float acc = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float a = sizeof(TIN) == 4 ? exp2_accurate(d2 * cur.a[q]) : ex2(d2 * cur.a[q]);
+            hv[q] = fmaf(a, hv[q], du * cur.b[q]);
+            acc = fmaf(cur.c[q], hv[q], acc);
+        }
+        if (ok) *reinterpret_cast<float4*>(p.state + r * N + 4 * k) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+#pragma unroll
+        for (int o = 1; o < QPR; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (ok && k == 0) {
+            float v = fmaf(cur.dd, cur.u, acc);
+            if (p.z) v *= cur.z * rcp(1.0f + ex2(-kLog2e * cur.z));
+            if (sizeof(TOUT) == 2)
+                static_cast<__nv_bfloat16*>(p.y)[r] = __float2bfloat16_rn(v);
+            else
+                static_cast<float*>(p.y)[r] = v;
+        }
+        cur = nxt;
+    }
+    cp_async_wait<0>();
+}
+
+// Streaming step for 64-channel tiles (D a multiple of 64 so a tile lies in
+// one batch row; N a multiple of 4, N <= 32).  One producer warp moves
+// everything a tile needs into an 8-slot shared-memory ring with bulk copies
+// -- the states (64 * N * 4 bytes), u, delta_raw and z of the 64 channels,
+// their rows of A, their bias and D skip, and the batch row's B and C -- so
+// the 8 consumer warps issue no global load at all: thread (row, quad) owns
+// 16 bytes of state, updates them and stores them straight back.  Tiles are
+// taken grid-stride.
+constexpr int kStepRows = 64;
+constexpr int kStepSlots = 8;
+
+template <typename TIN, int QPR>
+struct StepSlot {
+    float4 st[kStepRows * QPR];               // states
+    float4 a[kStepRows * QPR];                // rows of A
+    float bias[kStepRows], dsk[kStepRows];    // delta bias, D skip
+    TIN in[3][kStepRows];                     // u, delta_raw, z
+    TIN bc[2][32];                            // B, C of the batch row (N <= 32)
+};
+
+template <typename TIN, typename TOUT, int QPR>
+__global__ void __launch_bounds__(32 * (8 * QPR / 4 + 1), 1) step_tma_kernel(const StepParams p) {
+    constexpr int CONS = kStepRows * QPR;     // consumer threads (one 16-byte quad each)
+    constexpr int NW = CONS / 32;             // consumer warps
+    constexpr int N = 4 * QPR;
+    extern __shared__ uint8_t smem_dyn[];
+    StepSlot<TIN, QPR>* ring = reinterpret_cast<StepSlot<TIN, QPR>*>(align_smem_1024(smem_dyn));
+    __shared__ __align__(8) uint64_t full_bar[kStepSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kStepSlots];
+    const int tid = threadIdx.x;
+    const int rows = (int)(p.Bt * p.D);       // < 2^31 (checked by the caller)
+    const int D = (int)p.D;
+    const int ntiles = rows / kStepRows;
+    if (tid == 0) {
+        for (int s = 0; s < kStepSlots; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const TIN* zz = static_cast<const TIN*>(p.z);
+
+    if (tid >= CONS) {                        // ---------------- producer warp
+        if (tid != CONS) return;
+        const TIN* u = static_cast<const TIN*>(p.u);
+        const TIN* dr = static_cast<const TIN*>(p.dr);
+        const TIN* Bv = static_cast<const TIN*>(p.B);
+        const TIN* Cv = static_cast<const TIN*>(p.C);
+        int j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            const int s = j % kStepSlots;
+            if (j >= kStepSlots &&
+                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kStepSlots) - 1) & 1), kDefaultTimeoutNs))
+                return;                       // the consumers time out on their own waits
+            const int r0 = tile * kStepRows;
+            const int b = r0 / D, d0 = r0 - b * D;
+            constexpr uint32_t sb = kStepRows * N * 4, ib = kStepRows * sizeof(TIN);
+            constexpr uint32_t fb = kStepRows * 4, bcb = N * sizeof(TIN) < 16 ? 16 : N * sizeof(TIN);
+            const uint32_t bytes = 2 * sb + (zz ? 3 : 2) * ib + (p.bias ? fb : 0) + (p.Dv ? fb : 0) +
+                                   2 * bcb;
+            mbar_arrive_expect_tx(&full_bar[s], bytes);
+            bulk_load(ring[s].st, p.state + (size_t)r0 * N, sb, &full_bar[s]);
+            bulk_load(ring[s].a, p.A + (size_t)d0 * N, sb, &full_bar[s]);
+            bulk_load(ring[s].in[0], u + r0, ib, &full_bar[s]);
+            bulk_load(ring[s].in[1], dr + r0, ib, &full_bar[s]);
+            if (zz) bulk_load(ring[s].in[2], zz + r0, ib, &full_bar[s]);
+            if (p.bias) bulk_load(ring[s].bias, p.bias + d0, fb, &full_bar[s]);
+            if (p.Dv) bulk_load(ring[s].dsk, p.Dv + d0, fb, &full_bar[s]);
+            bulk_load(ring[s].bc[0], Bv + (size_t)b * N, bcb, &full_bar[s]);
+            bulk_load(ring[s].bc[1], Cv + (size_t)b * N, bcb, &full_bar[s]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int lane = tid & 31;
+    const int k = tid % QPR;                  // quad of the row
+    const int lr = tid / QPR;                 // row of the tile
+    int j = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        const int s = j % kStepSlots;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((j / kStepSlots) & 1), kDefaultTimeoutNs)))
+            return;                           // bounded wait expired: nothing more is written
+        const StepSlot<TIN, QPR>& sl = ring[s];
+        const float4 h4 = sl.st[tid];
+        const float4 a4 = sl.a[tid];
+        float bq[4], cq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            bq[q] = Elem<TIN>::to_f(sl.bc[0][4 * k + q]);
+            cq[q] = Elem<TIN>::to_f(sl.bc[1][4 * k + q]);
+        }
+        const float uu = Elem<TIN>::to_f(sl.in[0][lr]);
+        const float dv = Elem<TIN>::to_f(sl.in[1][lr]);
+        const float zv = zz ? Elem<TIN>::to_f(sl.in[2][lr]) : 0.0f;
+        const float bias = p.bias ? sl.bias[lr] : 0.0f;
+        const float Dd = p.Dv ? sl.dsk[lr] : 0.0f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);   // the slot's contents are in registers
+
+        const float x = fmaf(dv, kLog2e, bias * kLog2e);
+        float d2;
+        if (sizeof(TIN) == 4) {
+            const float e = ex2(-fabsf(x));
+            float q = fmaf(e, 0.2f, -0.25f);
+            q = fmaf(e, q, 0.33333334f);
+            q = fmaf(e, q, -0.5f);
+            q = fmaf(e, q, 1.0f);
+            d2 = fmaxf(x, 0.0f) + (e < 0.0625f ? e * q * kLog2e : lg2(1.0f + e));
+        } else {
+            d2 = fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
+        }
+        const float du = d2 * uu * kLn2;   // delta * u
+        float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        float acc = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float a = sizeof(TIN) == 4 ? exp2_accurate(d2 * av[q]) : ex2(d2 * av[q]);
+            hv[q] = fmaf(a, hv[q], du * bq[q]);
+            acc = fmaf(cq[q], hv[q], acc);
+        }
+        const int r = tile * kStepRows + lr;
+        *reinterpret_cast<float4*>(p.state + (size_t)r * N + 4 * k) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+#pragma unroll
+        for (int o = 1; o < QPR; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (k == 0) {
+            float v = fmaf(Dd, uu, acc);
+            if (zz) v *= zv * rcp(1.0f + ex2(-kLog2e * zv));
+            if (sizeof(TOUT) == 2)
+                static_cast<__nv_bfloat16*>(p.y)[r] = __float2bfloat16_rn(v);
+            else
+                static_cast<float*>(p.y)[r] = v;
+        }
+    }
+}
+
+template <typename TIN, typename TOUT, int QPR>
+static cudaError_t launch_step_tma(const StepParams& p, cudaStream_t st) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    auto kern = step_tma_kernel<TIN, TOUT, QPR>;
+    const size_t smem = kStepSlots * sizeof(StepSlot<TIN, QPR>) + 1024;
+    static bool attr[64] = {};
+    static int per_sm[64] = {};
+    if (dev >= 0 && dev < 64 && !attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, 32 * (8 * QPR / 4 + 1), smem) !=
+                cudaSuccess || nb < 1)
+            nb = 1;
+        cudaGetLastError();
+        per_sm[dev] = nb;
+        attr[dev] = true;
+    }
+    const int nb = (dev >= 0 && dev < 64) ? per_sm[dev] : 1;
+    const int64_t ntiles = p.Bt * p.D / kStepRows;
+    int64_t grid = (int64_t)sms * nb;
+    if (grid > ntiles) grid = ntiles;
+    kern<<<(unsigned)grid, 32 * (8 * QPR / 4 + 1), smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TIN, typename TOUT, int QPR>
+static cudaError_t launch_step_pipe(const StepParams& p, cudaStream_t st) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    const int64_t rows = p.Bt * p.D;
+    const int64_t ntiles = (rows + (256 / QPR) - 1) / (256 / QPR);
+    static int per_sm[64] = {};
+    if (dev >= 0 && dev < 64 && per_sm[dev] == 0) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_pipe_kernel<TIN, TOUT, QPR>, 256, 0) !=
+                cudaSuccess || nb < 1)
+            nb = 4;
+        cudaGetLastError();
+        per_sm[dev] = nb;
+    }
+    const int nb = (dev >= 0 && dev < 64) ? per_sm[dev] : 4;
+    int64_t grid = (int64_t)sms * nb;                 // every CTA resident at once
+    if (grid > ntiles) grid = ntiles;
+    step_pipe_kernel<TIN, TOUT, QPR><<<(unsigned)grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename TIN, typename TOUT, int S, int GT>
 static cudaError_t launch_step_s(const StepParams& p, cudaStream_t st) {
     const int64_t threads = p.Bt * p.D * GT;
@@ -210,8 +528,19 @@ static cudaError_t launch_step_s(const StepParams& p, cudaStream_t st) {
 
 template <typename TIN, typename TOUT>
 static cudaError_t launch_step_t(const StepParams& p, cudaStream_t st) {
-    // S states per thread (a multiple of 4 when N allows vector loads), GT
-    // threads per channel (a power of two, for the shuffle reduction)
+    // state sizes that are a multiple of 4 (up to 32) take the pipelined kernel
+    // whole 64-channel tiles inside one batch row: the bulk-copy stream
+    if (p.D % kStepRows == 0 && p.Bt * p.D < (int64_t(1) << 31)) {
+        if (p.N == 16) return launch_step_tma<TIN, TOUT, 4>(p, st);
+        if (p.N == 8) return launch_step_tma<TIN, TOUT, 2>(p, st);
+        if (p.N == 32) return launch_step_tma<TIN, TOUT, 8>(p, st);
+    }
+    if (p.N == 16) return launch_step_pipe<TIN, TOUT, 4>(p, st);
+    if (p.N == 8) return launch_step_pipe<TIN, TOUT, 2>(p, st);
+    if (p.N == 32) return launch_step_pipe<TIN, TOUT, 8>(p, st);
+    if (p.N == 4) return launch_step_pipe<TIN, TOUT, 1>(p, st);
+    // otherwise: S states per thread (a multiple of 4 when N allows vector
+    // loads), GT threads per channel (a power of two, for the shuffle reduction)
     if (p.N <= 4) return launch_step_s<TIN, TOUT, 4, 1>(p, st);
     if (p.N <= 8) return launch_step_s<TIN, TOUT, 8, 1>(p, st);
     if (p.N <= 16) return launch_step_s<TIN, TOUT, 16, 1>(p, st);

@@ -48,11 +48,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// Named barrier over the compute warps only (the producer warp never joins).
-__device__ __forceinline__ void consumers_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
 // Sum the W warps' partials of one chunk (red[w][n][t]) and add them to
 // out[(b*N + n)*L + t0 + t] for n < N, t < nvalid, scaled by `scale`.
 template <int NP>
@@ -162,10 +157,16 @@ __device__ __forceinline__ void bwd_load_stage(
 }
 
 // Producer warp: stream the chunks (forward or reverse order) through the
-// ring.  Gives up (status set) if a bounded wait expires.
+// ring, and add each finished chunk's cross-channel sums (the W warps'
+// slices of the double-buffered chunk buffer) to `out` with vector atomics:
+// the flush of chunk i-1 follows the loads of chunk i, so the compute warps
+// never wait for it and never meet at a CTA barrier.  Gives up (status set)
+// if a bounded wait expires.
 template <typename TIN, int NP, bool REV, bool TMA_RAW>
 __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAGE,
                                              uint64_t* full_bar, uint64_t* empty_bar,
+                                             uint64_t* rfull, uint64_t* rempty, const float* red,
+                                             int W, float* out, float scale,
                                              const BwdParams& p, const CUtensorMap* tm_u,
                                              const CUtensorMap* tm_dr, const CUtensorMap* tm_z,
                                              const CUtensorMap* tm_dy, const CUtensorMap* tm_phi,
@@ -181,9 +182,26 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
             if (REV) prefetch_tmap(tm_phi);
         }
     }
-    const int64_t nchunks = (p.L + kT - 1) / kT;
+    const int64_t L = p.L;
+    const int64_t nchunks = (L + kT - 1) / kT;
     const int64_t row0 = b * p.D + d0;
     const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
+    const int N = p.N;
+    // flush of the chunk processed i-th: wait until all W warps wrote their
+    // slices, add them up, then hand the buffer back to the compute warps
+    auto flush = [&](int64_t i) -> bool {
+        const int buf = (int)(i & 1);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&rfull[buf], (uint32_t)((i >> 1) & 1), p.timeout_ns);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        const int64_t k = REV ? nchunks - 1 - i : i;
+        const int nvalid = (int)min((int64_t)kT, L - k * kT);
+        flush_red<NP>(red + (size_t)buf * W * NP * kT, W, out, b, N, L, k * kT, nvalid, scale, lane, 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[buf]);
+        return true;
+    };
     for (int64_t i = 0; i < nchunks; ++i) {
         const int64_t k = REV ? nchunks - 1 - i : i;
         const int s = (int)(i % STAGES);
@@ -200,6 +218,13 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
         bwd_load_stage<TIN, NP, REV, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr, tm_z,
                                               tm_dy, tm_phi, tm_bc, b, row0, rows_valid, k, has_z,
                                               lane, CH);
+        if (i >= 1 && !flush(i - 1)) {
+            if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+            return;
+        }
+    }
+    if (nchunks >= 1 && !flush(nchunks - 1)) {
+        if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
     }
 }
 
@@ -273,14 +298,15 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int RAW = CH * kT * EB;
     const int STAGE = 4 * RAW + BCB;
     const int STAGES = p.stages;
-    const int NTH = 32 * W;
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
-    float* trb = red + W * NP * kT;
+    float* trb = red + 2 * W * NP * kT;                // after the two chunk buffers
     __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t rfull[2];     // chunk buffer written by all W warps
+    __shared__ __align__(8) uint64_t rempty[2];    // chunk buffer added up by the producer
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -296,14 +322,18 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], W);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&rfull[s], W);
+            mbar_init(&rempty[s], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == W) {
-        bwd_producer<TIN, NP, false, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, p, &tm_u,
-                                              &tm_dr, &tm_z, &tm_dy, nullptr, &tm_bc, b, d0, has_z,
-                                              lane, CH);
+        bwd_producer<TIN, NP, false, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, rfull, rempty,
+                                              red, W, p.dC, 1.0f, p, &tm_u, &tm_dr, &tm_z, &tm_dy,
+                                              nullptr, &tm_bc, b, d0, has_z, lane, CH);
         return;
     }
 
@@ -314,7 +344,6 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
-    float* redw = red + warp * NP * kT;
     float* tb = trb + warp * Lay::TBUF;
 
     f2 Ap[G / 2], h[G / 2], m[G / 2], dAc[G / 2];
@@ -338,8 +367,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const bool vec_phi = (L % 4) == 0;
     const int src_base = lane & ~(NT - 1);
 
-    // A warp whose bounded wait expires records the error and stops working,
-    // but keeps joining the named barriers so the other warps never hang.
+    // A warp whose bounded wait expires records the error and stops working.
     bool dead = false;
     for (int64_t k = 0; k < nchunks; ++k) {
         const int s = (int)(k % STAGES);
@@ -354,6 +382,17 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const uint8_t* st = smem + s * STAGE;
         const float* bct = reinterpret_cast<const float*>(st + 4 * RAW);
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
+        // this chunk's cross-channel sums go to chunk buffer (k & 1), free once
+        // the producer has added up the chunk processed two before
+        const int rb = (int)(k & 1);
+        if (!dead && k >= 2) {
+            const bool okr = __all_sync(0xffffffffu, mbar_wait(&rempty[rb], (uint32_t)(((k >> 1) - 1) & 1), p.timeout_ns));
+            if (!okr) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        float* redw = red + ((size_t)rb * W + warp) * NP * kT;
 
 #pragma unroll 1
         for (int sb = 0; sb < kT / SB; ++sb) {
@@ -458,10 +497,10 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
         }
         __syncwarp();
-        if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
-        consumers_sync(NTH);
-        if (!dead) flush_red<NP>(red, W, p.dC, b, N, L, k * kT, nvalid, 1.0f, tid, NTH);
-        consumers_sync(NTH);
+        if (lane == 0 && !dead) {
+            mbar_arrive(&empty_bar[s]);
+            mbar_arrive(&rfull[rb]);
+        }
     }
 
     if (ch_ok && !dead) {
@@ -504,14 +543,15 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int RAWF = CH * kT * 4;
     const int STAGE = 4 * RAW + RAWF + BCB;
     const int STAGES = p.stages;
-    const int NTH = 32 * W;
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = align_smem_1024(smem_dyn);
     float* red = reinterpret_cast<float*>(smem + STAGES * STAGE);
-    float* trb = red + W * NP * kT;
+    float* trb = red + 2 * W * NP * kT;                // after the two chunk buffers
     __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t rfull[2];     // chunk buffer written by all W warps
+    __shared__ __align__(8) uint64_t rempty[2];    // chunk buffer added up by the producer
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -527,14 +567,18 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], W);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&rfull[s], W);
+            mbar_init(&rempty[s], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == W) {
-        bwd_producer<TIN, NP, true, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, p, &tm_u,
-                                             &tm_dr, &tm_z, &tm_dy, &tm_phi, &tm_bc, b, d0, has_z,
-                                             lane, CH);
+        bwd_producer<TIN, NP, true, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, rfull, rempty,
+                                              red, W, p.dB, kLn2, p, &tm_u, &tm_dr, &tm_z, &tm_dy,
+                                              &tm_phi, &tm_bc, b, d0, has_z, lane, CH);
         return;
     }
 
@@ -545,7 +589,6 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
-    float* redw = red + warp * NP * kT;
     float* tb = trb + warp * Lay::TBUF;
 
     // lambda starts at dhL, the decay "after the last token" is 1, and
@@ -592,6 +635,17 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const uint8_t* phit = st + 4 * RAW;
         const float* bct = reinterpret_cast<const float*>(st + 4 * RAW + RAWF);
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
+        // this chunk's cross-channel sums go to chunk buffer (i & 1), free once
+        // the producer has added up the chunk processed two before
+        const int rb = (int)(i & 1);
+        if (!dead && i >= 2) {
+            const bool okr = __all_sync(0xffffffffu, mbar_wait(&rempty[rb], (uint32_t)(((i >> 1) - 1) & 1), p.timeout_ns));
+            if (!okr) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        float* redw = red + ((size_t)rb * W + warp) * NP * kT;
 
 #pragma unroll 1
         for (int sb = kT / SB - 1; sb >= 0; --sb) {
@@ -726,10 +780,10 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             carry = part;
         }
         __syncwarp();
-        if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
-        consumers_sync(NTH);
-        if (!dead) flush_red<NP>(red, W, p.dB, b, N, L, k * kT, nvalid, kLn2, tid, NTH);
-        consumers_sync(NTH);
+        if (lane == 0 && !dead) {
+            mbar_arrive(&empty_bar[s]);
+            mbar_arrive(&rfull[rb]);
+        }
     }
 
 #pragma unroll
