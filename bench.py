@@ -67,6 +67,33 @@ SMS = 148
 L2_BYTES = 126 * 1024 * 1024
 
 
+# dram traffic per launch of a kernel, from an ncu capture recorded in
+# profiles/traffic.json together with a hash of the kernel's sources; it is
+# reported only while those sources are unchanged
+KERNEL_SOURCES = {
+    "fwd_kernel": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu"],
+    "bwd": ["ssm_bwd.cuh", "ssm_bwd_launch.cuh", "ssm_bwd_np16.cu"],
+    "step_kernel": ["ssm_aux.cu"],
+}
+
+
+def kernel_source_hash(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "selective_state_space_123_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind, workload):
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kind + ":" + workload]
+    except Exception:
+        return None
+    return rec["bytes_per_launch"] if rec.get("src_hash") == kernel_source_hash(kind) else None
+
+
 def load_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -473,9 +500,14 @@ def run_ours(args):
         "frac_of_roofline_time": max(t_hbm, t_sfu) / t_s,
         "algorithmic_bytes": wl.bytes,
         "exps": wl.exps,
-        "traffic": None,
+        "traffic": recorded_traffic({"fwd": "fwd_kernel", "fwdbwd": "bwd", "step": "step_kernel"}[wl.mode],
+                                    w["name"]),
+        "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
+                        "kernel (ncu, profiles/traffic.json); null when the kernel changed since",
+        "fp32_ops_per_update": 4,
         "timing_note": "achieved uses the whole step's CUDA-event time, which includes the small "
-                       "B/C preparation kernel",
+                       "B/C preparation kernel; 32 ex2/clk/SM equals the FP32 pipe's rate at the "
+                       "4 FP32 operations an update needs, so the SFU bound is also the FP32 bound",
     }
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
