@@ -177,8 +177,10 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 // Forward kernel.  blockDim.x = 32 * (W + 1): W compute warps and one
 // producer warp (the last).  A CTA owns CH = W * 32 / NT channels of one
 // batch row for one segment of the sequence.  Per super-block of SB = 8 * NT
-// tokens each lane computes softplus and delta * u of all SB tokens of its
-// channel, runs the recurrence over them for its G = NP / NT states, writes
+// tokens each lane computes softplus and delta * u of its own 8 tokens and
+// gathers the channel's other tokens from its NT - 1 partner lanes by
+// shuffles, runs the recurrence over the SB tokens for its G = NP / NT
+// states, writes
 // its per-token partial read-outs to the warp's exchange buffer, and then
 // finishes its own 8 tokens (sum over the NT lanes, D skip, SiLU gate,
 // store).  All exchange stays inside the warp.
@@ -298,6 +300,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t row = b * p.D + d;
     const int N = p.N;
     float* xy = xy_all + warp * Lay::XY_FLOATS;   // this warp's exchange buffer
+    const int src_base = lane & ~(NT - 1);         // lane g = 0 of this channel
 
     f2 Ap[G / 2], h[G / 2];
 #pragma unroll
@@ -343,22 +346,30 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (sb * SB >= nvalid) break;
 
-            // 1. every lane of the channel computes delta2 = softplus / ln2 and
-            //    delta2 * u for all SB tokens itself: the recurrence then reads
-            //    them from registers (recomputing is cheaper than an exchange
-            //    through shared memory at the head of every token)
+            // 1. each lane computes delta2 = softplus / ln2 and delta2 * u of its
+            //    own 8 tokens, then gathers all SB tokens of the channel from
+            //    the NT lanes with shuffles (one softplus per token)
+            const int tb = sb * SB + g * TPL;
+            float u8[8];
             float d2[SB], du[SB];
-#pragma unroll
-            for (int k8 = 0; k8 < SB / 8; ++k8) {
-                float dv[8], u8[8];
-                load_raw8r<TIN>(st, CH, c, sb * SB + 8 * k8, u8);
-                load_raw8r<TIN>(st + RAW, CH, c, sb * SB + 8 * k8, dv);
+            {
+                float dv[8], d2o[8], duo[8];
+                load_raw8r<TIN>(st, CH, c, tb, u8);
+                load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float dd = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
-                    if (sb * SB + 8 * k8 + q >= nvalid) dd = 0.0f;
-                    d2[8 * k8 + q] = dd;
-                    du[8 * k8 + q] = dd * u8[q];
+                    if (tb + q >= nvalid) dd = 0.0f;
+                    d2o[q] = dd;
+                    duo[q] = dd * u8[q];
+                }
+#pragma unroll
+                for (int jj = 0; jj < NT; ++jj) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        d2[8 * jj + q] = NT == 1 ? d2o[q] : __shfl_sync(0xffffffffu, d2o[q], src_base + jj);
+                        du[8 * jj + q] = NT == 1 ? duo[q] : __shfl_sync(0xffffffffu, duo[q], src_base + jj);
+                    }
                 }
             }
             if (SUMMARY) {
@@ -375,7 +386,6 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
 
             if (!SUMMARY) {
                 // 3. partial read-outs through the buffer; finish the own tokens
-                const int tb = sb * SB + g * TPL;
                 float* yb = xy + cw * Lay::YROW;
 #pragma unroll
                 for (int q = 0; q < SB; q += 4)
@@ -392,8 +402,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                         yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
                         yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
                     }
-                    float zv[8], u8[8];
-                    load_raw8r<TIN>(st, CH, c, tb + 8 * k8, u8);
+                    float zv[8];
                     if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb + 8 * k8, zv);
                     float out[8];
 #pragma unroll
