@@ -313,6 +313,21 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
     return r == CUDA_SUCCESS;
 }
 
+// rows x 16 fp32 (64-byte rows), box 16 x 128, 64-byte swizzle: the decode
+// step's state and A tiles
+bool make_map_swz64(CUtensorMap* m, const void* base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {16, rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {16, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, const FwdParams& p,
                        const FwdMaps& m, dim3 grid, cudaStream_t st) {
     switch (pl.NP) {
@@ -589,6 +604,16 @@ int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, 
     p.Bt = batch; p.D = dim; p.N = (int)dstate;
     p.u = u; p.dr = delta_raw; p.z = z; p.A = A; p.Dv = D; p.bias = delta_bias;
     p.B = B; p.C = C; p.state = state; p.y = y;
+    if (dstate == 16 && dim % 128 == 0 && bd < (int64_t(1) << 31)) {
+        // whole 128-channel tiles: the state and A stream through 2-D TMA tiles
+        CUtensorMap tm_st, tm_a;
+        if (!make_map_swz64(&tm_st, state, (uint64_t)bd) || !make_map_swz64(&tm_a, A, (uint64_t)dim))
+            return cuda_fail();
+        if (launch_step_dec16_any(in_dtype, out_dtype, p, tm_st, tm_a, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
     if (launch_step(in_dtype, out_dtype, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;

@@ -153,17 +153,7 @@ __global__ void __launch_bounds__(256) step_kernel(const StepParams p) {
     }
     const float uu = Elem<TIN>::to_f(u[r]);
     const float x = fmaf(Elem<TIN>::to_f(dr[r]), kLog2e, p.bias ? p.bias[d] * kLog2e : 0.0f);
-    float d2;
-    if (sizeof(TIN) == 4) {
-        const float e = ex2(-fabsf(x));
-        float q = fmaf(e, 0.2f, -0.25f);
-        q = fmaf(e, q, 0.33333334f);
-        q = fmaf(e, q, -0.5f);
-        q = fmaf(e, q, 1.0f);
-        d2 = fmaxf(x, 0.0f) + (e < 0.0625f ? e * q * kLog2e : lg2(1.0f + e));
-    } else {
-        d2 = fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
-    }
+    const float d2 = softplus2<sizeof(TIN) == 4>(x);
     const float du = d2 * uu * kLn2;   // delta * u
 
     float acc = 0.0f;
@@ -291,17 +281,7 @@ __global__ void __launch_bounds__(256) step_pipe_kernel(const StepParams p) {
         const int64_t r = tile * RPT + lr;
         const bool ok = r < rows;
         const float x = fmaf(cur.x2, kLog2e, cur.bias * kLog2e);
-        float d2;
-        if (sizeof(TIN) == 4) {
-            const float e = ex2(-fabsf(x));
-            float q = fmaf(e, 0.2f, -0.25f);
-            q = fmaf(e, q, 0.33333334f);
-            q = fmaf(e, q, -0.5f);
-            q = fmaf(e, q, 1.0f);
-            d2 = fmaxf(x, 0.0f) + (e < 0.0625f ? e * q * kLog2e : lg2(1.0f + e));
-        } else {
-            d2 = fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
-        }
+        const float d2 = softplus2<sizeof(TIN) == 4>(x);
         const float du = d2 * cur.u * kLn2;   // delta * u
         float hv[4] = {h4.x, h4.y, h4.z, h4.w};
         float acc = 0.0f;
@@ -429,17 +409,7 @@ __global__ void __launch_bounds__(32 * (8 * QPR / 4 + 1), 1) step_tma_kernel(con
         if (lane == 0) mbar_arrive(&empty_bar[s]);   // the slot's contents are in registers
 
         const float x = fmaf(dv, kLog2e, bias * kLog2e);
-        float d2;
-        if (sizeof(TIN) == 4) {
-            const float e = ex2(-fabsf(x));
-            float q = fmaf(e, 0.2f, -0.25f);
-            q = fmaf(e, q, 0.33333334f);
-            q = fmaf(e, q, -0.5f);
-            q = fmaf(e, q, 1.0f);
-            d2 = fmaxf(x, 0.0f) + (e < 0.0625f ? e * q * kLog2e : lg2(1.0f + e));
-        } else {
-            d2 = fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
-        }
+        const float d2 = softplus2<sizeof(TIN) == 4>(x);
         const float du = d2 * uu * kLn2;   // delta * u
         float hv[4] = {h4.x, h4.y, h4.z, h4.w};
         const float av[4] = {a4.x, a4.y, a4.z, a4.w};
@@ -492,6 +462,199 @@ static cudaError_t launch_step_tma(const StepParams& p, cudaStream_t st) {
     if (grid > ntiles) grid = ntiles;
     kern<<<(unsigned)grid, 32 * (8 * QPR / 4 + 1), smem, st>>>(p);
     return cudaGetLastError();
+}
+
+// Decode step for N = 16 and D a multiple of 128: one thread per channel.
+// A producer warp moves each 128-channel tile into a ring of 6 slots (5 for
+// fp32 inputs, so that two CTAs still fit on an SM): the states and the rows
+// of A as 2-D TMA tiles with the 64-byte swizzle (a thread reads its 64-byte
+// row as four 16-byte chunks; the swizzle spreads the 32 lanes' chunks over
+// all banks), u, delta_raw, z, bias, D skip and the batch row's B and C as
+// bulk copies.  4 consumer warps do the per-channel work once per channel
+// and write the new states into the slot in place; one thread then stores
+// the tile with a TMA tile store (whole 32-byte sectors, where per-thread
+// stores of 64-byte rows would write half sectors) and releases the slot
+// once that store has read it.
+constexpr int kDecRows = 128;
+template <typename TIN>
+constexpr int dec_slots() { return sizeof(TIN) == 2 ? 6 : 5; }
+
+template <typename TIN>
+struct __align__(1024) DecSlot {
+    float st[kDecRows * 16];                  // 64-byte rows, 64-byte swizzle
+    float a[kDecRows * 16];
+    float bias[kDecRows], dsk[kDecRows];
+    TIN in[3][kDecRows];                      // u, delta_raw, z
+    TIN bc[2][16];                            // B, C of the batch row
+};
+
+// 16-byte chunk q of row r of a 64-byte-row tile written by TMA with the
+// 64-byte swizzle (chunk bits XOR address bits 7-8, i.e. (r >> 1) & 3)
+__device__ __forceinline__ float4 ld_swz64(const float* tile, int r, int q) {
+    return *reinterpret_cast<const float4*>(tile + r * 16 + 4 * (q ^ ((r >> 1) & 3)));
+}
+
+template <typename TIN, typename TOUT>
+__global__ void __launch_bounds__(160, 2) step_dec16_kernel(const StepParams p,
+                                                           const __grid_constant__ CUtensorMap tm_st,
+                                                           const __grid_constant__ CUtensorMap tm_a) {
+    extern __shared__ uint8_t smem_dyn[];
+    constexpr int kDecSlots = dec_slots<TIN>();
+    DecSlot<TIN>* ring = reinterpret_cast<DecSlot<TIN>*>(align_smem_1024(smem_dyn));
+    __shared__ __align__(8) uint64_t full_bar[kDecSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kDecSlots];
+    __shared__ int dead;                      // a consumer warp's wait expired
+    const int tid = threadIdx.x;
+    const int rows = (int)(p.Bt * p.D);       // < 2^31 (checked by the caller)
+    const int D = (int)p.D;
+    const int ntiles = rows / kDecRows;
+    if (tid == 0) {
+        for (int s = 0; s < kDecSlots; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        dead = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const TIN* zz = static_cast<const TIN*>(p.z);
+
+    if (tid >= 128) {                         // ---------------- producer warp
+        if (tid != 128) return;
+        prefetch_tmap(&tm_st);
+        prefetch_tmap(&tm_a);
+        const TIN* u = static_cast<const TIN*>(p.u);
+        const TIN* dr = static_cast<const TIN*>(p.dr);
+        const TIN* Bv = static_cast<const TIN*>(p.B);
+        const TIN* Cv = static_cast<const TIN*>(p.C);
+        int j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            const int s = j % kDecSlots;
+            if (j >= kDecSlots &&
+                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kDecSlots) - 1) & 1), kDefaultTimeoutNs))
+                return;                       // the consumers time out on their own waits
+            const int r0 = tile * kDecRows;
+            const int b = r0 / D, d0 = r0 - b * D;
+            constexpr uint32_t tb = kDecRows * 64, ib = kDecRows * sizeof(TIN), fb = kDecRows * 4;
+            constexpr uint32_t bcb = 16 * sizeof(TIN);
+            const uint32_t bytes = 2 * tb + (zz ? 3 : 2) * ib + (p.bias ? fb : 0) + (p.Dv ? fb : 0) + 2 * bcb;
+            DecSlot<TIN>& sl = ring[s];
+            mbar_arrive_expect_tx(&full_bar[s], bytes);
+            tma_load_2d(sl.st, &tm_st, &full_bar[s], 0, r0);
+            tma_load_2d(sl.a, &tm_a, &full_bar[s], 0, d0);
+            bulk_load(sl.in[0], u + r0, ib, &full_bar[s]);
+            bulk_load(sl.in[1], dr + r0, ib, &full_bar[s]);
+            if (zz) bulk_load(sl.in[2], zz + r0, ib, &full_bar[s]);
+            if (p.bias) bulk_load(sl.bias, p.bias + d0, fb, &full_bar[s]);
+            if (p.Dv) bulk_load(sl.dsk, p.Dv + d0, fb, &full_bar[s]);
+            bulk_load(sl.bc[0], Bv + (size_t)b * 16, bcb, &full_bar[s]);
+            bulk_load(sl.bc[1], Cv + (size_t)b * 16, bcb, &full_bar[s]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    // Every consumer warp reaches the per-tile barrier even when its wait
+    // expired, so that the barrier always completes; the flag then ends the
+    // loop for all of them.
+    int j = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        const int s = j % kDecSlots;
+        DecSlot<TIN>& sl = ring[s];
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((j / kDecSlots) & 1), kDefaultTimeoutNs))) {
+            dead = 1;
+            named_bar_sync(1, 128);
+            break;
+        }
+        float hv[16], av[16], bq[16], cq[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 h4 = ld_swz64(sl.st, tid, q);
+            const float4 a4 = ld_swz64(sl.a, tid, q);
+            hv[4 * q] = h4.x; hv[4 * q + 1] = h4.y; hv[4 * q + 2] = h4.z; hv[4 * q + 3] = h4.w;
+            av[4 * q] = a4.x; av[4 * q + 1] = a4.y; av[4 * q + 2] = a4.z; av[4 * q + 3] = a4.w;
+            float t4[4];
+            load_vec4_in<TIN>(&sl.bc[0][4 * q], t4);
+            bq[4 * q] = t4[0]; bq[4 * q + 1] = t4[1]; bq[4 * q + 2] = t4[2]; bq[4 * q + 3] = t4[3];
+            load_vec4_in<TIN>(&sl.bc[1][4 * q], t4);
+            cq[4 * q] = t4[0]; cq[4 * q + 1] = t4[1]; cq[4 * q + 2] = t4[2]; cq[4 * q + 3] = t4[3];
+        }
+        const float uu = Elem<TIN>::to_f(sl.in[0][tid]);
+        const float dv = Elem<TIN>::to_f(sl.in[1][tid]);
+        const float zv = zz ? Elem<TIN>::to_f(sl.in[2][tid]) : 0.0f;
+        const float bias = p.bias ? sl.bias[tid] : 0.0f;
+        const float Dd = p.Dv ? sl.dsk[tid] : 0.0f;
+
+        const float x = fmaf(dv, kLog2e, bias * kLog2e);
+        const float d2 = softplus2<sizeof(TIN) == 4>(x);
+        const float du = d2 * uu * kLn2;   // delta * u
+        float acc = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float a = sizeof(TIN) == 4 ? exp2_accurate(d2 * av[q]) : ex2(d2 * av[q]);
+            hv[q] = fmaf(a, hv[q], du * bq[q]);
+            acc = fmaf(cq[q], hv[q], acc);
+        }
+        const int r = tile * kDecRows + tid;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(sl.st + tid * 16 + 4 * (q ^ ((tid >> 1) & 3))) =
+                make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+        fence_proxy_async();
+        named_bar_sync(1, 128);
+        if (dead) break;
+        if (tid == 0) {
+            tma_store_2d(&tm_st, sl.st, 0, tile * kDecRows);
+            bulk_commit();
+            bulk_wait_read<1>();              // the previous tile's store has read its slot
+            if (j > 0) mbar_arrive(&empty_bar[(j - 1) % kDecSlots]);
+        }
+        float v = fmaf(Dd, uu, acc);
+        if (zz) v *= zv * rcp(1.0f + ex2(-kLog2e * zv));
+        if (sizeof(TOUT) == 2)
+            static_cast<__nv_bfloat16*>(p.y)[r] = __float2bfloat16_rn(v);
+        else
+            static_cast<float*>(p.y)[r] = v;
+    }
+    if (tid == 0) bulk_wait<0>();             // the tile stores finish before the CTA exits
+}
+
+template <typename TIN, typename TOUT>
+static cudaError_t launch_step_dec16(const StepParams& p, const CUtensorMap& tm_st,
+                                     const CUtensorMap& tm_a, cudaStream_t st) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    auto kern = step_dec16_kernel<TIN, TOUT>;
+    const size_t smem = dec_slots<TIN>() * sizeof(DecSlot<TIN>) + 1024;
+    static bool attr[64] = {};
+    static int per_sm[64] = {};
+    if (dev >= 0 && dev < 64 && !attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, 160, smem) != cudaSuccess || nb < 1)
+            nb = 1;
+        cudaGetLastError();
+        per_sm[dev] = nb;
+        attr[dev] = true;
+    }
+    const int nb = (dev >= 0 && dev < 64) ? per_sm[dev] : 1;
+    const int64_t ntiles = p.Bt * p.D / kDecRows;
+    int64_t grid = (int64_t)sms * nb;
+    if (grid > ntiles) grid = ntiles;
+    kern<<<(unsigned)grid, 160, smem, st>>>(p, tm_st, tm_a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_step_dec16_any(int tin, int tout, const StepParams& p, const CUtensorMap& tm_st,
+                                  const CUtensorMap& tm_a, cudaStream_t st) {
+    if (tin == SSM_BF16)
+        return tout == SSM_BF16 ? launch_step_dec16<__nv_bfloat16, __nv_bfloat16>(p, tm_st, tm_a, st)
+                                : launch_step_dec16<__nv_bfloat16, float>(p, tm_st, tm_a, st);
+    return tout == SSM_BF16 ? launch_step_dec16<float, __nv_bfloat16>(p, tm_st, tm_a, st)
+                            : launch_step_dec16<float, float>(p, tm_st, tm_a, st);
 }
 
 template <typename TIN, typename TOUT, int QPR>

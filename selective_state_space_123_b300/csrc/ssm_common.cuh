@@ -95,6 +95,31 @@ __device__ __forceinline__ f2 exp2_accurate_x2(f2 x) {
     return pk(exp2_accurate(lo), exp2_accurate(hi));
 }
 
+// softplus in log2 units: for x = (delta_raw + bias) * log2(e) return
+// log2(1 + 2^x) = delta / ln 2.
+//  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), where for 2^-|x| <
+//  1/16 the logarithm is its Taylor series to the fifth power (relative
+//  truncation error < 2e-7) instead of the MUFU lg2, whose absolute error
+//  near 1 would dominate small results.
+//  fast (bf16 inputs): max(x, lg2(1 + 2^min(x, 64))); the absolute error of
+//  lg2 near 1 (~1e-7) is far below the bf16 tolerance.
+template <bool ACCURATE>
+__device__ __forceinline__ float softplus2(float x) {
+    if (ACCURATE) {
+        const float e = ex2(-fabsf(x));
+        float p = fmaf(e, 0.2f, -0.25f);
+        p = fmaf(e, p, 0.33333334f);
+        p = fmaf(e, p, -0.5f);
+        p = fmaf(e, p, 1.0f);
+        const float series = e * p * kLog2e;
+        const float direct = lg2(1.0f + e);
+        return fmaxf(x, 0.0f) + (e < 0.0625f ? series : direct);
+    } else {
+        return fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
+    }
+}
+
+
 // ------------------------------------------------------- element types ---
 template <typename T> struct Elem;
 template <> struct Elem<float> {
@@ -189,6 +214,35 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(smem_dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+// 2-D tiled store of box {x, y} from shared memory (bulk-group completion).
+// The writing threads order their shared-memory stores before it with
+// fence_proxy_async() and a barrier.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t x,
+                                             int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(tmap), "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N committed bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until at most N committed bulk groups are incomplete (writes visible)
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA)
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// named barrier `id` over `count` threads (a multiple of 32)
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

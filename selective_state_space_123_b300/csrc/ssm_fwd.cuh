@@ -32,30 +32,6 @@ namespace ssm {
 template <int NP>
 constexpr int bc_tile_bytes() { return kT * 2 * NP * 4; }
 
-// softplus in log2 units: for x = (delta_raw + bias) * log2(e) return
-// log2(1 + 2^x) = delta / ln 2.
-//  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), where for 2^-|x| <
-//  1/16 the logarithm is its Taylor series to the fifth power (relative
-//  truncation error < 2e-7) instead of the MUFU lg2, whose absolute error
-//  near 1 would dominate small results.
-//  fast (bf16 inputs): max(x, lg2(1 + 2^min(x, 64))); the absolute error of
-//  lg2 near 1 (~1e-7) is far below the bf16 tolerance.
-template <bool ACCURATE>
-__device__ __forceinline__ float softplus2(float x) {
-    if (ACCURATE) {
-        const float e = ex2(-fabsf(x));
-        float p = fmaf(e, 0.2f, -0.25f);
-        p = fmaf(e, p, 0.33333334f);
-        p = fmaf(e, p, -0.5f);
-        p = fmaf(e, p, 1.0f);
-        const float series = e * p * kLog2e;
-        const float direct = lg2(1.0f + e);
-        return fmaxf(x, 0.0f) + (e < 0.0625f ? series : direct);
-    } else {
-        return fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
-    }
-}
-
 // 8 consecutive tokens [tb, tb+8) of local channel c from a raw tile of
 // `ch` channel rows (TMA 128-byte swizzle; fp32 tiles are two boxes of 32
 // tokens, each ch x 128 bytes).

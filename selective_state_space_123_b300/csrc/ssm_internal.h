@@ -70,6 +70,11 @@ cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const f
                          const float* h0, const float* hloc, const float* sumd, float* hin,
                          cudaStream_t st);
 cudaError_t launch_step(int tin, int tout, const StepParams& p, cudaStream_t st);
+// Decode step for N = 16 and D a multiple of 128 (one thread per channel, 2-D
+// TMA tiles of the states and of A given by tm_st (rows = batch*dim) and tm_a
+// (rows = dim), 16 fp32 columns, 64-byte swizzle, box 16 x 128).
+cudaError_t launch_step_dec16_any(int tin, int tout, const StepParams& p, const CUtensorMap& tm_st,
+                                  const CUtensorMap& tm_a, cudaStream_t st);
 cudaError_t launch_expired_wait(int* status, int64_t spin_limit, cudaStream_t st);
 
 }  // namespace ssm

@@ -8,7 +8,7 @@ import torch
 import oracle
 from scan_inputs import WORKLOADS, make_inputs, make_step_inputs
 from tests.gpu_util import TIN, gpu_fwd, load_ssm, to_dev
-from tests.parity import TOL, assert_close
+from tests.parity import TOL, assert_bf16_output, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +39,44 @@ def test_step_small(ssm, shape, dt):
                               s["Dv"], s["z"], s["delta_bias"])
     assert_close(y, yo, TOL[dt], "y")
     assert_close(st, so, TOL[dt], "state")
+
+
+# Shapes that reach each decode kernel: N = 16 with D a multiple of 128 (one
+# thread per channel, 128-channel tiles), D a multiple of 64 with N in
+# {8, 16, 32} (64-channel tiles), and the per-element kernel otherwise.
+# (64, 1280, 16) has more 128-channel tiles than six per CTA of any grid the
+# launch picks, so the tile ring wraps.
+@pytest.mark.parametrize("shape", [(3, 256, 16), (1, 128, 16), (64, 1280, 16), (2, 192, 16),
+                                   (2, 128, 8), (3, 64, 32), (2, 320, 4)])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_step_tiled_paths(ssm, shape, dt):
+    Bt, D, N = shape
+    s = make_step_inputs(Bt, D, N, seed=30 + D + N, in_dtype=dt)
+    y, st = _step(ssm, s, dt)
+    yo, so = oracle.scan_step(s["u"], s["delta_raw"], s["A"], s["Bm"], s["Cm"], s["state"],
+                              s["Dv"], s["z"], s["delta_bias"])
+    assert_close(y, yo, TOL[dt], "y")
+    assert_close(st, so, TOL[dt], "state")
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 16), (2, 192, 16), (2, 40, 16)])
+@pytest.mark.parametrize("absent", ["z", "Dv", "delta_bias", "all"])
+def test_step_optional_inputs_absent(ssm, shape, absent):
+    Bt, D, N = shape
+    s = make_step_inputs(Bt, D, N, seed=40 + D, in_dtype="bf16")
+    for k in (("z", "Dv", "delta_bias") if absent == "all" else (absent,)):
+        s[k] = None
+    tin, f32 = TIN["bf16"], torch.float32
+    opt = lambda v, t: None if v is None else to_dev(v, t)
+    st = to_dev(s["state"], f32)
+    y = ssm.ssm_scan_step(to_dev(s["u"], tin), to_dev(s["delta_raw"], tin), to_dev(s["A"], f32),
+                          to_dev(s["Bm"], tin), to_dev(s["Cm"], tin), st, opt(s["Dv"], f32),
+                          opt(s["z"], tin), opt(s["delta_bias"], f32), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    yo, so = oracle.scan_step(s["u"], s["delta_raw"], s["A"], s["Bm"], s["Cm"], s["state"],
+                              s["Dv"], s["z"], s["delta_bias"])
+    assert_bf16_output(y.float().cpu().numpy(), yo, TOL["bf16"], "y")
+    assert_close(st.cpu().numpy(), so, TOL["bf16"], "state")
 
 
 def test_step_decode_workload_all_channels(ssm):
