@@ -71,9 +71,10 @@ L2_BYTES = 126 * 1024 * 1024
 # profiles/traffic.json together with a hash of the kernel's sources; it is
 # reported only while those sources are unchanged
 KERNEL_SOURCES = {
-    "fwd_kernel": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu"],
-    "bwd": ["ssm_bwd.cuh", "ssm_bwd_launch.cuh", "ssm_bwd_np16.cu"],
-    "step_kernel": ["ssm_aux.cu"],
+    "fwd_kernel": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu", "ssm_common.cuh",
+                   "ssm_kernels.cuh"],
+    "bwd": ["ssm_bwd.cuh", "ssm_bwd_launch.cuh", "ssm_bwd_np16.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
+    "step_dec16_kernel": ["ssm_aux.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
 }
 
 

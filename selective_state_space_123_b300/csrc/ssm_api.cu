@@ -135,6 +135,7 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
     const int want_nt = env_int("SSM_FWD_NT", 0);
     const int want_w = env_int("SSM_FWD_W", 0);
     const int want_seg = env_int("SSM_FWD_NSEG", 0);
+    const int want_cps = env_int("SSM_FWD_CPS", 0);
     double best = -1.0;
     for (int ci = 0; ci < cnt; ++ci) {
         const int NT = nts[ci];
@@ -149,6 +150,7 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
             int cps = 2048 / (32 * (W + 1));
             const int by_regs = 65536 / (fwd_reg_cap(NT) * 32 * (W + 1));
             if (by_regs < cps) cps = by_regs;
+            if (want_cps > 0) cps = want_cps;
             while (cps > 1 && 2 * stage + xy + 2048 > (size_t)(228 * 1024) / cps) --cps;
             if (cps < 1 || 2 * stage + xy + 2048 > (size_t)kMaxSmemPerCta) continue;
             size_t avail = (size_t)(228 * 1024) / cps - 2048;

@@ -152,14 +152,13 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 
 // Forward kernel.  blockDim.x = 32 * (W + 1): W compute warps and one
 // producer warp (the last).  A CTA owns CH = W * 32 / NT channels of one
-// batch row for one segment of the sequence.  Per super-block of SB = 8 * NT
-// tokens each lane computes softplus and delta * u of its own 8 tokens and
-// gathers the channel's other tokens from its NT - 1 partner lanes by
+// batch row for one segment of the sequence.  Per super-block of SB = TPL *
+// NT tokens each lane computes softplus and delta * u of its own TPL tokens
+// and gathers the channel's other tokens from its NT - 1 partner lanes by
 // shuffles, runs the recurrence over the SB tokens for its G = NP / NT
-// states, writes
-// its per-token partial read-outs to the warp's exchange buffer, and then
-// finishes its own 8 tokens (sum over the NT lanes, D skip, SiLU gate,
-// store).  All exchange stays inside the warp.
+// states, writes its per-token partial read-outs to the warp's exchange
+// buffer, and then finishes its own TPL tokens (sum over the NT lanes, D
+// skip, SiLU gate, store).  All exchange stays inside the warp.
 template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW>
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
@@ -323,38 +322,44 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if (sb * SB >= nvalid) break;
 
             // 1. each lane computes delta2 = softplus / ln2 and delta2 * u of its
-            //    own 8 tokens, then gathers all SB tokens of the channel from
+            //    own TPL tokens, then gathers all SB tokens of the channel from
             //    the NT lanes with shuffles (one softplus per token)
             const int tb = sb * SB + g * TPL;
-            float u8[8];
+            float uo[TPL];
             float d2[SB], du[SB];
             {
-                float dv[8], d2o[8], duo[8];
-                load_raw8r<TIN>(st, CH, c, tb, u8);
-                load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
+                float dv[TPL], d2o[TPL], duo[TPL];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float dd = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
-                    if (tb + q >= nvalid) dd = 0.0f;
-                    d2o[q] = dd;
-                    duo[q] = dd * u8[q];
+                for (int k8 = 0; k8 < TPL / 8; ++k8) {
+                    float t8[8], r8[8];
+                    load_raw8r<TIN>(st, CH, c, tb + 8 * k8, t8);
+                    load_raw8r<TIN>(st + RAW, CH, c, tb + 8 * k8, r8);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uo[8 * k8 + q] = t8[q];
+                        dv[8 * k8 + q] = r8[q];
+                    }
                 }
+                const bool full = nvalid == kT;   // warp-uniform: no padded token
+                float s8 = 0.0f;
+#pragma unroll
+                for (int q = 0; q < TPL; ++q) {
+                    float dd = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+                    if (!full && tb + q >= nvalid) dd = 0.0f;
+                    d2o[q] = dd;
+                    duo[q] = dd * uo[q];
+                    if (SUMMARY) s8 += dd;
+                }
+                if (SUMMARY) sum_d2 += (double)s8;   // this lane's own tokens
 #pragma unroll
                 for (int jj = 0; jj < NT; ++jj) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        d2[8 * jj + q] = NT == 1 ? d2o[q] : __shfl_sync(0xffffffffu, d2o[q], src_base + jj);
-                        du[8 * jj + q] = NT == 1 ? duo[q] : __shfl_sync(0xffffffffu, duo[q], src_base + jj);
+                    for (int q = 0; q < TPL; ++q) {
+                        d2[TPL * jj + q] = NT == 1 ? d2o[q] : __shfl_sync(0xffffffffu, d2o[q], src_base + jj);
+                        du[TPL * jj + q] = NT == 1 ? duo[q] : __shfl_sync(0xffffffffu, duo[q], src_base + jj);
                     }
                 }
             }
-            if (SUMMARY) {
-                float s8 = 0.0f;   // every lane of the channel sums all SB tokens
-#pragma unroll
-                for (int q = 0; q < SB; ++q) s8 += d2[q];
-                sum_d2 += (double)s8;
-            }
-
             // 2. the recurrence over the SB tokens for this lane's G states
             float yp[SB];
             fwd_chain<NP, G, SB, SUMMARY, ACCURATE>(d2, du, bct + sb * SB * (2 * NP) + g * G, Ap,
@@ -370,20 +375,25 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 __syncwarp();
 #pragma unroll
                 for (int k8 = 0; k8 < TPL / 8; ++k8) {
-                    float yt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    float yt[8];
 #pragma unroll
                     for (int gg = 0; gg < NT; ++gg) {
                         const float4 a = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8);
                         const float4 bq = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8 + 4);
-                        yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
-                        yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
+                        if (gg == 0) {
+                            yt[0] = a.x; yt[1] = a.y; yt[2] = a.z; yt[3] = a.w;
+                            yt[4] = bq.x; yt[5] = bq.y; yt[6] = bq.z; yt[7] = bq.w;
+                        } else {
+                            yt[0] += a.x; yt[1] += a.y; yt[2] += a.z; yt[3] += a.w;
+                            yt[4] += bq.x; yt[5] += bq.y; yt[6] += bq.z; yt[7] += bq.w;
+                        }
                     }
                     float zv[8];
                     if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb + 8 * k8, zv);
                     float out[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        float v = fmaf(Dd, u8[q], yt[q]);
+                        float v = fmaf(Dd, uo[8 * k8 + q], yt[q]);
                         if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
                         out[q] = v;
                     }
@@ -400,9 +410,11 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (dead) return;
 
     if (SUMMARY) {
-        // one thread per channel records the segment's sum of delta2 (every
-        // lane of the channel holds the whole sum)
-        const double tot = sum_d2;
+        // one thread per channel records the segment's sum of delta2 (each
+        // lane summed its own tokens)
+        double tot = sum_d2;
+#pragma unroll
+        for (int o = 1; o < NT; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if (ch_ok) {
             float* hl = p.hloc + ((int64_t)seg * p.Bt * p.D + row) * NP + g * G;
 #pragma unroll
