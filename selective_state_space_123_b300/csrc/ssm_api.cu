@@ -111,17 +111,34 @@ int fwd_reg_cap(int NT) {
 // kernel body: more lanes per channel means more per-token exchange).
 double fwd_nt_cost(int NT) { return NT == 4 ? 1.15 : NT == 1 ? 1.05 : 1.0; }
 
+// Relative throughput of one SM running `w` compute warps of the scan
+// (channel-tokens per unit time), measured on the B300 with 2 lanes per
+// channel: one warp per sub-partition up to 4 warps, then the sub-partitions
+// holding two warps set the pace (5 warps are no faster than 4).
+double fwd_sm_rate(int w) {
+    static const double rate[9] = {0.0, 0.268, 0.536, 0.804, 1.071, 1.071, 1.179, 1.382, 1.396};
+    if (w <= 0) return rate[1];
+    return w <= 8 ? rate[w] : rate[8];
+}
+
 // Time model of one launch: `ctas` CTAs of W compute warps, each doing `work`
-// units; an SM runs up to `cps` CTAs at once and reaches full throughput
-// with about 6 compute warps.
+// units; an SM runs up to `cps` CTAs at once.  The busiest SM sets the time.
 double fwd_launch_cost(int64_t ctas, int sms, int cps, int W, double work) {
     if (ctas <= 0) return 0.0;
     const int64_t k = (ctas + sms - 1) / sms;          // CTAs on the busiest SM
     const int64_t res = k < cps ? k : cps;            // resident together
     const int64_t waves = (k + res - 1) / res;
-    double sat = (double)(res * W) / 6.0;
+    return (double)waves * (double)res * work / fwd_sm_rate((int)(res * W));
+}
+
+// The backward sweeps' time model: one CTA per SM, full throughput from
+// about 6 compute warps.
+double bwd_launch_cost(int64_t ctas, int sms, int W, double work) {
+    if (ctas <= 0) return 0.0;
+    const int64_t waves = (ctas + sms - 1) / sms;
+    double sat = (double)W / 6.0;
     if (sat > 1.0) sat = 1.0;
-    return (double)waves * (double)res * work / sat;
+    return (double)waves * work / sat;
 }
 
 FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
@@ -255,7 +272,7 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
             if (2 * str + fixed > (size_t)kMaxSmemPerCta) continue;
             const int64_t tiles = (s.dim + CH - 1) / CH;
             const double work = (double)CH * (NT == 4 ? 1.15 : 1.0);
-            const double cost = fwd_launch_cost(s.batch * tiles, sm_count, 1, W, work);
+            const double cost = bwd_launch_cost(s.batch * tiles, sm_count, W, work);
             if (best < 0.0 || cost < best * 0.999) {
                 best = cost;
                 pl.NT = NT; pl.W = W; pl.CH = CH;
