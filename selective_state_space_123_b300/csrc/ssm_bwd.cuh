@@ -684,8 +684,8 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             const f2 Bj = e ? Bq.y : Bq.x;
                             const f2 Cj = e ? Cq.y : Cq.x;
                             const f2 al = mul2(anext[jj], lam[jj]);   // a_{t+1} lambda_{t+1}
-                            lam[jj] = fma2(anext[jj], lam[jj], mul2(gqp, Cj));
-                            accb = add2(accb, mul2(lam[jj], Bj));
+                            lam[jj] = fma2(gqp, Cj, al);
+                            accb = fma2(lam[jj], Bj, accb);
                             accab = fma2(Ap[jj], mul2(al, Bj), accab);
                             ld[jj] = mul2(lam[jj], dup);              // dB partial / ln2
                             const f2 arg = mul2(d2p, Ap[jj]);
