@@ -15,7 +15,7 @@ import torch
 import oracle
 from scan_inputs import WORKLOADS, device_inputs, make_inputs
 from tests.gpu_util import gpu_fwd, load_ssm, oracle_fwd, rows_to_host
-from tests.parity import TOL, assert_bf16_output, assert_close
+from tests.parity import TOL, TOL_F32_LONG, assert_bf16_output, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -86,6 +86,25 @@ def test_segmented_plan(ssm, nseg, monkeypatch):
     _check(ssm, x)
     x = make_inputs(1, 20, 16, 64 * 30, seed=10, in_dtype="f32", h0=True)
     _check(ssm, x)
+
+
+@pytest.mark.parametrize("dt,L,bias_shift", [("bf16", 64 * 160, 0.0), ("bf16", 64 * 160, 3.0),
+                                             ("bf16", 64 * 40, -1.0), ("f32", 64 * 160, 3.0),
+                                             ("f32", 64 * 64, 0.0)])
+def test_segmented_plan_long_segments(ssm, dt, L, bias_shift, monkeypatch):
+    """Two segments of 1280 to 5120 tokens: with the recipe's delta, with a
+    larger one (+3 on the bias: the decay over a segment underflows to zero,
+    so the carry passes on the segment's own summary alone) and with a
+    smaller one (-1: long memory across the segment boundary).  fp32 inputs
+    over these lengths are held to the long-sequence fp32 bar."""
+    monkeypatch.setenv("SSM_FWD_NSEG", "2")
+    x = make_inputs(1, 40, 16, L, seed=13, in_dtype=dt, h0=True)
+    x.delta_bias = (x.delta_bias + np.float32(bias_shift)).astype(np.float32)
+    tol = TOL_F32_LONG if dt == "f32" else TOL[dt]
+    y, hL = gpu_fwd(ssm, x)
+    yo, ho = oracle_fwd(x)
+    assert_close(y, yo, tol, "y")
+    assert_close(hL, ho, tol, "hL")
 
 
 def test_bf16_output(ssm):
