@@ -89,7 +89,7 @@ struct FwdPlan {
     int nseg = 1;
     int64_t nchunks = 0, seg_chunks = 0;
     bool tma_raw = false;
-    size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, bytes = 0;
+    size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, off_tstart = 0, bytes = 0;
 };
 
 // Per-NT constants of the forward kernel, on the host.
@@ -107,9 +107,12 @@ int fwd_reg_cap(int NT) {
     return r & ~7;
 }
 
-// Relative cost of one state update per NT (instructions per update of the
-// kernel body: more lanes per channel means more per-token exchange).
-double fwd_nt_cost(int NT) { return NT == 4 ? 1.15 : NT == 1 ? 1.05 : 1.0; }
+// Relative cost of one state update per NT, against the per-SM rates below
+// (measured with NT = 2): at the Mamba-1.4B shape 4 lanes per channel ran
+// 1.5x slower than 2, and one lane per channel (4 warps, 128 channels per
+// SM) 1.23x slower; the rates of one-lane warps at higher warp counts are not
+// measured, so NT = 1 is taken only where NT = 2 does not apply.
+double fwd_nt_cost(int NT) { return NT == 4 ? 1.5 : NT == 1 ? 1.3 : 1.0; }
 
 // Relative throughput of one SM running `w` compute warps of the scan
 // (channel-tokens per unit time), measured on the B300 with 2 lanes per
@@ -192,7 +195,16 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
                 const double work = (double)CH * (double)seg_chunks * fwd_nt_cost(NT);
                 const int64_t ctas = s.batch * tiles;
                 double cost = fwd_launch_cost(ctas * nseg, sm_count, cps, W, work);
-                if (nseg > 1) cost += 0.6 * fwd_launch_cost(ctas * (nseg - 1), sm_count, cps, W, work);
+                // pass 1 costs ~0.6 of pass 2 per chunk; with the tail search it
+                // runs only the last part of each segment, about 16K tokens with
+                // the usual delta range (softplus of dt in [1e-3, 1e-1]): the slowest
+                // state's decay reaches 2^-40 after ~29 units of accumulated delta
+                double sfrac = 0.6;
+                if (pl.tma_raw) {
+                    const double tail = 16384.0 / ((double)seg_chunks * kT);
+                    sfrac *= tail < 1.0 ? tail : 1.0;
+                }
+                if (nseg > 1) cost += sfrac * fwd_launch_cost(ctas * (nseg - 1), sm_count, cps, W, work);
                 // near-ties go to the plan that keeps more SMs busy: with the
                 // inputs cold in L2 (a fresh batch), plans that leave SMs idle
                 // measured up to 20 % slower than the model says
@@ -227,6 +239,8 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
         off += align256(st * pl.NP * 4);
         pl.off_sumd = off;
         off += align256(st * 4);
+        pl.off_tstart = off;
+        off += align256((size_t)pl.nseg * s.batch * ((s.dim + pl.CH - 1) / pl.CH) * 4);
     }
     pl.bytes = off;
     if (env_int("SSM_DEBUG_PLAN", 0))
@@ -492,9 +506,16 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
         p.hin = reinterpret_cast<float*>(ws + pl.off_hin);
         p.hloc = reinterpret_cast<float*>(ws + pl.off_hloc);
         p.sumd = reinterpret_cast<float*>(ws + pl.off_sumd);
-        // pass 1: summaries of every segment but the last
+        // pass 1: summaries of every segment but the last, each from the
+        // chunk the tail search finds (it needs 16-byte row loads)
         FwdParams p1 = p;
         p1.hin = nullptr;
+        if (pl.tma_raw) {
+            int* tstart = reinterpret_cast<int*>(ws + pl.off_tstart);
+            if (launch_tail(s.in_dtype, p, pl.CH, gx, tstart, p.sumd, st) != cudaSuccess)
+                return cuda_fail();
+            p1.tstart = tstart;
+        }
         if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, p1, maps,
                        dim3(gx, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess)
             return cuda_fail();

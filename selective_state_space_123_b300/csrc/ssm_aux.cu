@@ -80,6 +80,108 @@ __global__ void carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg, con
     }
 }
 
+// Tail search for the segmented plan.  Pass 1 needs each segment's end
+// state from a zero start, h_end = sum_t P(t -> end) delta_t u_t B_t, where
+// the decay of state n from token t to the segment's end is
+// P = 2^(A_n * S_t), S_t = sum of delta2 over the tokens after t.  Once the
+// slowest state's decay, 2^(max_n A_n * S_t), is below 2^-kTailLog2, the
+// earlier tokens change h_end by less than 2^-40 of the state at that point,
+// far below fp32 resolution, so pass 1 may start after them (the hot-path
+// table's truncation option, with the full segment as the fallback).  The
+// search walks delta backwards from each segment's end (one warp per
+// channel, 16-byte loads) until that point or the segment's start, and
+// writes per (segment, batch row, channel tile) the earliest chunk any
+// channel of the tile needs, and per saturated channel kTailSat into sumd,
+// so that the carry drops the incoming state (2^(A * kTailSat) = 0 for
+// A < 0).  Where a tile needs its whole segment, pass 1 writes the exact
+// sums.  Segments 0 .. nseg-2 (whole chunks); L * sizeof(TIN) % 16 == 0.
+constexpr float kTailLog2 = 40.0f;
+constexpr float kTailSat = 1e30f;
+
+template <typename TIN>
+__global__ void __launch_bounds__(1024) tail_kernel(const FwdParams p, int CH, int* __restrict__ tstart,
+                                                    float* __restrict__ sumd) {
+    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    constexpr int VEC = 16 / (int)sizeof(TIN);        // tokens per 16-byte load
+    constexpr int LOADS = 4;                            // loads per lane per step
+    constexpr int STEP = LOADS * 32 * VEC;              // tokens per warp step
+    const int tile = blockIdx.x;
+    const int64_t b = blockIdx.y;
+    const int seg = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t c_begin = (int64_t)seg * p.seg_chunks;
+    const int64_t c_end = c_begin + p.seg_chunks;       // segments 0 .. nseg-2 are full
+    const int64_t s0 = c_begin * kT, s1 = c_end * kT;
+    __shared__ int cmin;
+    if (threadIdx.x == 0) cmin = (int)(c_end - c_begin);
+    __syncthreads();
+    const TIN* dr = static_cast<const TIN*>(p.dr);
+    int my_min = (int)(c_end - c_begin);               // chunk offsets within the segment
+    for (int c = warp; c < CH; c += nwarps) {
+        const int64_t d = (int64_t)tile * CH + c;
+        if (d >= p.D) break;
+        if (*reinterpret_cast<volatile int*>(&cmin) == 0) break;   // the tile needs its whole segment
+        const int64_t row = b * p.D + d;
+        float amax = -INFINITY;
+        for (int n = 0; n < p.N; ++n) amax = fmaxf(amax, p.A[d * p.N + n]);
+        const float bias2 = p.bias ? p.bias[d] * kLog2e : 0.0f;
+        const TIN* rp = dr + row * p.L;
+        double tot = 0.0;
+        int64_t t0 = s0;
+        bool sat = false;
+        for (int64_t hi = s1; hi > s0; hi -= STEP) {
+            const int64_t lo = hi - STEP > s0 ? hi - STEP : s0;
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < LOADS; ++j) {
+                const int64_t t = lo + (int64_t)(j * 32 + lane) * VEC;
+                if (t < hi) {
+                    float v[VEC];
+                    if constexpr (sizeof(TIN) == 2) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(rp + t);
+                        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+                        v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+                    } else {
+                        const float4 w = *reinterpret_cast<const float4*>(rp + t);
+                        v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+                    }
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) part += softplus2<ACCURATE>(fmaf(v[q], kLog2e, bias2));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            tot += (double)part;
+            if (amax < 0.0f && (double)amax * tot <= -(double)kTailLog2) {
+                t0 = lo;
+                sat = true;
+                break;
+            }
+        }
+        const int need = (int)((t0 - s0) / kT);
+        if (need < my_min) my_min = need;
+        if (lane == 0) {
+            if (sat) sumd[(int64_t)seg * p.Bt * p.D + row] = kTailSat;
+            if (need == 0) atomicMin(&cmin, 0);
+        }
+    }
+    if (lane == 0) atomicMin(&cmin, my_min);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        tstart[((int64_t)seg * p.Bt + b) * gridDim.x + tile] = (int)c_begin + cmin;
+}
+
+cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int* tstart, float* sumd,
+                        cudaStream_t st) {
+    const dim3 grid(tiles, (unsigned)p.Bt, (unsigned)(p.nseg - 1));
+    if (tin == SSM_BF16)
+        tail_kernel<__nv_bfloat16><<<grid, 1024, 0, st>>>(p, CH, tstart, sumd);
+    else
+        tail_kernel<float><<<grid, 1024, 0, st>>>(p, CH, tstart, sumd);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,
                          cudaStream_t st) {

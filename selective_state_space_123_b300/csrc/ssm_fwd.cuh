@@ -196,8 +196,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int seg = blockIdx.z;
     const int64_t L = p.L;
     const int64_t nchunks = (L + kT - 1) / kT;
-    const int64_t k_begin = (int64_t)seg * p.seg_chunks;
-    const int64_t k_end = min(nchunks, k_begin + p.seg_chunks);
+    const int64_t k_seg = (int64_t)seg * p.seg_chunks;
+    const int64_t k_end = min(nchunks, k_seg + p.seg_chunks);
+    // a summary starts where the tail search found that the segment's end
+    // state no longer depends on earlier tokens (their decay is below 2^-40)
+    const int64_t k_begin =
+        (SUMMARY && p.tstart)
+            ? max(k_seg, min(k_end - 1, (int64_t)p.tstart[((int64_t)seg * p.Bt + blockIdx.y) * gridDim.x + blockIdx.x]))
+            : k_seg;
     const bool has_z = !SUMMARY && p.z != nullptr;
 
     if (tid == 0) {
@@ -424,7 +430,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 hl[2 * j] = lo;
                 hl[2 * j + 1] = hi;
             }
-            if (g == 0) p.sumd[(int64_t)seg * p.Bt * p.D + row] = (float)tot;
+            // a summary over the whole segment has the exact sum; a shortened one
+            // keeps the search's saturation marker
+            if (g == 0 && k_begin == k_seg) p.sumd[(int64_t)seg * p.Bt * p.D + row] = (float)tot;
         }
     } else if (k_end == nchunks && p.hL && ch_ok) {
 #pragma unroll

@@ -66,6 +66,11 @@ cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams
 
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);
+// Tail search of the segmented plan (see ssm_aux.cu): per (segment, batch
+// row, channel tile) the first chunk pass 1 needs; per saturated channel a
+// marker in sumd.  Segments 0 .. nseg-2.
+cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int* tstart, float* sumd,
+                        cudaStream_t st);
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,
                          cudaStream_t st);

@@ -52,6 +52,10 @@ struct FwdParams {
     float* hin;             // (nseg, Bt, D, NP) initial state of each segment (pass 2)
     float* hloc;            // (nseg, Bt, D, NP) end state from a zero start (pass 1)
     float* sumd;            // (nseg, Bt, D) sum of delta/ln2 over the segment (pass 1)
+    // pass 1 with a tail search (nullable): first chunk each (segment, batch
+    // row, channel tile) must run, (nseg, Bt, tiles); sumd is then written by
+    // the search, or by pass 1 where it runs the whole segment
+    const int* tstart;
     int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
     int* status;
     uint64_t timeout_ns;
