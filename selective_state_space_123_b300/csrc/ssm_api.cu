@@ -258,6 +258,7 @@ struct BwdPlan {
     int stages_f = 2, stages_r = 2;
     size_t smem_f = 0, smem_r = 0;
     bool tma_raw = false;
+    bool ok = false;        // a tile shape fits the shared memory
     size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, bytes = 0;
 };
 
@@ -273,9 +274,12 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
     const int eb = dtype_bytes(s.in_dtype);
     pl.tma_raw = (s.seqlen * eb) % 16 == 0;
     const int nts_all[2] = {2, 4};
-    const int want_nt = env_int("SSM_BWD_NT", 0);
-    const int want_w = env_int("SSM_BWD_W", 0);
+    int want_nt = env_int("SSM_BWD_NT", 0);
+    int want_w = env_int("SSM_BWD_W", 0);
     double best = -1.0;
+    // a second search without the overrides when none of them fits
+    for (int attempt = 0; attempt < 2 && best < 0.0; ++attempt) {
+    if (attempt == 1) want_nt = want_w = 0;
     for (int ni = 0; ni < 2; ++ni) {
         const int NT = nts_all[ni];
         if (pl.NP == 8 && NT != 2) continue;       // G = NP / NT must be 4, 8 or 16
@@ -304,6 +308,8 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
             }
         }
     }
+    }
+    pl.ok = best >= 0.0;
     size_t off = kHeaderBytes;
     pl.off_bc = off;
     off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
@@ -567,6 +573,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const BwdPlan pl = plan_bwd(s, device_sm_count());
+    if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);

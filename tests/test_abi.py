@@ -167,3 +167,21 @@ def test_workspace_query_edge_shapes(pkg, for_backward):
                 assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), for_backward) >= 256
         finally:
             del os.environ["SSM_FWD_NSEG"]
+
+
+def test_plan_overrides_that_do_not_fit_fall_back(pkg, monkeypatch):
+    """Tile-shape overrides that exceed the shared memory leave the planner's
+    own choice in place (same workspace), instead of an unsized plan."""
+    shapes = [(2, 5120, 16, 8192), (1, 64, 64, 1000), (1, 8, 8, 100)]
+    base = [pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), True) for sh in shapes]
+    for nt, w in (("2", "6"), ("2", "7"), ("4", "9"), ("3", "1")):
+        monkeypatch.setenv("SSM_BWD_NT", nt)
+        monkeypatch.setenv("SSM_BWD_W", w)
+        for sh, b in zip(shapes, base):
+            n = pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), True)
+            assert n >= 256, (sh, nt, w)
+    for nt, w in (("2", "9"), ("3", "1")):
+        monkeypatch.setenv("SSM_FWD_NT", nt)
+        monkeypatch.setenv("SSM_FWD_W", w)
+        for sh in shapes:
+            assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), False) >= 256

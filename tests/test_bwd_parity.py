@@ -114,6 +114,16 @@ def test_threads_per_channel_variants(ssm, nt, monkeypatch):
     _check(ssm, x)
 
 
+@pytest.mark.parametrize("nt,w", [("2", "7"), ("4", "9")])
+def test_plan_override_that_does_not_fit(ssm, nt, w, monkeypatch):
+    """A tile-shape override too large for the shared memory falls back to
+    the planner's own choice and the result stays correct."""
+    monkeypatch.setenv("SSM_BWD_NT", nt)
+    monkeypatch.setenv("SSM_BWD_W", w)
+    x = make_inputs(2, 100, 16, 200, seed=77, in_dtype="bf16", dy=True)
+    _check(ssm, x)
+
+
 def test_bf16_outputs(ssm):
     x = make_inputs(2, 64, 16, 256, seed=19, in_dtype="bf16", dy=True)
     _check(ssm, x, out_dtype=torch.bfloat16)
