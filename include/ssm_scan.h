@@ -87,7 +87,7 @@ enum {
     SSM_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -6,        /* a CUDA runtime call failed (launch, attribute query) */
     SSM_ERR_TIMEOUT = -7,     /* device side: a bounded wait expired; outputs undefined */
-    SSM_ERR_UNSUPPORTED = -8  /* valid request this build does not implement */
+    SSM_ERR_UNSUPPORTED = -8  /* valid request the library does not implement */
 };
 
 /* Bytes of device workspace the call needs for this shape on the current
@@ -151,9 +151,9 @@ SSM_API int ssm_get_status(void* workspace, ssm_stream_t stream);
 /* Human-readable text of a status code (static storage, never NULL). */
 SSM_API const char* ssm_strerror(int code);
 
-/* ssm_scan_fwd for callers that cannot allocate device memory.  The paper has
- * no counterpart to this entry point; it exists for callers that are handed
- * only their input and output buffers and may not allocate on the device
+/* ssm_scan_fwd for callers that cannot allocate device memory.  The method's
+ * description has no counterpart to this entry point; it exists for callers
+ * that are handed only their input and output buffers and may not allocate on the device
  * themselves (a plug-in inside a host engine whose allocator owns all device
  * memory, or a latency-bound loop that must not call cudaMalloc after
  * start-up, since it can synchronise the device and take unbounded time).
