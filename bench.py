@@ -73,7 +73,8 @@ L2_BYTES = 126 * 1024 * 1024
 KERNEL_SOURCES = {
     "fwd_kernel": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu", "ssm_common.cuh",
                    "ssm_kernels.cuh"],
-    "bwd": ["ssm_bwd.cuh", "ssm_bwd_launch.cuh", "ssm_bwd_np16.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
+    "fwdbwd": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu", "ssm_bwd.cuh", "ssm_bwd_launch.cuh",
+               "ssm_bwd_np16.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
     "step_dec16_kernel": ["ssm_aux.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
 }
 
@@ -624,10 +625,13 @@ def run_ours(args):
         "frac_of_roofline_time": max(t_hbm, t_sfu) / t_s,
         "algorithmic_bytes": wl.bytes,
         "exps": wl.exps,
-        "traffic": recorded_traffic({"fwd": "fwd_kernel", "fwdbwd": "bwd", "step": "step_dec16_kernel"}[wl.mode],
+        "traffic": recorded_traffic({"fwd": "fwd_kernel", "fwdbwd": "fwdbwd", "step": "step_dec16_kernel"}[wl.mode],
                                     w["name"]),
-        "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
-                        "kernel (ncu, profiles/traffic.json); null when the kernel changed since",
+        "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
+                         "kernel" if wl.mode != "fwdbwd" else
+                         "dram__bytes_read.sum + dram__bytes_write.sum of the forward and the two "
+                         "backward sweeps of one step") +
+                        " (ncu, profiles/traffic.json); null when the kernels changed since",
         "fp32_ops_per_update": 4,
         "timing_note": ("achieved uses the whole step's CUDA-event time (one kernel per decode "
                         "step)" if wl.mode == "step" else
