@@ -580,8 +580,7 @@ static cudaError_t launch_step_tma(const StepParams& p, cudaStream_t st) {
 // stores of 64-byte rows would write half sectors) and releases the slot
 // once that store has read it.
 constexpr int kDecRows = 128;
-template <typename TIN>
-constexpr int dec_slots() { return 3; }
+constexpr int kDecSlots = 3;
 
 template <typename TIN>
 struct __align__(1024) DecSlot {
@@ -603,7 +602,6 @@ __global__ void __launch_bounds__(160, 2) step_dec16_kernel(const StepParams p,
                                                            const __grid_constant__ CUtensorMap tm_st,
                                                            const __grid_constant__ CUtensorMap tm_a) {
     extern __shared__ uint8_t smem_dyn[];
-    constexpr int kDecSlots = dec_slots<TIN>();
     DecSlot<TIN>* ring = reinterpret_cast<DecSlot<TIN>*>(align_smem_1024(smem_dyn));
     __shared__ __align__(8) uint64_t full_bar[kDecSlots];
     __shared__ __align__(8) uint64_t empty_bar[kDecSlots];
@@ -731,7 +729,7 @@ static cudaError_t launch_step_dec16(const StepParams& p, const CUtensorMap& tm_
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaGetLastError();
     auto kern = step_dec16_kernel<TIN, TOUT>;
-    const size_t smem = dec_slots<TIN>() * sizeof(DecSlot<TIN>) + 1024;
+    const size_t smem = kDecSlots * sizeof(DecSlot<TIN>) + 1024;
     static bool attr[64] = {};
     static int per_sm[64] = {};
     if (dev >= 0 && dev < 64 && !attr[dev]) {
