@@ -88,6 +88,30 @@ def kernel_source_hash(kind):
     return h.hexdigest()[:16]
 
 
+def rank_seed(seed, rank):
+    """Each rank's replica draws its own inputs."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x, world):
+    """The largest of the ranks' values: the job is as slow as its slowest
+    rank (NCCL on the GPUs, gloo on the host)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, updates_per_rank, ms_per_step):
+    """Whole-job state updates per second: every rank runs one replica of
+    the workload, so the job does world * updates_per_rank per step."""
+    return world * updates_per_rank / (ms_per_step * 1e-3)
+
+
 def recorded_traffic(kind, workload):
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kind + ":" + workload]
@@ -284,7 +308,7 @@ class Workload:
         self.mode = w["mode"]
         bf = torch.bfloat16
         if self.mode == "step":
-            a = device_inputs(Bt, D, N, 1, seed=w["seed"] + 1000 * rank, in_dtype="bf16", h0=True)
+            a = device_inputs(Bt, D, N, 1, seed=rank_seed(w["seed"], rank), in_dtype="bf16", h0=True)
             self.inp = {"u": a["u"][:, :, 0].contiguous(), "delta_raw": a["delta_raw"][:, :, 0].contiguous(),
                         "z": a["z"][:, :, 0].contiguous(), "Bm": a["Bm"][:, :, 0].contiguous(),
                         "Cm": a["Cm"][:, :, 0].contiguous(), "A": a["A"], "Dv": a["Dv"],
@@ -306,7 +330,7 @@ class Workload:
             self.launches = 1
             self.outs = [self.y, self.state]
         else:
-            a = device_inputs(Bt, D, N, L, seed=w["seed"] + 1000 * rank, in_dtype="bf16",
+            a = device_inputs(Bt, D, N, L, seed=rank_seed(w["seed"], rank), in_dtype="bf16",
                               dy=(self.mode == "fwdbwd"))
             self.inp = {k: v for k, v in a.items() if v is not None}
             self.y = torch.empty(Bt, D, L, dtype=bf, device="cuda")
@@ -542,12 +566,9 @@ def run_ours(args):
     ms = e0.elapsed_time(e1) - flush_ms
     if wl.ws is not None and ssm.ssm_get_status(wl.ws) != ssm.SSM_OK:
         raise RuntimeError("device status not ok after the timed region")
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     ms_step = ms / args.steps
-    value = world * wl.updates / (ms_step * 1e-3)
+    value = job_rate(world, wl.updates, ms_step)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -589,11 +610,8 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * wl.updates / (e2e_ms * 1e-3), "unit": UNIT,
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": job_rate(world, wl.updates, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "how": e2e_how}
 
