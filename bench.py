@@ -80,11 +80,17 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kind):
+    """Hash of the sources a kernel is built from, comments and blank space
+    left out (a comment edit does not change the kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "selective_state_space_123_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "selective_state_space_123_b300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -793,13 +793,13 @@ static cudaError_t launch_step_s(const StepParams& p, cudaStream_t st) {
 
 template <typename TIN, typename TOUT>
 static cudaError_t launch_step_t(const StepParams& p, cudaStream_t st) {
-    // state sizes that are a multiple of 4 (up to 32) take the pipelined kernel
     // whole 64-channel tiles inside one batch row: the bulk-copy stream
     if (p.D % kStepRows == 0 && p.Bt * p.D < (int64_t(1) << 31)) {
         if (p.N == 16) return launch_step_tma<TIN, TOUT, 4>(p, st);
         if (p.N == 8) return launch_step_tma<TIN, TOUT, 2>(p, st);
         if (p.N == 32) return launch_step_tma<TIN, TOUT, 8>(p, st);
     }
+    // state sizes 4, 8, 16, 32 otherwise: the cp.async pipeline
     if (p.N == 16) return launch_step_pipe<TIN, TOUT, 4>(p, st);
     if (p.N == 8) return launch_step_pipe<TIN, TOUT, 2>(p, st);
     if (p.N == 32) return launch_step_pipe<TIN, TOUT, 8>(p, st);
