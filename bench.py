@@ -180,9 +180,19 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def wait_first(self, limit_s=3.0):
+        """Wait (bounded) until the sampler has produced its first line."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < limit_s:
+            time.sleep(0.02)
+
+    def stop(self, t_begin=None, t_end=None):
+        """Summary of the samples taken between t_begin and t_end (wall
+        clock; a sample lands up to one period after its reading), or of the
+        nearest samples before and after when the region is shorter than the
+        sampling period."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -191,9 +201,17 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
+        lines = self.lines
+        if t_begin is not None and t_end is not None:
+            inside = [(t, ln) for t, ln in lines if t_begin <= t <= t_end + 0.15]
+            if not inside:
+                before = [(t, ln) for t, ln in lines if t < t_begin][-1:]
+                after = [(t, ln) for t, ln in lines if t > t_end][:1]
+                inside = before + after
+            lines = inside
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -536,6 +554,11 @@ def run_ours(args):
             do_flush()
         wl.step()
 
+    # clocks are sampled from before the warm-up, so that the timed region
+    # follows the warm-up without an idle pause
+    clocks = ClockSampler(local)
+    clocks.start()
+    clocks.wait_first()
     if wl.mode == "step":
         wl.capture_graphs()
     for _ in range(args.warmup):
@@ -555,18 +578,16 @@ def run_ours(args):
         torch.cuda.synchronize()
         flush_ms = e0.elapsed_time(e1)
 
-    clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
+    t_begin = time.time()
     e0.record(stream)
     for _ in range(args.steps):
         timed_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop(t_begin, time.time())
     if world > 1:
         dist.barrier()
     ms = e0.elapsed_time(e1) - flush_ms
