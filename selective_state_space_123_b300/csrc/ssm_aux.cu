@@ -1,9 +1,12 @@
-// ssm_aux.cu -- the small kernels around the forward scan:
+// ssm_aux.cu -- the kernels around the forward scan:
 //   * prep_bc:   B, C (batch, N, L) -> fp32 (batch, L, 2*NP) with ln2 folded
 //                into B (the scan then uses delta/ln2 throughout);
+//   * tail:      where each segment's summary pass may start (segmented plan);
 //   * carry:     per-segment initial states of the segmented forward,
 //                h_in[s+1] = 2^(A * sum_delta2[s]) * h_in[s] + h_loc[s];
-//   * step:      the single-token recurrent update (decode), state in place;
+//   * step:      the single-token recurrent update (decode), state in place:
+//                step_dec16 (N = 16, whole 128-channel tiles), step_tma
+//                (whole 64-channel tiles), step_pipe and step_kernel;
 //   * expired_wait: the failure-detection self test (a wait nothing ends).
 #include "ssm_common.cuh"
 #include "ssm_kernels.cuh"

@@ -6,13 +6,14 @@
 // Mamba lesson 2: keep the recurrence on chip, write back only the final
 // state; "State Space Models (SSMs) & Mamba", section "Hardware-Aware
 // Parallelism": the recurrence is a scan over the sequence):
-//   * it owns CH = 128/NT channels of one batch row for a whole segment of
-//     the sequence (normally the whole sequence);
+//   * it owns CH = 32 W / NT channels of one batch row (W <= 7 compute warps,
+//     chosen by the host planner) for a whole segment of the sequence
+//     (normally the whole sequence);
 //   * a producer warp streams 64-token chunks of u, delta_raw, z (TMA, 128-B
 //     swizzle) and of the prepared B/C tile into a multi-stage shared-memory
 //     ring guarded by mbarriers;
-//   * each of the 128 compute threads keeps G = NP/NT states of one channel
-//     in registers; the NT threads of a channel split the per-token work
+//   * each compute thread keeps G = NP/NT states of one channel in
+//     registers; the NT threads of a channel split the per-token work
 //     (softplus, gate, D skip) and exchange it with warp shuffles;
 //   * per token and state: dA = 2^(delta2 * A) on the MUFU (delta2 = delta /
 //     ln 2, so no extra scaling), h = dA h + delta u B, y += C h, in packed
@@ -21,7 +22,8 @@
 // SUMMARY = true is pass 1 of the segmented plan for very long sequences: no
 // read-out, the kernel records each segment's end state from a zero start and
 // the segment's sum of delta2 (the decay of the carried state over the
-// segment is 2^(A * sum)).
+// segment is 2^(A * sum)); it starts at the chunk a tail search found (the
+// earlier tokens' decay to the segment end is below 2^-40).
 #pragma once
 
 #include "ssm_common.cuh"
