@@ -366,8 +366,9 @@ class Workload:
             self.bytes = fwd_bytes(Bt, D, N, L)
             self.exps = Bt * D * L * N
             # B/C preparation + scan; the million-length sequence takes the
-            # segmented plan (preparation, summary pass, carry, scan)
-            self.launches = 4 if L >= (1 << 18) and Bt * D <= 4096 else 2
+            # segmented plan (preparation, tail search, summary pass, carry,
+            # scan)
+            self.launches = 5 if L >= (1 << 18) and Bt * D <= 4096 else 2
             self.outs = [self.y, self.hL]
             self.grads = None
             if self.mode == "fwdbwd":
