@@ -120,7 +120,9 @@ SSM_API int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delt
  *     (dB and dC are sums over all channels).
  *   dD, ddelta_bias (dim), dh0 (batch,dim,dstate) : fp32, nullable.
  *   ddelta_raw is the derivative with respect to delta_raw (before softplus).
- * workspace : >= ssm_scan_workspace_bytes(shape, 1) bytes. */
+ * workspace : >= ssm_scan_workspace_bytes(shape, 1) bytes.  The backward
+ * reruns the forward recurrence itself (with the derivative of the state
+ * with respect to A beside it); nothing from ssm_scan_fwd is needed. */
 SSM_API int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw,
                  const float* A, const void* B, const void* C, const float* D,
                  const void* z, const float* delta_bias, const float* h0,
