@@ -185,3 +185,18 @@ def test_plan_overrides_that_do_not_fit_fall_back(pkg, monkeypatch):
         monkeypatch.setenv("SSM_FWD_W", w)
         for sh in shapes:
             assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), False) >= 256
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No CPU fallback: without libssmscan.so the package does not import."""
+    import importlib.util
+    import shutil
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "selective_state_space_123_b300", "__init__.py")
+    pkg_dir = tmp_path / "ssm_copy"
+    pkg_dir.mkdir()
+    shutil.copy(src, pkg_dir / "__init__.py")
+    spec = importlib.util.spec_from_file_location("ssm_copy", pkg_dir / "__init__.py")
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)
