@@ -57,6 +57,8 @@ def _load():
             I = ctypes.c_int64
             lib.oracle_softplus.argtypes = [ctypes.c_double]
             lib.oracle_softplus.restype = ctypes.c_double
+            lib.oracle_conv_silu.argtypes = [I, I, I, I, P, P, P, P]
+            lib.oracle_conv_silu.restype = None
             lib.oracle_silu.argtypes = [ctypes.c_double]
             lib.oracle_silu.restype = ctypes.c_double
             lib.oracle_scan_fwd.argtypes = [I, I, I, I] + [P] * 11
@@ -85,6 +87,26 @@ def softplus(x: float) -> float:
 
 def silu(x: float) -> float:
     return _load().oracle_silu(float(x))
+
+
+def conv_silu(x, conv_w, conv_b=None):
+    """Causal depthwise convolution of width K = conv_w.shape[1] with left
+    zero padding, then SiLU: u[b,d,t] = silu(conv_b[d] + sum_k conv_w[d,k] *
+    x[b,d,t-(K-1)+k]).  x (Bt,D,L) -> u (Bt,D,L)."""
+    x, conv_w = _f64(x), _f64(conv_w)
+    conv_b = _f64(conv_b)
+    Bt, D, L = x.shape
+    K = conv_w.shape[1]
+    assert conv_w.shape == (D, K)
+    u = np.empty((Bt, D, L), np.float64)
+    _load().oracle_conv_silu(Bt, D, L, K, _ptr(x), _ptr(conv_w), _ptr(conv_b), _ptr(u))
+    return u
+
+
+def scan_fwd_conv(x, conv_w, conv_b, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None,
+                  h0=None):
+    """The scan fed by the block's conv prologue: scan_fwd(conv_silu(x), ...)."""
+    return scan_fwd(conv_silu(x, conv_w, conv_b), delta_raw, A, Bm, Cm, Dv, z, delta_bias, h0)
 
 
 def scan_fwd(u, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None, h0=None):

@@ -53,6 +53,22 @@ static double token_update(int64_t N, double u, double dr, double bias,
     return ys + Dskip * u;
 }
 
+void oracle_conv_silu(int64_t Bt, int64_t D, int64_t L, int64_t K, const double* x,
+                      const double* conv_w, const double* conv_b, double* u) {
+    for (int64_t b = 0; b < Bt; ++b)
+        for (int64_t d = 0; d < D; ++d) {
+            const int64_t row = (b * D + d) * L;
+            for (int64_t t = 0; t < L; ++t) {
+                double s = conv_b ? conv_b[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t tt = t - (K - 1) + k;
+                    if (tt >= 0) s += conv_w[d * K + k] * x[row + tt];
+                }
+                u[row + t] = oracle_silu(s);
+            }
+        }
+}
+
 void oracle_scan_fwd(int64_t Bt, int64_t D, int64_t N, int64_t L,
                      const double* u, const double* delta_raw, const double* A,
                      const double* Bm, const double* Cm,

@@ -42,6 +42,17 @@ double oracle_softplus(double x);
 /* silu(z) = z / (1 + e^-z). */
 double oracle_silu(double z);
 
+/* The block's local-processing step before the scan ("Mamba Architecture
+ * Explained", section "The Architecture in Practice": a 1-D convolution with
+ * a SiLU activation, per channel; "The convolution trick is gone -- what
+ * now?": one branch goes through a Conv1D and then the selective SSM).
+ * Reading: causal depthwise convolution of width K with left zero padding,
+ * so that the output keeps length L:
+ *   u[b,d,t] = silu(conv_b[d] + sum_{k<K} conv_w[d,k] * x[b,d,t-(K-1)+k]),
+ * x at t < 0 being 0.  x, u: (Bt, D, L); conv_w: (D, K); conv_b: (D), nullable. */
+void oracle_conv_silu(int64_t Bt, int64_t D, int64_t L, int64_t K, const double* x,
+                      const double* conv_w, const double* conv_b /* nullable */, double* u);
+
 /* Forward selective scan over the whole sequence, sequential in t. */
 void oracle_scan_fwd(int64_t Bt, int64_t D, int64_t N, int64_t L,
                      const double* u, const double* delta_raw, const double* A,

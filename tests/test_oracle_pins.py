@@ -334,3 +334,58 @@ def test_backward_closed_form_dD():
     z = x.z.astype(np.float64)
     ref = np.sum(x.dy.astype(np.float64) * _silu_lib(z) * x.u, axis=(0, 2))
     np.testing.assert_allclose(g["dD"], ref, rtol=1e-12)
+
+
+# ----- the block's conv prologue ("Mamba Architecture Explained", section
+# "The Architecture in Practice": Conv1D then SiLU before the selective SSM)
+
+def _silu(v):
+    return v * expit(v)
+
+
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_conv_silu_matches_library_convolution(K):
+    """Causal depthwise convolution = numpy's full convolution with the
+    reversed kernel, cut to the first L outputs (left zero padding)."""
+    rng = np.random.default_rng(40 + K)
+    Bt, D, L = 2, 5, 37
+    x = rng.standard_normal((Bt, D, L))
+    w = rng.standard_normal((D, K))
+    b = rng.standard_normal(D)
+    u = oracle.conv_silu(x, w, b)
+    ref = np.empty_like(u)
+    for bb in range(Bt):
+        for d in range(D):
+            ref[bb, d] = _silu(b[d] + np.convolve(x[bb, d], w[d, ::-1])[:L])
+    np.testing.assert_allclose(u, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_conv_silu_impulse_and_bias():
+    """An impulse at t = 0 reads the kernel out backwards over the first K
+    tokens (w[K-1] at t = 0 ... w[0] at t = K-1) and only the bias after;
+    without a bias the output there is silu(0) = 0."""
+    K, L = 4, 9
+    w = np.array([[0.5, -1.0, 2.0, 0.25]])
+    x = np.zeros((1, 1, L))
+    x[0, 0, 0] = 1.0
+    b = np.array([0.3])
+    u = oracle.conv_silu(x, w, b)[0, 0]
+    for t in range(L):
+        pre = 0.3 + (w[0, K - 1 - t] if t < K else 0.0)
+        assert u[t] == pytest.approx(_silu(pre), abs=1e-15)
+    u0 = oracle.conv_silu(x, w, None)[0, 0]
+    assert np.all(u0[K:] == 0.0)
+
+
+def test_scan_fwd_conv_is_scan_of_conv_output():
+    """The prologue feeds u: scanning conv_silu(x) equals scan_fwd_conv."""
+    rng = np.random.default_rng(44)
+    x = make_inputs(2, 6, 4, 30, seed=44, in_dtype="f32", h0=True)
+    w = rng.standard_normal((6, 4))
+    b = rng.standard_normal(6)
+    y1, h1 = oracle.scan_fwd_conv(x.u, w, b, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z,
+                                  x.delta_bias, x.h0)
+    u = oracle.conv_silu(x.u, w, b)
+    y2, h2 = oracle.scan_fwd(u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(h1, h2)
