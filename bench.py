@@ -56,6 +56,9 @@ WORKLOADS = {
                         title="million-length forward"),
     "decode_step": dict(mode="step", Bt=256, D=5120, N=16, L=1, seed=4,
                         title="single-token decode step"),
+    "mamba1p4b_conv_fwd": dict(mode="fwd", conv=4, Bt=4, D=4096, N=16, L=4096, seed=2,
+                               title="Mamba-1.4B layer forward from the conv branch input "
+                                     "(width-4 causal conv + SiLU fused)"),
 }
 WORKLOAD = WORKLOADS["mamba1p4b_fwd"]
 METRIC = "selective scan: achieved HBM GB/s (% of roofline) and B*D*L*N state updates/s"
@@ -234,7 +237,8 @@ _INPUT_CACHE = {}
 def _oracle_worker(args):
     """Run the oracle on a slice of channels; returns (updates, seconds of the
     oracle call alone -- drawing the inputs is not timed, and is cached)."""
-    mode, seed, Bt, D, N, L, chans = args
+    mode, seed, Bt, D, N, L, chans = args[:7]
+    conv_k = args[7] if len(args) > 7 else 0
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
     import oracle
@@ -250,8 +254,16 @@ def _oracle_worker(args):
             x = make_inputs(Bt, D, N, L, seed=seed, in_dtype="bf16", channels=chans,
                             dy=(mode == "fwdbwd"))
         _INPUT_CACHE[key] = x
+    cw = cb = None
+    if conv_k:
+        import numpy as np
+        g = np.random.default_rng(seed + 1000)
+        cw = (0.5 * g.standard_normal((D, conv_k))).astype(np.float32)[chans]
+        cb = (0.1 * g.standard_normal(D)).astype(np.float32)[chans]
     t0 = time.perf_counter()
-    if mode == "fwd":
+    if mode == "fwd" and conv_k:
+        oracle.scan_fwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    elif mode == "fwd":
         oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
     elif mode == "fwdbwd":
         oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
@@ -276,11 +288,12 @@ class OracleTimer:
         w = WORKLOAD
         self.bt = w["Bt"] if w["mode"] == "step" else 1   # decode: all sequences of a channel
         warm_L = min(64, w["L"])
+        self.conv_k = w.get("conv", 0)
         self.pool.map(_oracle_worker, [(w["mode"], w["seed"], self.bt, w["D"], w["N"], warm_L,
-                                        [0])] * self.cores)
+                                        [0], self.conv_k)] * self.cores)
         probe = 16 if w["mode"] == "step" else 1
         _, t = _oracle_worker((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
-                               list(range(probe))))
+                               list(range(probe)), self.conv_k))
         self.t_channel = t / probe
         self.next = 0
 
@@ -294,13 +307,15 @@ class OracleTimer:
         start = 0 if fixed else self.next
         for i in range(self.cores):
             jobs.append((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
-                         [(start + i * per + j) % w["D"] for j in range(per)]))
+                         [(start + i * per + j) % w["D"] for j in range(per)], self.conv_k))
         if not fixed:
             self.next = (start + per * self.cores) % w["D"]
         res = self.pool.map(_oracle_worker, jobs)
         upd = sum(r[0] for r in res)
         busy = max(r[1] for r in res)
         what = {"fwd": "forward", "fwdbwd": "forward + backward", "step": "decode step"}[w["mode"]]
+        if self.conv_k:
+            what = "conv prologue + forward"
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
                 "sample": "%s of %d channels x %d batch rows x %d tokens x %d states of the %s "
                           "workload, one spawned process per core (%d channels each); slowest "
@@ -365,6 +380,14 @@ class Workload:
             self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
             self.bytes = fwd_bytes(Bt, D, N, L)
             self.exps = Bt * D * L * N
+            self.conv_k = w.get("conv", 0)
+            if self.conv_k:
+                # depthwise conv weights (D, K) and bias (D), read once
+                g = torch.Generator(device="cuda")
+                g.manual_seed(rank_seed(w["seed"], rank) + 1000)
+                self.conv_w = 0.5 * torch.randn(D, self.conv_k, generator=g, device="cuda")
+                self.conv_b = 0.1 * torch.randn(D, generator=g, device="cuda")
+                self.bytes += D * (self.conv_k + 1) * 4
             # B/C preparation + scan; the million-length sequence takes the
             # segmented plan (preparation, tail search, summary pass, carry,
             # scan)
@@ -414,6 +437,12 @@ class Workload:
                 self.rot_i = (self.rot_i + 1) % len(self.rot)
             ssm.ssm_scan_step(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], state,
                               a["Dv"], a["z"], a["delta_bias"], out_dtype=torch.bfloat16, y=self.y)
+            return
+        if self.conv_k:
+            # u holds the conv branch input x
+            ssm.ssm_scan_fwd_conv(a["u"], self.conv_w, self.conv_b, a["delta_raw"], a["A"], a["Bm"],
+                                  a["Cm"], a["Dv"], a["z"], a["delta_bias"], None,
+                                  out_dtype=torch.bfloat16, y=self.y, hL=self.hL, workspace=self.ws)
             return
         ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
                          a["delta_bias"], None, out_dtype=torch.bfloat16, y=self.y, hL=self.hL,
@@ -623,7 +652,7 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if wl.mode in ("fwd", "step"):
+        if wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0):
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
                        "scans and copies" % ("batch rows" if wl.w["Bt"] > 1 else "channels"))

@@ -111,6 +111,27 @@ SSM_API int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delt
                  void* y, float* hL, void* workspace, size_t ws_bytes,
                  ssm_stream_t stream);
 
+/* ssm_scan_fwd fed by the block's local-processing step ("Mamba Architecture
+ * Explained", section "The Architecture in Practice": a 1-D convolution with
+ * a SiLU activation before the selective SSM; "The convolution trick is gone
+ * -- what now?": one branch goes through a Conv1D and then the selective
+ * SSM).  Instead of u the call takes the branch input x and computes, per
+ * channel, a causal depthwise convolution of width conv_k with left zero
+ * padding, then SiLU:
+ *   u[b,d,t] = silu(conv_b[d] + sum_{k<conv_k} conv_w[d,k] * x[b,d,t-(conv_k-1)+k])
+ * (x at t < 0 is 0), inside the scan kernel; u never reaches HBM.
+ *   x : in_dtype (batch, dim, seqlen), required (layout of u).
+ *   conv_w : fp32 (dim, conv_k), required; conv_b : fp32 (dim), nullable (no bias).
+ *   conv_k : 1..4 (else SSM_ERR_SHAPE).
+ * Everything else as ssm_scan_fwd (same workspace size).  Built for 9 to 16
+ * states and rows of seqlen * element size a multiple of 16 bytes; other
+ * shapes return SSM_ERR_UNSUPPORTED before anything is enqueued. */
+SSM_API int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,
+                 const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, void* y, float* hL,
+                 void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
 /* Reverse mode of ssm_scan_fwd (the pages give no backward; it is the exact
  * derivative of the recurrence above).  Inputs are the forward inputs plus
  *   dy  : in_dtype (batch, dim, seqlen), required;   dhL : fp32, nullable (= 0).

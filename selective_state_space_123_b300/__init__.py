@@ -40,8 +40,9 @@ SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = -1, -2, -3, -4
 SSM_ERR_WORKSPACE, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_UNSUPPORTED = -5, -6, -7, -8
 
 # Every symbol include/ssm_scan.h declares.
-EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
-           "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait", "ssm_scan_fwd_noalloc")
+EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_bwd",
+           "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
+           "ssm_scan_fwd_noalloc")
 
 
 class ssm_shape(ctypes.Structure):
@@ -56,6 +57,9 @@ lib.ssm_scan_workspace_bytes.argtypes = [ctypes.POINTER(ssm_shape), ctypes.c_int
 lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
 lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 12 + [ctypes.c_size_t, _P]
 lib.ssm_scan_fwd.restype = ctypes.c_int
+lib.ssm_scan_fwd_conv.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, _P, ctypes.c_int] + [_P] * 11
+                                  + [ctypes.c_size_t, _P])
+lib.ssm_scan_fwd_conv.restype = ctypes.c_int
 lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 21 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd.restype = ctypes.c_int
 lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 11
@@ -168,6 +172,52 @@ def ssm_scan_fwd(u, delta_raw, A, B, C, D=None, z=None, delta_bias=None, h0=None
                           _ptr(hL), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_fwd")
+    return y, hL
+
+
+def ssm_scan_fwd_conv(x, conv_w, conv_b, delta_raw, A, B, C, D=None, z=None, delta_bias=None,
+                      h0=None, *, out_dtype: Optional[torch.dtype] = None, y=None, hL=None,
+                      return_final_state: bool = True, workspace=None,
+                      stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Forward scan fed by the block's conv prologue: x (Bt,D,L) is the branch
+    input, conv_w (D,K) fp32 with K <= 4, conv_b (D,) fp32 or None; the scan
+    input is u = silu(causal depthwise conv of x), computed in the kernel.
+    Other arguments and the result as ssm_scan_fwd."""
+    Bt, Dm, L = x.shape
+    N = A.shape[1]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_fwd_conv runs on CUDA tensors only")
+    tin = x.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    if conv_w is None or conv_w.dim() != 2:
+        raise ValueError("conv_w must be a (D, K) tensor")
+    K = conv_w.shape[1]
+    _check(x, "x", (Bt, Dm, L), tin, dev)
+    _check(conv_w, "conv_w", (Dm, K), torch.float32, dev)
+    _check(conv_b, "conv_b", (Dm,), torch.float32, dev)
+    _check(delta_raw, "delta_raw", (Bt, Dm, L), tin, dev)
+    _check(z, "z", (Bt, Dm, L), tin, dev)
+    _check(B, "B", (Bt, N, L), tin, dev)
+    _check(C, "C", (Bt, N, L), tin, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    _check(h0, "h0", (Bt, Dm, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev)
+    _check(y, "y", (Bt, Dm, L), out_dtype, dev)
+    if hL is None and return_final_state:
+        hL = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    _check(hL, "hL", (Bt, Dm, N), torch.float32, dev)
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, False, dev, workspace)
+    rc = lib.ssm_scan_fwd_conv(ctypes.byref(shape), _ptr(x), _ptr(conv_w), _ptr(conv_b), int(K),
+                               _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                               _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(hL), _ptr(workspace),
+                               workspace.numel(), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_fwd_conv")
     return y, hL
 
 

@@ -372,8 +372,9 @@ bool make_map_swz64(CUtensorMap* m, const void* base, uint64_t rows) {
     return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, const FwdParams& p,
-                       const FwdMaps& m, dim3 grid, cudaStream_t st) {
+cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, bool conv,
+                       const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    if (conv) return launch_fwd_conv_np16(pl.NT, tin, tout, summary, p, m, grid, pl.W, pl.smem, st);
     switch (pl.NP) {
         case 4: return launch_fwd_np4(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
         case 8: return launch_fwd_np8(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
@@ -443,24 +444,30 @@ size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     return bytes < kHeaderBytes ? kHeaderBytes : bytes;
 }
 
-int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
-                 const void* B, const void* C, const float* D, const void* z,
-                 const float* delta_bias, const float* h0, void* y, float* hL, void* workspace,
-                 size_t ws_bytes, ssm_stream_t stream) {
+// The forward, with or without the conv prologue (conv_w non-null: `u` is the
+// branch input x and u = silu(causal depthwise conv of x)).
+static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* conv_w,
+                         const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                         const void* B, const void* C, const float* D, const void* z,
+                         const float* delta_bias, const float* h0, void* y, float* hL,
+                         void* workspace, size_t ws_bytes, ssm_stream_t stream) {
     const int sc = shape_check(shape);
     if (sc != SSM_OK) return sc;
     const ssm_shape s = *shape;
     const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    const bool conv = conv_w != nullptr;
     const bool any_work = Bt > 0 && Dm > 0;
     if (!any_work) return SSM_OK;
     if (!A || !workspace) return !A ? SSM_ERR_NULL : SSM_ERR_WORKSPACE;
     if (L > 0 && (!u || !delta_raw || !B || !C || !y)) return SSM_ERR_NULL;
-    const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, hL, workspace};
+    const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, hL, workspace, conv_w, conv_b};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const FwdPlan pl = plan_fwd(s, device_sm_count());
+    // the conv prologue is built for 9..16 states and 16-byte token rows
+    if (conv && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
@@ -506,6 +513,9 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     p.stages = pl.stages;
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
+    p.conv_w = conv_w;
+    p.conv_b = conv_b;
+    p.conv_k = conv_k;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
 
     if (pl.nseg > 1) {
@@ -522,17 +532,36 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
                 return cuda_fail();
             p1.tstart = tstart;
         }
-        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, p1, maps,
+        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, conv, p1, maps,
                        dim3(gx, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess)
             return cuda_fail();
         if (launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, p.hloc, p.sumd, p.hin, st) !=
             cudaSuccess)
             return cuda_fail();
     }
-    if (launch_fwd(pl, s.in_dtype, s.out_dtype, false, p, maps,
+    if (launch_fwd(pl, s.in_dtype, s.out_dtype, false, conv, p, maps,
                    dim3(gx, (unsigned)Bt, (unsigned)pl.nseg), st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
+}
+
+int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, void* y, float* hL, void* workspace,
+                 size_t ws_bytes, ssm_stream_t stream) {
+    return scan_fwd_impl(shape, u, nullptr, nullptr, 0, delta_raw, A, B, C, D, z, delta_bias, h0, y,
+                         hL, workspace, ws_bytes, stream);
+}
+
+int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,
+                      const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                      const void* B, const void* C, const float* D, const void* z,
+                      const float* delta_bias, const float* h0, void* y, float* hL,
+                      void* workspace, size_t ws_bytes, ssm_stream_t stream) {
+    if (!conv_w) return SSM_ERR_NULL;
+    if (conv_k < 1 || conv_k > 4) return SSM_ERR_SHAPE;
+    return scan_fwd_impl(shape, x, conv_w, conv_b, conv_k, delta_raw, A, B, C, D, z, delta_bias, h0,
+                         y, hL, workspace, ws_bytes, stream);
 }
 
 int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,

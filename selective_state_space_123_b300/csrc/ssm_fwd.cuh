@@ -161,7 +161,7 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 // states, writes its per-token partial read-outs to the warp's exchange
 // buffer, and then finishes its own TPL tokens (sum over the NT lanes, D
 // skip, SiLU gate, store).  All exchange stays inside the warp.
-template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW>
+template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW, bool CONV = false>
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
            const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -309,6 +309,24 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
     const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
     double sum_d2 = 0.0;
+    // conv prologue: weights right-aligned to width 4 (leading zeros for a
+    // narrower kernel) and the last 3 branch inputs before the current chunk
+    float cw4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cbias = 0.0f, xhalo[3] = {0.0f, 0.0f, 0.0f};
+    if constexpr (CONV) {
+        if (ch_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // static indices: the weights stay in registers
+                const int kk = q - (4 - p.conv_k);
+                if (kk >= 0) cw4[q] = p.conv_w[d * p.conv_k + kk];
+            }
+            cbias = p.conv_b ? p.conv_b[d] : 0.0f;
+            const int64_t t0 = k_begin * kT;   // a segment starting inside the sequence
+            const TIN* xr = static_cast<const TIN*>(p.u) + row * L;
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+                if (t0 - 3 + q >= 0) xhalo[q] = Elem<TIN>::to_f(xr[t0 - 3 + q]);
+        }
+    }
     bool dead = false;   // a bounded wait expired: stop working (warp-uniform)
 
     for (int64_t k = k_begin; k < k_end && !dead; ++k) {
@@ -346,6 +364,26 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     for (int q = 0; q < 8; ++q) {
                         uo[8 * k8 + q] = t8[q];
                         dv[8 * k8 + q] = r8[q];
+                    }
+                }
+                if constexpr (CONV) {
+                    // the tile holds the branch input x: u = silu(conv of x);
+                    // the 3 inputs before this lane's first token come from
+                    // the tile, or from the previous chunk at token 0
+                    float prev[8];
+                    load_raw8r<TIN>(st, CH, c, tb >= 8 ? tb - 8 : 0, prev);
+                    float xw[TPL + 3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) xw[q] = tb > 0 ? prev[5 + q] : xhalo[q];
+#pragma unroll
+                    for (int q = 0; q < TPL; ++q) xw[3 + q] = uo[q];
+#pragma unroll
+                    for (int q = 0; q < TPL; ++q) {
+                        float a = fmaf(cw4[0], xw[q], cbias);
+                        a = fmaf(cw4[1], xw[q + 1], a);
+                        a = fmaf(cw4[2], xw[q + 2], a);
+                        a = fmaf(cw4[3], xw[q + 3], a);
+                        uo[q] = a * rcp(1.0f + ex2(-kLog2e * a));
                     }
                 }
                 const bool full = nvalid == kT;   // warp-uniform: no padded token
@@ -411,6 +449,13 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
                 __syncwarp();   // before the next super-block overwrites the buffer
             }
+        }
+        if constexpr (CONV) {
+            // the chunk's last 3 inputs start the next chunk's convolution
+            float last[8];
+            load_raw8r<TIN>(st, CH, c, kT - 8, last);
+#pragma unroll
+            for (int q = 0; q < 3; ++q) xhalo[q] = last[5 + q];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);

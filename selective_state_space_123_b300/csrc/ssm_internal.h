@@ -28,6 +28,9 @@ cudaError_t launch_fwd_np8(int NT, int tin, int tout, bool summary, bool tma_raw
 cudaError_t launch_fwd_np16(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                             size_t smem, cudaStream_t st);
+// The forward with the conv prologue, padded state size 16, TMA tiles.
+cudaError_t launch_fwd_conv_np16(int NT, int tin, int tout, bool summary, const FwdParams& p,
+                                 const FwdMaps& m, dim3 grid, int warps, size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                             size_t smem, cudaStream_t st);

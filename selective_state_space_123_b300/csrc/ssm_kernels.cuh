@@ -57,6 +57,12 @@ struct FwdParams {
     // the search, or by pass 1 where it runs the whole segment
     const int* tstart;
     int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
+    // conv prologue (the kernel instantiated with CONV): u is computed from
+    // the branch input x (passed as `u`) by a causal depthwise convolution of
+    // width conv_k <= 4 and SiLU; conv_w (D, conv_k), conv_b (D) nullable
+    const float* conv_w;
+    const float* conv_b;
+    int conv_k;
     int* status;
     uint64_t timeout_ns;
 };
@@ -101,6 +107,12 @@ struct BwdParams {
     float* dbias;           // nullable, accumulated (zeroed by the host)
     float* dh0;             // nullable
     int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
+    // conv prologue (the kernel instantiated with CONV): u is computed from
+    // the branch input x (passed as `u`) by a causal depthwise convolution of
+    // width conv_k <= 4 and SiLU; conv_w (D, conv_k), conv_b (D) nullable
+    const float* conv_w;
+    const float* conv_b;
+    int conv_k;
     int* status;
     uint64_t timeout_ns;
 };

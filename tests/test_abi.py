@@ -73,6 +73,27 @@ def test_fwd_argument_errors(pkg):
     assert _call_fwd(pkg, S(d=0), {"u": None, "y": None}) == pkg.SSM_OK
 
 
+def _call_fwd_conv(pkg, shape, conv_w=0x8000, conv_k=4, ws_bytes=1 << 24, ws=0x10000):
+    V = lambda x: None if x is None else ctypes.c_void_p(x)
+    return pkg.lib.ssm_scan_fwd_conv(ctypes.byref(shape), V(0x1000), V(conv_w), None, conv_k,
+                                     V(0x2000), V(0x3000), V(0x4000), V(0x5000), None, None, None,
+                                     None, V(0x6000), None, V(ws), ws_bytes, None)
+
+
+def test_fwd_conv_argument_errors(pkg):
+    """The conv entry point refuses what it does not build before any GPU work."""
+    S = lambda n=16, l=64, ti=1: pkg.make_shape(2, 8, n, l, ti, 0)
+    assert _call_fwd_conv(pkg, S(), conv_w=None) == pkg.SSM_ERR_NULL
+    assert _call_fwd_conv(pkg, S(), conv_k=0) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd_conv(pkg, S(), conv_k=5) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd_conv(pkg, S(), conv_w=0x8004) == pkg.SSM_ERR_ALIGN
+    # built for 9..16 states and 16-byte token rows
+    assert _call_fwd_conv(pkg, S(n=32)) == pkg.SSM_ERR_UNSUPPORTED
+    assert _call_fwd_conv(pkg, S(n=4)) == pkg.SSM_ERR_UNSUPPORTED
+    assert _call_fwd_conv(pkg, S(l=63)) == pkg.SSM_ERR_UNSUPPORTED
+    assert _call_fwd_conv(pkg, S(l=62, ti=0)) == pkg.SSM_ERR_UNSUPPORTED
+
+
 def test_workspace_query(pkg):
     ok = pkg.make_shape(4, 4096, 16, 4096, 1, 1)
     n = pkg.ssm_scan_workspace_bytes(ok)
