@@ -15,6 +15,8 @@ Selective State Spaces Achieve 5x Faster Inference Than Transformers"
 Architecture Explained" (section "How State Space Models Work"), closed forms,
 the remember/forget limits of "State Space Models (SSMs) & Mamba" (section
 "The Magic of Selective Scan"), and finite differences for the backward.
+The packed-sequence form (``scan_fwd_varlen``) is pinned against the batched
+scan with one sequence per batch row, and by the independence of sequences.
 """
 from __future__ import annotations
 
@@ -107,6 +109,42 @@ def scan_fwd_conv(x, conv_w, conv_b, delta_raw, A, Bm, Cm, Dv=None, z=None, delt
                   h0=None):
     """The scan fed by the block's conv prologue: scan_fwd(conv_silu(x), ...)."""
     return scan_fwd(conv_silu(x, conv_w, conv_b), delta_raw, A, Bm, Cm, Dv, z, delta_bias, h0)
+
+
+def scan_fwd_varlen(u, delta_raw, A, Bm, Cm, cu_seqlens, Dv=None, z=None, delta_bias=None,
+                    h0=None, conv_w=None, conv_b=None):
+    """Packed sequences ("Mamba Architecture Explained", section "Problem 3:
+    Ecosystem maturity": several sequences packed into one row): every batch
+    row holds nseq = len(cu_seqlens) - 1 sequences, sequence s at tokens
+    [cu_seqlens[s], cu_seqlens[s+1]).  Each is an independent sequence: its
+    state starts at h0[s] (zeros when h0 is None), its conv window (conv_w
+    given) starts from zeros, and its final state is returned.  Shapes as in
+    scan_fwd, with h0 and the returned final states (nseq, Bt, D, N); an empty
+    sequence's final state is its initial state."""
+    u, delta_raw, Bm, Cm, z = map(_f64, (u, delta_raw, Bm, Cm, z))
+    cu = [int(v) for v in cu_seqlens]
+    Bt, D, L = u.shape
+    N = A.shape[1]
+    nseq = len(cu) - 1
+    assert nseq >= 1 and cu[0] == 0 and cu[-1] == L
+    assert all(cu[s] <= cu[s + 1] for s in range(nseq))
+    h0 = None if h0 is None else _f64(h0)
+    assert h0 is None or h0.shape == (nseq, Bt, D, N)
+    y = np.empty((Bt, D, L), np.float64)
+    hL = np.empty((nseq, Bt, D, N), np.float64)
+    for s in range(nseq):
+        lo, hi = cu[s], cu[s + 1]
+        hs = None if h0 is None else h0[s]
+        if hi == lo:
+            hL[s] = 0.0 if hs is None else hs
+            continue
+        us = u[:, :, lo:hi]
+        if conv_w is not None:
+            us = conv_silu(us, conv_w, conv_b)
+        ys, hL[s] = scan_fwd(us, delta_raw[:, :, lo:hi], A, Bm[:, :, lo:hi], Cm[:, :, lo:hi], Dv,
+                             None if z is None else z[:, :, lo:hi], delta_bias, hs)
+        y[:, :, lo:hi] = ys
+    return y, hL
 
 
 def scan_fwd(u, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None, h0=None):

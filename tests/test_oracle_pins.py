@@ -389,3 +389,66 @@ def test_scan_fwd_conv_is_scan_of_conv_output():
     y2, h2 = oracle.scan_fwd(u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
     np.testing.assert_array_equal(y1, y2)
     np.testing.assert_array_equal(h1, h2)
+
+
+# ---- packed sequences ("Mamba Architecture Explained", section "Problem 3:
+# Ecosystem maturity": sequence packing)
+
+def _pack(rows):
+    """Concatenate per-sequence arrays (Bt, X, Ls) along the token axis."""
+    return np.concatenate(rows, axis=2)
+
+
+@pytest.mark.parametrize("conv", [False, True])
+def test_varlen_equal_lengths_match_batched_rows(conv):
+    """Four equal-length sequences packed into one row give what the batched
+    scan gives with each sequence as its own batch row (a different loop of
+    the oracle: the batch dimension, not slicing)."""
+    S, D, N, Ls = 4, 5, 4, 13
+    x = make_inputs(S, D, N, Ls, seed=50, in_dtype="f32", h0=True)
+    rng = np.random.default_rng(51)
+    w = rng.standard_normal((D, 3)) if conv else None
+    b = rng.standard_normal(D) if conv else None
+    rows = lambda a: _pack([a[s:s + 1] for s in range(S)])
+    cu = [Ls * s for s in range(S + 1)]
+    y, hL = oracle.scan_fwd_varlen(rows(x.u), rows(x.delta_raw), x.A, rows(x.Bm), rows(x.Cm), cu,
+                                   x.Dv, rows(x.z), x.delta_bias, x.h0[:, None], w, b)
+    u = oracle.conv_silu(x.u, w, b) if conv else x.u
+    yb, hb = oracle.scan_fwd(u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    np.testing.assert_allclose(y[0], np.concatenate(list(yb), axis=1), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(hL[:, 0], hb, rtol=1e-13, atol=1e-13)
+
+
+def test_varlen_one_sequence_is_the_plain_scan():
+    x = make_inputs(2, 4, 4, 29, seed=52, in_dtype="f32", h0=True)
+    y, hL = oracle.scan_fwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, [0, 29], x.Dv, x.z,
+                                   x.delta_bias, x.h0[None])
+    y2, h2 = oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+    np.testing.assert_array_equal(y, y2)
+    np.testing.assert_array_equal(hL[0], h2)
+
+
+def test_varlen_sequences_do_not_see_each_other():
+    """Changing one sequence's inputs changes no other sequence's outputs;
+    empty sequences return their initial state and change nothing."""
+    x = make_inputs(1, 3, 4, 40, seed=53, in_dtype="f32")
+    cu = [0, 0, 11, 11, 25, 40, 40]
+    h0 = np.random.default_rng(54).standard_normal((6, 1, 3, 4))
+    y, hL = oracle.scan_fwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, cu, x.Dv, x.z,
+                                   x.delta_bias, h0)
+    u2 = x.u.copy()
+    u2[:, :, 11:25] += 1.0
+    y2, h2 = oracle.scan_fwd_varlen(u2, x.delta_raw, x.A, x.Bm, x.Cm, cu, x.Dv, x.z,
+                                    x.delta_bias, h0)
+    assert np.array_equal(y[:, :, :11], y2[:, :, :11]) and np.array_equal(y[:, :, 25:], y2[:, :, 25:])
+    assert not np.allclose(y[:, :, 11:25], y2[:, :, 11:25])
+    for s in (0, 1, 4, 5):
+        np.testing.assert_array_equal(hL[s], h2[s])
+    for s in (0, 2, 5):                   # empty sequences
+        np.testing.assert_array_equal(hL[s], h0[s])
+    # a sequence boundary is a reset: zero B*u in front of sequence 3 leaves it unchanged
+    y3, _ = oracle.scan_fwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, [0, 25, 40], x.Dv, x.z,
+                                   x.delta_bias, None)
+    y4, _ = oracle.scan_fwd(x.u[:, :, 25:], x.delta_raw[:, :, 25:], x.A, x.Bm[:, :, 25:],
+                            x.Cm[:, :, 25:], x.Dv, x.z[:, :, 25:], x.delta_bias, None)
+    np.testing.assert_array_equal(y3[:, :, 25:], y4)
