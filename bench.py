@@ -59,6 +59,13 @@ WORKLOADS = {
     "mamba1p4b_conv_fwd": dict(mode="fwd", conv=4, Bt=4, D=4096, N=16, L=4096, seed=2,
                                title="Mamba-1.4B layer forward from the conv branch input "
                                      "(width-4 causal conv + SiLU fused)"),
+    # 17 sequences of 256..16384 tokens (log-uniform) packed into one row;
+    # the planner cuts the row into 4 segments at 148 SMs: B/C preparation,
+    # sequence check, tail search, summary pass, carry, scan = 6 launches
+    "packed_mamba1p4b_fwd": dict(mode="fwd", varlen=True, Bt=1, D=4096, N=16, L=65536, seed=5,
+                                 launches=6,
+                                 title="Mamba-1.4B layer forward over packed sequences of mixed "
+                                       "length"),
 }
 WORKLOAD = WORKLOADS["mamba1p4b_fwd"]
 METRIC = "selective scan: achieved HBM GB/s (% of roofline) and B*D*L*N state updates/s"
@@ -239,6 +246,7 @@ def _oracle_worker(args):
     oracle call alone -- drawing the inputs is not timed, and is cached)."""
     mode, seed, Bt, D, N, L, chans = args[:7]
     conv_k = args[7] if len(args) > 7 else 0
+    varlen = args[8] if len(args) > 8 else False
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
     import oracle
@@ -261,7 +269,12 @@ def _oracle_worker(args):
         cw = (0.5 * g.standard_normal((D, conv_k))).astype(np.float32)[chans]
         cb = (0.1 * g.standard_normal(D)).astype(np.float32)[chans]
     t0 = time.perf_counter()
-    if mode == "fwd" and conv_k:
+    if mode == "fwd" and varlen:
+        from scan_inputs import packed_seqlens
+        cu = packed_seqlens(L, seed=seed)
+        t0 = time.perf_counter()
+        oracle.scan_fwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, cu, x.Dv, x.z, x.delta_bias)
+    elif mode == "fwd" and conv_k:
         oracle.scan_fwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
     elif mode == "fwd":
         oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
@@ -289,11 +302,12 @@ class OracleTimer:
         self.bt = w["Bt"] if w["mode"] == "step" else 1   # decode: all sequences of a channel
         warm_L = min(64, w["L"])
         self.conv_k = w.get("conv", 0)
+        self.varlen = bool(w.get("varlen"))
         self.pool.map(_oracle_worker, [(w["mode"], w["seed"], self.bt, w["D"], w["N"], warm_L,
-                                        [0], self.conv_k)] * self.cores)
+                                        [0], self.conv_k, self.varlen)] * self.cores)
         probe = 16 if w["mode"] == "step" else 1
         _, t = _oracle_worker((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
-                               list(range(probe)), self.conv_k))
+                               list(range(probe)), self.conv_k, self.varlen))
         self.t_channel = t / probe
         self.next = 0
 
@@ -307,7 +321,8 @@ class OracleTimer:
         start = 0 if fixed else self.next
         for i in range(self.cores):
             jobs.append((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
-                         [(start + i * per + j) % w["D"] for j in range(per)], self.conv_k))
+                         [(start + i * per + j) % w["D"] for j in range(per)], self.conv_k,
+                         self.varlen))
         if not fixed:
             self.next = (start + per * self.cores) % w["D"]
         res = self.pool.map(_oracle_worker, jobs)
@@ -316,6 +331,8 @@ class OracleTimer:
         what = {"fwd": "forward", "fwdbwd": "forward + backward", "step": "decode step"}[w["mode"]]
         if self.conv_k:
             what = "conv prologue + forward"
+        if self.varlen:
+            what = "packed-sequence forward"
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
                 "sample": "%s of %d channels x %d batch rows x %d tokens x %d states of the %s "
                           "workload, one spawned process per core (%d channels each); slowest "
@@ -381,6 +398,15 @@ class Workload:
             self.bytes = fwd_bytes(Bt, D, N, L)
             self.exps = Bt * D * L * N
             self.conv_k = w.get("conv", 0)
+            self.cu = None
+            if w.get("varlen"):
+                from scan_inputs import packed_seqlens
+                self.cu = torch.tensor(packed_seqlens(L, seed=rank_seed(w["seed"], rank)),
+                                       dtype=torch.int32, device="cuda")
+                nseq = self.cu.numel() - 1
+                # one final state per sequence, and the starts
+                self.hL = torch.empty(nseq, Bt, D, N, dtype=torch.float32, device="cuda")
+                self.bytes += (nseq - 1) * Bt * D * N * 4 + (nseq + 1) * 4
             if self.conv_k:
                 # depthwise conv weights (D, K) and bias (D), read once
                 g = torch.Generator(device="cuda")
@@ -391,7 +417,7 @@ class Workload:
             # B/C preparation + scan; the million-length sequence takes the
             # segmented plan (preparation, tail search, summary pass, carry,
             # scan)
-            self.launches = 5 if L >= (1 << 18) and Bt * D <= 4096 else 2
+            self.launches = w.get("launches", 5 if L >= (1 << 18) and Bt * D <= 4096 else 2)
             self.outs = [self.y, self.hL]
             self.grads = None
             if self.mode == "fwdbwd":
@@ -437,6 +463,11 @@ class Workload:
                 self.rot_i = (self.rot_i + 1) % len(self.rot)
             ssm.ssm_scan_step(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], state,
                               a["Dv"], a["z"], a["delta_bias"], out_dtype=torch.bfloat16, y=self.y)
+            return
+        if self.cu is not None:
+            ssm.ssm_scan_fwd_varlen(a["u"], self.cu, a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"],
+                                    a["z"], a["delta_bias"], None, out_dtype=torch.bfloat16, y=self.y,
+                                    hL=self.hL, workspace=self.ws)
             return
         if self.conv_k:
             # u holds the conv branch input x
@@ -652,7 +683,7 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0):
+        if wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0) and getattr(wl, "cu", None) is None:
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
                        "scans and copies" % ("batch rows" if wl.w["Bt"] > 1 else "channels"))

@@ -87,7 +87,8 @@ enum {
     SSM_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -6,        /* a CUDA runtime call failed (launch, attribute query) */
     SSM_ERR_TIMEOUT = -7,     /* device side: a bounded wait expired; outputs undefined */
-    SSM_ERR_UNSUPPORTED = -8  /* valid request the library does not implement */
+    SSM_ERR_UNSUPPORTED = -8, /* valid request the library does not implement */
+    SSM_ERR_SEQLENS = -9      /* device side: packed-sequence starts not 0 <= ... <= seqlen */
 };
 
 /* Bytes of device workspace the call needs for this shape on the current
@@ -132,6 +133,34 @@ SSM_API int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float
                  const float* delta_bias, const float* h0, void* y, float* hL,
                  void* workspace, size_t ws_bytes, ssm_stream_t stream);
 
+/* ssm_scan_fwd (or ssm_scan_fwd_conv) over packed sequences ("Mamba
+ * Architecture Explained", section "Problem 3: Ecosystem maturity": packing
+ * several sequences into one row needs its own kernel support).  Every batch
+ * row holds the same nseq >= 1 sequences back to back: sequence s covers
+ * tokens [cu_seqlens[s], cu_seqlens[s+1]), with
+ * 0 = cu_seqlens[0] <= cu_seqlens[1] <= ... <= cu_seqlens[nseq] = seqlen
+ * (empty sequences allowed).  Each sequence is scanned on its own: its state
+ * starts at h0[s] (zero when h0 is NULL) and, with conv_w given, its
+ * convolution window starts from zeros; nothing crosses a start.
+ *   cu_seqlens : int32 (nseq + 1), device memory, required.  Start values
+ *     that break the order above are reported as SSM_ERR_SEQLENS in the
+ *     workspace status word (ssm_get_status); the outputs are then undefined,
+ *     and no access goes outside the buffers.
+ *   u : in_dtype (batch, dim, seqlen): u itself (conv_w NULL) or the conv
+ *     branch input x (conv_w given; conv_b, conv_k as in ssm_scan_fwd_conv).
+ *   h0 : fp32 (nseq, batch, dim, dstate), nullable.
+ *   hL : fp32 (nseq, batch, dim, dstate), nullable: every sequence's final
+ *     state (an empty sequence's is its initial state).
+ * Everything else as ssm_scan_fwd (same workspace size).  Built for 9 to 16
+ * states and rows of seqlen * element size a multiple of 16 bytes (pad the
+ * packed row with a last sequence); other shapes return SSM_ERR_UNSUPPORTED
+ * before anything is enqueued. */
+SSM_API int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,
+                 int nseq, const float* conv_w, const float* conv_b, int conv_k,
+                 const void* delta_raw, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, const float* h0,
+                 void* y, float* hL, void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
 /* Reverse mode of ssm_scan_fwd (the pages give no backward; it is the exact
  * derivative of the recurrence above).  Inputs are the forward inputs plus
  *   dy  : in_dtype (batch, dim, seqlen), required;   dhL : fp32, nullable (= 0).
@@ -166,7 +195,7 @@ SSM_API int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in
                   ssm_stream_t stream);
 
 /* Synchronise `stream`, then return the device status word held in
- * `workspace` (SSM_OK or SSM_ERR_TIMEOUT) and reset it to SSM_OK.  Returns
+ * `workspace` (SSM_OK, SSM_ERR_TIMEOUT or SSM_ERR_SEQLENS) and reset it to SSM_OK.  Returns
  * SSM_ERR_CUDA if the synchronisation itself fails, SSM_ERR_NULL for a NULL
  * workspace. */
 SSM_API int ssm_get_status(void* workspace, ssm_stream_t stream);

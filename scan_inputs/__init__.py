@@ -143,6 +143,20 @@ def make_step_inputs(Bt: int, D: int, N: int, *, seed: int, in_dtype: str = "bf1
                 A=x.A, Dv=x.Dv, delta_bias=x.delta_bias, state=x.h0)
 
 
+def packed_seqlens(L: int, *, seed: int, lo: int = 256, hi: int = 16384) -> list:
+    """Start offsets (nseq + 1 ints, 0 first, L last) of sequences packed into
+    one row of L tokens: lengths log-uniform in [lo, hi], drawn until the row
+    is full, the last one cut to fit (documents of mixed length packed for
+    one pass, "Mamba Architecture Explained", section "Problem 3: Ecosystem
+    maturity")."""
+    g = np.random.default_rng(np.random.SeedSequence([seed, 0x5EC]))
+    cu = [0]
+    while cu[-1] < L:
+        n = int(np.exp(g.uniform(np.log(lo), np.log(hi))))
+        cu.append(min(L, cu[-1] + max(1, n)))
+    return cu
+
+
 # ----------------------------------------------------------------------------
 # The five workloads (shape, dtype and recipe switches).
 # ----------------------------------------------------------------------------

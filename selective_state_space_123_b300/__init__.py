@@ -38,10 +38,11 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_OK = 0
 SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = -1, -2, -3, -4
 SSM_ERR_WORKSPACE, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_UNSUPPORTED = -5, -6, -7, -8
+SSM_ERR_SEQLENS = -9
 
 # Every symbol include/ssm_scan.h declares.
-EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_bwd",
-           "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
+EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_fwd_varlen",
+           "ssm_scan_bwd", "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
            "ssm_scan_fwd_noalloc")
 
 
@@ -60,6 +61,9 @@ lib.ssm_scan_fwd.restype = ctypes.c_int
 lib.ssm_scan_fwd_conv.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, _P, ctypes.c_int] + [_P] * 11
                                   + [ctypes.c_size_t, _P])
 lib.ssm_scan_fwd_conv.restype = ctypes.c_int
+lib.ssm_scan_fwd_varlen.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, ctypes.c_int, _P, _P,
+                                     ctypes.c_int] + [_P] * 11 + [ctypes.c_size_t, _P])
+lib.ssm_scan_fwd_varlen.restype = ctypes.c_int
 lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 21 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd.restype = ctypes.c_int
 lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 11
@@ -218,6 +222,62 @@ def ssm_scan_fwd_conv(x, conv_w, conv_b, delta_raw, A, B, C, D=None, z=None, del
                                workspace.numel(), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_fwd_conv")
+    return y, hL
+
+
+def ssm_scan_fwd_varlen(u, cu_seqlens, delta_raw, A, B, C, D=None, z=None, delta_bias=None,
+                        h0=None, *, conv_w=None, conv_b=None, out_dtype: Optional[torch.dtype] = None,
+                        y=None, hL=None, return_final_state: bool = True, workspace=None,
+                        stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Forward scan over packed sequences: every batch row holds nseq
+    sequences, sequence s at tokens [cu_seqlens[s], cu_seqlens[s+1])
+    (cu_seqlens: int32 (nseq+1,) on the device, 0 first, L last).  Each
+    sequence starts from h0[s] (h0: (nseq,Bt,D,N) fp32, or zeros) and, with
+    conv_w (D,K) given, u is the conv branch input x with the window
+    restarting at every sequence start.  Returns (y (Bt,D,L), hL (nseq,Bt,D,N)
+    fp32 or None); other arguments as ssm_scan_fwd."""
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_fwd_varlen runs on CUDA tensors only")
+    if not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D tensor of nseq + 1 >= 2 offsets")
+    nseq = cu_seqlens.numel() - 1
+    tin = u.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    _check(cu_seqlens, "cu_seqlens", (nseq + 1,), torch.int32, dev)
+    K = 0
+    if conv_w is not None:
+        if conv_w.dim() != 2:
+            raise ValueError("conv_w must be a (D, K) tensor")
+        K = conv_w.shape[1]
+        _check(conv_w, "conv_w", (Dm, K), torch.float32, dev)
+        _check(conv_b, "conv_b", (Dm,), torch.float32, dev)
+    _check(u, "u", (Bt, Dm, L), tin, dev)
+    _check(delta_raw, "delta_raw", (Bt, Dm, L), tin, dev)
+    _check(z, "z", (Bt, Dm, L), tin, dev)
+    _check(B, "B", (Bt, N, L), tin, dev)
+    _check(C, "C", (Bt, N, L), tin, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    _check(h0, "h0", (nseq, Bt, Dm, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev)
+    _check(y, "y", (Bt, Dm, L), out_dtype, dev)
+    if hL is None and return_final_state:
+        hL = torch.empty((nseq, Bt, Dm, N), dtype=torch.float32, device=dev)
+    _check(hL, "hL", (nseq, Bt, Dm, N), torch.float32, dev)
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, False, dev, workspace)
+    rc = lib.ssm_scan_fwd_varlen(ctypes.byref(shape), _ptr(u), _ptr(cu_seqlens), int(nseq),
+                                 _ptr(conv_w), _ptr(conv_b if conv_w is not None else None), int(K),
+                                 _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                 _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(hL), _ptr(workspace),
+                                 workspace.numel(), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_fwd_varlen")
     return y, hL
 
 

@@ -372,8 +372,10 @@ bool make_map_swz64(CUtensorMap* m, const void* base, uint64_t rows) {
     return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, bool conv,
+cudaError_t launch_fwd(const FwdPlan& pl, int tin, int tout, bool summary, bool conv, bool varlen,
                        const FwdParams& p, const FwdMaps& m, dim3 grid, cudaStream_t st) {
+    if (varlen)
+        return launch_fwd_varlen_np16(pl.NT, tin, tout, summary, conv, p, m, grid, pl.W, pl.smem, st);
     if (conv) return launch_fwd_conv_np16(pl.NT, tin, tout, summary, p, m, grid, pl.W, pl.smem, st);
     switch (pl.NP) {
         case 4: return launch_fwd_np4(pl.NT, tin, tout, summary, pl.tma_raw, p, m, grid, pl.W, pl.smem, st);
@@ -433,6 +435,7 @@ const char* ssm_strerror(int code) {
         case SSM_ERR_CUDA: return "a CUDA runtime call failed";
         case SSM_ERR_TIMEOUT: return "device-side bounded wait expired";
         case SSM_ERR_UNSUPPORTED: return "unsupported request";
+        case SSM_ERR_SEQLENS: return "packed-sequence starts out of order or out of range";
         default: return "unknown status";
     }
 }
@@ -445,9 +448,11 @@ size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
 }
 
 // The forward, with or without the conv prologue (conv_w non-null: `u` is the
-// branch input x and u = silu(causal depthwise conv of x)).
+// branch input x and u = silu(causal depthwise conv of x)), over whole rows
+// or over packed sequences (cu_seqlens non-null).
 static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* conv_w,
-                         const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                         const float* conv_b, int conv_k, const int32_t* cu_seqlens, int nseq,
+                         const void* delta_raw, const float* A,
                          const void* B, const void* C, const float* D, const void* z,
                          const float* delta_bias, const float* h0, void* y, float* hL,
                          void* workspace, size_t ws_bytes, ssm_stream_t stream) {
@@ -456,22 +461,31 @@ static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* con
     const ssm_shape s = *shape;
     const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
     const bool conv = conv_w != nullptr;
+    const bool varlen = cu_seqlens != nullptr;
     const bool any_work = Bt > 0 && Dm > 0;
     if (!any_work) return SSM_OK;
     if (!A || !workspace) return !A ? SSM_ERR_NULL : SSM_ERR_WORKSPACE;
     if (L > 0 && (!u || !delta_raw || !B || !C || !y)) return SSM_ERR_NULL;
     const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, y, hL, workspace, conv_w, conv_b};
+    if (varlen && ((uintptr_t)cu_seqlens % 4) != 0) return SSM_ERR_ALIGN;
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const FwdPlan pl = plan_fwd(s, device_sm_count());
     // the conv prologue is built for 9..16 states and 16-byte token rows
-    if (conv && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
+    if ((conv || varlen) && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
 
+    const int64_t per_seq = Bt * Dm * N;   // floats of one sequence's state (packed h0, hL)
+    if (L == 0 && varlen) {
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+        if (launch_varlen_prep(cu_seqlens, nseq, 0, per_seq, h0, hL, status, st) != cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
     if (L == 0) {
         if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
         if (hL) {
@@ -485,6 +499,8 @@ static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* con
 
     float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
     if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
+        return cuda_fail();
+    if (varlen && launch_varlen_prep(cu_seqlens, nseq, L, per_seq, h0, hL, status, st) != cudaSuccess)
         return cuda_fail();
 
     const int eb = dtype_bytes(s.in_dtype);
@@ -516,6 +532,8 @@ static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* con
     p.conv_w = conv_w;
     p.conv_b = conv_b;
     p.conv_k = conv_k;
+    p.cu_seqlens = cu_seqlens;
+    p.nseq = nseq;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
 
     if (pl.nseg > 1) {
@@ -532,14 +550,14 @@ static int scan_fwd_impl(const ssm_shape* shape, const void* u, const float* con
                 return cuda_fail();
             p1.tstart = tstart;
         }
-        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, conv, p1, maps,
+        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, conv, varlen, p1, maps,
                        dim3(gx, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess)
             return cuda_fail();
         if (launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, p.hloc, p.sumd, p.hin, st) !=
             cudaSuccess)
             return cuda_fail();
     }
-    if (launch_fwd(pl, s.in_dtype, s.out_dtype, false, conv, p, maps,
+    if (launch_fwd(pl, s.in_dtype, s.out_dtype, false, conv, varlen, p, maps,
                    dim3(gx, (unsigned)Bt, (unsigned)pl.nseg), st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
@@ -549,8 +567,8 @@ int ssm_scan_fwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
                  const void* B, const void* C, const float* D, const void* z,
                  const float* delta_bias, const float* h0, void* y, float* hL, void* workspace,
                  size_t ws_bytes, ssm_stream_t stream) {
-    return scan_fwd_impl(shape, u, nullptr, nullptr, 0, delta_raw, A, B, C, D, z, delta_bias, h0, y,
-                         hL, workspace, ws_bytes, stream);
+    return scan_fwd_impl(shape, u, nullptr, nullptr, 0, nullptr, 0, delta_raw, A, B, C, D, z,
+                         delta_bias, h0, y, hL, workspace, ws_bytes, stream);
 }
 
 int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,
@@ -560,8 +578,23 @@ int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float* conv_w
                       void* workspace, size_t ws_bytes, ssm_stream_t stream) {
     if (!conv_w) return SSM_ERR_NULL;
     if (conv_k < 1 || conv_k > 4) return SSM_ERR_SHAPE;
-    return scan_fwd_impl(shape, x, conv_w, conv_b, conv_k, delta_raw, A, B, C, D, z, delta_bias, h0,
-                         y, hL, workspace, ws_bytes, stream);
+    return scan_fwd_impl(shape, x, conv_w, conv_b, conv_k, nullptr, 0, delta_raw, A, B, C, D, z,
+                         delta_bias, h0, y, hL, workspace, ws_bytes, stream);
+}
+
+int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens, int nseq,
+                        const float* conv_w, const float* conv_b, int conv_k,
+                        const void* delta_raw, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, const float* h0,
+                        void* y, float* hL, void* workspace, size_t ws_bytes,
+                        ssm_stream_t stream) {
+    if (!cu_seqlens) return SSM_ERR_NULL;
+    if (nseq < 1) return SSM_ERR_SHAPE;
+    if (conv_w && (conv_k < 1 || conv_k > 4)) return SSM_ERR_SHAPE;
+    if (!conv_w) conv_k = 0;
+    return scan_fwd_impl(shape, u, conv_w, conv_w ? conv_b : nullptr, conv_k, cu_seqlens, nseq,
+                         delta_raw, A, B, C, D, z, delta_bias, h0, y, hL, workspace, ws_bytes,
+                         stream);
 }
 
 int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,

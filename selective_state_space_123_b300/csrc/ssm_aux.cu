@@ -78,9 +78,41 @@ __global__ void carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg, con
     float h = (h0 && n < N) ? h0[row * N + n] : 0.0f;
     for (int s = 0; s < nseg; ++s) {
         hin[(s * seg_stride + row) * NP + n] = h;
-        if (s + 1 < nseg)
-            h = ex2(a * sumd[s * seg_stride + row]) * h + hloc[(s * seg_stride + row) * NP + n];
+        if (s + 1 < nseg) {
+            const float sd = sumd[s * seg_stride + row];
+            h = (sd >= kTailSat ? 0.0f : ex2(a * sd) * h) + hloc[(s * seg_stride + row) * NP + n];
+        }
     }
+}
+
+// Packed sequences: block 0 checks the starts; every block takes a share of
+// the sequences and gives each empty one its initial state as final state
+// (the scan kernels write the others).  per_seq = Bt * D * N floats.
+__global__ void varlen_prep_kernel(const int* __restrict__ cu, int nseq, int64_t L, int64_t per_seq,
+                                   const float* __restrict__ h0, float* __restrict__ hL,
+                                   int* status) {
+    if (blockIdx.x == 0) {
+        for (int s = threadIdx.x; s <= nseq; s += blockDim.x) {
+            const int64_t v = cu[s];
+            const bool bad = v < 0 || v > L || (s == 0 && v != 0) || (s == nseq && v != L) ||
+                             (s > 0 && v < (int64_t)cu[s - 1]);
+            if (bad) set_status(status, SSM_ERR_SEQLENS);
+        }
+    }
+    if (!hL) return;
+    for (int s = blockIdx.x; s < nseq; s += gridDim.x) {
+        if (cu[s] != cu[s + 1]) continue;
+        float* o = hL + (int64_t)s * per_seq;
+        const float* i0 = h0 ? h0 + (int64_t)s * per_seq : nullptr;
+        for (int64_t i = threadIdx.x; i < per_seq; i += blockDim.x) o[i] = i0 ? i0[i] : 0.0f;
+    }
+}
+
+cudaError_t launch_varlen_prep(const int* cu, int nseq, int64_t L, int64_t per_seq, const float* h0,
+                               float* hL, int* status, cudaStream_t st) {
+    const int blocks = nseq < 1184 ? (nseq > 0 ? nseq : 1) : 1184;
+    varlen_prep_kernel<<<blocks, 256, 0, st>>>(cu, nseq, L, per_seq, h0, hL, status);
+    return cudaGetLastError();
 }
 
 // Tail search for the segmented plan.  Pass 1 needs each segment's end
@@ -99,7 +131,6 @@ __global__ void carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg, con
 // A < 0).  Where a tile needs its whole segment, pass 1 writes the exact
 // sums.  Segments 0 .. nseg-2 (whole chunks); L * sizeof(TIN) % 16 == 0.
 constexpr float kTailLog2 = 40.0f;
-constexpr float kTailSat = 1e30f;
 
 template <typename TIN>
 __global__ void __launch_bounds__(1024) tail_kernel(const FwdParams p, int CH, int* __restrict__ tstart,

@@ -116,16 +116,41 @@ __device__ __forceinline__ void fill_raw_tile(uint8_t* tile, const void* src, in
     fill_raw_tile_r<TIN>(tile, CH, src, row0, rows_valid, L, t0, lane);
 }
 
+// First s in [0, nseq) with cu[s] >= t (nseq if none); a bounded binary
+// search, also on unsorted input.
+__device__ __forceinline__ int seq_lower_bound(const int* cu, int nseq, int64_t t) {
+    int lo = 0, hi = nseq;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] < t) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// No restart inside a super-block.
+struct NoRestart {
+    template <typename H>
+    __device__ __forceinline__ void operator()(int, H&) const {}
+};
+
 // The recurrence over one super-block of SB tokens for one lane's G states.
 //   d2, du: delta/ln2 and delta2*u of the SB tokens (registers)
 //   bcb:    prepared B/C row of the super-block's first token at this lane's states
-template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE>
+// With RESTART, tokens whose bit is set in `rmask` begin a packed sequence:
+// `restart(tt, h)` replaces the state before that token's update.
+template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE, bool RESTART = false,
+          typename F = NoRestart>
 __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&du)[SB],
                                           const float* bcb, const f2 (&Ap)[G / 2],
-                                          f2 (&h)[G / 2], float (&yp)[SB]) {
+                                          f2 (&h)[G / 2], float (&yp)[SB], uint32_t rmask = 0,
+                                          F restart = F()) {
     constexpr int Q = G / 4;
 #pragma unroll
     for (int tt = 0; tt < SB; ++tt) {
+        if constexpr (RESTART) {
+            if ((rmask >> tt) & 1u) restart(tt, h);
+        }
         const f2 d2p = pk(d2[tt], d2[tt]), dup = pk(du[tt], du[tt]);
         const float* bcrow = bcb + tt * (2 * NP);
         f2 acc = pk(0.0f, 0.0f);
@@ -161,7 +186,8 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 // states, writes its per-token partial read-outs to the warp's exchange
 // buffer, and then finishes its own TPL tokens (sum over the NT lanes, D
 // skip, SiLU gate, store).  All exchange stays inside the warp.
-template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW, bool CONV = false>
+template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW, bool CONV = false,
+          bool VARLEN = false>
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
            const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -327,6 +353,50 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 if (t0 - 3 + q >= 0) xhalo[q] = Elem<TIN>::to_f(xr[t0 - 3 + q]);
         }
     }
+    // packed sequences: every thread walks the sequence starts in token
+    // order (the same walk in all threads, so branches on it are uniform).
+    // sp = index of the first start after the last token scanned, next_start
+    // = that start, cur_start = start of the sequence being scanned.
+    int sp = 0;
+    int64_t next_start = INT64_MAX, cur_start = 0;
+    bool seg_restart = false;   // a sequence starts inside this segment
+    if constexpr (VARLEN) {
+        const int* cu = p.cu_seqlens;
+        sp = seq_lower_bound(cu, p.nseq, k_begin * kT);
+        next_start = sp < p.nseq ? (int64_t)cu[sp] : INT64_MAX;
+        cur_start = sp > 0 ? (int64_t)cu[sp - 1] : 0;
+        const int j = seq_lower_bound(cu, p.nseq, k_seg * kT);
+        seg_restart = j < p.nseq && (int64_t)cu[j] < min(k_end * kT, L);
+    }
+    // a sequence starting at token t: write the final state of the one that
+    // ended at t - 1 (pass 2), then start from h0 of the new one (or zero)
+    auto restart = [&](int64_t t, f2 (&hh)[G / 2]) {
+        if constexpr (VARLEN) {
+            const int* cu = p.cu_seqlens;
+            const int last = p.nseq - 1;
+            if (!SUMMARY && ch_ok && p.hL && t > 0) {
+                const int sf = min(max(sp - 1, 0), last);
+                float* hl = p.hL + ((int64_t)sf * p.Bt * p.D + row) * N;
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    float lo, hi;
+                    upk(hh[j], lo, hi);
+                    const int n0 = g * G + 2 * j;
+                    if (n0 < N) hl[n0] = lo;
+                    if (n0 + 1 < N) hl[n0 + 1] = hi;
+                }
+            }
+            while (sp < p.nseq && (int64_t)cu[sp] <= t) ++sp;
+            const int sn = min(max(sp - 1, 0), last);
+            const float* hs = (p.h0 && ch_ok) ? p.h0 + ((int64_t)sn * p.Bt * p.D + row) * N : nullptr;
+#pragma unroll
+            for (int j = 0; j < G / 2; ++j) {
+                const int n0 = g * G + 2 * j;
+                hh[j] = pk((hs && n0 < N) ? hs[n0] : 0.0f, (hs && n0 + 1 < N) ? hs[n0 + 1] : 0.0f);
+            }
+            next_start = sp < p.nseq ? (int64_t)cu[sp] : INT64_MAX;
+        }
+    };
     bool dead = false;   // a bounded wait expired: stop working (warp-uniform)
 
     for (int64_t k = k_begin; k < k_end && !dead; ++k) {
@@ -346,6 +416,19 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll 1
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (sb * SB >= nvalid) break;
+            const int64_t t_sb = k * kT + sb * SB;
+            uint32_t rmask = 0;   // tokens of this super-block that start a sequence
+            if constexpr (VARLEN) {
+                if (next_start < t_sb + SB) {
+                    for (int j = sp; j < p.nseq; ++j) {
+                        const int64_t cs = p.cu_seqlens[j];
+                        if (cs >= t_sb + SB || cs >= L) break;
+                        if (cs >= t_sb) rmask |= 1u << (int)(cs - t_sb);
+                        else sp = j + 1;   // out of order (invalid starts): skip for good
+                    }
+                    next_start = sp < p.nseq ? (int64_t)p.cu_seqlens[sp] : INT64_MAX;
+                }
+            }
 
             // 1. each lane computes delta2 = softplus / ln2 and delta2 * u of its
             //    own TPL tokens, then gathers all SB tokens of the channel from
@@ -377,13 +460,30 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     for (int q = 0; q < 3; ++q) xw[q] = tb > 0 ? prev[5 + q] : xhalo[q];
 #pragma unroll
                     for (int q = 0; q < TPL; ++q) xw[3 + q] = uo[q];
-#pragma unroll
-                    for (int q = 0; q < TPL; ++q) {
-                        float a = fmaf(cw4[0], xw[q], cbias);
-                        a = fmaf(cw4[1], xw[q + 1], a);
-                        a = fmaf(cw4[2], xw[q + 2], a);
+                    // taps before the token's sequence start (kmin of them) read zero
+                    auto conv_tok = [&](int q, int kmin) {
+                        float a = fmaf(cw4[0], kmin > 0 ? 0.0f : xw[q], cbias);
+                        a = fmaf(cw4[1], kmin > 1 ? 0.0f : xw[q + 1], a);
+                        a = fmaf(cw4[2], kmin > 2 ? 0.0f : xw[q + 2], a);
                         a = fmaf(cw4[3], xw[q + 3], a);
                         uo[q] = a * rcp(1.0f + ex2(-kLog2e * a));
+                    };
+                    bool masked = false;
+                    if constexpr (VARLEN) {
+                        if (rmask != 0 || cur_start > t_sb - 3) {
+#pragma unroll
+                            for (int q = 0; q < TPL; ++q) {
+                                const int r = g * TPL + q;   // token within the super-block
+                                const uint32_t m = rmask & ((2u << r) - 1u);
+                                const int64_t st0 = m ? t_sb + (31 - __clz(m)) : cur_start;
+                                conv_tok(q, (int)(st0 - (t_sb + r)) + 3);
+                            }
+                            masked = true;
+                        }
+                    }
+                    if (!masked) {
+#pragma unroll
+                        for (int q = 0; q < TPL; ++q) conv_tok(q, 0);
                     }
                 }
                 const bool full = nvalid == kT;   // warp-uniform: no padded token
@@ -408,8 +508,19 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             // 2. the recurrence over the SB tokens for this lane's G states
             float yp[SB];
-            fwd_chain<NP, G, SB, SUMMARY, ACCURATE>(d2, du, bct + sb * SB * (2 * NP) + g * G, Ap,
-                                                    h, yp);
+            bool restarted = false;
+            if constexpr (VARLEN) {
+                if (rmask != 0) {
+                    fwd_chain<NP, G, SB, SUMMARY, ACCURATE, true>(
+                        d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, yp, rmask,
+                        [&](int tt, f2 (&hh)[G / 2]) { restart(t_sb + tt, hh); });
+                    cur_start = t_sb + (31 - __clz(rmask));
+                    restarted = true;
+                }
+            }
+            if (!restarted)
+                fwd_chain<NP, G, SB, SUMMARY, ACCURATE>(d2, du, bct + sb * SB * (2 * NP) + g * G, Ap,
+                                                        h, yp);
 
             if (!SUMMARY) {
                 // 3. partial read-outs through the buffer; finish the own tokens
@@ -479,16 +590,21 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             // a summary over the whole segment has the exact sum; a shortened one
             // keeps the search's saturation marker
-            if (g == 0 && k_begin == k_seg) p.sumd[(int64_t)seg * p.Bt * p.D + row] = (float)tot;
+            // (a sequence starting inside the segment cuts the carried state off)
+            if (g == 0 && (seg_restart || k_begin == k_seg))
+                p.sumd[(int64_t)seg * p.Bt * p.D + row] = seg_restart ? kTailSat : (float)tot;
         }
     } else if (k_end == nchunks && p.hL && ch_ok) {
+        // the last sequence's final state (packed: the one holding token L-1)
+        const int64_t sf = VARLEN ? (int64_t)min(max(sp - 1, 0), p.nseq - 1) : 0;
+        float* hl = p.hL + (sf * p.Bt * p.D + row) * N;
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) {
             float lo, hi;
             upk(h[j], lo, hi);
             const int n0 = g * G + 2 * j;
-            if (n0 < N) p.hL[row * N + n0] = lo;
-            if (n0 + 1 < N) p.hL[row * N + n0 + 1] = hi;
+            if (n0 < N) hl[n0] = lo;
+            if (n0 + 1 < N) hl[n0 + 1] = hi;
         }
     }
 }

@@ -31,6 +31,11 @@ cudaError_t launch_fwd_np16(int NT, int tin, int tout, bool summary, bool tma_ra
 // The forward with the conv prologue, padded state size 16, TMA tiles.
 cudaError_t launch_fwd_conv_np16(int NT, int tin, int tout, bool summary, const FwdParams& p,
                                  const FwdMaps& m, dim3 grid, int warps, size_t smem, cudaStream_t st);
+// The forward over packed sequences (restarts at cu_seqlens), padded state
+// size 16, TMA tiles, with or without the conv prologue.
+cudaError_t launch_fwd_varlen_np16(int NT, int tin, int tout, bool summary, bool conv,
+                                   const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                                   size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                             size_t smem, cudaStream_t st);
@@ -77,6 +82,12 @@ cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,
                          cudaStream_t st);
+// Packed sequences: checks cu_seqlens (0 = c_0 <= c_1 <= ... <= c_nseq = L,
+// else SSM_ERR_SEQLENS in the status word) and writes the final state of
+// every empty sequence (its h0, or zero).  After prep_bc, which clears the
+// status word.
+cudaError_t launch_varlen_prep(const int* cu, int nseq, int64_t L, int64_t per_seq, const float* h0,
+                               float* hL, int* status, cudaStream_t st);
 cudaError_t launch_step(int tin, int tout, const StepParams& p, cudaStream_t st);
 // Decode step for N = 16 and D a multiple of 128 (one thread per channel, 2-D
 // TMA tiles of the states and of A given by tm_st (rows = batch*dim) and tm_a

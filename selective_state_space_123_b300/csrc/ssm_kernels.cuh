@@ -31,6 +31,11 @@ constexpr int kMaxSmemPerCta = 226 * 1024;   // dynamic shared memory per CTA (2
 // Forward scan parameters.  Layouts are the public ones (see ssm_scan.h);
 // `bc` is the prepared copy of B and C: (batch, seqlen, 2*NP) fp32 with
 // [0, NP) = ln2 * B[b, n, t] and [NP, 2NP) = C[b, n, t], zero for n >= N.
+// Marker in a segment's sum of delta2 (segmented plan): the carry drops the
+// state coming into the segment (the tail search found its decay below
+// 2^-40, or a packed sequence starts inside the segment).
+constexpr float kTailSat = 1e30f;
+
 struct FwdParams {
     int64_t Bt, D, L;
     int N;
@@ -63,6 +68,13 @@ struct FwdParams {
     const float* conv_w;
     const float* conv_b;
     int conv_k;
+    // packed sequences (the kernel instantiated with VARLEN): every batch row
+    // holds nseq sequences, sequence s at tokens [cu_seqlens[s],
+    // cu_seqlens[s+1]); the state restarts at each start (from h0[s], h0 then
+    // (nseq, Bt, D, N)) and hL receives every sequence's final state (nseq,
+    // Bt, D, N)
+    const int* cu_seqlens;
+    int nseq;
     int* status;
     uint64_t timeout_ns;
 };
@@ -113,6 +125,13 @@ struct BwdParams {
     const float* conv_w;
     const float* conv_b;
     int conv_k;
+    // packed sequences (the kernel instantiated with VARLEN): every batch row
+    // holds nseq sequences, sequence s at tokens [cu_seqlens[s],
+    // cu_seqlens[s+1]); the state restarts at each start (from h0[s], h0 then
+    // (nseq, Bt, D, N)) and hL receives every sequence's final state (nseq,
+    // Bt, D, N)
+    const int* cu_seqlens;
+    int nseq;
     int* status;
     uint64_t timeout_ns;
 };

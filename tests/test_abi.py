@@ -32,7 +32,7 @@ def test_exports_every_declared_symbol(pkg):
 
 
 def test_strerror_covers_codes(pkg):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = pkg.ssm_strerror(code)
         assert s and s != "unknown status"
     assert pkg.ssm_strerror(-99) == "unknown status"
@@ -92,6 +92,27 @@ def test_fwd_conv_argument_errors(pkg):
     assert _call_fwd_conv(pkg, S(n=4)) == pkg.SSM_ERR_UNSUPPORTED
     assert _call_fwd_conv(pkg, S(l=63)) == pkg.SSM_ERR_UNSUPPORTED
     assert _call_fwd_conv(pkg, S(l=62, ti=0)) == pkg.SSM_ERR_UNSUPPORTED
+
+
+def _call_fwd_varlen(pkg, shape, cu=0x9000, nseq=3, conv_w=None, conv_k=0, ws_bytes=1 << 24):
+    V = lambda x: None if x is None else ctypes.c_void_p(x)
+    return pkg.lib.ssm_scan_fwd_varlen(ctypes.byref(shape), V(0x1000), V(cu), nseq, V(conv_w), None,
+                                       conv_k, V(0x2000), V(0x3000), V(0x4000), V(0x5000), None,
+                                       None, None, None, V(0x6000), None, V(0x10000), ws_bytes, None)
+
+
+def test_fwd_varlen_argument_errors(pkg):
+    """The packed-sequence entry point refuses what it does not build before
+    any GPU work."""
+    S = lambda n=16, l=64, ti=1: pkg.make_shape(2, 8, n, l, ti, 0)
+    assert _call_fwd_varlen(pkg, S(), cu=None) == pkg.SSM_ERR_NULL
+    assert _call_fwd_varlen(pkg, S(), nseq=0) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd_varlen(pkg, S(), conv_w=0x8000, conv_k=5) == pkg.SSM_ERR_SHAPE
+    assert _call_fwd_varlen(pkg, S(), cu=0x9002) == pkg.SSM_ERR_ALIGN
+    assert _call_fwd_varlen(pkg, S(n=32)) == pkg.SSM_ERR_UNSUPPORTED
+    assert _call_fwd_varlen(pkg, S(l=60)) == pkg.SSM_ERR_UNSUPPORTED
+    assert _call_fwd_varlen(pkg, S(), ws_bytes=16) == pkg.SSM_ERR_WORKSPACE
+    assert pkg.lib.ssm_strerror(pkg.SSM_ERR_SEQLENS).startswith(b"packed-sequence")
 
 
 def test_workspace_query(pkg):
