@@ -16,7 +16,9 @@ Architecture Explained" (section "How State Space Models Work"), closed forms,
 the remember/forget limits of "State Space Models (SSMs) & Mamba" (section
 "The Magic of Selective Scan"), and finite differences for the backward.
 The packed-sequence form (``scan_fwd_varlen``) is pinned against the batched
-scan with one sequence per batch row, and by the independence of sequences.
+scan with one sequence per batch row, and by the independence of sequences;
+the bidirectional form (``scan_fwd_bidir``) against its materialised upper-
+and lower-triangular time-varying kernels.
 """
 from __future__ import annotations
 
@@ -145,6 +147,25 @@ def scan_fwd_varlen(u, delta_raw, A, Bm, Cm, cu_seqlens, Dv=None, z=None, delta_
                              None if z is None else z[:, :, lo:hi], delta_bias, hs)
         y[:, :, lo:hi] = ys
     return y, hL
+
+
+def scan_fwd_bidir(u, z, fwd, rev):
+    """Bidirectional scan ("Mamba Architecture Explained", section "Frequently
+    Asked Questions": bidirectional SSM variants beside the causal scan): the
+    sum of two selective scans over the same input u and gate z, one over
+    t = 0 .. L-1 and one over t = L-1 .. 0.  `fwd` and `rev` are dicts with
+    each direction's delta_raw, A, Bm, Cm and optional Dv, delta_bias, h0.
+    Returns (y, hL of the left-to-right scan (state after token L-1), hL of the
+    right-to-left scan (state after token 0))."""
+    def one(d, flip):
+        f = (lambda a: None if a is None else np.ascontiguousarray(np.asarray(a)[..., ::-1])) \
+            if flip else (lambda a: a)
+        y, h = scan_fwd(f(u), f(d["delta_raw"]), d["A"], f(d["Bm"]), f(d["Cm"]), d.get("Dv"),
+                        f(z), d.get("delta_bias"), d.get("h0"))
+        return f(y), h
+    yf, hf = one(fwd, False)
+    yr, hr = one(rev, True)
+    return yf + yr, hf, hr
 
 
 def scan_fwd(u, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None, h0=None):

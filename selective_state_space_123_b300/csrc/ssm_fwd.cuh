@@ -228,10 +228,19 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t k_end = min(nchunks, k_seg + p.seg_chunks);
     // a summary starts where the tail search found that the segment's end
     // state no longer depends on earlier tokens (their decay is below 2^-40)
-    const int64_t k_begin =
+    int64_t k_begin =
         (SUMMARY && p.tstart)
             ? max(k_seg, min(k_end - 1, (int64_t)p.tstart[((int64_t)seg * p.Bt + blockIdx.y) * gridDim.x + blockIdx.x]))
             : k_seg;
+    if constexpr (VARLEN && SUMMARY) {
+        // packed: the segment's end state depends only on the tokens from the
+        // last sequence start inside the segment on
+        const int j = seq_lower_bound(p.cu_seqlens, p.nseq, k_end * kT);
+        if (j > 0) {
+            const int64_t ls = p.cu_seqlens[j - 1];
+            if (ls >= k_seg * kT && ls < k_end * kT) k_begin = max(k_begin, ls / kT);
+        }
+    }
     const bool has_z = !SUMMARY && p.z != nullptr;
 
     if (tid == 0) {

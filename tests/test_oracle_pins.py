@@ -452,3 +452,68 @@ def test_varlen_sequences_do_not_see_each_other():
     y4, _ = oracle.scan_fwd(x.u[:, :, 25:], x.delta_raw[:, :, 25:], x.A, x.Bm[:, :, 25:],
                             x.Cm[:, :, 25:], x.Dv, x.z[:, :, 25:], x.delta_bias, None)
     np.testing.assert_array_equal(y3[:, :, 25:], y4)
+
+
+# ---- bidirectional scan ("Mamba Architecture Explained", section "Frequently
+# Asked Questions": bidirectional SSM variants)
+
+def test_bidirectional_materialised_kernels():
+    """y = silu(z) * ((M_f + M_r) u + (D_f + D_r) u): M_f lower triangular
+    with prefix sums of delta (left-to-right scan), M_r upper triangular with
+    suffix sums P_t = sum_{r>=t} delta_r of the other direction's delta,
+    M_r[t,s] = sum_n C_t[n] exp(A_n (P_t - P_s)) delta_s B_s[n] for s >= t."""
+    rng = _rng(60)
+    Bt, D, N, L = 1, 2, 3, 21
+    u = rng.standard_normal((Bt, D, L))
+    z = rng.standard_normal((Bt, D, L))
+
+    def params():
+        return dict(delta_raw=rng.standard_normal((Bt, D, L)), A=-rng.uniform(0.2, 2.0, (D, N)),
+                    Bm=rng.standard_normal((Bt, N, L)), Cm=rng.standard_normal((Bt, N, L)),
+                    Dv=rng.standard_normal(D), delta_bias=rng.uniform(-3, 0, D))
+    f, r = params(), params()
+    y, _, _ = oracle.scan_fwd_bidir(u, z, f, r)
+    for d in range(D):
+        M = np.zeros((L, L))
+        df = _softplus_lib(f["delta_raw"][0, d] + f["delta_bias"][d])
+        S = np.cumsum(df)
+        for t in range(L):
+            for s in range(t + 1):
+                M[t, s] += np.sum(f["Cm"][0, :, t] * np.exp(f["A"][d] * (S[t] - S[s])) * df[s]
+                                  * f["Bm"][0, :, s])
+        dr = _softplus_lib(r["delta_raw"][0, d] + r["delta_bias"][d])
+        P = np.cumsum(dr[::-1])[::-1]
+        for t in range(L):
+            for s in range(t, L):
+                M[t, s] += np.sum(r["Cm"][0, :, t] * np.exp(r["A"][d] * (P[t] - P[s])) * dr[s]
+                                  * r["Bm"][0, :, s])
+        ys = M @ u[0, d] + (f["Dv"][d] + r["Dv"][d]) * u[0, d]
+        np.testing.assert_allclose(y[0, d], ys * _silu_lib(z[0, d]), rtol=1e-10, atol=1e-12)
+
+
+def test_bidirectional_final_states_and_mirror():
+    """The right-to-left scan's final state is the state after token 0, and
+    mirroring every input swaps the two directions."""
+    x = make_inputs(2, 3, 4, 17, seed=61, in_dtype="f32", h0=True)
+    f = dict(delta_raw=x.delta_raw, A=x.A, Bm=x.Bm, Cm=x.Cm, Dv=x.Dv, delta_bias=x.delta_bias, h0=x.h0)
+    x2 = make_inputs(2, 3, 4, 17, seed=62, in_dtype="f32", h0=True)
+    r = dict(delta_raw=x2.delta_raw, A=x2.A, Bm=x2.Bm, Cm=x2.Cm, Dv=x2.Dv, delta_bias=x2.delta_bias,
+             h0=x2.h0)
+    y, hf, hr = oracle.scan_fwd_bidir(x.u, x.z, f, r)
+    # the state after token 0 of the right-to-left scan: one step from its
+    # state after token 1, by the single-token closed form
+    _, h1 = oracle.scan_fwd(x.u[..., ::-1][..., :16].copy(), x2.delta_raw[..., ::-1][..., :16].copy(),
+                            x2.A, x2.Bm[..., ::-1][..., :16].copy(), x2.Cm[..., ::-1][..., :16].copy(),
+                            x2.Dv, None, x2.delta_bias, x2.h0)
+    f64 = lambda a: np.asarray(a, np.float64)
+    delta0 = _softplus_lib(f64(x2.delta_raw[..., 0]) + f64(x2.delta_bias)[None, :])
+    step = np.exp(delta0[..., None] * f64(x2.A)[None]) * h1 + \
+        (delta0 * f64(x.u[..., 0]))[..., None] * f64(x2.Bm)[:, None, :, 0]
+    np.testing.assert_allclose(hr, step, rtol=1e-12, atol=1e-12)
+    flip = lambda a: np.ascontiguousarray(a[..., ::-1])
+    fm = {k: (flip(v) if k in ("delta_raw", "Bm", "Cm") else v) for k, v in f.items()}
+    rm = {k: (flip(v) if k in ("delta_raw", "Bm", "Cm") else v) for k, v in r.items()}
+    ym, hfm, hrm = oracle.scan_fwd_bidir(flip(x.u), flip(x.z), rm, fm)
+    np.testing.assert_allclose(flip(ym), y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hfm, hr, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hrm, hf, rtol=1e-12, atol=1e-12)
