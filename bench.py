@@ -62,6 +62,12 @@ WORKLOADS = {
     # 17 sequences of 256..16384 tokens (log-uniform) packed into one row;
     # the planner cuts the row into 4 segments at 148 SMs: B/C preparation,
     # sequence check, tail search, summary pass, carry, scan = 6 launches
+    # two directions, each with its own delta/A/B/C/D/bias (B/C preparation
+    # twice, right-to-left pass, left-to-right pass = 4 launches)
+    "bidir_mamba1p4b_fwd": dict(mode="fwd", bidir=True, Bt=4, D=4096, N=16, L=4096, seed=6,
+                                launches=4,
+                                title="Mamba-1.4B layer bidirectional scan (left-to-right + "
+                                      "right-to-left)"),
     "packed_mamba1p4b_fwd": dict(mode="fwd", varlen=True, Bt=1, D=4096, N=16, L=65536, seed=5,
                                  launches=6,
                                  title="Mamba-1.4B layer forward over packed sequences of mixed "
@@ -247,11 +253,12 @@ def _oracle_worker(args):
     mode, seed, Bt, D, N, L, chans = args[:7]
     conv_k = args[7] if len(args) > 7 else 0
     varlen = args[8] if len(args) > 8 else False
+    bidir = args[9] if len(args) > 9 else False
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
     import oracle
     from scan_inputs import make_inputs, make_step_inputs
-    key = (mode, seed, Bt, D, N, L, tuple(chans))
+    key = (mode, seed, Bt, D, N, L, tuple(chans), bidir)
     x = _INPUT_CACHE.get(key)
     if x is None:
         if len(_INPUT_CACHE) > 64:
@@ -261,6 +268,8 @@ def _oracle_worker(args):
         else:
             x = make_inputs(Bt, D, N, L, seed=seed, in_dtype="bf16", channels=chans,
                             dy=(mode == "fwdbwd"))
+            if bidir:
+                x = (x, make_inputs(Bt, D, N, L, seed=seed + 1, in_dtype="bf16", channels=chans))
         _INPUT_CACHE[key] = x
     cw = cb = None
     if conv_k:
@@ -269,6 +278,12 @@ def _oracle_worker(args):
         cw = (0.5 * g.standard_normal((D, conv_k))).astype(np.float32)[chans]
         cb = (0.1 * g.standard_normal(D)).astype(np.float32)[chans]
     t0 = time.perf_counter()
+    if mode == "fwd" and bidir:
+        xf, xr = x
+        d = lambda v: dict(delta_raw=v.delta_raw, A=v.A, Bm=v.Bm, Cm=v.Cm, Dv=v.Dv,
+                           delta_bias=v.delta_bias)
+        oracle.scan_fwd_bidir(xf.u, xf.z, d(xf), d(xr))
+        return 2 * Bt * len(chans) * N * L, time.perf_counter() - t0
     if mode == "fwd" and varlen:
         from scan_inputs import packed_seqlens
         cu = packed_seqlens(L, seed=seed)
@@ -303,11 +318,12 @@ class OracleTimer:
         warm_L = min(64, w["L"])
         self.conv_k = w.get("conv", 0)
         self.varlen = bool(w.get("varlen"))
+        self.bidir = bool(w.get("bidir"))
         self.pool.map(_oracle_worker, [(w["mode"], w["seed"], self.bt, w["D"], w["N"], warm_L,
-                                        [0], self.conv_k, self.varlen)] * self.cores)
+                                        [0], self.conv_k, self.varlen, self.bidir)] * self.cores)
         probe = 16 if w["mode"] == "step" else 1
         _, t = _oracle_worker((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
-                               list(range(probe)), self.conv_k, self.varlen))
+                               list(range(probe)), self.conv_k, self.varlen, self.bidir))
         self.t_channel = t / probe
         self.next = 0
 
@@ -322,7 +338,7 @@ class OracleTimer:
         for i in range(self.cores):
             jobs.append((w["mode"], w["seed"], self.bt, w["D"], w["N"], w["L"],
                          [(start + i * per + j) % w["D"] for j in range(per)], self.conv_k,
-                         self.varlen))
+                         self.varlen, self.bidir))
         if not fixed:
             self.next = (start + per * self.cores) % w["D"]
         res = self.pool.map(_oracle_worker, jobs)
@@ -333,6 +349,8 @@ class OracleTimer:
             what = "conv prologue + forward"
         if self.varlen:
             what = "packed-sequence forward"
+        if self.bidir:
+            what = "bidirectional scan"
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
                 "sample": "%s of %d channels x %d batch rows x %d tokens x %d states of the %s "
                           "workload, one spawned process per core (%d channels each); slowest "
@@ -399,6 +417,20 @@ class Workload:
             self.exps = Bt * D * L * N
             self.conv_k = w.get("conv", 0)
             self.cu = None
+            self.bidir = bool(w.get("bidir"))
+            if self.bidir:
+                # the right-to-left direction's own parameters (u and z are shared)
+                r = device_inputs(Bt, D, N, L, seed=rank_seed(w["seed"], rank) + 1, in_dtype="bf16")
+                for k in ("delta_raw", "Bm", "Cm", "A", "Dv", "delta_bias"):
+                    self.inp[k + "_r"] = r[k]
+                del r
+                self.hL_r = torch.empty(Bt, D, N, dtype=torch.float32, device="cuda")
+                nb = ssm.ssm_scan_workspace_bytes(shape, 2)
+                self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+                # second direction: delta_raw, B, C, A, D, bias read, final state written
+                self.bytes += (Bt * D * L * 2 + 2 * Bt * N * L * 2 + D * N * 4 + 2 * D * 4
+                               + Bt * D * N * 4)
+                self.exps *= 2
             if w.get("varlen"):
                 from scan_inputs import packed_seqlens
                 self.cu = torch.tensor(packed_seqlens(L, seed=rank_seed(w["seed"], rank)),
@@ -424,7 +456,10 @@ class Workload:
                 self.bytes += bwd_bytes(Bt, D, N, L)
                 self.exps *= 3     # forward, and the backward's two sweeps
                 self.launches += 3
-        self.updates = Bt * D * L * N
+        # state updates per step (the bidirectional scan runs two)
+        self.updates = Bt * D * L * N * (2 if getattr(self, "bidir", False) else 1)
+        if getattr(self, "bidir", False):
+            self.outs.append(self.hL_r)
 
     def capture_graphs(self):
         """Decode: one CUDA graph per rotating copy, each holding one
@@ -463,6 +498,14 @@ class Workload:
                 self.rot_i = (self.rot_i + 1) % len(self.rot)
             ssm.ssm_scan_step(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], state,
                               a["Dv"], a["z"], a["delta_bias"], out_dtype=torch.bfloat16, y=self.y)
+            return
+        if self.bidir:
+            f = dict(delta_raw=a["delta_raw"], A=a["A"], B=a["Bm"], C=a["Cm"], D=a["Dv"],
+                     delta_bias=a["delta_bias"])
+            r = dict(delta_raw=a["delta_raw_r"], A=a["A_r"], B=a["Bm_r"], C=a["Cm_r"], D=a["Dv_r"],
+                     delta_bias=a["delta_bias_r"])
+            ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=torch.bfloat16, y=self.y,
+                                   hL=self.hL, hL_r=self.hL_r, workspace=self.ws)
             return
         if self.cu is not None:
             ssm.ssm_scan_fwd_varlen(a["u"], self.cu, a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"],
@@ -683,7 +726,8 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0) and getattr(wl, "cu", None) is None:
+        if (wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0)
+                and getattr(wl, "cu", None) is None and not getattr(wl, "bidir", False)):
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
                        "scans and copies" % ("batch rows" if wl.w["Bt"] > 1 else "channels"))

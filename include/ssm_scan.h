@@ -92,7 +92,8 @@ enum {
 };
 
 /* Bytes of device workspace the call needs for this shape on the current
- * device: for_backward = 0 for ssm_scan_fwd, 1 for ssm_scan_bwd.  Always at
+ * device: for_backward = 0 for ssm_scan_fwd (and its _conv and _varlen forms),
+ * 1 for ssm_scan_bwd, 2 for ssm_scan_fwd_bidir.  Always at
  * least 256 (the status word lives at offset 0).  Returns 0 for an invalid
  * shape. */
 SSM_API size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward);
@@ -160,6 +161,33 @@ SSM_API int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int
                  const void* delta_raw, const float* A, const void* B, const void* C,
                  const float* D, const void* z, const float* delta_bias, const float* h0,
                  void* y, float* hL, void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/* Bidirectional scan ("Mamba Architecture Explained", section "Frequently
+ * Asked Questions": the standard scan is causal, bidirectional SSM variants
+ * run a second scan the other way).  Two selective scans over the same u
+ * and gate z, each with its own parameters: the left-to-right scan of
+ * ssm_scan_fwd with (delta_raw, A, B, C, D, delta_bias, h0), and a
+ * right-to-left scan with (delta_raw_r, A_r, B_r, C_r, D_r, delta_bias_r,
+ * h0_r) whose state runs from token seqlen-1 down to token 0:
+ *   h_r[t] = exp(delta_r[t] A_r) h_r[t+1] + delta_r[t] B_r[t] u[t],  h_r[seqlen] = h0_r
+ *   y[t] = (C[t].h[t] + D u[t]) silu(z[t]) + (C_r[t].h_r[t] + D_r u[t]) silu(z[t]).
+ * (The same pointers for both directions give the weight-tied variant.)
+ *   Shapes and dtypes as ssm_scan_fwd, per direction; z nullable (no gate).
+ *   hL : the left-to-right state after token seqlen-1; hL_r : the
+ *     right-to-left state after token 0; both fp32 (batch, dim, dstate), nullable.
+ *   workspace : >= ssm_scan_workspace_bytes(shape, 2) bytes (it holds the
+ *     right-to-left pass's fp32 output, batch * dim * seqlen floats).
+ * Runs as two kernels (right to left, then left to right adding the first's
+ * output); long sequences are not split into segments.  Built for 9 to 16
+ * states and rows of seqlen * element size a multiple of 16 bytes; other
+ * shapes return SSM_ERR_UNSUPPORTED before anything is enqueued. */
+SSM_API int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
+                 const void* delta_raw, const float* A, const void* B, const void* C,
+                 const float* D, const float* delta_bias, const float* h0,
+                 const void* delta_raw_r, const float* A_r, const void* B_r, const void* C_r,
+                 const float* D_r, const float* delta_bias_r, const float* h0_r,
+                 void* y, float* hL, float* hL_r, void* workspace, size_t ws_bytes,
+                 ssm_stream_t stream);
 
 /* Reverse mode of ssm_scan_fwd (the pages give no backward; it is the exact
  * derivative of the recurrence above).  Inputs are the forward inputs plus

@@ -42,7 +42,7 @@ SSM_ERR_SEQLENS = -9
 
 # Every symbol include/ssm_scan.h declares.
 EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_fwd_varlen",
-           "ssm_scan_bwd", "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
+           "ssm_scan_fwd_bidir", "ssm_scan_bwd", "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
            "ssm_scan_fwd_noalloc")
 
 
@@ -64,6 +64,8 @@ lib.ssm_scan_fwd_conv.restype = ctypes.c_int
 lib.ssm_scan_fwd_varlen.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, ctypes.c_int, _P, _P,
                                      ctypes.c_int] + [_P] * 11 + [ctypes.c_size_t, _P])
 lib.ssm_scan_fwd_varlen.restype = ctypes.c_int
+lib.ssm_scan_fwd_bidir.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 20 + [ctypes.c_size_t, _P]
+lib.ssm_scan_fwd_bidir.restype = ctypes.c_int
 lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 21 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd.restype = ctypes.c_int
 lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 11
@@ -127,11 +129,14 @@ def make_shape(batch, dim, dstate, seqlen, in_dtype, out_dtype) -> ssm_shape:
                      int(out_dtype))
 
 
-def ssm_scan_workspace_bytes(shape: ssm_shape, for_backward: bool = False) -> int:
-    return int(lib.ssm_scan_workspace_bytes(ctypes.byref(shape), int(bool(for_backward))))
+def ssm_scan_workspace_bytes(shape: ssm_shape, for_backward=False) -> int:
+    """Workspace bytes: for_backward False/0 forward, True/1 backward, 2 the
+    bidirectional forward."""
+    kind = 2 if (not isinstance(for_backward, bool) and for_backward == 2) else int(bool(for_backward))
+    return int(lib.ssm_scan_workspace_bytes(ctypes.byref(shape), kind))
 
 
-def _workspace(shape: ssm_shape, for_backward: bool, device, workspace):
+def _workspace(shape: ssm_shape, for_backward, device, workspace):
     need = ssm_scan_workspace_bytes(shape, for_backward)
     if need == 0:
         raise SSMError(SSM_ERR_SHAPE, "ssm_scan_workspace_bytes")
@@ -279,6 +284,57 @@ def ssm_scan_fwd_varlen(u, cu_seqlens, delta_raw, A, B, C, D=None, z=None, delta
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_fwd_varlen")
     return y, hL
+
+
+def ssm_scan_fwd_bidir(u, z, fwd: dict, rev: dict, *, out_dtype: Optional[torch.dtype] = None,
+                       y=None, hL=None, hL_r=None, return_final_state: bool = True,
+                       workspace=None, stream=None):
+    """Bidirectional scan: the left-to-right scan with the parameters in
+    `fwd` plus a right-to-left scan with those in `rev`, over the same u and
+    gate z (nullable).  Each dict holds delta_raw, A, B, C and optional D,
+    delta_bias, h0, shaped as for ssm_scan_fwd.  Returns (y, hL, hL_r): hL the
+    left-to-right state after the last token, hL_r the right-to-left state
+    after the first (fp32 (Bt,D,N) or None)."""
+    Bt, Dm, L = u.shape
+    N = fwd["A"].shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_fwd_bidir runs on CUDA tensors only")
+    tin = u.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    _check(u, "u", (Bt, Dm, L), tin, dev)
+    _check(z, "z", (Bt, Dm, L), tin, dev)
+    for tag, d in (("fwd", fwd), ("rev", rev)):
+        _check(d["delta_raw"], tag + ".delta_raw", (Bt, Dm, L), tin, dev)
+        _check(d["B"], tag + ".B", (Bt, N, L), tin, dev)
+        _check(d["C"], tag + ".C", (Bt, N, L), tin, dev)
+        _check(d["A"], tag + ".A", (Dm, N), torch.float32, dev)
+        _check(d.get("D"), tag + ".D", (Dm,), torch.float32, dev)
+        _check(d.get("delta_bias"), tag + ".delta_bias", (Dm,), torch.float32, dev)
+        _check(d.get("h0"), tag + ".h0", (Bt, Dm, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev)
+    _check(y, "y", (Bt, Dm, L), out_dtype, dev)
+    if return_final_state:
+        if hL is None:
+            hL = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+        if hL_r is None:
+            hL_r = torch.empty((Bt, Dm, N), dtype=torch.float32, device=dev)
+    _check(hL, "hL", (Bt, Dm, N), torch.float32, dev)
+    _check(hL_r, "hL_r", (Bt, Dm, N), torch.float32, dev)
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, 2, dev, workspace)
+    f, r = fwd, rev
+    rc = lib.ssm_scan_fwd_bidir(ctypes.byref(shape), _ptr(u), _ptr(z),
+                                _ptr(f["delta_raw"]), _ptr(f["A"]), _ptr(f["B"]), _ptr(f["C"]),
+                                _ptr(f.get("D")), _ptr(f.get("delta_bias")), _ptr(f.get("h0")),
+                                _ptr(r["delta_raw"]), _ptr(r["A"]), _ptr(r["B"]), _ptr(r["C"]),
+                                _ptr(r.get("D")), _ptr(r.get("delta_bias")), _ptr(r.get("h0")),
+                                _ptr(y), _ptr(hL), _ptr(hL_r), _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_fwd_bidir")
+    return y, hL, hL_r
 
 
 def ssm_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None,

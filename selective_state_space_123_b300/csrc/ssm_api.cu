@@ -90,6 +90,9 @@ struct FwdPlan {
     int64_t nchunks = 0, seg_chunks = 0;
     bool tma_raw = false;
     size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, off_tstart = 0, bytes = 0;
+    // bidirectional scan: the right-to-left pass's prepared B/C and its gated
+    // output (Bt, D, L) fp32
+    size_t off_bc_r = 0, off_yrev = 0;
 };
 
 // Per-NT constants of the forward kernel, on the host.
@@ -144,7 +147,7 @@ double bwd_launch_cost(int64_t ctas, int sms, int W, double work) {
     return (double)waves * work / sat;
 }
 
-FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
+FwdPlan plan_fwd(const ssm_shape& s, int sm_count, bool segments = true) {
     FwdPlan pl;
     pl.NP = padded_state(s.dstate);
     const int eb = dtype_bytes(s.in_dtype);
@@ -181,8 +184,8 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
             // segments of the sequence (two passes and a carry) when there
             // are too few channel tiles to fill the GPU
             int seg_lo = 1, seg_hi = 1;
-            if (want_seg > 0) seg_lo = seg_hi = want_seg;
-            else if (pl.nchunks >= 16 && s.batch * tiles * 2 <= (int64_t)sm_count * cps)
+            if (want_seg > 0 && segments) seg_lo = seg_hi = want_seg;
+            else if (segments && pl.nchunks >= 16 && s.batch * tiles * 2 <= (int64_t)sm_count * cps)
                 seg_hi = 64;
             const int64_t nch = pl.nchunks > 0 ? pl.nchunks : 1;   // L = 0: no chunk at all
             for (int nseg0 = seg_lo; nseg0 <= seg_hi; ++nseg0) {
@@ -246,6 +249,19 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count) {
     if (env_int("SSM_DEBUG_PLAN", 0))
         std::fprintf(stderr, "ssm fwd plan: NP=%d NT=%d W=%d CH=%d stages=%d smem=%zu nseg=%d seg_chunks=%lld\n",
                      pl.NP, pl.NT, pl.W, pl.CH, pl.stages, pl.smem, pl.nseg, (long long)pl.seg_chunks);
+    return pl;
+}
+
+// The bidirectional scan runs both directions in one segment each (the
+// two-pass split of a long sequence is not built for the right-to-left pass).
+FwdPlan plan_fwd_bidir(const ssm_shape& s, int sm_count) {
+    FwdPlan pl = plan_fwd(s, sm_count, false);
+    size_t off = pl.bytes;
+    pl.off_bc_r = off;
+    off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
+    pl.off_yrev = off;
+    off += align256((size_t)s.batch * s.dim * s.seqlen * 4);
+    pl.bytes = off;
     return pl;
 }
 
@@ -442,8 +458,9 @@ const char* ssm_strerror(int code) {
 
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     if (shape_check(shape) != SSM_OK) return 0;
-    const size_t bytes = for_backward ? plan_bwd(*shape, device_sm_count()).bytes
-                                      : plan_fwd(*shape, device_sm_count()).bytes;
+    const size_t bytes = for_backward == 2 ? plan_fwd_bidir(*shape, device_sm_count()).bytes
+                         : for_backward ? plan_bwd(*shape, device_sm_count()).bytes
+                                        : plan_fwd(*shape, device_sm_count()).bytes;
     return bytes < kHeaderBytes ? kHeaderBytes : bytes;
 }
 
@@ -580,6 +597,94 @@ int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float* conv_w
     if (conv_k < 1 || conv_k > 4) return SSM_ERR_SHAPE;
     return scan_fwd_impl(shape, x, conv_w, conv_b, conv_k, nullptr, 0, delta_raw, A, B, C, D, z,
                          delta_bias, h0, y, hL, workspace, ws_bytes, stream);
+}
+
+int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
+                       const void* delta_raw, const float* A, const void* B, const void* C,
+                       const float* D, const float* delta_bias, const float* h0,
+                       const void* delta_raw_r, const float* A_r, const void* B_r, const void* C_r,
+                       const float* D_r, const float* delta_bias_r, const float* h0_r,
+                       void* y, float* hL, float* hL_r, void* workspace, size_t ws_bytes,
+                       ssm_stream_t stream) {
+    const int sc = shape_check(shape);
+    if (sc != SSM_OK) return sc;
+    const ssm_shape s = *shape;
+    const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    if (Bt == 0 || Dm == 0) return SSM_OK;
+    if (!A || !A_r) return SSM_ERR_NULL;
+    if (!workspace) return SSM_ERR_WORKSPACE;
+    if (L > 0 && (!u || !delta_raw || !B || !C || !delta_raw_r || !B_r || !C_r || !y))
+        return SSM_ERR_NULL;
+    const void* ptrs[] = {u, z, delta_raw, A, B, C, D, delta_bias, h0, delta_raw_r, A_r, B_r,
+                          C_r, D_r, delta_bias_r, h0_r, y, hL, hL_r, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const FwdPlan pl = plan_fwd_bidir(s, device_sm_count());
+    // built for 9..16 states and 16-byte token rows
+    if (L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
+    if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    if (L == 0) {
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+        const size_t bytes = (size_t)(Bt * Dm * N) * sizeof(float);
+        const float* h0s[2] = {h0, h0_r};
+        float* hLs[2] = {hL, hL_r};
+        for (int i = 0; i < 2; ++i) {
+            if (!hLs[i]) continue;
+            cudaError_t e = h0s[i] ? cudaMemcpyAsync(hLs[i], h0s[i], bytes, cudaMemcpyDeviceToDevice, st)
+                                   : cudaMemsetAsync(hLs[i], 0, bytes, st);
+            if (e != cudaSuccess) return cuda_fail();
+        }
+        return SSM_OK;
+    }
+    float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
+    float* bc_r = reinterpret_cast<float*>(ws + pl.off_bc_r);
+    float* yrev = reinterpret_cast<float*>(ws + pl.off_yrev);
+    if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess ||
+        launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B_r, C_r, bc_r, nullptr, st) != cudaSuccess)
+        return cuda_fail();
+
+    const int eb = dtype_bytes(s.in_dtype);
+    const CUtensorMapDataType tdt =
+        s.in_dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const uint32_t box_t = 128 / eb;
+    FwdMaps mf, mr;
+    std::memset(&mf, 0, sizeof(mf));
+    std::memset(&mr, 0, sizeof(mr));
+    if (!make_map(&mf.bc, bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT, false) ||
+        !make_map(&mr.bc, bc_r, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * pl.NP, Bt * L, 2 * pl.NP, kT, false) ||
+        !make_map(&mf.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+        !make_map(&mf.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+        !make_map(&mr.dr, delta_raw_r, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
+        (z && !make_map(&mf.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)))
+        return cuda_fail();
+    mr.u = mf.u;
+    mr.z = mf.z;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Bt = Bt; p.D = Dm; p.L = L; p.N = (int)N;
+    p.u = u; p.z = z;
+    p.seg_chunks = pl.seg_chunks;
+    p.nseg = 1;
+    p.stages = pl.stages;
+    p.status = status;
+    p.timeout_ns = kDefaultTimeoutNs;
+    FwdParams pr = p;   // right to left: fp32 gated output into the workspace
+    pr.dr = delta_raw_r; pr.A = A_r; pr.Dv = D_r; pr.bias = delta_bias_r; pr.h0 = h0_r;
+    pr.bc = bc_r; pr.y = yrev; pr.hL = hL_r;
+    FwdParams pf = p;   // left to right, adding it
+    pf.dr = delta_raw; pf.A = A; pf.Dv = D; pf.bias = delta_bias; pf.h0 = h0;
+    pf.bc = bc; pf.y = y; pf.hL = hL; pf.yadd = yrev;
+    const dim3 grid((unsigned)((Dm + pl.CH - 1) / pl.CH), (unsigned)Bt, 1);
+    if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, SSM_F32, 1, pr, mr, grid, pl.W, pl.smem, st) !=
+            cudaSuccess ||
+        launch_fwd_bidir_np16(pl.NT, s.in_dtype, s.out_dtype, 2, pf, mf, grid, pl.W, pl.smem, st) !=
+            cudaSuccess)
+        return cuda_fail();
+    return SSM_OK;
 }
 
 int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens, int nseq,

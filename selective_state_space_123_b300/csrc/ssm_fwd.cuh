@@ -138,16 +138,18 @@ struct NoRestart {
 //   d2, du: delta/ln2 and delta2*u of the SB tokens (registers)
 //   bcb:    prepared B/C row of the super-block's first token at this lane's states
 // With RESTART, tokens whose bit is set in `rmask` begin a packed sequence:
-// `restart(tt, h)` replaces the state before that token's update.
-template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE, bool RESTART = false,
-          typename F = NoRestart>
+// `restart(tt, h)` replaces the state before that token's update.  With REV
+// the tokens are taken from the last to the first.
+template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE, bool REV = false,
+          bool RESTART = false, typename F = NoRestart>
 __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&du)[SB],
                                           const float* bcb, const f2 (&Ap)[G / 2],
                                           f2 (&h)[G / 2], float (&yp)[SB], uint32_t rmask = 0,
                                           F restart = F()) {
     constexpr int Q = G / 4;
 #pragma unroll
-    for (int tt = 0; tt < SB; ++tt) {
+    for (int t0 = 0; t0 < SB; ++t0) {
+        const int tt = REV ? SB - 1 - t0 : t0;
         if constexpr (RESTART) {
             if ((rmask >> tt) & 1u) restart(tt, h);
         }
@@ -187,7 +189,7 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 // buffer, and then finishes its own TPL tokens (sum over the NT lanes, D
 // skip, SiLU gate, store).  All exchange stays inside the warp.
 template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RAW, bool CONV = false,
-          bool VARLEN = false>
+          bool VARLEN = false, int DIR = 0>
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
            const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -266,8 +268,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
         constexpr int BOX_T = 128 / EB;        // tokens per box
         const int64_t row0 = b * p.D + d0;
         const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
-        for (int64_t k = k_begin; k < k_end; ++k) {
-            const int64_t i = k - k_begin;
+        for (int64_t i = 0; i < k_end - k_begin; ++i) {
+            const int64_t k = DIR == 1 ? k_end - 1 - i : k_begin + i;   // right to left: last chunk first
             const int s = (int)(i % STAGES);
             if (i >= STAGES) {
                 bool ok = true;
@@ -408,8 +410,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     };
     bool dead = false;   // a bounded wait expired: stop working (warp-uniform)
 
-    for (int64_t k = k_begin; k < k_end && !dead; ++k) {
-        const int64_t i = k - k_begin;
+    for (int64_t i = 0; i < k_end - k_begin && !dead; ++i) {
+        const int64_t k = DIR == 1 ? k_end - 1 - i : k_begin + i;
         const int s = (int)(i % STAGES);
         const bool ok = __all_sync(
             0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns));
@@ -423,8 +425,12 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
 
 #pragma unroll 1
-        for (int sb = 0; sb < kT / SB; ++sb) {
-            if (sb * SB >= nvalid) break;
+        for (int sbi = 0; sbi < kT / SB; ++sbi) {
+            const int sb = DIR == 1 ? kT / SB - 1 - sbi : sbi;
+            if (sb * SB >= nvalid) {
+                if (DIR == 1) continue;   // right to left: padded super-blocks come first
+                break;
+            }
             const int64_t t_sb = k * kT + sb * SB;
             uint32_t rmask = 0;   // tokens of this super-block that start a sequence
             if constexpr (VARLEN) {
@@ -520,7 +526,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             bool restarted = false;
             if constexpr (VARLEN) {
                 if (rmask != 0) {
-                    fwd_chain<NP, G, SB, SUMMARY, ACCURATE, true>(
+                    fwd_chain<NP, G, SB, SUMMARY, ACCURATE, false, true>(
                         d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, yp, rmask,
                         [&](int tt, f2 (&hh)[G / 2]) { restart(t_sb + tt, hh); });
                     cur_start = t_sb + (31 - __clz(rmask));
@@ -528,8 +534,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
             }
             if (!restarted)
-                fwd_chain<NP, G, SB, SUMMARY, ACCURATE>(d2, du, bct + sb * SB * (2 * NP) + g * G, Ap,
-                                                        h, yp);
+                fwd_chain<NP, G, SB, SUMMARY, ACCURATE, DIR == 1>(
+                    d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, yp);
 
             if (!SUMMARY) {
                 // 3. partial read-outs through the buffer; finish the own tokens
@@ -562,6 +568,23 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                         float v = fmaf(Dd, uo[8 * k8 + q], yt[q]);
                         if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
                         out[q] = v;
+                    }
+                    if constexpr (DIR == 2) {
+                        // the right-to-left scan's gated output of these tokens
+                        const int nv = nvalid - (tb + 8 * k8);
+                        if (ch_ok && nv > 0) {
+                            const float* ya = p.yadd + row * L + k * kT + tb + 8 * k8;
+                            if (nv >= 8) {
+                                const float4 a0 = reinterpret_cast<const float4*>(ya)[0];
+                                const float4 a1 = reinterpret_cast<const float4*>(ya)[1];
+                                out[0] += a0.x; out[1] += a0.y; out[2] += a0.z; out[3] += a0.w;
+                                out[4] += a1.x; out[5] += a1.y; out[6] += a1.z; out[7] += a1.w;
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    if (q < nv) out[q] += ya[q];
+                            }
+                        }
                     }
                     if (ch_ok)
                         store_out8<TOUT>(p.y, row * L + k * kT + tb + 8 * k8, out,

@@ -8,10 +8,10 @@
 namespace ssm {
 
 template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA, bool CONV = false,
-          bool VARLEN = false>
+          bool VARLEN = false, int DIR = 0>
 cudaError_t launch_fwd_one(const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                            size_t smem, cudaStream_t st) {
-    auto kern = fwd_kernel<NP, NT, TIN, TOUT, SUMMARY, TMA, CONV, VARLEN>;
+    auto kern = fwd_kernel<NP, NT, TIN, TOUT, SUMMARY, TMA, CONV, VARLEN, DIR>;
     // raise the kernel's dynamic shared-memory limit when a launch needs more
     // than any earlier one on this device
     static size_t attr_val[64] = {};

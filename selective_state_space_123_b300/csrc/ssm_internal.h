@@ -36,6 +36,12 @@ cudaError_t launch_fwd_conv_np16(int NT, int tin, int tout, bool summary, const 
 cudaError_t launch_fwd_varlen_np16(int NT, int tin, int tout, bool summary, bool conv,
                                    const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                                    size_t smem, cudaStream_t st);
+// The bidirectional scan's two passes, padded state size 16, TMA tiles, one
+// segment: dir 1 = right to left (fp32 gated output into p.y), dir 2 = left
+// to right adding p.yadd.
+cudaError_t launch_fwd_bidir_np16(int NT, int tin, int tout, int dir, const FwdParams& p,
+                                  const FwdMaps& m, dim3 grid, int warps, size_t smem,
+                                  cudaStream_t st);
 cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                             size_t smem, cudaStream_t st);

@@ -75,6 +75,9 @@ struct FwdParams {
     // Bt, D, N)
     const int* cu_seqlens;
     int nseq;
+    // bidirectional forward (the kernel instantiated with DIR = 2): the other
+    // direction's gated output (Bt, D, L) fp32, added to y
+    const float* yadd;
     int* status;
     uint64_t timeout_ns;
 };
@@ -132,6 +135,9 @@ struct BwdParams {
     // Bt, D, N)
     const int* cu_seqlens;
     int nseq;
+    // bidirectional forward (the kernel instantiated with DIR = 2): the other
+    // direction's gated output (Bt, D, L) fp32, added to y
+    const float* yadd;
     int* status;
     uint64_t timeout_ns;
 };

@@ -115,6 +115,28 @@ def test_fwd_varlen_argument_errors(pkg):
     assert pkg.lib.ssm_strerror(pkg.SSM_ERR_SEQLENS).startswith(b"packed-sequence")
 
 
+def test_fwd_bidir_argument_errors(pkg):
+    """The bidirectional entry point refuses what it does not build before
+    any GPU work; its workspace holds the second pass's fp32 output."""
+    V = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def call(shape, A_r=0x3100, B_r=0x4100, ws_bytes=1 << 26):
+        return pkg.lib.ssm_scan_fwd_bidir(
+            ctypes.byref(shape), V(0x1000), None, V(0x2000), V(0x3000), V(0x4000), V(0x5000),
+            None, None, None, V(0x2100), V(A_r), V(B_r), V(0x5100), None, None, None,
+            V(0x6000), None, None, V(0x10000), ws_bytes, None)
+    S = lambda n=16, l=64, ti=1: pkg.make_shape(2, 8, n, l, ti, 0)
+    assert call(S(), A_r=None) == pkg.SSM_ERR_NULL
+    assert call(S(), B_r=None) == pkg.SSM_ERR_NULL
+    assert call(S(), B_r=0x4108) == pkg.SSM_ERR_ALIGN
+    assert call(S(n=32)) == pkg.SSM_ERR_UNSUPPORTED
+    assert call(S(l=60)) == pkg.SSM_ERR_UNSUPPORTED
+    assert call(S(), ws_bytes=1024) == pkg.SSM_ERR_WORKSPACE
+    big = pkg.make_shape(4, 4096, 16, 4096, 1, 1)
+    extra = pkg.ssm_scan_workspace_bytes(big, 2) - pkg.ssm_scan_workspace_bytes(big, False)
+    assert extra >= 4 * 4096 * 4096 * 4 + 4 * 4096 * 32 * 4
+
+
 def test_workspace_query(pkg):
     ok = pkg.make_shape(4, 4096, 16, 4096, 1, 1)
     n = pkg.ssm_scan_workspace_bytes(ok)
