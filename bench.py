@@ -91,7 +91,7 @@ KERNEL_SOURCES = {
                    "ssm_kernels.cuh"],
     "fwdbwd": ["ssm_fwd.cuh", "ssm_fwd_launch.cuh", "ssm_fwd_np16.cu", "ssm_bwd.cuh", "ssm_bwd_launch.cuh",
                "ssm_bwd_np16.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
-    "step_dec16_kernel": ["ssm_aux.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
+    "step_dec16_kernel": ["ssm_step.cu", "ssm_common.cuh", "ssm_kernels.cuh"],
 }
 
 
@@ -352,10 +352,11 @@ class OracleTimer:
         if self.bidir:
             what = "bidirectional scan"
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
-                "sample": "%s of %d channels x %d batch rows x %d tokens x %d states of the %s "
-                          "workload, one spawned process per core (%d channels each); slowest "
-                          "process %.2f s" % (what, per * self.cores, self.bt, w["L"], w["N"],
-                                              w["name"], per, busy)}
+                "sample": "%s of %d (channel, batch row) sequences x %d tokens x %d states of the "
+                          "%s workload (channels taken in turn from its %d, batch row 0%s), one "
+                          "spawned process per core (%d each); slowest process %.2f s"
+                          % (what, per * self.cores * self.bt, w["L"], w["N"], w["name"], w["D"],
+                             " .. %d" % (self.bt - 1) if self.bt > 1 else "", per * self.bt, busy)}
 
     def close(self):
         self.pool.close()
@@ -777,10 +778,12 @@ def run_ours(args):
         "exps": wl.exps,
         "traffic": recorded_traffic({"fwd": "fwd_kernel", "fwdbwd": "fwdbwd", "step": "step_dec16_kernel"}[wl.mode],
                                     w["name"]),
-        "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
-                         "kernel" if wl.mode != "fwdbwd" else
-                         "dram__bytes_read.sum + dram__bytes_write.sum of the forward and the two "
-                         "backward sweeps of one step") +
+        "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of the forward and the two "
+                         "backward sweeps of one step" if wl.mode == "fwdbwd" else
+                         "dram__bytes_read.sum + dram__bytes_write.sum of the two passes (right to "
+                         "left, left to right) of one step" if getattr(wl, "bidir", False) else
+                         "dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
+                         "kernel") +
                         " (ncu, profiles/traffic.json); null when the kernels changed since",
         "fp32_ops_per_update": 4,
         "timing_note": ("achieved uses the whole step's CUDA-event time (one kernel per decode "

@@ -45,7 +45,7 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     shutil.copytree(csrc, root / "selective_state_space_123_b300" / "csrc")
     monkeypatch.setattr(bench, "ROOT", str(root))
     base = bench.kernel_source_hash("step_dec16_kernel")
-    f = root / "selective_state_space_123_b300" / "csrc" / "ssm_aux.cu"
+    f = root / "selective_state_space_123_b300" / "csrc" / "ssm_step.cu"
     text = f.read_text(encoding="utf-8")
     f.write_text(text + "\n// a comment\n/* another\n comment */\n", encoding="utf-8")
     assert bench.kernel_source_hash("step_dec16_kernel") == base
