@@ -145,6 +145,23 @@ __global__ void __launch_bounds__(1024) tail_kernel(const FwdParams p, int CH, i
     const int64_t c_begin = (int64_t)seg * p.seg_chunks;
     const int64_t c_end = c_begin + p.seg_chunks;       // segments 0 .. nseg-2 are full
     const int64_t s0 = c_begin * kT, s1 = c_end * kT;
+    if (p.cu_seqlens) {
+        // packed sequences: a segment holding a sequence start needs only the
+        // tokens from its last start on (the carry then drops the incoming
+        // state); the condition is the same for the whole block
+        int lo = 0, hi = p.nseq;   // first start at or after the segment's end
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)p.cu_seqlens[mid] < s1) lo = mid + 1;
+            else hi = mid;
+        }
+        if (lo > 0 && (int64_t)p.cu_seqlens[lo - 1] >= s0) {
+            if (threadIdx.x == 0)
+                tstart[((int64_t)seg * p.Bt + b) * gridDim.x + tile] =
+                    (int)((int64_t)p.cu_seqlens[lo - 1] / kT);
+            return;
+        }
+    }
     __shared__ int cmin;
     if (threadIdx.x == 0) cmin = (int)(c_end - c_begin);
     __syncthreads();
