@@ -381,6 +381,8 @@ class Workload:
         self.ssm, self.w = ssm, w
         Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
         self.mode = w["mode"]
+        # forward variants: conv prologue width, packed-sequence starts, two directions
+        self.conv_k, self.cu, self.bidir = w.get("conv", 0), None, bool(w.get("bidir"))
         bf = torch.bfloat16
         if self.mode == "step":
             a = device_inputs(Bt, D, N, 1, seed=rank_seed(w["seed"], rank), in_dtype="bf16", h0=True)
@@ -416,9 +418,6 @@ class Workload:
             self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
             self.bytes = fwd_bytes(Bt, D, N, L)
             self.exps = Bt * D * L * N
-            self.conv_k = w.get("conv", 0)
-            self.cu = None
-            self.bidir = bool(w.get("bidir"))
             if self.bidir:
                 # the right-to-left direction's own parameters (u and z are shared)
                 r = device_inputs(Bt, D, N, L, seed=rank_seed(w["seed"], rank) + 1, in_dtype="bf16")
@@ -458,8 +457,8 @@ class Workload:
                 self.exps *= 3     # forward, and the backward's two sweeps
                 self.launches += 3
         # state updates per step (the bidirectional scan runs two)
-        self.updates = Bt * D * L * N * (2 if getattr(self, "bidir", False) else 1)
-        if getattr(self, "bidir", False):
+        self.updates = Bt * D * L * N * (2 if self.bidir else 1)
+        if self.bidir:
             self.outs.append(self.hL_r)
 
     def capture_graphs(self):
@@ -727,8 +726,7 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if (wl.mode in ("fwd", "step") and not getattr(wl, "conv_k", 0)
-                and getattr(wl, "cu", None) is None and not getattr(wl, "bidir", False)):
+        if wl.mode in ("fwd", "step") and not wl.conv_k and wl.cu is None and not wl.bidir:
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
                        "scans and copies" % ("batch rows" if wl.w["Bt"] > 1 else "channels"))
@@ -781,7 +779,7 @@ def run_ours(args):
         "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of the forward and the two "
                          "backward sweeps of one step" if wl.mode == "fwdbwd" else
                          "dram__bytes_read.sum + dram__bytes_write.sum of the two passes (right to "
-                         "left, left to right) of one step" if getattr(wl, "bidir", False) else
+                         "left, left to right) of one step" if wl.bidir else
                          "dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant "
                          "kernel") +
                         " (ncu, profiles/traffic.json); null when the kernels changed since",

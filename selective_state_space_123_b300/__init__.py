@@ -132,8 +132,7 @@ def make_shape(batch, dim, dstate, seqlen, in_dtype, out_dtype) -> ssm_shape:
 def ssm_scan_workspace_bytes(shape: ssm_shape, for_backward=False) -> int:
     """Workspace bytes: for_backward False/0 forward, True/1 backward, 2 the
     bidirectional forward."""
-    kind = 2 if (not isinstance(for_backward, bool) and for_backward == 2) else int(bool(for_backward))
-    return int(lib.ssm_scan_workspace_bytes(ctypes.byref(shape), kind))
+    return int(lib.ssm_scan_workspace_bytes(ctypes.byref(shape), int(for_backward)))
 
 
 def _workspace(shape: ssm_shape, for_backward, device, workspace):

@@ -173,8 +173,16 @@ def test_status_and_debug_argument_errors(pkg):
 def test_binding_refuses_cpu_tensors(pkg):
     import torch
     u = torch.zeros(1, 2, 8)
+    A, Bm = torch.zeros(2, 4), torch.zeros(1, 4, 8)
     with pytest.raises(ValueError):
-        pkg.ssm_scan_fwd(u, u, torch.zeros(2, 4), torch.zeros(1, 4, 8), torch.zeros(1, 4, 8))
+        pkg.ssm_scan_fwd(u, u, A, Bm, Bm)
+    with pytest.raises(ValueError):
+        pkg.ssm_scan_fwd_conv(u, torch.zeros(2, 4), None, u, A, Bm, Bm)
+    with pytest.raises(ValueError):
+        pkg.ssm_scan_fwd_varlen(u, torch.tensor([0, 8], dtype=torch.int32), u, A, Bm, Bm)
+    d = dict(delta_raw=u, A=A, B=Bm, C=Bm)
+    with pytest.raises(ValueError):
+        pkg.ssm_scan_fwd_bidir(u, None, d, d)
 
 
 def _call_bwd(pkg, shape, ptrs=None, ws_bytes=1 << 30, ws=0x10000):

@@ -51,3 +51,45 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("step_dec16_kernel") == base
     f.write_text(text + "\nstatic int extra_symbol = 1;\n", encoding="utf-8")
     assert bench.kernel_source_hash("step_dec16_kernel") != base
+
+
+@pytest.mark.parametrize("variant,factor", [((0, False, False), 1), ((4, False, False), 1),
+                                            ((0, True, False), 1), ((0, False, True), 2)])
+def test_oracle_worker_variants(variant, factor):
+    """The CPU baseline's worker runs every forward variant and counts the
+    state updates it did (two scans for the bidirectional one)."""
+    conv_k, varlen, bidir = variant
+    upd, secs = bench._oracle_worker(("fwd", 7, 1, 64, 16, 256, [0, 5], conv_k, varlen, bidir))
+    assert upd == factor * 2 * 16 * 256
+    assert secs >= 0.0
+
+
+def _plan_lines(shape, kind):
+    """The planner's choice for `shape`, printed by the library itself."""
+    import subprocess
+    import sys
+    code = ("import selective_state_space_123_b300 as m\n"
+            "m.ssm_scan_workspace_bytes(m.make_shape(%d, %d, %d, %d, 1, 1), %d)\n" % (shape + (kind,)))
+    env = dict(os.environ, SSM_DEBUG_PLAN="1")
+    for k in ("SSM_FWD_NT", "SSM_FWD_W", "SSM_FWD_NSEG", "SSM_FWD_CPS"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, "-c", code], cwd=bench.ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    return [ln for ln in r.stderr.splitlines() if ln.startswith("ssm fwd plan")]
+
+
+def test_launch_counts_follow_the_plan():
+    """The bench's launch claims for the packed and bidirectional workloads
+    rest on the plan: 4 segments for the packed row (preparation, sequence
+    check, tail search, summary, carry, scan), one segment per direction for
+    the bidirectional scan even on a long row."""
+    from tests.buildlib import ensure_built
+    ensure_built()
+    w = bench.WORKLOADS["packed_mamba1p4b_fwd"]
+    lines = _plan_lines((w["Bt"], w["D"], w["N"], w["L"]), 0)
+    assert lines and "nseg=4 " in lines[-1] and w["launches"] == 6
+    w = bench.WORKLOADS["bidir_mamba1p4b_fwd"]
+    assert w["launches"] == 4
+    lines = _plan_lines((1, 1536, 16, 1 << 20), 2)
+    assert lines and "nseg=1 " in lines[-1]
