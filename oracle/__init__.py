@@ -52,26 +52,30 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def bind(lib):
+    """Declare the C functions' argument types on a loaded oracle library."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int64
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_conv_silu.argtypes = [I, I, I, I, P, P, P, P]
+    lib.oracle_conv_silu.restype = None
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_scan_fwd.argtypes = [I, I, I, I] + [P] * 11
+    lib.oracle_scan_fwd.restype = None
+    lib.oracle_scan_step.argtypes = [I, I, I] + [P] * 10
+    lib.oracle_scan_step.restype = None
+    lib.oracle_scan_bwd.argtypes = [I, I, I, I] + [P] * 20
+    lib.oracle_scan_bwd.restype = None
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            I = ctypes.c_int64
-            lib.oracle_softplus.argtypes = [ctypes.c_double]
-            lib.oracle_softplus.restype = ctypes.c_double
-            lib.oracle_conv_silu.argtypes = [I, I, I, I, P, P, P, P]
-            lib.oracle_conv_silu.restype = None
-            lib.oracle_silu.argtypes = [ctypes.c_double]
-            lib.oracle_silu.restype = ctypes.c_double
-            lib.oracle_scan_fwd.argtypes = [I, I, I, I] + [P] * 11
-            lib.oracle_scan_fwd.restype = None
-            lib.oracle_scan_step.argtypes = [I, I, I] + [P] * 10
-            lib.oracle_scan_step.restype = None
-            lib.oracle_scan_bwd.argtypes = [I, I, I, I] + [P] * 20
-            lib.oracle_scan_bwd.restype = None
-            _lib = lib
+            _lib = bind(ctypes.CDLL(build()))
     return _lib
 
 
