@@ -24,6 +24,16 @@
 // the segment's sum of delta2 (the decay of the carried state over the
 // segment is 2^(A * sum)); it starts at the chunk a tail search found (the
 // earlier tokens' decay to the segment end is below 2^-40).
+// Variants, each its own instantiation ("Mamba Architecture Explained"):
+//   CONV = true   the raw tile holds the conv branch input x; u = silu(causal
+//                 depthwise conv of x) is formed per lane from the tile
+//                 (section "The Architecture in Practice");
+//   VARLEN = true packed sequences: the state restarts at every start in
+//                 cu_seqlens (section "Problem 3: Ecosystem maturity");
+//   DIR = 1 / 2   the bidirectional scan's right-to-left pass (chunks,
+//                 super-blocks and tokens in reverse order) and its
+//                 left-to-right pass, which adds the first pass's output
+//                 (section "Frequently Asked Questions").
 #pragma once
 
 #include "ssm_common.cuh"
