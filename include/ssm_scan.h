@@ -45,7 +45,8 @@
  *    stream) and runs asynchronously.  Argument errors are detected on the
  *    host before anything is enqueued and returned synchronously.  Errors
  *    detected on the device (a bounded wait that expired) are written to the
- *    status word in the workspace and read with ssm_get_status.
+ *    status word in the workspace and read with ssm_get_status; so are
+ *    packed-sequence starts out of order (ssm_scan_fwd_varlen).
  *  - Gradient outputs are overwritten, never accumulated into.
  *  - Return value: SSM_OK (0) or one of the negative SSM_ERR_* codes.
  */
@@ -143,7 +144,8 @@ SSM_API int ssm_scan_fwd_conv(const ssm_shape* shape, const void* x, const float
  * (empty sequences allowed).  Each sequence is scanned on its own: its state
  * starts at h0[s] (zero when h0 is NULL) and, with conv_w given, its
  * convolution window starts from zeros; nothing crosses a start.
- *   cu_seqlens : int32 (nseq + 1), device memory, required.  Start values
+ *   cu_seqlens : int32 (nseq + 1), device memory (4-byte alignment is
+ *     enough for this one pointer), required.  Start values
  *     that break the order above are reported as SSM_ERR_SEQLENS in the
  *     workspace status word (ssm_get_status); the outputs are then undefined,
  *     and no access goes outside the buffers.

@@ -272,3 +272,27 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_header_is_plain_c_and_links(pkg, tmp_path):
+    """include/ssm_scan.h compiles as C99 with warnings as errors, and a C
+    program that takes the address of every declared function links against
+    the library (no torch, no C++ in the interface)."""
+    import subprocess
+    names = _declared_symbols()
+    src = tmp_path / "use_abi.c"
+    src.write_text('#include "ssm_scan.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   "    const void* fns[] = {%s};\n"
+                   "    ssm_shape s = {1, 1, 16, 64, SSM_BF16, SSM_F32};\n"
+                   "    printf(\"%%d %%d\\n\", (int)(sizeof(fns) / sizeof(fns[0])),\n"
+                   "           ssm_scan_workspace_bytes(&s, 0) > 0);\n"
+                   "    return 0;\n}\n" % ", ".join("(const void*)%s" % n for n in names))
+    exe = tmp_path / "use_abi"
+    lib_dir = os.path.dirname(pkg.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror",
+                           "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                           str(exe), "-L", lib_dir, "-lssmscan", "-Wl,-rpath," + lib_dir])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(len(names)), "1"]
