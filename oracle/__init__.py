@@ -153,6 +153,48 @@ def scan_fwd_varlen(u, delta_raw, A, Bm, Cm, cu_seqlens, Dv=None, z=None, delta_
     return y, hL
 
 
+def scan_bwd_varlen(u, delta_raw, A, Bm, Cm, dy, cu_seqlens, Dv=None, z=None, delta_bias=None,
+                    h0=None, dhL=None):
+    """Reverse mode of scan_fwd_varlen (without the conv prologue): each
+    packed sequence's own reverse mode (scan_bwd on its token range, from its
+    h0[s] and with its dhL[s]); the per-token gradients land in the sequence's
+    range and the per-channel ones (dA, dD, ddelta_bias) are summed over the
+    sequences.  dh0 is (nseq, Bt, D, N); an empty sequence passes dhL[s]
+    straight to dh0[s]."""
+    u, delta_raw, Bm, Cm, dy, z = map(_f64, (u, delta_raw, Bm, Cm, dy, z))
+    cu = [int(v) for v in cu_seqlens]
+    Bt, D, L = u.shape
+    N = A.shape[1]
+    nseq = len(cu) - 1
+    assert nseq >= 1 and cu[0] == 0 and cu[-1] == L
+    assert all(cu[s] <= cu[s + 1] for s in range(nseq))
+    h0 = None if h0 is None else _f64(h0)
+    dhL = None if dhL is None else _f64(dhL)
+    out = {
+        "du": np.zeros((Bt, D, L)), "ddelta_raw": np.zeros((Bt, D, L)),
+        "dA": np.zeros((D, N)), "dB": np.zeros((Bt, N, L)), "dC": np.zeros((Bt, N, L)),
+        "dD": np.zeros((D,)), "dz": np.zeros((Bt, D, L)), "ddelta_bias": np.zeros((D,)),
+        "dh0": np.zeros((nseq, Bt, D, N)),
+    }
+    for s in range(nseq):
+        lo, hi = cu[s], cu[s + 1]
+        if hi == lo:
+            if dhL is not None:
+                out["dh0"][s] = dhL[s]
+            continue
+        cut = lambda a: None if a is None else a[:, :, lo:hi]
+        g = scan_bwd(cut(u), cut(delta_raw), A, cut(Bm), cut(Cm), cut(dy), Dv, cut(z),
+                     delta_bias, None if h0 is None else h0[s], None if dhL is None else dhL[s])
+        for k in ("du", "ddelta_raw", "dB", "dC", "dz"):
+            out[k][:, :, lo:hi] = g[k]
+        for k in ("dA", "dD", "ddelta_bias"):
+            out[k] += g[k]
+        out["dh0"][s] = g["dh0"]
+    if z is None:
+        out["dz"][:] = 0.0
+    return out
+
+
 def scan_fwd_bidir(u, z, fwd, rev):
     """Bidirectional scan ("Mamba Architecture Explained", section "Frequently
     Asked Questions": bidirectional SSM variants beside the causal scan): the

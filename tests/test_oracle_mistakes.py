@@ -52,8 +52,9 @@ C_MISTAKES = [
 
 # (name, text in oracle/__init__.py, replacement)
 PY_MISTAKES = [
-    ("packed sequence one token too long", "        lo, hi = cu[s], cu[s + 1]\n",
-     "        lo, hi = cu[s], min(cu[s + 1] + 1, L)\n"),
+    ("packed sequence one token too long",
+     "        lo, hi = cu[s], cu[s + 1]\n        hs = None if h0 is None else h0[s]\n",
+     "        lo, hi = cu[s], min(cu[s + 1] + 1, L)\n        hs = None if h0 is None else h0[s]\n"),
     ("packed h0 of the first sequence", "        hs = None if h0 is None else h0[s]\n",
      "        hs = None if h0 is None else h0[0]\n"),
     ("packed conv window across starts",
@@ -62,13 +63,19 @@ PY_MISTAKES = [
     ("right-to-left output not mirrored back", "        return f(y), h\n", "        return y, h\n"),
     ("right-to-left scan with the left-to-right parameters", "    yr, hr = one(rev, True)\n",
      "    yr, hr = one(fwd, True)\n"),
+    ("packed backward: channel gradients of the last sequence only", "            out[k] += g[k]\n",
+     "            out[k] = g[k]\n"),
+    ("packed backward: dh0 into the first sequence", "        out[\"dh0\"][s] = g[\"dh0\"]\n",
+     "        out[\"dh0\"][0] = g[\"dh0\"]\n"),
+    ("packed backward: the first sequence's dhL", "None if dhL is None else dhL[s])",
+     "None if dhL is None else dhL[0])"),
     ("right-to-left output not gated",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        f(z),",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        None if flip else f(z),"),
 ]
 
-PUBLIC = ("softplus", "silu", "conv_silu", "scan_fwd_conv", "scan_fwd_varlen", "scan_fwd_bidir",
-          "scan_fwd", "scan_step", "scan_bwd")
+PUBLIC = ("softplus", "silu", "conv_silu", "scan_fwd_conv", "scan_fwd_varlen", "scan_bwd_varlen",
+          "scan_fwd_bidir", "scan_fwd", "scan_step", "scan_bwd")
 
 
 def _pin_calls():

@@ -517,3 +517,55 @@ def test_bidirectional_final_states_and_mirror():
     np.testing.assert_allclose(flip(ym), y, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(hfm, hr, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(hrm, hf, rtol=1e-12, atol=1e-12)
+
+
+def test_varlen_backward_equal_lengths_match_batched_rows():
+    """Packed equal-length sequences: the reverse mode equals the batched
+    reverse mode with one sequence per batch row (the channel sums dA, dD,
+    ddelta_bias match the sums over batch rows)."""
+    S, D, N, Ls = 3, 4, 3, 9
+    x = make_inputs(S, D, N, Ls, seed=63, in_dtype="f32", h0=True, dy=True)
+    dhL = _rng(64).standard_normal((S, D, N))
+    rows = lambda a: _pack([a[s:s + 1] for s in range(S)])
+    cu = [Ls * s for s in range(S + 1)]
+    g = oracle.scan_bwd_varlen(rows(x.u), rows(x.delta_raw), x.A, rows(x.Bm), rows(x.Cm),
+                               rows(x.dy), cu, x.Dv, rows(x.z), x.delta_bias, x.h0[:, None],
+                               dhL[:, None])
+    r = oracle.scan_bwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, x.Dv, x.z, x.delta_bias, x.h0, dhL)
+    for k in ("du", "ddelta_raw", "dB", "dC", "dz"):
+        np.testing.assert_allclose(g[k][0], np.concatenate(list(r[k]), axis=1), rtol=1e-12,
+                                   atol=1e-13, err_msg=k)
+    for k in ("dA", "dD", "ddelta_bias"):
+        np.testing.assert_allclose(g[k], r[k], rtol=1e-12, atol=1e-13, err_msg=k)
+    np.testing.assert_allclose(g["dh0"][:, 0], r["dh0"], rtol=1e-12, atol=1e-13)
+
+
+def test_varlen_backward_adjoint_identity():
+    """<dy, J v> + <dhL, J_h v> = <J^T (dy, dhL), v> through the packed forward,
+    with empty sequences and a one-token sequence among them."""
+    x = make_inputs(1, 3, 4, 20, seed=65, in_dtype="f32", dy=True)
+    cu = [0, 0, 1, 9, 9, 20]
+    nseq = len(cu) - 1
+    rng = _rng(66)
+    names = ["u", "delta_raw", "A", "Bm", "Cm", "Dv", "z", "delta_bias"]
+    base = {n: getattr(x, n).astype(np.float64) for n in names}
+    base["h0"] = rng.standard_normal((nseq, 1, 3, 4))
+    v = {n: rng.standard_normal(base[n].shape) for n in base}
+    dy = x.dy.astype(np.float64)
+    dhL = rng.standard_normal((nseq, 1, 3, 4))
+
+    def fwd(p):
+        return oracle.scan_fwd_varlen(p["u"], p["delta_raw"], p["A"], p["Bm"], p["Cm"], cu,
+                                      p["Dv"], p["z"], p["delta_bias"], p["h0"])
+    g = oracle.scan_bwd_varlen(base["u"], base["delta_raw"], base["A"], base["Bm"], base["Cm"],
+                               dy, cu, base["Dv"], base["z"], base["delta_bias"], base["h0"], dhL)
+    eps = 1e-5
+    yp, hp = fwd({n: base[n] + eps * v[n] for n in base})
+    ym, hm = fwd({n: base[n] - eps * v[n] for n in base})
+    lhs = (np.sum(dy * (yp - ym)) + np.sum(dhL * (hp - hm))) / (2 * eps)
+    gn = dict(u="du", delta_raw="ddelta_raw", A="dA", Bm="dB", Cm="dC", Dv="dD", z="dz",
+              delta_bias="ddelta_bias", h0="dh0")
+    rhs = sum(np.sum(g[gn[n]] * v[n]) for n in base)
+    assert lhs == pytest.approx(rhs, rel=1e-7)
+    np.testing.assert_array_equal(g["dh0"][0], dhL[0])   # empty sequences pass dhL through
+    np.testing.assert_array_equal(g["dh0"][3], dhL[3])
