@@ -214,6 +214,26 @@ def scan_fwd_bidir(u, z, fwd, rev):
     return yf + yr, hf, hr
 
 
+def scan_bwd_bidir(u, z, fwd, rev, dy, dhL=None, dhL_r=None):
+    """Reverse mode of scan_fwd_bidir: each direction's reverse mode (the
+    right-to-left one on mirrored tensors, mirrored back); du and dz are the
+    sums of the two directions'.  Returns (shared, grads_fwd, grads_rev):
+    shared = {du, dz}; each grads dict holds ddelta_raw, dA, dB, dC, dD,
+    ddelta_bias, dh0 for its direction."""
+    def one(d, flip, dh):
+        f = (lambda a: None if a is None else np.ascontiguousarray(np.asarray(a)[..., ::-1])) \
+            if flip else (lambda a: a)
+        g = scan_bwd(f(u), f(d["delta_raw"]), d["A"], f(d["Bm"]), f(d["Cm"]), f(dy), d.get("Dv"),
+                     f(z), d.get("delta_bias"), d.get("h0"), dh)
+        for k in ("du", "ddelta_raw", "dB", "dC", "dz"):
+            g[k] = f(g[k])
+        return g
+    gf = one(fwd, False, dhL)
+    gr = one(rev, True, dhL_r)
+    shared = {"du": gf.pop("du") + gr.pop("du"), "dz": gf.pop("dz") + gr.pop("dz")}
+    return shared, gf, gr
+
+
 def scan_fwd(u, delta_raw, A, Bm, Cm, Dv=None, z=None, delta_bias=None, h0=None):
     """Forward selective scan.  Shapes: u, delta_raw, z (Bt,D,L); Bm, Cm (Bt,N,L);
     A (D,N); Dv, delta_bias (D); h0 (Bt,D,N).  Returns (y (Bt,D,L), hL (Bt,D,N))."""

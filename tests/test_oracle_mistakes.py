@@ -69,13 +69,19 @@ PY_MISTAKES = [
      "        out[\"dh0\"][0] = g[\"dh0\"]\n"),
     ("packed backward: the first sequence's dhL", "None if dhL is None else dhL[s])",
      "None if dhL is None else dhL[0])"),
+    ("bidirectional backward: right-to-left gradients not mirrored back",
+     "        for k in (\"du\", \"ddelta_raw\", \"dB\", \"dC\", \"dz\"):\n            g[k] = f(g[k])\n", ""),
+    ("bidirectional backward: dz of one direction", "\"dz\": gf.pop(\"dz\") + gr.pop(\"dz\")",
+     "\"dz\": gf.pop(\"dz\") + 0.0 * gr.pop(\"dz\")"),
+    ("bidirectional backward: the other direction's dhL", "    gr = one(rev, True, dhL_r)\n",
+     "    gr = one(rev, True, dhL)\n"),
     ("right-to-left output not gated",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        f(z),",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        None if flip else f(z),"),
 ]
 
 PUBLIC = ("softplus", "silu", "conv_silu", "scan_fwd_conv", "scan_fwd_varlen", "scan_bwd_varlen",
-          "scan_fwd_bidir", "scan_fwd", "scan_step", "scan_bwd")
+          "scan_fwd_bidir", "scan_bwd_bidir", "scan_fwd", "scan_step", "scan_bwd")
 
 
 def _pin_calls():

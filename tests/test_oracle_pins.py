@@ -569,3 +569,38 @@ def test_varlen_backward_adjoint_identity():
     assert lhs == pytest.approx(rhs, rel=1e-7)
     np.testing.assert_array_equal(g["dh0"][0], dhL[0])   # empty sequences pass dhL through
     np.testing.assert_array_equal(g["dh0"][3], dhL[3])
+
+
+def test_bidirectional_backward_adjoint_identity():
+    """<dy, J v> + <dhL, J_f v> + <dhL_r, J_r v> = <J^T (dy, dhL, dhL_r), v>
+    over both directions' parameters and the shared u, z."""
+    rng = _rng(67)
+    Bt, D, N, L = 2, 3, 4, 11
+    u = rng.standard_normal((Bt, D, L))
+    z = rng.standard_normal((Bt, D, L))
+
+    def params():
+        return dict(delta_raw=rng.standard_normal((Bt, D, L)), A=-rng.uniform(0.2, 2.0, (D, N)),
+                    Bm=rng.standard_normal((Bt, N, L)), Cm=rng.standard_normal((Bt, N, L)),
+                    Dv=rng.standard_normal(D), delta_bias=rng.uniform(-3, 0, D),
+                    h0=rng.standard_normal((Bt, D, N)))
+    f, r = params(), params()
+    dy = rng.standard_normal((Bt, D, L))
+    dhL, dhL_r = rng.standard_normal((Bt, D, N)), rng.standard_normal((Bt, D, N))
+    vu, vz = rng.standard_normal(u.shape), rng.standard_normal(z.shape)
+    vf = {k: rng.standard_normal(np.shape(a)) for k, a in f.items()}
+    vr = {k: rng.standard_normal(np.shape(a)) for k, a in r.items()}
+    eps = 1e-5
+
+    def at(sign):
+        return oracle.scan_fwd_bidir(u + sign * eps * vu, z + sign * eps * vz,
+                                     {k: a + sign * eps * vf[k] for k, a in f.items()},
+                                     {k: a + sign * eps * vr[k] for k, a in r.items()})
+    (yp, hp, hrp), (ym, hm, hrm) = at(1), at(-1)
+    lhs = (np.sum(dy * (yp - ym)) + np.sum(dhL * (hp - hm)) + np.sum(dhL_r * (hrp - hrm))) / (2 * eps)
+    shared, gf, gr = oracle.scan_bwd_bidir(u, z, f, r, dy, dhL, dhL_r)
+    names = dict(delta_raw="ddelta_raw", A="dA", Bm="dB", Cm="dC", Dv="dD",
+                 delta_bias="ddelta_bias", h0="dh0")
+    rhs = np.sum(shared["du"] * vu) + np.sum(shared["dz"] * vz)
+    rhs += sum(np.sum(gf[names[k]] * vf[k]) for k in f) + sum(np.sum(gr[names[k]] * vr[k]) for k in r)
+    assert lhs == pytest.approx(rhs, rel=1e-7)
