@@ -95,36 +95,3 @@ def test_conv_prologue_unsupported_shape(ssm, N, L):
     w, b = _conv_params(16, 4, 79)
     with pytest.raises(ssm.SSMError):
         _check(ssm, x, w, b)
-
-
-def _bench_workload(name):
-    import bench
-    return dict(bench.WORKLOADS[name], name=name)
-
-
-def test_conv_full_size_sampled(ssm):
-    """The bench's conv workload (Mamba-1.4B shape, width 4) on sampled
-    channels of every batch row, in the launch configuration the bench times."""
-    from scan_inputs import device_inputs
-    from tests.gpu_util import rows_to_host
-    w = _bench_workload("mamba1p4b_conv_fwd")
-    Bt, D, N, L, K = w["Bt"], w["D"], w["N"], w["L"], w["conv"]
-    a = device_inputs(Bt, D, N, L, seed=w["seed"], in_dtype="bf16")
-    cw, cb = _conv_params(D, K, 7)
-    y, hL = ssm.ssm_scan_fwd_conv(a["u"], to_dev(cw, torch.float32), to_dev(cb, torch.float32),
-                                  a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
-                                  a["delta_bias"], None, out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(1235)
-    for b in range(Bt):
-        ds = np.sort(rng.choice(D, size=6, replace=False))
-        ds[0], ds[-1] = 0, D - 1
-        host = lambda t: rows_to_host(t, [b], ds)
-        yo, ho = oracle.scan_fwd_conv(host(a["u"]), cw[ds], cb[ds], host(a["delta_raw"]),
-                                      a["A"][ds].cpu().numpy(), a["Bm"][[b]].float().cpu().numpy(),
-                                      a["Cm"][[b]].float().cpu().numpy(), a["Dv"][ds].cpu().numpy(),
-                                      host(a["z"]), a["delta_bias"][ds].cpu().numpy(), None)
-        assert_close(y[[b]][:, ds].cpu().numpy(), yo, TOL["bf16"], "y b=%d" % b)
-        assert_close(hL[[b]][:, ds].cpu().numpy(), ho, TOL["bf16"], "hL b=%d" % b)
-    del a, y, hL
-    torch.cuda.empty_cache()

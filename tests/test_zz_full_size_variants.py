@@ -1,0 +1,113 @@
+"""Full-size sampled parity of the forward variants, each at the size and in
+the launch configuration the bench times: the conv prologue (Mamba-1.4B shape,
+width 4), packed sequences (Mamba-1.4B channels, one 65,536-token row of 17
+sequences, four segments) and the bidirectional scan (Mamba-1.4B shape, two
+parameter sets).  Sampled channels of every batch row are compared with the
+oracle (channels are independent).  The smaller parity cases of each variant
+live in test_conv_parity.py, test_varlen_parity.py and test_bidir_parity.py;
+this file is collected after them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from scan_inputs import device_inputs, packed_seqlens
+from tests.gpu_util import load_ssm, rows_to_host, to_dev
+from tests.parity import TOL, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssm():
+    return load_ssm()
+
+
+def _conv_params(D, K, seed):
+    rng = np.random.default_rng(seed)
+    return ((0.5 * rng.standard_normal((D, K))).astype(np.float32),
+            (0.1 * rng.standard_normal(D)).astype(np.float32))
+
+
+def test_conv_full_size_sampled(ssm):
+    """The bench's conv workload (Mamba-1.4B shape, width 4) on sampled
+    channels of every batch row, in the launch configuration the bench times."""
+    w = bench.WORKLOADS["mamba1p4b_conv_fwd"]
+    Bt, D, N, L, K = w["Bt"], w["D"], w["N"], w["L"], w["conv"]
+    a = device_inputs(Bt, D, N, L, seed=w["seed"], in_dtype="bf16")
+    cw, cb = _conv_params(D, K, 7)
+    y, hL = ssm.ssm_scan_fwd_conv(a["u"], to_dev(cw, torch.float32), to_dev(cb, torch.float32),
+                                  a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
+                                  a["delta_bias"], None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1235)
+    for b in range(Bt):
+        ds = np.sort(rng.choice(D, size=6, replace=False))
+        ds[0], ds[-1] = 0, D - 1
+        host = lambda t: rows_to_host(t, [b], ds)
+        yo, ho = oracle.scan_fwd_conv(host(a["u"]), cw[ds], cb[ds], host(a["delta_raw"]),
+                                      a["A"][ds].cpu().numpy(), a["Bm"][[b]].float().cpu().numpy(),
+                                      a["Cm"][[b]].float().cpu().numpy(), a["Dv"][ds].cpu().numpy(),
+                                      host(a["z"]), a["delta_bias"][ds].cpu().numpy(), None)
+        assert_close(y[[b]][:, ds].cpu().numpy(), yo, TOL["bf16"], "y b=%d" % b)
+        assert_close(hL[[b]][:, ds].cpu().numpy(), ho, TOL["bf16"], "hL b=%d" % b)
+    del a, y, hL
+    torch.cuda.empty_cache()
+
+
+def test_varlen_full_size_sampled(ssm):
+    """The bench's packed workload (Mamba-1.4B channels, one 65,536-token row
+    of 17 sequences, four segments) on sampled channels."""
+    w = bench.WORKLOADS["packed_mamba1p4b_fwd"]
+    Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
+    a = device_inputs(Bt, D, N, L, seed=w["seed"], in_dtype="bf16")
+    cu = packed_seqlens(L, seed=w["seed"])
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    y, hL = ssm.ssm_scan_fwd_varlen(a["u"], cu_d, a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"],
+                                    a["z"], a["delta_bias"], None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ds = np.sort(np.random.default_rng(1236).choice(D, size=6, replace=False))
+    ds[0], ds[-1] = 0, D - 1
+    host = lambda t: rows_to_host(t, [0], ds)
+    yo, ho = oracle.scan_fwd_varlen(host(a["u"]), host(a["delta_raw"]), a["A"][ds].cpu().numpy(),
+                                    a["Bm"][[0]].float().cpu().numpy(),
+                                    a["Cm"][[0]].float().cpu().numpy(), cu, a["Dv"][ds].cpu().numpy(),
+                                    host(a["z"]), a["delta_bias"][ds].cpu().numpy())
+    assert_close(y[[0]][:, ds].cpu().numpy(), yo, TOL["bf16"], "y")
+    assert_close(hL[:, [0]][:, :, ds].cpu().numpy(), ho, TOL["bf16"], "hL")
+    del a, y, hL
+    torch.cuda.empty_cache()
+
+
+def test_bidir_full_size_sampled(ssm):
+    """The bench's bidirectional workload (Mamba-1.4B shape, two parameter
+    sets) on sampled channels of every batch row."""
+    w = bench.WORKLOADS["bidir_mamba1p4b_fwd"]
+    Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
+    a = device_inputs(Bt, D, N, L, seed=w["seed"], in_dtype="bf16")
+    r = device_inputs(Bt, D, N, L, seed=w["seed"] + 1, in_dtype="bf16")
+
+    def dev_dir(x):
+        return dict(delta_raw=x["delta_raw"], A=x["A"], B=x["Bm"], C=x["Cm"], D=x["Dv"],
+                    delta_bias=x["delta_bias"])
+    y, hL, hL_r = ssm.ssm_scan_fwd_bidir(a["u"], a["z"], dev_dir(a), dev_dir(r),
+                                         out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1237)
+    for b in range(Bt):
+        ds = np.sort(rng.choice(D, size=6, replace=False))
+        ds[0], ds[-1] = 0, D - 1
+        host = lambda t: rows_to_host(t, [b], ds)
+
+        def host_dir(x):
+            return dict(delta_raw=host(x["delta_raw"]), A=x["A"][ds].cpu().numpy(),
+                        Bm=x["Bm"][[b]].float().cpu().numpy(), Cm=x["Cm"][[b]].float().cpu().numpy(),
+                        Dv=x["Dv"][ds].cpu().numpy(), delta_bias=x["delta_bias"][ds].cpu().numpy())
+        yo, ho, hro = oracle.scan_fwd_bidir(host(a["u"]), host(a["z"]), host_dir(a), host_dir(r))
+        assert_close(y[[b]][:, ds].cpu().numpy(), yo, TOL["bf16"], "y b=%d" % b)
+        assert_close(hL[[b]][:, ds].cpu().numpy(), ho, TOL["bf16"], "hL b=%d" % b)
+        assert_close(hL_r[[b]][:, ds].cpu().numpy(), hro, TOL["bf16"], "hL_r b=%d" % b)
+    del a, r, y, hL, hL_r
+    torch.cuda.empty_cache()
