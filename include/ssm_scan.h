@@ -217,12 +217,18 @@ SSM_API int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delt
  *   u, delta_raw, z, y : (batch, dim);  B, C : (batch, dstate);  in_dtype / out_dtype.
  *   A : fp32 (dim, dstate), required.  D, z, delta_bias : nullable.
  *   state : fp32 (batch, dim, dstate), read and overwritten with the new state.
+ *   status : nullable device int32 (4-byte aligned).  If a bounded wait in
+ *     the kernel expires, SSM_ERR_TIMEOUT is written there (only if it still
+ *     holds SSM_OK) and y and the state are left partly updated, i.e.
+ *     undefined.  Read and clear it with ssm_get_status(status, stream) (a
+ *     256-byte workspace whose first word is the status serves as well).
+ *     With status NULL an expired wait is not reported.
  * Needs no workspace. */
 SSM_API int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype,
                   int32_t out_dtype, const void* u, const void* delta_raw,
                   const float* A, const void* B, const void* C, const float* D,
                   const void* z, const float* delta_bias, float* state, void* y,
-                  ssm_stream_t stream);
+                  int32_t* status, ssm_stream_t stream);
 
 /* Synchronise `stream`, then return the device status word held in
  * `workspace` (SSM_OK, SSM_ERR_TIMEOUT or SSM_ERR_SEQLENS) and reset it to SSM_OK.  Returns
@@ -233,6 +239,10 @@ SSM_API int ssm_get_status(void* workspace, ssm_stream_t stream);
 /* Human-readable text of a status code (static storage, never NULL). */
 SSM_API const char* ssm_strerror(int code);
 
+/* Size in bytes of the fixed scratch array ssm_scan_fwd_noalloc runs in
+ * (32 MiB). */
+#define SSM_NOALLOC_SCRATCH_BYTES 33554432
+
 /* ssm_scan_fwd for callers that cannot allocate device memory.  The method's
  * description has no counterpart to this entry point; it exists for callers
  * that are handed only their input and output buffers and may not allocate on the device
@@ -241,13 +251,19 @@ SSM_API const char* ssm_strerror(int code);
  * start-up, since it can synchronise the device and take unbounded time).
  * Arguments are those of ssm_scan_fwd without the workspace; nothing is
  * allocated or freed.
- *  - The scratch is a fixed 32 MiB array inside the library, held on every GPU
- *    that loads it until the process exits.  A shape whose
- *    ssm_scan_workspace_bytes(shape, 0) exceeds 32 MiB is rejected with
- *    SSM_ERR_WORKSPACE before anything is enqueued (at 16 states that is about
- *    262,000 tokens summed over the batch).
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - The scratch is a fixed array of SSM_NOALLOC_SCRATCH_BYTES (32 MiB)
+ *    inside the library.  A shape whose ssm_scan_workspace_bytes(shape, 0)
+ *    exceeds it is rejected with SSM_ERR_WORKSPACE before anything is
+ *    enqueued (at 16 states that is about 262,000 tokens summed over the
+ *    batch).
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress; a host-side lookup once the library's device code
+ *    is loaded, so a new CUDA context after cudaDeviceReset gets its own
+ *    address).  With CUDA's default lazy module loading the FIRST call on
+ *    each device (or context) loads the library's device code and so reserves
+ *    the 32 MiB there, which can allocate and synchronise: make one warm-up
+ *    call at start-up, before any stream capture.  The array then stays
+ *    reserved on that device until the process exits.
  *  - Every call shares the one array: calls whose work overlaps on the GPU
  *    (different streams, or several host threads) race and corrupt each
  *    other's results; issue them in order on one stream.  Each call rewrites
@@ -259,7 +275,9 @@ SSM_API int ssm_scan_fwd_noalloc(const ssm_shape* shape, const void* u, const vo
                  const void* z, const float* delta_bias, const float* h0,
                  void* y, float* hL, ssm_stream_t stream);
 
-/* Failure-detection self test: launches one block that waits on a device
+/* DIAGNOSTIC, not part of the scan: a failure-detection self test for the
+ * test suite and for a caller who wants to check that expired device waits
+ * reach the status word on their system.  Launches one block that waits on a device
  * flag nothing ever sets, giving up after `spin_limit` polls; the expired
  * wait is reported through the workspace status word (SSM_ERR_TIMEOUT, read
  * with ssm_get_status).  No copy is in flight while it waits. */

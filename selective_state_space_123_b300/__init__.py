@@ -68,7 +68,7 @@ lib.ssm_scan_fwd_bidir.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 20 + [cty
 lib.ssm_scan_fwd_bidir.restype = ctypes.c_int
 lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 21 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd.restype = ctypes.c_int
-lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 11
+lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 12
 lib.ssm_scan_step.restype = ctypes.c_int
 lib.ssm_get_status.argtypes = [_P, _P]
 lib.ssm_get_status.restype = ctypes.c_int
@@ -79,6 +79,7 @@ lib.ssm_debug_expired_wait.restype = ctypes.c_int
 # scratch-free forward (no workspace argument; see include/ssm_scan.h)
 lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 12
 lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+# SSM_NOALLOC_SCRATCH_BYTES of include/ssm_scan.h (a CPU test compares the two)
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -380,9 +381,12 @@ def ssm_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=
 
 
 def ssm_scan_step(u, delta_raw, A, B, C, state, D=None, z=None, delta_bias=None, *,
-                  out_dtype: Optional[torch.dtype] = None, y=None, stream=None) -> torch.Tensor:
+                  out_dtype: Optional[torch.dtype] = None, y=None, status=None,
+                  stream=None) -> torch.Tensor:
     """One decode step.  u, delta_raw, z: (Bt,D); B, C: (Bt,N); A: (D,N);
-    state: (Bt,D,N) fp32, updated in place.  Returns y (Bt,D)."""
+    state: (Bt,D,N) fp32, updated in place.  Returns y (Bt,D).  status: an
+    optional int32 CUDA tensor whose first element receives SSM_ERR_TIMEOUT
+    if a bounded wait in the kernel expires (read it with ssm_get_status)."""
     Bt, Dm = u.shape
     N = A.shape[1]
     dev = u.device
@@ -400,9 +404,12 @@ def ssm_scan_step(u, delta_raw, A, B, C, state, D=None, z=None, delta_bias=None,
     if y is None:
         y = torch.empty((Bt, Dm), dtype=out_dtype, device=dev)
     _check(y, "y", (Bt, Dm), out_dtype, dev)
+    if status is not None:
+        if status.dtype != torch.int32 or status.device != dev or status.numel() < 1:
+            raise ValueError("status must be an int32 tensor on %s" % dev)
     rc = lib.ssm_scan_step(Bt, Dm, N, _dt(tin), _dt(out_dtype), _ptr(u), _ptr(delta_raw),
                            _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-                           _ptr(state), _ptr(y), _stream_ptr(stream))
+                           _ptr(state), _ptr(y), _ptr(status), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_step")
     return y

@@ -809,7 +809,7 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
 int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, int32_t out_dtype,
                   const void* u, const void* delta_raw, const float* A, const void* B,
                   const void* C, const float* D, const void* z, const float* delta_bias,
-                  float* state, void* y, ssm_stream_t stream) {
+                  float* state, void* y, int* status, ssm_stream_t stream) {
     if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64) return SSM_ERR_SHAPE;
     if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
     int64_t bd, tmp;
@@ -819,10 +819,11 @@ int ssm_scan_step(int64_t batch, int64_t dim, int64_t dstate, int32_t in_dtype, 
     const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, state, y};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_ALIGN;
+    if (((uintptr_t)status % 4) != 0) return SSM_ERR_ALIGN;
     StepParams p;
     p.Bt = batch; p.D = dim; p.N = (int)dstate;
     p.u = u; p.dr = delta_raw; p.z = z; p.A = A; p.Dv = D; p.bias = delta_bias;
-    p.B = B; p.C = C; p.state = state; p.y = y;
+    p.B = B; p.C = C; p.state = state; p.y = y; p.status = status;
     if (dstate == 16 && dim % 128 == 0 && bd < (int64_t(1) << 31)) {
         // whole 128-channel tiles: the state and A stream through 2-D TMA tiles
         CUtensorMap tm_st, tm_a;

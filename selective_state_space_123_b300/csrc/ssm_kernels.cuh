@@ -155,6 +155,7 @@ struct StepParams {
     const void* C;
     float* state;
     void* y;
+    int* status;            // nullable: SSM_ERR_TIMEOUT on an expired wait
 };
 
 }  // namespace ssm

@@ -9,14 +9,16 @@
 // workspace; this entry point instead uses a fixed scratch array that lives in
 // the library itself, so the call allocates nothing.
 //
-// The scratch is a file-scope __device__ array of kScratchBytes (32 MiB).
-// Every GPU that loads this library holds it until the process exits.  Host
-// code must not use the array's name as a device address (on the host it only
-// stands in for the symbol); the device address is looked up once per device
-// with cudaGetSymbolAddress, with that device current, on the first call made
-// on it.
+// The scratch is a file-scope __device__ array of SSM_NOALLOC_SCRATCH_BYTES
+// (32 MiB, defined in ssm_scan.h).  Every GPU on which the library's device
+// code has been loaded holds it until the process exits.  Host code must not
+// use the array's name as a device address (on the host it only stands in for
+// the symbol); the device address is looked up on every call with
+// cudaGetSymbolAddress, with the caller's device current.  After the first
+// call on a device that is a host-side lookup; it is not cached, so a context
+// created after cudaDeviceReset (where the module can load at another
+// address) never receives a stale pointer.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -24,32 +26,20 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;
+constexpr size_t kScratchBytes = SSM_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device (looked up once per
-// device).  Returns nullptr on failure.
+// Device address of g_scratch in the current context.  Returns nullptr on
+// failure (the CUDA error state is cleared).  Under lazy module loading the
+// first lookup in a context loads the module, which reserves the array.
 void* scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return nullptr;
     }
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    return g_scratch_ptr[dev];
+    return p;
 }
 
 }  // namespace

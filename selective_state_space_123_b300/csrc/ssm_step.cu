@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(32 * (8 * QPR / 4 + 1), 1) step_tma_kernel(con
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
             const int s = j % kStepSlots;
             if (j >= kStepSlots &&
-                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kStepSlots) - 1) & 1), kDefaultTimeoutNs))
+                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kStepSlots) - 1) & 1), kDefaultTimeoutNs)) {
+                set_status(p.status, SSM_ERR_TIMEOUT);
                 return;                       // the consumers time out on their own waits
+            }
             const int r0 = tile * kStepRows;
             const int b = r0 / D, d0 = r0 - b * D;
             constexpr uint32_t sb = kStepRows * N * 4, ib = kStepRows * sizeof(TIN);
@@ -307,8 +309,10 @@ __global__ void __launch_bounds__(32 * (8 * QPR / 4 + 1), 1) step_tma_kernel(con
     int j = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
         const int s = j % kStepSlots;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((j / kStepSlots) & 1), kDefaultTimeoutNs)))
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((j / kStepSlots) & 1), kDefaultTimeoutNs))) {
+            if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
             return;                           // bounded wait expired: nothing more is written
+        }
         const StepSlot<TIN, QPR>& sl = ring[s];
         const float4 h4 = sl.st[tid];
         const float4 a4 = sl.a[tid];
@@ -449,8 +453,10 @@ __global__ void __launch_bounds__(160, 2) step_dec16_kernel(const StepParams p,
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
             const int s = j % kDecSlots;
             if (j >= kDecSlots &&
-                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kDecSlots) - 1) & 1), kDefaultTimeoutNs))
+                !mbar_wait(&empty_bar[s], (uint32_t)(((j / kDecSlots) - 1) & 1), kDefaultTimeoutNs)) {
+                set_status(p.status, SSM_ERR_TIMEOUT);
                 return;                       // the consumers time out on their own waits
+            }
             const int r0 = tile * kDecRows;
             const int b = r0 / D, d0 = r0 - b * D;
             constexpr uint32_t tb = kDecRows * 64, ib = kDecRows * sizeof(TIN), fb = kDecRows * 4;
@@ -480,6 +486,7 @@ __global__ void __launch_bounds__(160, 2) step_dec16_kernel(const StepParams p,
         const int s = j % kDecSlots;
         DecSlot<TIN>& sl = ring[s];
         if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((j / kDecSlots) & 1), kDefaultTimeoutNs))) {
+            if ((tid & 31) == 0) set_status(p.status, SSM_ERR_TIMEOUT);
             dead = 1;
             named_bar_sync(1, 128);
             break;

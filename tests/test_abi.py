@@ -153,7 +153,7 @@ def test_step_argument_errors(pkg):
     V = ctypes.c_void_p
     f = pkg.lib.ssm_scan_step
     args = [V(0x1000), V(0x2000), V(0x3000), V(0x4000), V(0x5000), None, None, None, V(0x6000),
-            V(0x7000), None]
+            V(0x7000), None, None]
     assert f(2, 8, 0, 1, 1, *args) == pkg.SSM_ERR_SHAPE
     assert f(2, 8, 16, 3, 1, *args) == pkg.SSM_ERR_DTYPE
     assert f(0, 8, 16, 1, 1, *args) == pkg.SSM_OK
@@ -161,6 +161,17 @@ def test_step_argument_errors(pkg):
     assert f(2, 8, 16, 1, 1, *bad) == pkg.SSM_ERR_NULL
     bad = list(args); bad[8] = V(0x6004)
     assert f(2, 8, 16, 1, 1, *bad) == pkg.SSM_ERR_ALIGN
+    bad = list(args); bad[10] = V(0x8002)   # the status word needs 4-byte alignment only
+    assert f(2, 8, 16, 1, 1, *bad) == pkg.SSM_ERR_ALIGN
+
+
+def test_noalloc_scratch_size_matches_header(pkg):
+    """The binding's copy of the no-alloc scratch size is the header's macro."""
+    import re
+    with open(os.path.join(ROOT, "include", "ssm_scan.h")) as f:
+        m = re.search(r"#define\s+SSM_NOALLOC_SCRATCH_BYTES\s+(\d+)", f.read())
+    assert m is not None
+    assert int(m.group(1)) == pkg.NOALLOC_SCRATCH_BYTES
 
 
 def test_status_and_debug_argument_errors(pkg):

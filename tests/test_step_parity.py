@@ -103,3 +103,24 @@ def test_steps_reproduce_forward(ssm):
     assert_close(np.stack(ys, -1), yo, TOL["bf16"], "stepped y vs oracle")
     assert_close(state, ho, TOL["bf16"], "stepped state vs oracle")
     assert_close(np.stack(ys, -1), yf, TOL["bf16"], "stepped y vs GPU forward")
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 16), (2, 192, 16), (2, 40, 16)])
+def test_step_status_word(ssm, shape):
+    """A status word passed to the decode step stays SSM_OK on a normal step
+    (each decode kernel path), the result is unchanged, and ssm_get_status
+    reads it back."""
+    Bt, D, N = shape
+    s = make_step_inputs(Bt, D, N, seed=50 + D, in_dtype="bf16")
+    tin, f32 = TIN["bf16"], torch.float32
+    status = torch.zeros(64, dtype=torch.int32, device="cuda")
+    st = to_dev(s["state"], f32)
+    y = ssm.ssm_scan_step(to_dev(s["u"], tin), to_dev(s["delta_raw"], tin), to_dev(s["A"], f32),
+                          to_dev(s["Bm"], tin), to_dev(s["Cm"], tin), st, to_dev(s["Dv"], f32),
+                          to_dev(s["z"], tin), to_dev(s["delta_bias"], f32),
+                          out_dtype=torch.float32, status=status)
+    assert ssm.ssm_get_status(status) == ssm.SSM_OK
+    yo, so = oracle.scan_step(s["u"], s["delta_raw"], s["A"], s["Bm"], s["Cm"], s["state"],
+                              s["Dv"], s["z"], s["delta_bias"])
+    assert_close(y.cpu().numpy(), yo, TOL["bf16"], "y")
+    assert_close(st.cpu().numpy(), so, TOL["bf16"], "state")
