@@ -850,7 +850,37 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def select_workload(name):
+    global WORKLOAD
+    WORKLOAD = dict(WORKLOADS[name], name=name)
+
+
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _rank_entry(rank, world, port, target, args):
+    """One spawned rank: the environment torchrun would give it, then the arm."""
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    select_workload(args.workload)   # a spawned process starts from a fresh import
+    target(args)
+
+
+def spawn_ranks(world, target, args):
+    """`--gpus N` without an outside launcher: start N processes (spawned, one
+    per GPU, ranks 0..N-1 on 127.0.0.1) that each run `target(args)`, as
+    torchrun would; the arm then forms its process group from the
+    environment.  Every rank runs an independent replica of the workload."""
+    import torch.multiprocessing as tmp
+    tmp.spawn(_rank_entry, args=(world, _free_port(), target, args), nprocs=world, join=True)
+
+
+def main(argv=None, target=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
@@ -861,15 +891,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end measurement (profiling runs)")
     ap.add_argument("--workload", default="mamba1p4b_fwd", choices=sorted(WORKLOADS))
-    args = ap.parse_args()
-    global WORKLOAD
-    WORKLOAD = dict(WORKLOADS[args.workload], name=args.workload)
+    args = ap.parse_args(argv)
+    select_workload(args.workload)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
-        run_reference(args)
+    if target is None:
+        target = run_reference if args.impl == "reference" else run_ours
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        spawn_ranks(args.gpus, target, args)
     else:
-        run_ours(args)
+        target(args)
 
 
 if __name__ == "__main__":
