@@ -76,8 +76,9 @@ WORKLOADS = {
 WORKLOAD = WORKLOADS["mamba1p4b_fwd"]
 METRIC = "selective scan: achieved HBM GB/s (% of roofline) and B*D*L*N state updates/s"
 UNIT = "state updates/s"
-# MUFU ex2 results per clock per SM on the B300 (31.3 measured with a
-# register-only probe; the part's exponential rate is 32 per clock per SM)
+# MUFU ex2 results per clock per SM, nominal for the B300; the roofline uses
+# the rate the register-only probe (selective_state_space_123_b300/peaks.py)
+# measures in the same process, and reports the nominal fraction beside it
 SFU_EX2_PER_CLK_SM = 32
 SMS = 148
 L2_BYTES = 126 * 1024 * 1024
@@ -636,6 +637,10 @@ def run_ours(args):
         cpu = cpu_oracle_rate(args.cpu_seconds)
 
     import selective_state_space_123_b300 as ssm
+    from selective_state_space_123_b300 import peaks as ssm_peaks
+
+    # the MUFU ex2 rate per SM clock, measured before the workload exists
+    ex2_clk = ssm_peaks.rate_per_clk_sm("ex2")
 
     w = WORKLOAD
     wl = Workload(ssm, w, rank)
@@ -753,7 +758,8 @@ def run_ours(args):
     hbm_basis = "MEASURED_PEAKS.json hbm_gbs (of measured)" if "hbm_gbs" in peaks else \
         "fallback 6400 GB/s (of fallback)"
     sm_mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
-    sfu_peak = SFU_EX2_PER_CLK_SM * SMS * sm_mhz * 1e6
+    sfu_peak = ex2_clk * SMS * sm_mhz * 1e6
+    sfu_nominal = SFU_EX2_PER_CLK_SM * SMS * sm_mhz * 1e6
     t_s = ms_step * 1e-3
     gbs = wl.bytes / t_s / 1e9
     t_hbm = wl.bytes / (hbm_peak * 1e9)
@@ -768,8 +774,12 @@ def run_ours(args):
         "peak": sfu_peak / 1e12 if bound == "alu" else hbm_peak,
         "unit": "Texp2/s" if bound == "alu" else "GB/s",
         "frac": (wl.exps / t_s / sfu_peak) if bound == "alu" else gbs / hbm_peak,
-        "peak_basis": ("MUFU ex2 32/clk/SM x 148 SMs x median SM clock %.0f MHz sampled in the "
-                       "timed region (probe-measured rate)" % sm_mhz) if bound == "alu" else hbm_basis,
+        "peak_basis": ("MUFU ex2 %.2f/clk/SM (measured in this process by the register-only "
+                       "probe, selective_state_space_123_b300/peaks.py) x 148 SMs x median SM clock "
+                       "%.0f MHz sampled in the timed region (of measured)" % (ex2_clk, sm_mhz))
+                      if bound == "alu" else hbm_basis,
+        "ex2_per_clk_sm_measured": ex2_clk,
+        "frac_of_nominal_32_per_clk": (wl.exps / t_s / sfu_nominal) if bound == "alu" else None,
         "roofline_time_us": max(t_hbm, t_sfu) * 1e6,
         "frac_of_roofline_time": max(t_hbm, t_sfu) / t_s,
         "algorithmic_bytes": wl.bytes,
@@ -852,7 +862,46 @@ def run_reference(args):
 
 def select_workload(name):
     global WORKLOAD
-    WORKLOAD = dict(WORKLOADS[name], name=name)
+    WORKLOAD = dict(WORKLOADS.get(name, WORKLOADS["mamba1p4b_fwd"]), name=name)
+
+
+def run_peaks(args):
+    """The roofline's denominators measured on this GPU: MUFU ex2 results,
+    FP32 lane operations (scalar and f32x2 FMA) and scan state updates per
+    SM clock cycle, at several warp counts per SM, with the SM clock sampled
+    meanwhile.  One JSON line."""
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    from selective_state_space_123_b300 import peaks as ssm_peaks
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    clocks.wait_first()
+    t0 = time.time()
+    by_threads = {}
+    for threads in (128, 256, 512, 1024):
+        by_threads[threads] = {k: ssm_peaks.rate_per_clk_sm(k, threads)
+                               for k in ("ex2", "fma", "fma2", "update_mix")}
+    clk = clocks.stop(t0, time.time())
+    best = {k: max(v[k] for v in by_threads.values()) for k in ("ex2", "fma", "fma2", "update_mix")}
+    sm_mhz = clk.get("sm_mhz") or 2032.0
+    line = {
+        "metric": "per-SM-clock peaks of the units that bound the scan",
+        "unit": "operations per clock per SM",
+        "ex2_per_clk_sm": best["ex2"],
+        "fp32_fma_lane_ops_per_clk_sm": best["fma"],
+        "fp32x2_fma_lane_ops_per_clk_sm": best["fma2"],
+        "update_mix_per_clk_sm": best["update_mix"],
+        "by_threads_per_sm": by_threads,
+        "sms": SMS,
+        "ex2_per_s_at_sampled_clock": best["ex2"] * SMS * sm_mhz * 1e6,
+        "nominal_ex2_per_clk_sm": SFU_EX2_PER_CLK_SM,
+        "method": "one CTA per SM, 8 independent register chains per thread, %clock64 per CTA, "
+                  "best of 3 launches, median over CTAs",
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def _free_port():
@@ -890,13 +939,15 @@ def main(argv=None, target=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end measurement (profiling runs)")
-    ap.add_argument("--workload", default="mamba1p4b_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="mamba1p4b_fwd", choices=sorted(WORKLOADS) + ["peaks"],
+                    help="'peaks': the register-only MUFU / FP32 / update-mix rate probes")
     args = ap.parse_args(argv)
     select_workload(args.workload)
     if args.warmup < 3:
         args.warmup = 3
     if target is None:
-        target = run_reference if args.impl == "reference" else run_ours
+        target = run_reference if args.impl == "reference" else \
+            run_peaks if args.workload == "peaks" else run_ours
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         spawn_ranks(args.gpus, target, args)
     else:

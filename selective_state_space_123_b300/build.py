@@ -24,6 +24,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libssmscan.so")
+# register-only rate probes for the roofline (bench.py --workload peaks)
+PROBE_SRC = os.path.join(CSRC, "probe", "ssm_peaks.cu")
+PEAKS_LIB = os.path.join(PKG, "libssmpeaks.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -73,7 +76,21 @@ def build(force: bool = False, jobs: int = 0, verbose_ptxas: bool = False) -> st
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
         os.replace(tmp, LIB)
+    build_peaks(force)
     return LIB
+
+
+def build_peaks(force: bool = False) -> str:
+    deps = [PROBE_SRC] + _headers()
+    if force or not os.path.exists(PEAKS_LIB) or \
+            os.path.getmtime(PEAKS_LIB) < max(os.path.getmtime(d) for d in deps):
+        tmp = PEAKS_LIB + ".tmp%d" % os.getpid()
+        cmd = [nvcc(), *NVCC_FLAGS, "-shared", PROBE_SRC, "-o", tmp, "-lcudart"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s%s" % (PROBE_SRC, r.stdout, r.stderr))
+        os.replace(tmp, PEAKS_LIB)
+    return PEAKS_LIB
 
 
 def main():

@@ -89,6 +89,48 @@ __device__ __forceinline__ float exp2_accurate(float x) {
     p = fmaf(p, f, 1.0f);
     return __int_as_float(__float_as_int(p) + (n << 23));
 }
+// 2^x - 1 with a small relative error for every x (the forgetting rate of a
+// decay 2^x close to 1 keeps its own digits instead of those of 1).  With x =
+// n + f as in exp2_accurate: (2^f - 1) / f = sum_{k>=1} ln2^k f^(k-1) / k! to
+// k = 8 (truncation < 1e-9 relative), 2^f - 1 = f times that, and for n != 0
+// 2^x - 1 = 2^n (2^f - 1) + (2^n - 1), where 2^n - 1 is exact for |n| <= 24
+// and the two terms do not cancel.
+__device__ __forceinline__ float exp2m1_accurate(float x) {
+    x = fminf(fmaxf(x, -125.0f), 127.0f);
+    const int n = __float2int_rn(x);
+    const float f = x - (float)n;
+    float q = 1.3215486790144307e-06f;            // ln2^8 / 8!
+    q = fmaf(q, f, 1.5252733804059840e-05f);      // ln2^7 / 7!
+    q = fmaf(q, f, 1.5403530393381606e-04f);      // ln2^6 / 6!
+    q = fmaf(q, f, 1.3333558146428443e-03f);      // ln2^5 / 5!
+    q = fmaf(q, f, 9.6181291076284770e-03f);      // ln2^4 / 4!
+    q = fmaf(q, f, 5.5504108664821580e-02f);      // ln2^3 / 3!
+    q = fmaf(q, f, 2.4022650695910070e-01f);      // ln2^2 / 2!
+    q = fmaf(q, f, 6.9314718055994530e-01f);      // ln2
+    const float em1f = f * q;
+    if (n == 0) return em1f;
+    const float p = __int_as_float((n + 127) << 23);   // 2^n, -125 <= n <= 127
+    return fmaf(p, em1f, p - 1.0f);
+}
+
+// log2(1 + e) for 0 <= e <= 1 on the FMA pipe, to a few fp32 ulps: with
+// s = e / (2 + e) (0 <= s <= 1/3), ln(1 + e) = 2 atanh(s) = 2 (s + s^3/3 +
+// s^5/5 + ...), summed to s^17 (truncation < 2e-9 relative at s = 1/3).
+__device__ __forceinline__ float log2_1p_accurate(float e) {
+    const float s = __fdiv_rn(e, 2.0f + e);
+    const float s2 = s * s;
+    float p = 1.0f / 17.0f;
+    p = fmaf(p, s2, 1.0f / 15.0f);
+    p = fmaf(p, s2, 1.0f / 13.0f);
+    p = fmaf(p, s2, 1.0f / 11.0f);
+    p = fmaf(p, s2, 1.0f / 9.0f);
+    p = fmaf(p, s2, 1.0f / 7.0f);
+    p = fmaf(p, s2, 1.0f / 5.0f);
+    p = fmaf(p, s2, 1.0f / 3.0f);
+    p = fmaf(p, s2, 1.0f);
+    return (2.0f * kLog2e) * (s * p);
+}
+
 __device__ __forceinline__ f2 exp2_accurate_x2(f2 x) {
     float lo, hi;
     upk(x, lo, hi);
@@ -97,25 +139,25 @@ __device__ __forceinline__ f2 exp2_accurate_x2(f2 x) {
 
 // softplus in log2 units: for x = (delta_raw + bias) * log2(e) return
 // log2(1 + 2^x) = delta / ln 2.
-//  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), where for 2^-|x| <
-//  1/16 the logarithm is its Taylor series to the fifth power (relative
-//  truncation error < 2e-7) instead of the MUFU lg2, whose absolute error
-//  near 1 would dominate small results.
-//  fast (bf16 inputs): max(x, lg2(1 + 2^min(x, 64))); the absolute error of
-//  lg2 near 1 (~1e-7) is far below the bf16 tolerance.
+//  ACCURATE (fp32 inputs): max(x, 0) + log2(1 + 2^-|x|), both the power and
+//  the logarithm on the FMA pipe (exp2_accurate, log2_1p_accurate), so that
+//  delta keeps fp32-level relative accuracy down to the smallest steps (the
+//  MUFU lg2's absolute error near 1 would dominate small results); 0 below
+//  x = -126, where delta / ln2 < 2^-126.
+//  fast (bf16 inputs): max(x, lg2(1 + e)) with e = 2^min(x, 64), except for
+//  e < 1/64, where 1 + e loses e's low bits to rounding and the lg2's
+//  absolute error near 1 would be a large relative error of a tiny delta
+//  (the long-memory regime): there log2(1 + e) = log2(e) (e - e^2/2 + ...)
+//  truncated after the quadratic term (relative error < e^2/3 < 8.2e-5).
 template <bool ACCURATE>
 __device__ __forceinline__ float softplus2(float x) {
     if (ACCURATE) {
-        const float e = ex2(-fabsf(x));
-        float p = fmaf(e, 0.2f, -0.25f);
-        p = fmaf(e, p, 0.33333334f);
-        p = fmaf(e, p, -0.5f);
-        p = fmaf(e, p, 1.0f);
-        const float series = e * p * kLog2e;
-        const float direct = lg2(1.0f + e);
-        return fmaxf(x, 0.0f) + (e < 0.0625f ? series : direct);
+        if (x < -126.0f) return 0.0f;
+        return fmaxf(x, 0.0f) + log2_1p_accurate(exp2_accurate(-fabsf(x)));
     } else {
-        return fmaxf(x, lg2(1.0f + ex2(fminf(x, 64.0f))));
+        const float e = ex2(fminf(x, 64.0f));
+        const float series = e * fmaf(e, -0.5f * kLog2e, kLog2e);
+        return e < 0.015625f ? series : fmaxf(x, lg2(1.0f + e));
     }
 }
 

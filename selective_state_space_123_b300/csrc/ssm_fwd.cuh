@@ -17,8 +17,9 @@
 //     (softplus, gate, D skip) and exchange it with warp shuffles;
 //   * per token and state: dA = 2^(delta2 * A) on the MUFU (delta2 = delta /
 //     ln 2, so no extra scaling), h = dA h + delta u B, y += C h, in packed
-//     f32x2 arithmetic.  With fp32 inputs the exp2 is the FMA-pipe series
-//     (exp2_accurate) so that long sequences keep fp32-level agreement.
+//     f32x2 arithmetic.  With fp32 inputs the state is carried compensated
+//     (comp_update: two floats, the decay as 2^x - 1 on the FMA pipe) so that
+//     long sequences and long memories keep fp32-level agreement.
 // SUMMARY = true is pass 1 of the segmented plan for very long sequences: no
 // read-out, the kernel records each segment's end state from a zero start and
 // the segment's sum of delta2 (the decay of the carried state over the
@@ -144,18 +145,41 @@ struct NoRestart {
     __device__ __forceinline__ void operator()(int, H&) const {}
 };
 
+// One state's update in the compensated form used for fp32 inputs.  The state
+// is hi + lo (two floats).  With e = 2^x - 1 (x = delta2 * A, exp2m1_accurate)
+// the update is h + (e h + xin): when the decay is close to 1 this keeps the
+// forgetting rate e to its own relative accuracy (2^x rounded to fp32 would
+// keep only that of 1), and the rounding error of adding the small increment
+// to hi is recovered exactly (TwoSum) into lo, so that it does not pile up
+// over the ~1/(delta |A|) tokens the state remembers.  For e < -1/2 (the
+// state forgets within a few tokens, nothing accumulates) the plain form
+// (1 + e) h + xin is used, 1 + e being exact there.
+__device__ __forceinline__ void comp_update(float x, float xin, float& hi, float& lo) {
+    const float e = exp2m1_accurate(x);
+    const float a = 1.0f + e;
+    const float plain = fmaf(a, hi, xin);
+    const float inc = fmaf(e, hi, xin);
+    const float s = hi + inc;
+    const float bb = s - hi;
+    const float err = (hi - (s - bb)) + (inc - bb);
+    const bool fast = e < -0.5f;
+    lo = fmaf(e, lo, lo) + (fast ? 0.0f : err);
+    hi = fast ? plain : s;
+}
+
 // The recurrence over one super-block of SB tokens for one lane's G states.
 //   d2, du: delta/ln2 and delta2*u of the SB tokens (registers)
 //   bcb:    prepared B/C row of the super-block's first token at this lane's states
+//   hl:     low parts of the compensated state (ACCURATE only; unused otherwise)
 // With RESTART, tokens whose bit is set in `rmask` begin a packed sequence:
-// `restart(tt, h)` replaces the state before that token's update.  With REV
-// the tokens are taken from the last to the first.
+// `restart(tt, h)` replaces the state (h and hl) before that token's update.
+// With REV the tokens are taken from the last to the first.
 template <int NP, int G, int SB, bool SUMMARY, bool ACCURATE, bool REV = false,
           bool RESTART = false, typename F = NoRestart>
 __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&du)[SB],
                                           const float* bcb, const f2 (&Ap)[G / 2],
-                                          f2 (&h)[G / 2], float (&yp)[SB], uint32_t rmask = 0,
-                                          F restart = F()) {
+                                          f2 (&h)[G / 2], f2 (&hl)[G / 2], float (&yp)[SB],
+                                          uint32_t rmask = 0, F restart = F()) {
     constexpr int Q = G / 4;
 #pragma unroll
     for (int t0 = 0; t0 < SB; ++t0) {
@@ -169,16 +193,34 @@ __device__ __forceinline__ void fwd_chain(const float (&d2)[SB], const float (&d
 #pragma unroll
         for (int q4 = 0; q4 < Q; ++q4) {
             const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
-            const f2 a0 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4]))
-                                   : ex2x2(mul2(d2p, Ap[2 * q4]));
-            const f2 a1 = ACCURATE ? exp2_accurate_x2(mul2(d2p, Ap[2 * q4 + 1]))
-                                   : ex2x2(mul2(d2p, Ap[2 * q4 + 1]));
-            h[2 * q4] = fma2(a0, h[2 * q4], mul2(dup, Bq.x));
-            h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
+            if constexpr (ACCURATE) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 2 * q4 + e;
+                    float x0, x1, i0, i1, h0, h1, l0, l1;
+                    upk(mul2(d2p, Ap[j]), x0, x1);
+                    upk(mul2(dup, e ? Bq.y : Bq.x), i0, i1);
+                    upk(h[j], h0, h1);
+                    upk(hl[j], l0, l1);
+                    comp_update(x0, i0, h0, l0);
+                    comp_update(x1, i1, h1, l1);
+                    h[j] = pk(h0, h1);
+                    hl[j] = pk(l0, l1);
+                }
+            } else {
+                const f2 a0 = ex2x2(mul2(d2p, Ap[2 * q4]));
+                const f2 a1 = ex2x2(mul2(d2p, Ap[2 * q4 + 1]));
+                h[2 * q4] = fma2(a0, h[2 * q4], mul2(dup, Bq.x));
+                h[2 * q4 + 1] = fma2(a1, h[2 * q4 + 1], mul2(dup, Bq.y));
+            }
             if (!SUMMARY) {
                 const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
                 acc = fma2(Cq.x, h[2 * q4], acc);
                 acc = fma2(Cq.y, h[2 * q4 + 1], acc);
+                if constexpr (ACCURATE) {
+                    acc = fma2(Cq.x, hl[2 * q4], acc);
+                    acc = fma2(Cq.y, hl[2 * q4 + 1], acc);
+                }
             }
         }
         if (!SUMMARY) {
@@ -333,12 +375,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int src_base = lane & ~(NT - 1);         // lane g = 0 of this channel
 
     f2 Ap[G / 2], h[G / 2];
+    f2 hl[G / 2];   // low parts of the compensated state (fp32 inputs), else zero
 #pragma unroll
     for (int j = 0; j < G / 2; ++j) {
         const int n0 = g * G + 2 * j, n1 = n0 + 1;
         const float a0 = (ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f;
         const float a1 = (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f;
         Ap[j] = pk(a0, a1);
+        hl[j] = pk(0.0f, 0.0f);
         float h0v = 0.0f, h1v = 0.0f;
         if (!SUMMARY && ch_ok) {
             if (p.hin) {
@@ -397,14 +441,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int last = p.nseq - 1;
             if (!SUMMARY && ch_ok && p.hL && t > 0) {
                 const int sf = min(max(sp - 1, 0), last);
-                float* hl = p.hL + ((int64_t)sf * p.Bt * p.D + row) * N;
+                float* hfin = p.hL + ((int64_t)sf * p.Bt * p.D + row) * N;
 #pragma unroll
                 for (int j = 0; j < G / 2; ++j) {
                     float lo, hi;
-                    upk(hh[j], lo, hi);
+                    upk(ACCURATE ? add2(hh[j], hl[j]) : hh[j], lo, hi);
                     const int n0 = g * G + 2 * j;
-                    if (n0 < N) hl[n0] = lo;
-                    if (n0 + 1 < N) hl[n0 + 1] = hi;
+                    if (n0 < N) hfin[n0] = lo;
+                    if (n0 + 1 < N) hfin[n0 + 1] = hi;
                 }
             }
             while (sp < p.nseq && (int64_t)cu[sp] <= t) ++sp;
@@ -414,6 +458,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             for (int j = 0; j < G / 2; ++j) {
                 const int n0 = g * G + 2 * j;
                 hh[j] = pk((hs && n0 < N) ? hs[n0] : 0.0f, (hs && n0 + 1 < N) ? hs[n0 + 1] : 0.0f);
+                hl[j] = pk(0.0f, 0.0f);
             }
             next_start = sp < p.nseq ? (int64_t)cu[sp] : INT64_MAX;
         }
@@ -537,7 +582,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if constexpr (VARLEN) {
                 if (rmask != 0) {
                     fwd_chain<NP, G, SB, SUMMARY, ACCURATE, false, true>(
-                        d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, yp, rmask,
+                        d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, hl, yp, rmask,
                         [&](int tt, f2 (&hh)[G / 2]) { restart(t_sb + tt, hh); });
                     cur_start = t_sb + (31 - __clz(rmask));
                     restarted = true;
@@ -545,7 +590,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             if (!restarted)
                 fwd_chain<NP, G, SB, SUMMARY, ACCURATE, DIR == 1>(
-                    d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, yp);
+                    d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, hl, yp);
 
             if (!SUMMARY) {
                 // 3. partial read-outs through the buffer; finish the own tokens
@@ -622,13 +667,13 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
         for (int o = 1; o < NT; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if (ch_ok) {
-            float* hl = p.hloc + ((int64_t)seg * p.Bt * p.D + row) * NP + g * G;
+            float* hsum = p.hloc + ((int64_t)seg * p.Bt * p.D + row) * NP + g * G;
 #pragma unroll
             for (int j = 0; j < G / 2; ++j) {
                 float lo, hi;
-                upk(h[j], lo, hi);
-                hl[2 * j] = lo;
-                hl[2 * j + 1] = hi;
+                upk(ACCURATE ? add2(h[j], hl[j]) : h[j], lo, hi);
+                hsum[2 * j] = lo;
+                hsum[2 * j + 1] = hi;
             }
             // a summary over the whole segment has the exact sum; a shortened one
             // keeps the search's saturation marker
@@ -639,14 +684,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     } else if (k_end == nchunks && p.hL && ch_ok) {
         // the last sequence's final state (packed: the one holding token L-1)
         const int64_t sf = VARLEN ? (int64_t)min(max(sp - 1, 0), p.nseq - 1) : 0;
-        float* hl = p.hL + (sf * p.Bt * p.D + row) * N;
+        float* hfin = p.hL + (sf * p.Bt * p.D + row) * N;
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) {
             float lo, hi;
-            upk(h[j], lo, hi);
+            upk(ACCURATE ? add2(h[j], hl[j]) : h[j], lo, hi);
             const int n0 = g * G + 2 * j;
-            if (n0 < N) hl[n0] = lo;
-            if (n0 + 1 < N) hl[n0 + 1] = hi;
+            if (n0 < N) hfin[n0] = lo;
+            if (n0 + 1 < N) hfin[n0 + 1] = hi;
         }
     }
 }

@@ -15,7 +15,7 @@ import torch
 import oracle
 from scan_inputs import WORKLOADS, device_inputs, make_inputs
 from tests.gpu_util import gpu_fwd, load_ssm, oracle_fwd, rows_to_host
-from tests.parity import TOL, TOL_F32_LONG, assert_bf16_output, assert_close
+from tests.parity import TOL, assert_bf16_output, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -100,7 +100,7 @@ def test_segmented_plan_long_segments(ssm, dt, L, bias_shift, monkeypatch):
     monkeypatch.setenv("SSM_FWD_NSEG", "2")
     x = make_inputs(1, 40, 16, L, seed=13, in_dtype=dt, h0=True)
     x.delta_bias = (x.delta_bias + np.float32(bias_shift)).astype(np.float32)
-    tol = TOL_F32_LONG if dt == "f32" else TOL[dt]
+    tol = TOL[dt]
     y, hL = gpu_fwd(ssm, x)
     yo, ho = oracle_fwd(x)
     assert_close(y, yo, tol, "y")

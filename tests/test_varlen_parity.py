@@ -9,7 +9,7 @@ import torch
 import oracle
 from scan_inputs import make_inputs, packed_seqlens
 from tests.gpu_util import device_args, load_ssm, to_dev
-from tests.parity import TOL, TOL_F32_LONG, assert_close
+from tests.parity import TOL, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -91,7 +91,7 @@ def test_varlen_segmented(ssm, nseg, monkeypatch):
     _run(ssm, x, cuts, _h0(len(cuts) - 1, 1, 40, 16, 89), conv=_conv(40, 90))
     _run(ssm, x, [0, 1000, L])
     xf = make_inputs(1, 24, 16, L, seed=91, in_dtype="f32")
-    _run(ssm, xf, cuts, tol=TOL_F32_LONG)
+    _run(ssm, xf, cuts)
 
 
 def test_varlen_packed_recipe(ssm):
