@@ -72,6 +72,18 @@ WORKLOADS = {
                                  launches=6,
                                  title="Mamba-1.4B layer forward over packed sequences of mixed "
                                        "length"),
+    # forward (6 launches as above) + packed backward (B/C preparation,
+    # sequence check, forward sweep, reverse sweep)
+    "packed_mamba1p4b_fwdbwd": dict(mode="fwdbwd", varlen=True, Bt=1, D=4096, N=16, L=65536,
+                                    seed=5, launches=10,
+                                    title="Mamba-1.4B layer forward + backward over packed "
+                                          "sequences of mixed length"),
+    # forward (4 launches) + backward of both directions: left-to-right
+    # backward (3), status fold, 6 token reversals, right-to-left backward (3),
+    # status fold, combine, 2 reversals of dB/dC
+    "bidir_mamba1p4b_fwdbwd": dict(mode="fwdbwd", bidir=True, Bt=4, D=4096, N=16, L=4096, seed=6,
+                                   launches=21,
+                                   title="Mamba-1.4B layer bidirectional scan, forward + backward"),
 }
 WORKLOAD = WORKLOADS["mamba1p4b_fwd"]
 METRIC = "selective scan: achieved HBM GB/s (% of roofline) and B*D*L*N state updates/s"
@@ -279,17 +291,22 @@ def _oracle_worker(args):
         cw = (0.5 * g.standard_normal((D, conv_k))).astype(np.float32)[chans]
         cb = (0.1 * g.standard_normal(D)).astype(np.float32)[chans]
     t0 = time.perf_counter()
-    if mode == "fwd" and bidir:
+    if bidir:
         xf, xr = x
         d = lambda v: dict(delta_raw=v.delta_raw, A=v.A, Bm=v.Bm, Cm=v.Cm, Dv=v.Dv,
                            delta_bias=v.delta_bias)
         oracle.scan_fwd_bidir(xf.u, xf.z, d(xf), d(xr))
+        if mode == "fwdbwd":
+            oracle.scan_bwd_bidir(xf.u, xf.z, d(xf), d(xr), xf.dy)
         return 2 * Bt * len(chans) * N * L, time.perf_counter() - t0
-    if mode == "fwd" and varlen:
+    if varlen:
         from scan_inputs import packed_seqlens
         cu = packed_seqlens(L, seed=seed)
         t0 = time.perf_counter()
         oracle.scan_fwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, cu, x.Dv, x.z, x.delta_bias)
+        if mode == "fwdbwd":
+            oracle.scan_bwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, cu, x.Dv, x.z,
+                                   x.delta_bias)
     elif mode == "fwd" and conv_k:
         oracle.scan_fwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
     elif mode == "fwd":
@@ -349,9 +366,9 @@ class OracleTimer:
         if self.conv_k:
             what = "conv prologue + forward"
         if self.varlen:
-            what = "packed-sequence forward"
+            what = "packed-sequence " + what
         if self.bidir:
-            what = "bidirectional scan"
+            what = "bidirectional scan " + what
         return {"value": upd / busy, "unit": UNIT, "cores": self.cores, "kind": "oracle",
                 "sample": "%s of %d (channel, batch row) sequences x %d tokens x %d states of the "
                           "%s workload (channels taken in turn from its %d, batch row 0%s), one "
@@ -427,6 +444,8 @@ class Workload:
                 del r
                 self.hL_r = torch.empty(Bt, D, N, dtype=torch.float32, device="cuda")
                 nb = ssm.ssm_scan_workspace_bytes(shape, 2)
+                if self.mode == "fwdbwd":
+                    nb = max(nb, ssm.ssm_scan_workspace_bytes(shape, 3))
                 self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
                 # second direction: delta_raw, B, C, A, D, bias read, final state written
                 self.bytes += (Bt * D * L * 2 + 2 * Bt * N * L * 2 + D * N * 4 + 2 * D * 4
@@ -454,9 +473,12 @@ class Workload:
             self.outs = [self.y, self.hL]
             self.grads = None
             if self.mode == "fwdbwd":
-                self.bytes += bwd_bytes(Bt, D, N, L)
+                # the backward's algorithmic bytes, once per direction (each
+                # reads its inputs and dy and writes its gradients)
+                self.bytes += bwd_bytes(Bt, D, N, L) * (2 if self.bidir else 1)
                 self.exps *= 3     # forward, and the backward's two sweeps
-                self.launches += 3
+                if "launches" not in w:
+                    self.launches += 3
         # state updates per step (the bidirectional scan runs two)
         self.updates = Bt * D * L * N * (2 if self.bidir else 1)
         if self.bidir:
@@ -507,11 +529,18 @@ class Workload:
                      delta_bias=a["delta_bias_r"])
             ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=torch.bfloat16, y=self.y,
                                    hL=self.hL, hL_r=self.hL_r, workspace=self.ws)
+            if self.mode == "fwdbwd":
+                self.grads = ssm.ssm_scan_bwd_bidir(a["u"], a["z"], f, r, a["dy"],
+                                                    out_dtype=torch.bfloat16, workspace=self.ws)
             return
         if self.cu is not None:
             ssm.ssm_scan_fwd_varlen(a["u"], self.cu, a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"],
                                     a["z"], a["delta_bias"], None, out_dtype=torch.bfloat16, y=self.y,
                                     hL=self.hL, workspace=self.ws)
+            if self.mode == "fwdbwd":
+                self.grads = ssm.ssm_scan_bwd_varlen(a["u"], self.cu, a["delta_raw"], a["A"], a["Bm"],
+                                                     a["Cm"], a["dy"], a["Dv"], a["z"], a["delta_bias"],
+                                                     out_dtype=torch.bfloat16, workspace=self.ws)
             return
         if self.conv_k:
             # u holds the conv branch input x
@@ -530,7 +559,9 @@ class Workload:
     def results(self):
         outs = list(self.outs)
         if self.mode == "fwdbwd" and self.grads is not None:
-            outs += [v for v in self.grads.values() if v is not None]
+            parts = self.grads if isinstance(self.grads, tuple) else (self.grads,)
+            for g in parts:
+                outs += [v for v in g.values() if v is not None]
         return outs
 
 
@@ -538,42 +569,47 @@ def pipelined_e2e(ssm, wl, host, dev, outs_host, state_host, ngroups=4):
     """End-to-end step through the public API with the host copies overlapped:
     the batch rows (or, for a single sequence, the channels) are split into
     `ngroups` groups that alternate between two streams; each group copies
-    its inputs in, runs its own scan call and copies its outputs back, so
-    one group's copies overlap another's scan and the two copy directions
-    run at once.  Inputs shared by all groups are copied first."""
+    its inputs in, runs its own call (decode step, forward, conv-prologue
+    forward, packed-sequence forward or bidirectional scan) and copies its
+    outputs back, so one group's copies overlap another's scan and the two
+    copy directions run at once.  Inputs shared by all groups are copied
+    first; the conv weights stay resident like the other layer parameters of
+    a serving loop do."""
     import torch
     bf = torch.bfloat16
     cur = torch.cuda.current_stream()
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    Bt, D = wl.w["Bt"], wl.w["D"]
+    Bt, D, N, L = wl.w["Bt"], wl.w["D"], wl.w["N"], wl.w["L"]
     by_batch = Bt > 1
     n = Bt if by_batch else D
     ngroups = max(1, min(ngroups, n))
     bounds = [(i * n // ngroups, (i + 1) * n // ngroups) for i in range(ngroups)]
     step = wl.mode == "step"
-    # per group: which tensors are sliced (first dim batch, or dim 1 / dim 0 = channels)
-    per_row = ["u", "delta_raw", "z"]
-    per_b = ["Bm", "Cm"]
-    per_d = ["A", "Dv", "delta_bias"]
+    # per group: which tensors are sliced (batch rows or channels)
+    per_row = [k for k in ("u", "delta_raw", "z", "delta_raw_r") if k in host]
+    per_b = [k for k in ("Bm", "Cm", "Bm_r", "Cm_r") if k in host]
+    per_d = [k for k in ("A", "Dv", "delta_bias", "A_r", "Dv_r", "delta_bias_r") if k in host]
     state_dev = wl.state if step else None
     y_dev, y_host = wl.outs[0], outs_host[0]
-    h_dev, h_host = wl.outs[1], outs_host[1]
     shared = (per_d if by_batch else per_b)
+    varlen = wl.cu is not None
+    nseq = wl.cu.numel() - 1 if varlen else 0
 
-    def cut(t, lo, hi, kind):
-        if kind == "row":
-            return t[lo:hi] if by_batch else t[:, lo:hi]
-        if kind == "b":
-            return t[lo:hi]
-        return t[lo:hi]            # per channel (first dim D)
+    def cut(t, lo, hi):
+        return t[lo:hi] if by_batch else t[:, lo:hi]
 
-    ws = None
+    ws = hv = None
     if not step:
         gb = (bounds[0][1] - bounds[0][0]) if by_batch else Bt
         gd = D if by_batch else max(hi - lo for lo, hi in bounds)
-        shape = ssm.make_shape(gb, gd, wl.w["N"], wl.w["L"], ssm.SSM_BF16, ssm.SSM_BF16)
-        nb = ssm.ssm_scan_workspace_bytes(shape)
+        shape = ssm.make_shape(gb, gd, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
+        nb = ssm.ssm_scan_workspace_bytes(shape, 2 if wl.bidir else 0)
         ws = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in streams]
+        if varlen:
+            # packed final states (nseq, Bt, D, N): one contiguous block per
+            # channel group, read back as such
+            hv = [torch.empty(nseq, Bt, hi - lo, N, dtype=torch.float32, device="cuda")
+                  for lo, hi in bounds]
 
     def one_step():
         for k in shared:
@@ -585,8 +621,8 @@ def pipelined_e2e(ssm, wl, host, dev, outs_host, state_host, ngroups=4):
             with torch.cuda.stream(s_):
                 a = {}
                 for k in per_row:
-                    a[k] = cut(dev[k], lo, hi, "row")
-                    a[k].copy_(cut(host[k], lo, hi, "row"), non_blocking=True)
+                    a[k] = cut(dev[k], lo, hi)
+                    a[k].copy_(cut(host[k], lo, hi), non_blocking=True)
                 for k in per_b:
                     if by_batch:
                         a[k] = dev[k][lo:hi]
@@ -599,21 +635,47 @@ def pipelined_e2e(ssm, wl, host, dev, outs_host, state_host, ngroups=4):
                     else:
                         a[k] = dev[k][lo:hi]
                         a[k].copy_(host[k][lo:hi], non_blocking=True)
+                yv = cut(y_dev, lo, hi)
                 if step:
-                    st = cut(state_dev, lo, hi, "row")
-                    st.copy_(cut(state_host, lo, hi, "row"), non_blocking=True)
-                    yv = cut(y_dev, lo, hi, "row")
+                    st = cut(state_dev, lo, hi)
+                    st.copy_(cut(state_host, lo, hi), non_blocking=True)
                     ssm.ssm_scan_step(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], st, a["Dv"],
                                       a["z"], a["delta_bias"], out_dtype=bf, y=yv, stream=s_)
-                    cut(y_host, lo, hi, "row").copy_(yv, non_blocking=True)
-                    cut(h_host, lo, hi, "row").copy_(st, non_blocking=True)
+                    cut(y_host, lo, hi).copy_(yv, non_blocking=True)
+                    cut(outs_host[1], lo, hi).copy_(st, non_blocking=True)
+                    continue
+                w_ = ws[gi % 2]
+                if wl.bidir:
+                    f = dict(delta_raw=a["delta_raw"], A=a["A"], B=a["Bm"], C=a["Cm"], D=a["Dv"],
+                             delta_bias=a["delta_bias"])
+                    r = dict(delta_raw=a["delta_raw_r"], A=a["A_r"], B=a["Bm_r"], C=a["Cm_r"],
+                             D=a["Dv_r"], delta_bias=a["delta_bias_r"])
+                    h1, h2 = cut(wl.outs[1], lo, hi), cut(wl.outs[2], lo, hi)
+                    ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=bf, y=yv, hL=h1, hL_r=h2,
+                                           workspace=w_, stream=s_)
+                    outs = [(yv, cut(y_host, lo, hi)), (h1, cut(outs_host[1], lo, hi)),
+                            (h2, cut(outs_host[2], lo, hi))]
+                elif varlen:
+                    ssm.ssm_scan_fwd_varlen(a["u"], wl.cu, a["delta_raw"], a["A"], a["Bm"], a["Cm"],
+                                            a["Dv"], a["z"], a["delta_bias"], None, out_dtype=bf,
+                                            y=yv, hL=hv[gi], workspace=w_, stream=s_)
+                    hh = outs_host[1].view(-1)[nseq * Bt * lo * N:nseq * Bt * hi * N].view_as(hv[gi])
+                    outs = [(yv, cut(y_host, lo, hi)), (hv[gi], hh)]
                 else:
-                    yv, hv = cut(y_dev, lo, hi, "row"), cut(h_dev, lo, hi, "row")
-                    ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
-                                     a["delta_bias"], None, out_dtype=bf, y=yv, hL=hv,
-                                     workspace=ws[gi % 2], stream=s_)
-                    cut(y_host, lo, hi, "row").copy_(yv, non_blocking=True)
-                    cut(h_host, lo, hi, "row").copy_(hv, non_blocking=True)
+                    h1 = cut(wl.outs[1], lo, hi)
+                    if wl.conv_k:
+                        cw = wl.conv_w if by_batch else wl.conv_w[lo:hi]
+                        cb = wl.conv_b if by_batch else wl.conv_b[lo:hi]
+                        ssm.ssm_scan_fwd_conv(a["u"], cw, cb, a["delta_raw"], a["A"], a["Bm"],
+                                              a["Cm"], a["Dv"], a["z"], a["delta_bias"], None,
+                                              out_dtype=bf, y=yv, hL=h1, workspace=w_, stream=s_)
+                    else:
+                        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"],
+                                         a["z"], a["delta_bias"], None, out_dtype=bf, y=yv, hL=h1,
+                                         workspace=w_, stream=s_)
+                    outs = [(yv, cut(y_host, lo, hi)), (h1, cut(outs_host[1], lo, hi))]
+                for d_, h_ in outs:
+                    h_.copy_(d_, non_blocking=True)
         for s_ in streams:
             cur.wait_stream(s_)
 
@@ -731,7 +793,7 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if wl.mode in ("fwd", "step") and not wl.conv_k and wl.cu is None and not wl.bidir:
+        if wl.mode in ("fwd", "step"):
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
                        "scans and copies" % ("batch rows" if wl.w["Bt"] > 1 else "channels"))
@@ -881,9 +943,10 @@ def run_peaks(args):
     by_threads = {}
     for threads in (128, 256, 512, 1024):
         by_threads[threads] = {k: ssm_peaks.rate_per_clk_sm(k, threads)
-                               for k in ("ex2", "fma", "fma2", "update_mix")}
+                               for k in ("ex2", "fma", "fma2", "update_mix", "lg2", "rcp")}
     clk = clocks.stop(t0, time.time())
-    best = {k: max(v[k] for v in by_threads.values()) for k in ("ex2", "fma", "fma2", "update_mix")}
+    best = {k: max(v[k] for v in by_threads.values())
+            for k in ("ex2", "fma", "fma2", "update_mix", "lg2", "rcp")}
     sm_mhz = clk.get("sm_mhz") or 2032.0
     line = {
         "metric": "per-SM-clock peaks of the units that bound the scan",
@@ -892,6 +955,8 @@ def run_peaks(args):
         "fp32_fma_lane_ops_per_clk_sm": best["fma"],
         "fp32x2_fma_lane_ops_per_clk_sm": best["fma2"],
         "update_mix_per_clk_sm": best["update_mix"],
+        "lg2_per_clk_sm": best["lg2"],
+        "rcp_per_clk_sm": best["rcp"],
         "by_threads_per_sm": by_threads,
         "sms": SMS,
         "ex2_per_s_at_sampled_clock": best["ex2"] * SMS * sm_mhz * 1e6,

@@ -94,7 +94,7 @@ enum {
 
 /* Bytes of device workspace the call needs for this shape on the current
  * device: for_backward = 0 for ssm_scan_fwd (and its _conv and _varlen forms),
- * 1 for ssm_scan_bwd, 2 for ssm_scan_fwd_bidir.  Always at
+ * 1 for ssm_scan_bwd, 2 for ssm_scan_fwd_bidir, 3 for ssm_scan_bwd_bidir.  Always at
  * least 256 (the status word lives at offset 0).  Returns 0 for an invalid
  * shape. */
 SSM_API size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward);
@@ -191,6 +191,39 @@ SSM_API int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void
                  void* y, float* hL, float* hL_r, void* workspace, size_t ws_bytes,
                  ssm_stream_t stream);
 
+/* Reverse mode of ssm_scan_fwd_bidir (the pages give no backward; it is the
+ * exact derivative of the two scans above).  The right-to-left scan is the
+ * left-to-right scan of the token-reversed sequence, so its reverse mode is
+ * ssm_scan_bwd run on token-reversed copies of its inputs (made in the
+ * workspace), with its per-token gradients reversed back; u and z feed both
+ * directions, so du and dz are the sums of the two directions' gradients.
+ *   Inputs: those of ssm_scan_fwd_bidir (both directions' parameters, u, z
+ *     nullable) plus dy : in_dtype (batch, dim, seqlen), required, and the
+ *     upstream gradients of the two final states, dhL (of hL) and dhL_r (of
+ *     hL_r) : fp32 (batch, dim, dstate), nullable (= 0).
+ *   Outputs (overwritten):
+ *     du : out_dtype, required;  dz : out_dtype, nullable (zeros without z);
+ *     per direction (suffix _r: right to left) ddelta_raw : out_dtype,
+ *     required; dA (dim, dstate), dB, dC (batch, dstate, seqlen) : fp32,
+ *     required; dD, ddelta_bias (dim), dh0 (batch, dim, dstate) : fp32,
+ *     nullable.  dh0_r is the gradient of h0_r, the right-to-left state
+ *     before token seqlen-1.
+ * workspace : >= ssm_scan_workspace_bytes(shape, 3) bytes (it holds the
+ * reversed copies, both directions' fp32 per-token gradients and one
+ * ssm_scan_bwd workspace); device errors of either direction are reported
+ * through its status word.  Any state size and sequence length that
+ * ssm_scan_bwd accepts. */
+SSM_API int ssm_scan_bwd_bidir(const ssm_shape* shape, const void* u, const void* z,
+                 const void* delta_raw, const float* A, const void* B, const void* C,
+                 const float* D, const float* delta_bias, const float* h0,
+                 const void* delta_raw_r, const float* A_r, const void* B_r, const void* C_r,
+                 const float* D_r, const float* delta_bias_r, const float* h0_r,
+                 const void* dy, const float* dhL, const float* dhL_r, void* du, void* dz,
+                 void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                 float* ddelta_bias, float* dh0, void* ddelta_raw_r, float* dA_r,
+                 float* dB_r, float* dC_r, float* dD_r, float* ddelta_bias_r, float* dh0_r,
+                 void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
 /* Reverse mode of ssm_scan_fwd (the pages give no backward; it is the exact
  * derivative of the recurrence above).  Inputs are the forward inputs plus
  *   dy  : in_dtype (batch, dim, seqlen), required;   dhL : fp32, nullable (= 0).
@@ -209,6 +242,29 @@ SSM_API int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delt
                  const void* dy, const float* dhL,
                  void* du, void* ddelta_raw, float* dA, float* dB, float* dC,
                  float* dD, void* dz, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/* ssm_scan_bwd over packed sequences: the reverse mode of ssm_scan_fwd_varlen
+ * without the conv prologue ("Mamba Architecture Explained", section
+ * "Problem 3: Ecosystem maturity": training on packed sequences needs its
+ * own kernel support).  Every packed sequence gets its own reverse mode:
+ * its per-token gradients land in its token range, dh0[s] is the gradient of
+ * its initial state h0[s], dhL[s] the upstream gradient of its final state,
+ * and nothing flows across a start; dA, dD, ddelta_bias are summed over all
+ * sequences, dB and dC over all channels.
+ *   cu_seqlens, nseq : as for ssm_scan_fwd_varlen (device int32, nseq + 1
+ *     starts; starts out of order are reported as SSM_ERR_SEQLENS in the
+ *     workspace status word, outputs then undefined, no access out of bounds).
+ *   h0, dhL, dh0 : fp32 (nseq, batch, dim, dstate), nullable; an empty
+ *     sequence gets dh0[s] = dhL[s] (zero when dhL is NULL).
+ *   Everything else as ssm_scan_bwd (same workspace size).  Built for 9 to 16
+ *   states and rows of seqlen * element size a multiple of 16 bytes; other
+ *   shapes return SSM_ERR_UNSUPPORTED before anything is enqueued. */
+SSM_API int ssm_scan_bwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,
+                 int nseq, const void* delta_raw, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, const float* h0,
+                 const void* dy, const float* dhL, void* du, void* ddelta_raw, float* dA,
+                 float* dB, float* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
                  void* workspace, size_t ws_bytes, ssm_stream_t stream);
 
 /* One recurrent (decode) step for a single token per sequence, with the

@@ -42,8 +42,9 @@ SSM_ERR_SEQLENS = -9
 
 # Every symbol include/ssm_scan.h declares.
 EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_fwd_varlen",
-           "ssm_scan_fwd_bidir", "ssm_scan_bwd", "ssm_scan_step", "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait",
-           "ssm_scan_fwd_noalloc")
+           "ssm_scan_fwd_bidir", "ssm_scan_bwd", "ssm_scan_bwd_varlen", "ssm_scan_bwd_bidir",
+           "ssm_scan_step",
+           "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait", "ssm_scan_fwd_noalloc")
 
 
 class ssm_shape(ctypes.Structure):
@@ -68,6 +69,11 @@ lib.ssm_scan_fwd_bidir.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 20 + [cty
 lib.ssm_scan_fwd_bidir.restype = ctypes.c_int
 lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 21 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd.restype = ctypes.c_int
+lib.ssm_scan_bwd_varlen.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, ctypes.c_int] + [_P] * 20
+                                    + [ctypes.c_size_t, _P])
+lib.ssm_scan_bwd_varlen.restype = ctypes.c_int
+lib.ssm_scan_bwd_bidir.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 36 + [ctypes.c_size_t, _P]
+lib.ssm_scan_bwd_bidir.restype = ctypes.c_int
 lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 12
 lib.ssm_scan_step.restype = ctypes.c_int
 lib.ssm_get_status.argtypes = [_P, _P]
@@ -337,6 +343,63 @@ def ssm_scan_fwd_bidir(u, z, fwd: dict, rev: dict, *, out_dtype: Optional[torch.
     return y, hL, hL_r
 
 
+def ssm_scan_bwd_bidir(u, z, fwd: dict, rev: dict, dy, dhL=None, dhL_r=None, *,
+                       out_dtype: Optional[torch.dtype] = None, workspace=None,
+                       stream=None) -> Tuple[dict, dict, dict]:
+    """Reverse mode of ssm_scan_fwd_bidir.  `fwd` and `rev` hold each
+    direction's delta_raw, A, B, C and optional D, delta_bias, h0 (as for
+    ssm_scan_fwd_bidir); dhL, dhL_r the upstream gradients of the two final
+    states (nullable).  Returns (shared, grads_fwd, grads_rev): shared = {du,
+    dz} (out_dtype; dz None without z), each grads dict ddelta_raw (out_dtype),
+    dA, dB, dC, dD, ddelta_bias, dh0 (fp32; dD, ddelta_bias, dh0 always
+    returned)."""
+    Bt, Dm, L = u.shape
+    N = fwd["A"].shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_bwd_bidir runs on CUDA tensors only")
+    tin = u.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    f32 = torch.float32
+    _check(u, "u", (Bt, Dm, L), tin, dev)
+    _check(z, "z", (Bt, Dm, L), tin, dev)
+    _check(dy, "dy", (Bt, Dm, L), tin, dev)
+    _check(dhL, "dhL", (Bt, Dm, N), f32, dev)
+    _check(dhL_r, "dhL_r", (Bt, Dm, N), f32, dev)
+    for tag, d in (("fwd", fwd), ("rev", rev)):
+        _check(d["delta_raw"], tag + ".delta_raw", (Bt, Dm, L), tin, dev)
+        _check(d["B"], tag + ".B", (Bt, N, L), tin, dev)
+        _check(d["C"], tag + ".C", (Bt, N, L), tin, dev)
+        _check(d["A"], tag + ".A", (Dm, N), f32, dev)
+        _check(d.get("D"), tag + ".D", (Dm,), f32, dev)
+        _check(d.get("delta_bias"), tag + ".delta_bias", (Dm,), f32, dev)
+        _check(d.get("h0"), tag + ".h0", (Bt, Dm, N), f32, dev)
+    emp = lambda shp, dt: torch.empty(shp, dtype=dt, device=dev)
+    shared = {"du": emp((Bt, Dm, L), out_dtype), "dz": emp((Bt, Dm, L), out_dtype) if z is not None else None}
+
+    def grads():
+        return {"ddelta_raw": emp((Bt, Dm, L), out_dtype), "dA": emp((Dm, N), f32),
+                "dB": emp((Bt, N, L), f32), "dC": emp((Bt, N, L), f32), "dD": emp((Dm,), f32),
+                "ddelta_bias": emp((Dm,), f32), "dh0": emp((Bt, Dm, N), f32)}
+    gf, gr = grads(), grads()
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, 3, dev, workspace)
+    f, r = fwd, rev
+    g_ptrs = lambda g: [_ptr(g[k]) for k in ("ddelta_raw", "dA", "dB", "dC", "dD", "ddelta_bias",
+                                             "dh0")]
+    rc = lib.ssm_scan_bwd_bidir(ctypes.byref(shape), _ptr(u), _ptr(z),
+                                _ptr(f["delta_raw"]), _ptr(f["A"]), _ptr(f["B"]), _ptr(f["C"]),
+                                _ptr(f.get("D")), _ptr(f.get("delta_bias")), _ptr(f.get("h0")),
+                                _ptr(r["delta_raw"]), _ptr(r["A"]), _ptr(r["B"]), _ptr(r["C"]),
+                                _ptr(r.get("D")), _ptr(r.get("delta_bias")), _ptr(r.get("h0")),
+                                _ptr(dy), _ptr(dhL), _ptr(dhL_r), _ptr(shared["du"]),
+                                _ptr(shared["dz"]), *g_ptrs(gf), *g_ptrs(gr),
+                                _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_bwd_bidir")
+    return shared, gf, gr
+
+
 def ssm_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=None,
                  dhL=None, *, out_dtype: Optional[torch.dtype] = None, workspace=None,
                  stream=None) -> dict:
@@ -377,6 +440,56 @@ def ssm_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=
                           workspace.numel(), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_bwd")
+    return g
+
+
+def ssm_scan_bwd_varlen(u, cu_seqlens, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None,
+                        h0=None, dhL=None, *, out_dtype: Optional[torch.dtype] = None,
+                        workspace=None, stream=None) -> dict:
+    """Reverse mode of ssm_scan_fwd_varlen (no conv prologue): packed
+    sequences at cu_seqlens (int32 CUDA tensor of nseq + 1 starts), h0, dhL
+    (nseq, Bt, D, N) fp32 or None.  Returns the dict of ssm_scan_bwd with dh0
+    (nseq, Bt, D, N)."""
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_bwd_varlen runs on CUDA tensors only")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor of nseq + 1 starts")
+    _check(cu_seqlens, "cu_seqlens", tuple(cu_seqlens.shape), torch.int32, dev)
+    nseq = cu_seqlens.numel() - 1
+    tin = u.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    for t, n, s in ((u, "u", (Bt, Dm, L)), (delta_raw, "delta_raw", (Bt, Dm, L)),
+                    (z, "z", (Bt, Dm, L)), (dy, "dy", (Bt, Dm, L)), (B, "B", (Bt, N, L)),
+                    (C, "C", (Bt, N, L))):
+        _check(t, n, s, tin, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    _check(h0, "h0", (nseq, Bt, Dm, N), torch.float32, dev)
+    _check(dhL, "dhL", (nseq, Bt, Dm, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {
+        "du": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev),
+        "ddelta_raw": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev),
+        "dz": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev) if z is not None else None,
+        "dA": torch.empty((Dm, N), **f32), "dB": torch.empty((Bt, N, L), **f32),
+        "dC": torch.empty((Bt, N, L), **f32), "dD": torch.empty((Dm,), **f32),
+        "ddelta_bias": torch.empty((Dm,), **f32), "dh0": torch.empty((nseq, Bt, Dm, N), **f32),
+    }
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, True, dev, workspace)
+    rc = lib.ssm_scan_bwd_varlen(ctypes.byref(shape), _ptr(u), _ptr(cu_seqlens), nseq,
+                                 _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                 _ptr(delta_bias), _ptr(h0), _ptr(dy), _ptr(dhL), _ptr(g["du"]),
+                                 _ptr(g["ddelta_raw"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                                 _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
+                                 _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), _ptr(workspace),
+                                 workspace.numel(), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_bwd_varlen")
     return g
 
 

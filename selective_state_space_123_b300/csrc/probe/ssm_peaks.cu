@@ -16,6 +16,8 @@
 //   kind 3  the scan's update mix per pair of states: mul.f32x2 (delta*A),
 //           two ex2, mul.f32x2 (delta*u*B), fma.f32x2 (state), fma.f32x2
 //           (read-out); counted in state updates
+//   kind 4  lg2.approx.ftz.f32                    (MUFU; softplus)
+//   kind 5  rcp.approx.ftz.f32                    (MUFU; the SiLU gate)
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -50,6 +52,40 @@ __global__ void ex2_kernel(int iters, long long* cycles, float* sink) {
     for (int i = 0; i < iters; ++i) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = ssm::ex2(-v[j]);   // stays in (0.5, 1]
+    }
+    end_clock(t0, cycles);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += v[j];
+    sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+__global__ void lg2_kernel(int iters, long long* cycles, float* sink) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 1.5f + 0.01f * (float)(threadIdx.x & 7) + 0.1f * (float)j;
+    long long t0;
+    begin_clock(t0);
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 2.0f + ssm::lg2(v[j]);   // stays in [2.5, 3.6]
+    }
+    end_clock(t0, cycles);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += v[j];
+    sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+__global__ void rcp_kernel(int iters, long long* cycles, float* sink) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 1.5f + 0.01f * (float)(threadIdx.x & 7) + 0.1f * (float)j;
+    long long t0;
+    begin_clock(t0);
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 1.0f + ssm::rcp(v[j]);   // stays in [1.3, 1.8]
     }
     end_clock(t0, cycles);
     float s = 0.0f;
@@ -135,7 +171,7 @@ __global__ void mix_kernel(int iters, long long* cycles, float* sink) {
 
 }  // namespace
 
-// Run probe `kind` (0..3, see above) with `blocks` CTAs of `threads` threads
+// Run probe `kind` (0..5, see above) with `blocks` CTAs of `threads` threads
 // for `iters` loop iterations.  `cycles` (device, blocks int64) receives each
 // CTA's clock cycles and `sink` (device, blocks * threads floats) the chains'
 // final values.  Returns the operations (kind 3: state updates) one CTA
@@ -143,17 +179,18 @@ __global__ void mix_kernel(int iters, long long* cycles, float* sink) {
 // `stream`.
 PEAKS_API long long ssm_peaks_launch(int kind, int blocks, int threads, int iters,
                                      long long* cycles, float* sink, void* stream) {
-    if (kind < 0 || kind > 3 || blocks < 1 || threads < 32 || threads > 1024 || threads % 32 ||
+    if (kind < 0 || kind > 5 || blocks < 1 || threads < 32 || threads > 1024 || threads % 32 ||
         iters < 1 || !cycles || !sink)
         return -1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const long long per_thread = kind == 0 ? 8LL * iters : kind == 1 ? 8LL * iters
-                                 : kind == 2 ? 16LL * iters : 16LL * iters;
+    const long long per_thread = (kind == 2 || kind == 3) ? 16LL * iters : 8LL * iters;
     switch (kind) {
         case 0: ex2_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
         case 1: fma_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
         case 2: fma2_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
-        default: mix_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
+        case 3: mix_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
+        case 4: lg2_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
+        default: rcp_kernel<<<blocks, threads, 0, st>>>(iters, cycles, sink); break;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;
     return per_thread * threads;

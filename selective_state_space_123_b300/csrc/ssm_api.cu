@@ -275,7 +275,7 @@ struct BwdPlan {
     size_t smem_f = 0, smem_r = 0;
     bool tma_raw = false;
     bool ok = false;        // a tile shape fits the shared memory
-    size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, bytes = 0;
+    size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, off_hprev = 0, bytes = 0;
 };
 
 int bwd_tbuf_floats(int NT, int NP) {
@@ -283,19 +283,22 @@ int bwd_tbuf_floats(int NT, int NP) {
     return 8 * (CW * NP + 4);
 }
 
-BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
+BwdPlan plan_bwd(const ssm_shape& s, int sm_count, bool nt2_only = false) {
     BwdPlan pl;
     pl.NP = padded_state(s.dstate);
     if (pl.NP < 8) pl.NP = 8;
     const int eb = dtype_bytes(s.in_dtype);
     pl.tma_raw = (s.seqlen * eb) % 16 == 0;
     const int nts_all[2] = {2, 4};
-    int want_nt = env_int("SSM_BWD_NT", 0);
+    int want_nt = nt2_only ? 2 : env_int("SSM_BWD_NT", 0);
     int want_w = env_int("SSM_BWD_W", 0);
     double best = -1.0;
     // a second search without the overrides when none of them fits
     for (int attempt = 0; attempt < 2 && best < 0.0; ++attempt) {
-    if (attempt == 1) want_nt = want_w = 0;
+    if (attempt == 1) {
+        want_nt = nt2_only ? 2 : 0;
+        want_w = 0;
+    }
     for (int ni = 0; ni < 2; ++ni) {
         const int NT = nts_all[ni];
         if (pl.NP == 8 && NT != 2) continue;       // G = NP / NT must be 4, 8 or 16
@@ -335,11 +338,47 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
     off += align256((size_t)s.batch * s.dim * pl.NP * 4);
     pl.off_hck = off;
     off += align256((size_t)s.batch * s.dim * ((s.seqlen + kT - 1) / kT) * pl.NP * 4);
+    // fp32 inputs: the state before every token (the reverse sweep forms the
+    // h-dependent term of ddelta from it directly)
+    pl.off_hprev = off;
+    if (s.in_dtype == SSM_F32) off += align256((size_t)s.batch * s.dim * s.seqlen * pl.NP * 4);
     pl.bytes = off;
     if (env_int("SSM_DEBUG_PLAN", 0))
         std::fprintf(stderr, "ssm bwd plan: NP=%d NT=%d W=%d CH=%d stages=%d/%d smem=%zu/%zu\n",
                      pl.NP, pl.NT, pl.W, pl.CH, pl.stages_f, pl.stages_r, pl.smem_f, pl.smem_r);
     return pl;
+}
+
+// Workspace of the bidirectional backward: the status word, one backward
+// workspace (fp32 per-token outputs) reused by the two directions in turn,
+// token-reversed copies of the right-to-left direction's inputs, and the
+// fp32 per-token gradients of both directions before they are combined.
+struct BidirBwdLayout {
+    size_t off_inner = 0, inner = 0, off_u = 0, off_dr = 0, off_z = 0, off_dy = 0, off_B = 0,
+           off_C = 0, off_g = 0, off_dB = 0, off_dC = 0, bytes = 0;
+};
+BidirBwdLayout bidir_bwd_layout(const ssm_shape& s, int sm_count) {
+    BidirBwdLayout w;
+    ssm_shape s32 = s;
+    s32.out_dtype = SSM_F32;
+    const size_t tok = (size_t)s.batch * s.dim * s.seqlen;
+    const size_t bnl = (size_t)s.batch * s.dstate * s.seqlen;
+    const size_t eb = s.in_dtype == SSM_BF16 ? 2 : 4;
+    size_t off = kHeaderBytes;
+    w.off_inner = off;
+    w.inner = plan_bwd(s32, sm_count).bytes;
+    off += align256(w.inner);
+    w.off_u = off;  off += align256(tok * eb);
+    w.off_dr = off; off += align256(tok * eb);
+    w.off_z = off;  off += align256(tok * eb);
+    w.off_dy = off; off += align256(tok * eb);
+    w.off_B = off;  off += align256(bnl * eb);
+    w.off_C = off;  off += align256(bnl * eb);
+    w.off_g = off;  off += 6 * align256(tok * 4);   // du, ddr, dz of each direction
+    w.off_dB = off; off += align256(bnl * 4);
+    w.off_dC = off; off += align256(bnl * 4);
+    w.bytes = off;
+    return w;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -458,7 +497,8 @@ const char* ssm_strerror(int code) {
 
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     if (shape_check(shape) != SSM_OK) return 0;
-    const size_t bytes = for_backward == 2 ? plan_fwd_bidir(*shape, device_sm_count()).bytes
+    const size_t bytes = for_backward == 3 ? bidir_bwd_layout(*shape, device_sm_count()).bytes
+                         : for_backward == 2 ? plan_fwd_bidir(*shape, device_sm_count()).bytes
                          : for_backward ? plan_bwd(*shape, device_sm_count()).bytes
                                         : plan_fwd(*shape, device_sm_count()).bytes;
     return bytes < kHeaderBytes ? kHeaderBytes : bytes;
@@ -702,16 +742,21 @@ int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu
                          stream);
 }
 
-int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
-                 const void* B, const void* C, const float* D, const void* z,
-                 const float* delta_bias, const float* h0, const void* dy, const float* dhL,
-                 void* du, void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
-                 void* dz, float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
-                 ssm_stream_t stream) {
+// The backward, over whole rows or over packed sequences (cu_seqlens non-null).
+static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,
+                         int nseq, const void* delta_raw, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         const float* h0, const void* dy, const float* dhL, void* du,
+                         void* ddelta_raw, float* dA, float* dB, float* dC, float* dD, void* dz,
+                         float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
+                         ssm_stream_t stream) {
     const int sc = shape_check(shape);
     if (sc != SSM_OK) return sc;
     const ssm_shape s = *shape;
     const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && nseq < 1) return SSM_ERR_SHAPE;
+    if (varlen && ((uintptr_t)cu_seqlens % 4) != 0) return SSM_ERR_ALIGN;
     if (Dm > 0 && !A) return SSM_ERR_NULL;
     if (Dm > 0 && !dA) return SSM_ERR_NULL;
     if (Bt == 0 || Dm == 0) {
@@ -739,17 +784,27 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const BwdPlan pl = plan_bwd(s, device_sm_count());
+    const BwdPlan pl = plan_bwd(s, device_sm_count(), varlen);
     if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
+    // packed sequences: built for 9..16 states and 16-byte token rows
+    if (varlen && L > 0 && (pl.NP != 16 || pl.NT != 2 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
+    const int64_t per_seq = Bt * Dm * N;   // floats of one sequence's state (packed dhL, dh0)
 
     // outputs summed with atomics start at zero
     if (cudaMemsetAsync(dA, 0, (size_t)(Dm * N) * 4, st) != cudaSuccess) return cuda_fail();
     if (dD && cudaMemsetAsync(dD, 0, (size_t)Dm * 4, st) != cudaSuccess) return cuda_fail();
     if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dm * 4, st) != cudaSuccess)
         return cuda_fail();
+    if (L == 0 && varlen) {
+        // every packed sequence is empty: dh0[s] = dhL[s]
+        if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+        if (launch_varlen_prep(cu_seqlens, nseq, 0, per_seq, dhL, dh0, status, st) != cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
     if (L == 0) {
         // an empty sequence passes dhL straight through to dh0
         if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
@@ -767,6 +822,9 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
 
     float* bc = reinterpret_cast<float*>(ws + pl.off_bc);
     if (launch_prep_bc(s.in_dtype, Bt, (int)N, pl.NP, L, B, C, bc, status, st) != cudaSuccess)
+        return cuda_fail();
+    // packed: check the starts; empty sequences pass dhL[s] to dh0[s]
+    if (varlen && launch_varlen_prep(cu_seqlens, nseq, L, per_seq, dhL, dh0, status, st) != cudaSuccess)
         return cuda_fail();
 
     const int eb = dtype_bytes(s.in_dtype);
@@ -796,12 +854,146 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     p.h0 = h0; p.dhL = dhL; p.bc = bc; p.phi = phi;
     p.hfin = reinterpret_cast<float*>(ws + pl.off_hfin);
     p.hck = reinterpret_cast<float*>(ws + pl.off_hck);
+    p.hprev = s.in_dtype == SSM_F32 ? reinterpret_cast<float*>(ws + pl.off_hprev) : nullptr;
     p.du = du; p.ddr = ddelta_raw; p.dz = dz;
     p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dbias = ddelta_bias; p.dh0 = dh0;
+    p.cu_seqlens = cu_seqlens; p.nseq = varlen ? nseq : 0;
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
+    if (varlen) {
+        BwdLaunch lc;
+        lc.grid = dim3(gx, (unsigned)Bt);
+        lc.warps = pl.W;
+        lc.stages_f = pl.stages_f;
+        lc.stages_r = pl.stages_r;
+        lc.smem_f = pl.smem_f;
+        lc.smem_r = pl.smem_r;
+        if (launch_bwd_varlen_np16(s.in_dtype, s.out_dtype, p, maps, lc, st) != cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
     if (launch_bwd(pl, s.in_dtype, s.out_dtype, p, maps, dim3(gx, (unsigned)Bt), st) != cudaSuccess)
+        return cuda_fail();
+    return SSM_OK;
+}
+
+int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, const void* dy, const float* dhL,
+                 void* du, void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                 void* dz, float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
+                 ssm_stream_t stream) {
+    return scan_bwd_impl(shape, u, nullptr, 0, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL,
+                         du, ddelta_raw, dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace,
+                         ws_bytes, stream);
+}
+
+int ssm_scan_bwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,
+                        int nseq, const void* delta_raw, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const float* delta_bias,
+                        const float* h0, const void* dy, const float* dhL, void* du,
+                        void* ddelta_raw, float* dA, float* dB, float* dC, float* dD, void* dz,
+                        float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
+                        ssm_stream_t stream) {
+    if (!cu_seqlens) return SSM_ERR_NULL;
+    return scan_bwd_impl(shape, u, cu_seqlens, nseq, delta_raw, A, B, C, D, z, delta_bias, h0,
+                         dy, dhL, du, ddelta_raw, dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace,
+                         ws_bytes, stream);
+}
+
+int ssm_scan_bwd_bidir(const ssm_shape* shape, const void* u, const void* z,
+                       const void* delta_raw, const float* A, const void* B, const void* C,
+                       const float* D, const float* delta_bias, const float* h0,
+                       const void* delta_raw_r, const float* A_r, const void* B_r, const void* C_r,
+                       const float* D_r, const float* delta_bias_r, const float* h0_r,
+                       const void* dy, const float* dhL, const float* dhL_r, void* du, void* dz,
+                       void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                       float* ddelta_bias, float* dh0, void* ddelta_raw_r, float* dA_r,
+                       float* dB_r, float* dC_r, float* dD_r, float* ddelta_bias_r, float* dh0_r,
+                       void* workspace, size_t ws_bytes, ssm_stream_t stream) {
+    const int sc = shape_check(shape);
+    if (sc != SSM_OK) return sc;
+    const ssm_shape s = *shape;
+    const int64_t Bt = s.batch, Dm = s.dim, N = s.dstate, L = s.seqlen;
+    if (Dm > 0 && (!A || !A_r || !dA || !dA_r)) return SSM_ERR_NULL;
+    if (Bt == 0 || Dm == 0) {
+        // nothing flows: each direction's per-channel gradients are zero
+        int rc = ssm_scan_bwd(shape, u, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL, du,
+                              ddelta_raw, dA, dB, dC, dD, dz, ddelta_bias, dh0, nullptr, 0, stream);
+        if (rc != SSM_OK) return rc;
+        return ssm_scan_bwd(shape, u, delta_raw_r, A_r, B_r, C_r, D_r, z, delta_bias_r, h0_r, dy,
+                            dhL_r, du, ddelta_raw_r, dA_r, dB_r, dC_r, dD_r, dz, ddelta_bias_r,
+                            dh0_r, nullptr, 0, stream);
+    }
+    if (!workspace) return SSM_ERR_WORKSPACE;
+    if (L > 0 && (!u || !dy || !du || !delta_raw || !B || !C || !ddelta_raw || !dB || !dC ||
+                  !delta_raw_r || !B_r || !C_r || !ddelta_raw_r || !dB_r || !dC_r))
+        return SSM_ERR_NULL;
+    const void* ptrs[] = {u, z, delta_raw, A, B, C, D, delta_bias, h0, delta_raw_r, A_r, B_r, C_r,
+                          D_r, delta_bias_r, h0_r, dy, dhL, dhL_r, du, dz, ddelta_raw, dA, dB, dC,
+                          dD, ddelta_bias, dh0, ddelta_raw_r, dA_r, dB_r, dC_r, dD_r,
+                          ddelta_bias_r, dh0_r, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SSM_ERR_ALIGN;
+    const BidirBwdLayout w = bidir_bwd_layout(s, device_sm_count());
+    if (ws_bytes < w.bytes) return SSM_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    void* inner = ws + w.off_inner;
+    const int* inner_status = reinterpret_cast<const int*>(inner);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return cuda_fail();
+
+    // both directions' per-token gradients in fp32 first, combined at the end
+    ssm_shape s32 = s;
+    s32.out_dtype = SSM_F32;
+    const size_t tokb = align256((size_t)(Bt * Dm * L) * 4);
+    float* g = reinterpret_cast<float*>(ws + w.off_g);
+    float* du1 = g;
+    float* ddr1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g) + tokb);
+    float* dz1 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g) + 2 * tokb);
+    float* du2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g) + 3 * tokb);
+    float* ddr2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g) + 4 * tokb);
+    float* dz2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(g) + 5 * tokb);
+    const bool gate = z != nullptr;
+    const bool want_dz = dz != nullptr;   // (zeros without a gate, as in ssm_scan_bwd)
+
+    // left to right: the ordinary backward
+    int rc = ssm_scan_bwd(&s32, u, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL, du1, ddr1,
+                          dA, dB, dC, dD, want_dz ? dz1 : nullptr, ddelta_bias, dh0, inner, w.inner,
+                          stream);
+    if (rc != SSM_OK) return rc;
+    if (launch_fold_status(status, inner_status, st) != cudaSuccess) return cuda_fail();
+
+    // right to left: the backward of the token-reversed sequence
+    void* u_f = ws + w.off_u;
+    void* dr_f = ws + w.off_dr;
+    void* z_f = gate ? ws + w.off_z : nullptr;
+    void* dy_f = ws + w.off_dy;
+    void* B_f = ws + w.off_B;
+    void* C_f = ws + w.off_C;
+    const int64_t rows = Bt * Dm, brows = Bt * N;
+    if (launch_flip_rows(s.in_dtype, u, u_f, rows, L, st) != cudaSuccess ||
+        launch_flip_rows(s.in_dtype, delta_raw_r, dr_f, rows, L, st) != cudaSuccess ||
+        (gate && launch_flip_rows(s.in_dtype, z, z_f, rows, L, st) != cudaSuccess) ||
+        launch_flip_rows(s.in_dtype, dy, dy_f, rows, L, st) != cudaSuccess ||
+        launch_flip_rows(s.in_dtype, B_r, B_f, brows, L, st) != cudaSuccess ||
+        launch_flip_rows(s.in_dtype, C_r, C_f, brows, L, st) != cudaSuccess)
+        return cuda_fail();
+    float* dB_f = reinterpret_cast<float*>(ws + w.off_dB);
+    float* dC_f = reinterpret_cast<float*>(ws + w.off_dC);
+    rc = ssm_scan_bwd(&s32, u_f, dr_f, A_r, B_f, C_f, D_r, z_f, delta_bias_r, h0_r, dy_f, dhL_r,
+                      du2, ddr2, dA_r, dB_f, dC_f, dD_r, want_dz ? dz2 : nullptr, ddelta_bias_r,
+                      dh0_r, inner, w.inner, stream);
+    if (rc != SSM_OK) return rc;
+    if (launch_fold_status(status, inner_status, st) != cudaSuccess) return cuda_fail();
+
+    // du, dz summed; each direction's ddelta_raw, dB, dC in token order
+    if (launch_bidir_combine(s.out_dtype, rows, L, du1, du2, dz1, dz2, ddr1, ddr2, du,
+                             want_dz ? dz : nullptr, ddelta_raw, ddelta_raw_r, st) != cudaSuccess ||
+        launch_flip_rows(SSM_F32, dB_f, dB_r, brows, L, st) != cudaSuccess ||
+        launch_flip_rows(SSM_F32, dC_f, dC_r, brows, L, st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
 }

@@ -277,9 +277,35 @@ __device__ __forceinline__ void put_tr(float* slot, const f2 (&v)[G / 2]) {
     }
 }
 
+// Packed sequences (VARLEN): the sequence holding token t is the last s with
+// cu_seqlens[s] <= t (empty sequences are skipped that way).
+__device__ __forceinline__ int seq_of_token(const int* cu, int nseq, int64_t t) {
+    return max(seq_lower_bound(cu, nseq, t + 1) - 1, 0);
+}
+
+// Bits i (0 <= i < SB) of the super-block starting at token t_sb for which
+// token t_sb + i + shift starts a sequence (shift 0: the token starts one;
+// shift 1: the token is the last of one), counting starts in (0, L) only.
+template <int SB>
+__device__ __forceinline__ uint32_t start_bits(const int* cu, int nseq, int64_t L, int64_t t_sb,
+                                               int shift) {
+    uint32_t m = 0;
+    const int64_t lo = t_sb + shift, hi = t_sb + shift + SB;
+    for (int j = seq_lower_bound(cu, nseq, lo); j < nseq; ++j) {
+        const int64_t c = cu[j];
+        if (c >= hi || c >= L) break;
+        if (c > 0) m |= 1u << (int)(c - lo);
+    }
+    return m;
+}
+
 // ===================================================== forward sweep ===
 // blockDim.x = 32 * (W + 1): W compute warps and one producer warp (the last).
-template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
+// VARLEN: packed sequences restart inside the row (cu_seqlens); at a start
+// the ending sequence's dhL term enters dA, its psi = sum_n A dhL h_end is
+// added to phi of its last token (so the reverse sweep's suffix sum restarts
+// from zero there), and h, m start again from the new sequence's h0 and 0.
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -346,6 +372,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int N = p.N;
     float* tb = trb + warp * Lay::TBUF;
 
+    // packed sequences: per-sequence state arrays are (nseq, Bt, D, N)
+    const int64_t seq_stride = p.Bt * p.D * (int64_t)N;
+    const int s_first = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, 0) : 0;
     f2 Ap[G / 2], h[G / 2], m[G / 2], dAc[G / 2];
 #pragma unroll
     for (int j = 0; j < G / 2; ++j) {
@@ -354,8 +383,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                    (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f);
         float h0v = 0.0f, h1v = 0.0f;
         if (ch_ok && p.h0) {
-            if (n0 < N) h0v = p.h0[row * N + n0];
-            if (n1 < N) h1v = p.h0[row * N + n1];
+            const float* hs = p.h0 + (int64_t)s_first * seq_stride;
+            if (n0 < N) h0v = hs[row * N + n0];
+            if (n1 < N) h1v = hs[row * N + n1];
         }
         h[j] = pk(h0v, h1v);
         m[j] = pk(0.0f, 0.0f);
@@ -369,6 +399,20 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 
     // A warp whose bounded wait expires records the error and stops working.
     bool dead = false;
+    // The state at the end of every chunk: the reverse sweep re-anchors its
+    // suffix sum with it.  With fp32 inputs the state before every token is
+    // stored as well (the reverse sweep forms the h-dependent term of ddelta
+    // from it directly).
+    auto store_anchor = [&](int64_t a) {
+        float4* hc = reinterpret_cast<float4*>(p.hck + (row * nchunks + a) * NP + g * G);
+#pragma unroll
+        for (int j = 0; j < G / 4; ++j) {
+            float x0, x1, x2, x3;
+            upk(h[2 * j], x0, x1);
+            upk(h[2 * j + 1], x2, x3);
+            hc[j] = make_float4(x0, x1, x2, x3);
+        }
+    };
     for (int64_t k = 0; k < nchunks; ++k) {
         const int s = (int)(k % STAGES);
         if (!dead) {
@@ -400,6 +444,36 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int tbk = sb * SB + g * 8;   // this lane's 8 tokens
             float d2[8], du[8], gq[8];
             token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            // packed: tokens of this super-block that start a sequence, and
+            // psi of an ending sequence to add to phi of its last own token
+            const int64_t t_sb = k * kT + sb * SB;
+            const uint32_t rmask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 0) : 0u;
+            float psi_add[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) psi_add[q] = 0.0f;
+            // restart before token t: close the sequence ending at t - 1, start
+            // the one holding t; returns psi of the closed sequence
+            auto restart = [&](int64_t t) -> float {
+                const int se = seq_of_token(p.cu_seqlens, p.nseq, t - 1);
+                const int sn = seq_of_token(p.cu_seqlens, p.nseq, t);
+                const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+                const float* hs = (p.h0 && ch_ok) ? p.h0 + (int64_t)sn * seq_stride + row * N : nullptr;
+                float psi = 0.0f;
+#pragma unroll
+                for (int jj = 0; jj < G / 2; ++jj) {
+                    const int n0 = g * G + 2 * jj;
+                    const f2 dhp = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                    dAc[jj] = fma2(dhp, m[jj], dAc[jj]);          // dhL[se] . dh/dA
+                    float x0, x1;
+                    upk(mul2(mul2(Ap[jj], dhp), h[jj]), x0, x1);  // A dhL[se] h_end
+                    psi += x0 + x1;
+                    h[jj] = pk((hs && n0 < N) ? hs[n0] : 0.0f, (hs && n0 + 1 < N) ? hs[n0 + 1] : 0.0f);
+                    m[jj] = pk(0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int o = 1; o < NT; o <<= 1) psi += __shfl_xor_sync(0xffffffffu, psi, o);
+                return psi;
+            };
 
             float ys_own[8], ph_own[8];        // sums over n of this lane's tokens
 #pragma unroll 1
@@ -416,6 +490,32 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 float yp[8], pp[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
+                    if (VARLEN && ((rmask >> (j * 8 + q)) & 1u)) {
+                        const float psi = restart(t_sb + j * 8 + q);
+                        // psi belongs to the token before: an own token of
+                        // this super-block, or one of the previous super-block
+                        // that its owner (the channel's last lane, the thread
+                        // that stored it) adds to in place
+                        if (q > 0) {
+                            if (g == j) psi_add[q - 1] += psi;
+                        } else if (j > 0) {
+                            if (g == j - 1) psi_add[7] += psi;
+                        } else if (g == NT - 1 && ch_ok) {
+                            atomicAdd(p.phi + row * L + t_sb - 1, psi);
+                        }
+                    }
+                    if (ACCURATE && ch_ok && t_grp + q < nvalid) {
+                        // h_{t-1} as this token's update uses it (after a restart)
+                        float4* hp = reinterpret_cast<float4*>(
+                            p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
+#pragma unroll
+                        for (int jj = 0; jj < G / 4; ++jj) {
+                            float x0, x1, x2, x3;
+                            upk(h[2 * jj], x0, x1);
+                            upk(h[2 * jj + 1], x2, x3);
+                            hp[jj] = make_float4(x0, x1, x2, x3);
+                        }
+                    }
                     const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
                     const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
                     f2 accy = pk(0.0f, 0.0f), accp = pk(0.0f, 0.0f);
@@ -476,7 +576,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 } else {
                     dzv[q] = 0.0f;
                 }
-                phv[q] = gq[q] * ph_own[q];
+                phv[q] = fmaf(gq[q], ph_own[q], psi_add[q]);
             }
             if (ch_ok) {
                 const int64_t off = row * L + k * kT + tbk;
@@ -484,18 +584,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 store_out8<float>(p.phi, off, phv, nvalid - tbk, vec_phi);
             }
         }
-        if (!dead && ch_ok && k + 1 < nchunks) {
-            // state at the end of this chunk: the reverse sweep re-anchors its
-            // suffix sum with it
-            float4* hc = reinterpret_cast<float4*>(p.hck + (row * nchunks + k) * NP + g * G);
-#pragma unroll
-            for (int j = 0; j < G / 4; ++j) {
-                float x0, x1, x2, x3;
-                upk(h[2 * j], x0, x1);
-                upk(h[2 * j + 1], x2, x3);
-                hc[j] = make_float4(x0, x1, x2, x3);
-            }
-        }
+        if (!dead && ch_ok && k + 1 < nchunks) store_anchor(k);
         __syncwarp();
         if (lane == 0 && !dead) {
             mbar_arrive(&empty_bar[s]);
@@ -504,6 +593,9 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     }
 
     if (ch_ok && !dead) {
+        // the last sequence's final-state gradient (packed: the one holding token L-1)
+        const int s_last = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, L - 1) : 0;
+        const float* dhl = p.dhL ? p.dhL + (int64_t)s_last * seq_stride + row * N : nullptr;
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) {
             const int n0 = g * G + 2 * j;
@@ -513,8 +605,8 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             upk(dAc[j], a0, a1);
             p.hfin[row * NP + n0] = hl0;
             p.hfin[row * NP + n0 + 1] = hl1;
-            const float g0 = (p.dhL && n0 < N) ? p.dhL[row * N + n0] : 0.0f;
-            const float g1 = (p.dhL && n0 + 1 < N) ? p.dhL[row * N + n0 + 1] : 0.0f;
+            const float g0 = (dhl && n0 < N) ? dhl[n0] : 0.0f;
+            const float g1 = (dhl && n0 + 1 < N) ? dhl[n0 + 1] : 0.0f;
             if (n0 < N) atomicAdd(p.dA + d * N + n0, kLn2 * fmaf(g0, m0, a0));
             if (n0 + 1 < N) atomicAdd(p.dA + d * N + n0 + 1, kLn2 * fmaf(g1, m1, a1));
         }
@@ -522,7 +614,11 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 }
 
 // ===================================================== reverse sweep ===
-template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW>
+// VARLEN: at the last token of a packed sequence the adjoint carried in from
+// the next token is replaced by that sequence's dhL (after the next
+// sequence's dh0 = a lambda has been written), and the suffix sum restarts
+// from zero there (the ending sequence's psi is already in phi of that token).
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -592,7 +688,11 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     float* tb = trb + warp * Lay::TBUF;
 
     // lambda starts at dhL, the decay "after the last token" is 1, and
-    // psi = sum_n A dhL h_L starts the suffix sum
+    // psi = sum_n A dhL h_L starts the suffix sum (packed: dhL of the
+    // sequence holding token L-1)
+    const int64_t seq_stride = p.Bt * p.D * (int64_t)N;
+    const int s_last = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, L - 1) : 0;
+    const float* dhl_last = p.dhL ? p.dhL + (int64_t)s_last * seq_stride : nullptr;
     f2 Ap[G / 2], lam[G / 2], anext[G / 2];
     float psi = 0.0f;
 #pragma unroll
@@ -602,9 +702,9 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const float a1 = (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f;
         Ap[j] = pk(a0, a1);
         float l0 = 0.0f, l1 = 0.0f;
-        if (ch_ok && p.dhL) {
-            if (n0 < N) l0 = p.dhL[row * N + n0];
-            if (n1 < N) l1 = p.dhL[row * N + n1];
+        if (ch_ok && dhl_last) {
+            if (n0 < N) l0 = dhl_last[row * N + n0];
+            if (n1 < N) l1 = dhl_last[row * N + n1];
         }
         lam[j] = pk(l0, l1);
         anext[j] = pk(1.0f, 1.0f);
@@ -619,6 +719,31 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int src_base = lane & ~(NT - 1);
     float dD_acc = 0.0f, db_acc = 0.0f;
     bool dead = false;   // see the forward sweep
+    // Re-anchor: the suffix sum equals sum_n A a_t lambda_t h_{t-1} at the
+    // first token t of a chunk, with h_{t-1} the state the forward sweep
+    // stored at the end of the chunk before.  Rounding in the running sum is
+    // thereby confined to one chunk instead of random-walking over the
+    // sequence.
+    auto reanchor = [&](int64_t a) -> float {
+        float part = 0.0f;
+        if (ch_ok && !dead) {
+            const float4* hc = reinterpret_cast<const float4*>(p.hck + (row * nchunks + a) * NP + g * G);
+#pragma unroll
+            for (int j = 0; j < G / 4; ++j) {
+                const float4 hv = hc[j];
+                float l0, l1, l2, l3;
+                upk(mul2(mul2(Ap[2 * j], anext[2 * j]), lam[2 * j]), l0, l1);
+                upk(mul2(mul2(Ap[2 * j + 1], anext[2 * j + 1]), lam[2 * j + 1]), l2, l3);
+                part = fmaf(l0, hv.x, part);
+                part = fmaf(l1, hv.y, part);
+                part = fmaf(l2, hv.z, part);
+                part = fmaf(l3, hv.w, part);
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < NT; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        return part;
+    };
 
     for (int64_t i = 0; i < nchunks; ++i) {
         const int64_t k = nchunks - 1 - i;
@@ -654,8 +779,12 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int tbk = sb * SB + g * 8;
             float d2[8], du[8], gq[8];
             token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            // packed: tokens of this super-block that end a sequence
+            const int64_t t_sb = k * kT + sb * SB;
+            const uint32_t emask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 1) : 0u;
 
             float sb_own[8], sab_own[8];       // sum_n lambda B', sum_n A a_{t+1} lambda_{t+1} B'
+            float qd_own[8];                   // fp32 inputs: Q of the own tokens, formed directly
 #pragma unroll 1
             for (int j = NT - 1; j >= 0; --j) {
                 const int src = src_base + j;
@@ -667,9 +796,30 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     GQ[q] = NT == 1 ? gq[q] : __shfl_sync(0xffffffffu, gq[q], src);
                 }
                 const int t_grp = sb * SB + j * 8;
-                float bp[8], abp[8];
+                float bp[8], abp[8], qd[8];
 #pragma unroll
                 for (int q = 7; q >= 0; --q) {
+                    if (VARLEN && ((emask >> (j * 8 + q)) & 1u)) {
+                        // token t ends sequence se, t + 1 starts sn: write
+                        // dh0[sn] = a_{t+1} lambda_{t+1}, then carry dhL[se]
+                        const int64_t t = t_sb + j * 8 + q;
+                        const int sn = seq_of_token(p.cu_seqlens, p.nseq, t + 1);
+                        const int se = seq_of_token(p.cu_seqlens, p.nseq, t);
+                        const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+                        float* d0p = (p.dh0 && ch_ok) ? p.dh0 + (int64_t)sn * seq_stride + row * N : nullptr;
+#pragma unroll
+                        for (int jj = 0; jj < G / 2; ++jj) {
+                            const int n0 = g * G + 2 * jj;
+                            if (d0p) {
+                                float v0, v1;
+                                upk(mul2(anext[jj], lam[jj]), v0, v1);
+                                if (n0 < N) d0p[n0] = v0;
+                                if (n0 + 1 < N) d0p[n0 + 1] = v1;
+                            }
+                            lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                            anext[jj] = pk(1.0f, 1.0f);
+                        }
+                    }
                     const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
                     const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
                     f2 accb = pk(0.0f, 0.0f), accab = pk(0.0f, 0.0f);
@@ -698,16 +848,38 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     bp[q] = lo + hi;
                     upk(accab, lo, hi);
                     abp[q] = lo + hi;
+                    if constexpr (ACCURATE) {
+                        // Q_t = sum_n A a_t lambda_t h_{t-1} from the stored state
+                        float qacc = 0.0f;
+                        if (ch_ok && t_grp + q < nvalid) {
+                            const float4* hp = reinterpret_cast<const float4*>(
+                                p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
+#pragma unroll
+                            for (int jj = 0; jj < G / 4; ++jj) {
+                                const float4 hv = hp[jj];
+                                float l0, l1, l2, l3;
+                                upk(mul2(mul2(Ap[2 * jj], anext[2 * jj]), lam[2 * jj]), l0, l1);
+                                upk(mul2(mul2(Ap[2 * jj + 1], anext[2 * jj + 1]), lam[2 * jj + 1]), l2, l3);
+                                qacc = fmaf(l0, hv.x, qacc);
+                                qacc = fmaf(l1, hv.y, qacc);
+                                qacc = fmaf(l2, hv.z, qacc);
+                                qacc = fmaf(l3, hv.w, qacc);
+                            }
+                        }
+                        qd[q] = qacc;
+                    }
                 }
                 __syncwarp();
                 transpose_reduce<NP, CW>(tb, redw, t_grp, lane);
                 allreduce_nt<NT, 8>(bp);
                 allreduce_nt<NT, 8>(abp);
+                if (ACCURATE) allreduce_nt<NT, 8>(qd);
                 if (j == g) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         sb_own[q] = bp[q];
                         sab_own[q] = abp[q];
+                        if (ACCURATE) qd_own[q] = qd[q];
                     }
                 }
                 __syncwarp();   // the transpose buffer is reused by the next group
@@ -722,23 +894,48 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             load_raw8r<TIN>(st + RAWB, CH, c, tbk, dv);
             float suf[8];
             float run = 0.0f;
+            // packed: the suffix restarts at zero at a sequence's last token;
+            // `top` = the highest own token at which it does (-1: none), above
+            // which the tokens still take the carry from later tokens
+            const uint32_t eown = VARLEN ? (emask >> (g * 8)) & 0xffu : 0u;
+            const int top = VARLEN ? 31 - __clz((int)eown) : -1;
 #pragma unroll
             for (int q = 7; q >= 0; --q) {
+                if (VARLEN && ((eown >> q) & 1u)) run = 0.0f;
                 run += phv[q] - du[q] * sab_own[q];
                 suf[q] = run;
             }
-            float incl = run;
+            float qv[8];   // the suffix sum Q at each own token
+            if (VARLEN) {
+                // carry into each lane's tokens, lane NT-1 first: a lane passes
+                // on its sum, plus what came in if it has no restart
+                float R = carry, rin = carry;
 #pragma unroll
-            for (int o = 1; o < NT; o <<= 1) {
-                const float v = __shfl_down_sync(0xffffffffu, incl, o, NT);
-                if (g + o < NT) incl += v;
+                for (int gg = NT - 1; gg >= 0; --gg) {
+                    if (g == gg) rin = R;
+                    const float cand = run + (top < 0 ? R : 0.0f);
+                    R = __shfl_sync(0xffffffffu, cand, src_base + gg);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) qv[q] = q > top ? rin + suf[q] : suf[q];
+                carry = R;
+            } else {
+                float incl = run;
+#pragma unroll
+                for (int o = 1; o < NT; o <<= 1) {
+                    const float v = __shfl_down_sync(0xffffffffu, incl, o, NT);
+                    if (g + o < NT) incl += v;
+                }
+                const float excl = incl - run;
+                const float total = __shfl_sync(0xffffffffu, incl, src_base);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) qv[q] = carry + excl + suf[q];
+                carry += total;
             }
-            const float excl = incl - run;
-            const float total = __shfl_sync(0xffffffffu, incl, src_base);
             float duv[8], ddv[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float dd = carry + excl + suf[q] + uv[q] * sb_own[q] * kLog2e;
+                const float dd = (ACCURATE ? qd_own[q] : qv[q]) + uv[q] * sb_own[q] * kLog2e;
                 const float sx = rcp(1.0f + ex2(-fmaf(dv[q], kLog2e, bias2)));  // d softplus / dx
                 ddv[q] = dd * sx;
                 duv[q] = fmaf(gq[q], Dd, d2[q] * sb_own[q]);
@@ -747,38 +944,13 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     db_acc += ddv[q];
                 }
             }
-            carry += total;
             if (ch_ok) {
                 const int64_t off = row * L + k * kT + tbk;
                 store_out8<TOUT>(p.du, off, duv, nvalid - tbk, vec_out);
                 store_out8<TOUT>(p.ddr, off, ddv, nvalid - tbk, vec_out);
             }
         }
-        if (k > 0) {
-            // Re-anchor: the suffix sum equals sum_n A a_t lambda_t h_{t-1} at
-            // this chunk's first token t, with h_{t-1} the state at the end of
-            // the previous chunk.  Rounding in the running sum is thereby
-            // confined to one chunk instead of random-walking over the sequence.
-            float part = 0.0f;
-            if (ch_ok && !dead) {
-                const float4* hc =
-                    reinterpret_cast<const float4*>(p.hck + (row * nchunks + k - 1) * NP + g * G);
-#pragma unroll
-                for (int j = 0; j < G / 4; ++j) {
-                    const float4 hv = hc[j];
-                    float l0, l1, l2, l3;
-                    upk(mul2(mul2(Ap[2 * j], anext[2 * j]), lam[2 * j]), l0, l1);
-                    upk(mul2(mul2(Ap[2 * j + 1], anext[2 * j + 1]), lam[2 * j + 1]), l2, l3);
-                    part = fmaf(l0, hv.x, part);
-                    part = fmaf(l1, hv.y, part);
-                    part = fmaf(l2, hv.z, part);
-                    part = fmaf(l3, hv.w, part);
-                }
-            }
-#pragma unroll
-            for (int o = 1; o < NT; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            carry = part;
-        }
+        if (k > 0) carry = reanchor(k - 1);
         __syncwarp();
         if (lane == 0 && !dead) {
             mbar_arrive(&empty_bar[s]);
@@ -797,13 +969,15 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if (p.dbias) atomicAdd(p.dbias + d, db_acc);
         }
         if (p.dh0) {
+            // packed: dh0 of the sequence holding token 0
+            float* d0p = p.dh0 + (VARLEN ? (int64_t)seq_of_token(p.cu_seqlens, p.nseq, 0) * seq_stride : 0);
 #pragma unroll
             for (int j = 0; j < G / 2; ++j) {
                 const int n0 = g * G + 2 * j;
                 float v0, v1;
                 upk(mul2(anext[j], lam[j]), v0, v1);
-                if (n0 < N) p.dh0[row * N + n0] = v0;
-                if (n0 + 1 < N) p.dh0[row * N + n0 + 1] = v1;
+                if (n0 < N) d0p[row * N + n0] = v0;
+                if (n0 + 1 < N) d0p[row * N + n0 + 1] = v1;
             }
         }
     }

@@ -593,18 +593,25 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     d2, du, bct + sb * SB * (2 * NP) + g * G, Ap, h, hl, yp);
 
             if (!SUMMARY) {
-                // 3. partial read-outs through the buffer; finish the own tokens
+                // 3. partial read-outs through the buffer (one lane per channel:
+                //    the lane's own sums); finish the own tokens
                 float* yb = xy + cw * Lay::YROW;
+                if (NT > 1) {
 #pragma unroll
-                for (int q = 0; q < SB; q += 4)
-                    *reinterpret_cast<float4*>(yb + g * SB + q) =
-                        make_float4(yp[q], yp[q + 1], yp[q + 2], yp[q + 3]);
-                __syncwarp();
+                    for (int q = 0; q < SB; q += 4)
+                        *reinterpret_cast<float4*>(yb + g * SB + q) =
+                            make_float4(yp[q], yp[q + 1], yp[q + 2], yp[q + 3]);
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int k8 = 0; k8 < TPL / 8; ++k8) {
                     float yt[8];
+                    if (NT == 1) {
 #pragma unroll
-                    for (int gg = 0; gg < NT; ++gg) {
+                        for (int q = 0; q < 8; ++q) yt[q] = yp[8 * k8 + q];
+                    }
+#pragma unroll
+                    for (int gg = 0; gg < (NT > 1 ? NT : 0); ++gg) {
                         const float4 a = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8);
                         const float4 bq = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8 + 4);
                         if (gg == 0) {

@@ -77,6 +77,10 @@ cudaError_t launch_bwd_np32(int NT, int tin, int tout, bool tma, const BwdParams
                             const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
                             const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
+// the same over packed sequences (p.cu_seqlens, p.nseq): padded state size 16,
+// two threads per channel, 16-byte token rows (TMA tiles)
+cudaError_t launch_bwd_varlen_np16(int tin, int tout, const BwdParams& p, const BwdMaps& m,
+                                   const BwdLaunch& lc, cudaStream_t st);
 
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);
@@ -101,5 +105,14 @@ cudaError_t launch_step(int tin, int tout, const StepParams& p, cudaStream_t st)
 cudaError_t launch_step_dec16_any(int tin, int tout, const StepParams& p, const CUtensorMap& tm_st,
                                   const CUtensorMap& tm_a, cudaStream_t st);
 cudaError_t launch_expired_wait(int* status, int64_t spin_limit, cudaStream_t st);
+
+// the bidirectional backward (ssm_flip.cu)
+cudaError_t launch_flip_rows(int dtype, const void* in, void* out, int64_t rows, int64_t L,
+                             cudaStream_t st);
+cudaError_t launch_bidir_combine(int tout, int64_t rows, int64_t L, const float* du1,
+                                 const float* du2, const float* dz1, const float* dz2,
+                                 const float* ddr1, const float* ddr2, void* du, void* dz,
+                                 void* ddr, void* ddr_r, cudaStream_t st);
+cudaError_t launch_fold_status(int* outer, const int* inner, cudaStream_t st);
 
 }  // namespace ssm

@@ -112,6 +112,8 @@ struct BwdParams {
     float* phi;             // (Bt*D, L) fp32 workspace, written by the forward sweep
     float* hfin;            // (Bt*D, NP) fp32 workspace: final state
     float* hck;             // (Bt*D, nchunks, NP) fp32 workspace: state at the end of each chunk
+    float* hprev;           // fp32 inputs: (Bt*D, L, NP) fp32 workspace, the state each
+                            // token's update starts from
     void* du;
     void* ddr;
     void* dz;               // nullable

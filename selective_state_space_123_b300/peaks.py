@@ -17,7 +17,7 @@ import statistics
 _HERE = os.path.dirname(os.path.abspath(__file__))
 PEAKS_LIB = os.path.join(_HERE, "libssmpeaks.so")
 
-KINDS = {"ex2": 0, "fma": 1, "fma2": 2, "update_mix": 3}
+KINDS = {"ex2": 0, "fma": 1, "fma2": 2, "update_mix": 3, "lg2": 4, "rcp": 5}
 _LIB = None
 
 
@@ -70,4 +70,6 @@ def measure(threads: int = 1024) -> dict:
         "fp32_fma_lane_ops_per_clk_sm": rate_per_clk_sm("fma", threads),
         "fp32x2_fma_lane_ops_per_clk_sm": rate_per_clk_sm("fma2", threads),
         "update_mix_per_clk_sm": rate_per_clk_sm("update_mix", threads),
+        "lg2_per_clk_sm": rate_per_clk_sm("lg2", threads),
+        "rcp_per_clk_sm": rate_per_clk_sm("rcp", threads),
     }

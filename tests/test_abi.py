@@ -31,6 +31,27 @@ def test_exports_every_declared_symbol(pkg):
         assert hasattr(raw, name), name
 
 
+def _declared_param_counts():
+    hdr = open(os.path.join(ROOT, "include", "ssm_scan.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(ssm_[a-z_]+)\s*\(([^)]*)\)\s*;", hdr):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header(pkg):
+    """Every function the binding calls is declared with as many parameters
+    in ssm_scan.h as the binding passes (a miscount would shift every later
+    argument)."""
+    counts = _declared_param_counts()
+    assert set(counts) == set(pkg.EXPORTS)
+    for name, n in counts.items():
+        argtypes = getattr(pkg.lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes and len(argtypes))
+
+
 def test_strerror_covers_codes(pkg):
     for code in range(-9, 1):
         s = pkg.ssm_strerror(code)

@@ -53,13 +53,19 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("step_dec16_kernel") != base
 
 
-@pytest.mark.parametrize("variant,factor", [((0, False, False), 1), ((4, False, False), 1),
-                                            ((0, True, False), 1), ((0, False, True), 2)])
-def test_oracle_worker_variants(variant, factor):
-    """The CPU baseline's worker runs every forward variant and counts the
+@pytest.mark.parametrize("mode,variant,factor", [("fwd", (0, False, False), 1),
+                                                 ("fwd", (4, False, False), 1),
+                                                 ("fwd", (0, True, False), 1),
+                                                 ("fwd", (0, False, True), 2),
+                                                 ("fwdbwd", (0, False, False), 1),
+                                                 ("fwdbwd", (0, True, False), 1),
+                                                 ("fwdbwd", (0, False, True), 2)])
+def test_oracle_worker_variants(mode, variant, factor):
+    """The CPU baseline's worker runs every forward variant, and the
+    backward of the plain, packed and bidirectional scans, and counts the
     state updates it did (two scans for the bidirectional one)."""
     conv_k, varlen, bidir = variant
-    upd, secs = bench._oracle_worker(("fwd", 7, 1, 64, 16, 256, [0, 5], conv_k, varlen, bidir))
+    upd, secs = bench._oracle_worker((mode, 7, 1, 64, 16, 256, [0, 5], conv_k, varlen, bidir))
     assert upd == factor * 2 * 16 * 256
     assert secs >= 0.0
 
