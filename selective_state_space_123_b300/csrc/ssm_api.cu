@@ -91,8 +91,11 @@ struct FwdPlan {
     bool tma_raw = false;
     size_t off_bc = 0, off_hin = 0, off_hloc = 0, off_sumd = 0, off_tstart = 0, bytes = 0;
     // bidirectional scan: the right-to-left pass's prepared B/C and its gated
-    // output (Bt, D, L) fp32
+    // output (Bt, D, L) fp32; the left-to-right pass streams that output as a
+    // fourth tile, with its own ring depth and shared memory
     size_t off_bc_r = 0, off_yrev = 0;
+    int stages_ltr = 2;
+    size_t smem_ltr = 0;
 };
 
 // Per-NT constants of the forward kernel, on the host.
@@ -256,6 +259,19 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count, bool segments = true) {
 // two-pass split of a long sequence is not built for the right-to-left pass).
 FwdPlan plan_fwd_bidir(const ssm_shape& s, int sm_count) {
     FwdPlan pl = plan_fwd(s, sm_count, false);
+    // the left-to-right pass's stage holds an fp32 tile of the other
+    // direction's output besides u, delta_raw, z and B/C
+    {
+        const int eb = dtype_bytes(s.in_dtype);
+        const size_t stage = (size_t)3 * pl.CH * kT * eb + (size_t)kT * 2 * pl.NP * 4 +
+                             (size_t)pl.CH * kT * 4;
+        const size_t xy = (size_t)pl.W * fwd_xy_bytes(pl.NT);
+        const size_t avail = (size_t)kMaxSmemPerCta - 1024 - xy;
+        int st = (int)(avail / stage);
+        if (st > 4) st = 4;
+        pl.stages_ltr = st;   // < 2: refused by the caller
+        pl.smem_ltr = (size_t)(st > 0 ? st : 0) * stage + xy + 1024;
+    }
     size_t off = pl.bytes;
     pl.off_bc_r = off;
     off += align256((size_t)s.batch * s.seqlen * 2 * pl.NP * 4);
@@ -283,22 +299,19 @@ int bwd_tbuf_floats(int NT, int NP) {
     return 8 * (CW * NP + 4);
 }
 
-BwdPlan plan_bwd(const ssm_shape& s, int sm_count, bool nt2_only = false) {
+BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
     BwdPlan pl;
     pl.NP = padded_state(s.dstate);
     if (pl.NP < 8) pl.NP = 8;
     const int eb = dtype_bytes(s.in_dtype);
     pl.tma_raw = (s.seqlen * eb) % 16 == 0;
     const int nts_all[2] = {2, 4};
-    int want_nt = nt2_only ? 2 : env_int("SSM_BWD_NT", 0);
+    int want_nt = env_int("SSM_BWD_NT", 0);
     int want_w = env_int("SSM_BWD_W", 0);
     double best = -1.0;
     // a second search without the overrides when none of them fits
     for (int attempt = 0; attempt < 2 && best < 0.0; ++attempt) {
-    if (attempt == 1) {
-        want_nt = nt2_only ? 2 : 0;
-        want_w = 0;
-    }
+    if (attempt == 1) want_nt = want_w = 0;
     for (int ni = 0; ni < 2; ++ni) {
         const int NT = nts_all[ni];
         if (pl.NP == 8 && NT != 2) continue;       // G = NP / NT must be 4, 8 or 16
@@ -662,7 +675,7 @@ int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const FwdPlan pl = plan_fwd_bidir(s, device_sm_count());
     // built for 9..16 states and 16-byte token rows
-    if (L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
+    if (L > 0 && (pl.NP != 16 || !pl.tma_raw || pl.stages_ltr < 2)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
@@ -698,7 +711,8 @@ int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
         !make_map(&mf.u, u, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
         !make_map(&mf.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
         !make_map(&mr.dr, delta_raw_r, tdt, eb, L, Bt * Dm, box_t, pl.CH, true) ||
-        (z && !make_map(&mf.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)))
+        (z && !make_map(&mf.z, z, tdt, eb, L, Bt * Dm, box_t, pl.CH, true)) ||
+        !make_map(&mf.ya, yrev, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, Bt * Dm, 32, pl.CH, true))
         return cuda_fail();
     mr.u = mf.u;
     mr.z = mf.z;
@@ -715,14 +729,15 @@ int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
     FwdParams pr = p;   // right to left: fp32 gated output into the workspace
     pr.dr = delta_raw_r; pr.A = A_r; pr.Dv = D_r; pr.bias = delta_bias_r; pr.h0 = h0_r;
     pr.bc = bc_r; pr.y = yrev; pr.hL = hL_r;
-    FwdParams pf = p;   // left to right, adding it
+    FwdParams pf = p;   // left to right, adding it (streamed through the ring)
     pf.dr = delta_raw; pf.A = A; pf.Dv = D; pf.bias = delta_bias; pf.h0 = h0;
     pf.bc = bc; pf.y = y; pf.hL = hL; pf.yadd = yrev;
+    pf.stages = pl.stages_ltr;
     const dim3 grid((unsigned)((Dm + pl.CH - 1) / pl.CH), (unsigned)Bt, 1);
     if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, SSM_F32, 1, pr, mr, grid, pl.W, pl.smem, st) !=
             cudaSuccess ||
-        launch_fwd_bidir_np16(pl.NT, s.in_dtype, s.out_dtype, 2, pf, mf, grid, pl.W, pl.smem, st) !=
-            cudaSuccess)
+        launch_fwd_bidir_np16(pl.NT, s.in_dtype, s.out_dtype, 2, pf, mf, grid, pl.W, pl.smem_ltr,
+                              st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
 }
@@ -784,10 +799,10 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const BwdPlan pl = plan_bwd(s, device_sm_count(), varlen);
+    const BwdPlan pl = plan_bwd(s, device_sm_count());
     if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
     // packed sequences: built for 9..16 states and 16-byte token rows
-    if (varlen && L > 0 && (pl.NP != 16 || pl.NT != 2 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
+    if (varlen && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
@@ -869,7 +884,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         lc.stages_r = pl.stages_r;
         lc.smem_f = pl.smem_f;
         lc.smem_r = pl.smem_r;
-        if (launch_bwd_varlen_np16(s.in_dtype, s.out_dtype, p, maps, lc, st) != cudaSuccess)
+        if (launch_bwd_varlen_np16(pl.NT, s.in_dtype, s.out_dtype, p, maps, lc, st) != cudaSuccess)
             return cuda_fail();
         return SSM_OK;
     }

@@ -245,7 +245,7 @@ template <int NP, int NT, typename TIN, typename TOUT, bool SUMMARY, bool TMA_RA
 __global__ void __launch_bounds__(32 * (FwdLayout<NT>::kMaxWarps + 1), FwdLayout<NT>::kMinBlocks)
 fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
            const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
-           const __grid_constant__ CUtensorMap tm_bc) {
+           const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ CUtensorMap tm_ya) {
     using Lay = FwdLayout<NT>;
     constexpr int G = NP / NT;
     constexpr int CW = Lay::CW;
@@ -254,6 +254,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     constexpr int EB = (int)sizeof(TIN);
     constexpr int NRAW = SUMMARY ? 2 : 3;
     constexpr int BCB = bc_tile_bytes<NP>();
+    // the left-to-right pass of the bidirectional scan streams the other
+    // direction's fp32 output through the ring as a fourth tile
+    constexpr bool YTILE = DIR == 2;
     constexpr bool ACCURATE = EB == 4;
     static_assert(G == 4 || G == 8 || G == 16, "states per thread");
     static_assert(NT == 1 || NT == 2 || NT == 4, "threads per channel");
@@ -261,7 +264,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int W = (int)(blockDim.x / 32) - 1;
     const int CH = W * CW;
     const int RAW = CH * kT * EB;
-    const int STAGE = NRAW * RAW + BCB;
+    const int RAWF = YTILE ? CH * kT * 4 : 0;
+    const int STAGE = NRAW * RAW + RAWF + BCB;
+    const int BCOFF = NRAW * RAW + RAWF;   // the B/C tile's offset in a stage
     const int STAGES = p.stages;
 
     extern __shared__ uint8_t smem_dyn[];
@@ -314,6 +319,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 prefetch_tmap(&tm_u);
                 prefetch_tmap(&tm_dr);
                 if (has_z) prefetch_tmap(&tm_z);
+                if (YTILE) prefetch_tmap(&tm_ya);
             }
         }
         constexpr int BOXES = kT * EB / 128;   // 128-byte TMA boxes per tile row
@@ -337,7 +343,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int32_t t0 = (int32_t)(k * kT);
             if (TMA_RAW) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)((has_z ? 3 : 2) * RAW + BCB));
+                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)((has_z ? 3 : 2) * RAW + RAWF + BCB));
 #pragma unroll
                     for (int bx = 0; bx < BOXES; ++bx) {
                         const int32_t x = t0 + bx * BOX_T;
@@ -347,7 +353,14 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             tma_load_2d(st + 2 * RAW + bx * CH * 128, &tm_z, &full_bar[s], x,
                                         (int32_t)row0);
                     }
-                    tma_load_2d(st + NRAW * RAW, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
+                    if (YTILE) {
+                        // fp32 rows: two boxes of 32 tokens per chunk
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx)
+                            tma_load_2d(st + NRAW * RAW + bx * CH * 128, &tm_ya, &full_bar[s],
+                                        t0 + bx * 32, (int32_t)row0);
+                    }
+                    tma_load_2d(st + BCOFF, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
                 }
             } else {
                 fill_raw_tile_r<TIN>(st, CH, p.u, row0, rows_valid, L, t0, lane);
@@ -356,7 +369,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full_bar[s], BCB);
-                    tma_load_2d(st + NRAW * RAW, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
+                    tma_load_2d(st + BCOFF, &tm_bc, &full_bar[s], 0, (int32_t)(b * L + t0));
                 }
             }
         }
@@ -476,7 +489,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             break;
         }
         const uint8_t* st = smem + s * STAGE;
-        const float* bct = reinterpret_cast<const float*>(st + NRAW * RAW);
+        const float* bct = reinterpret_cast<const float*>(st + BCOFF);
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
 
 #pragma unroll 1
@@ -631,22 +644,13 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                         if (has_z) v *= zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q]));
                         out[q] = v;
                     }
-                    if constexpr (DIR == 2) {
-                        // the right-to-left scan's gated output of these tokens
-                        const int nv = nvalid - (tb + 8 * k8);
-                        if (ch_ok && nv > 0) {
-                            const float* ya = p.yadd + row * L + k * kT + tb + 8 * k8;
-                            if (nv >= 8) {
-                                const float4 a0 = reinterpret_cast<const float4*>(ya)[0];
-                                const float4 a1 = reinterpret_cast<const float4*>(ya)[1];
-                                out[0] += a0.x; out[1] += a0.y; out[2] += a0.z; out[3] += a0.w;
-                                out[4] += a1.x; out[5] += a1.y; out[6] += a1.z; out[7] += a1.w;
-                            } else {
+                    if constexpr (YTILE) {
+                        // the right-to-left scan's gated output of these tokens,
+                        // from the ring (zeros past the row's end)
+                        float ya[8];
+                        load_raw8r<float>(st + NRAW * RAW, CH, c, tb + 8 * k8, ya);
 #pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    if (q < nv) out[q] += ya[q];
-                            }
-                        }
+                        for (int q = 0; q < 8; ++q) out[q] += ya[q];
                     }
                     if (ch_ok)
                         store_out8<TOUT>(p.y, row * L + k * kT + tb + 8 * k8, out,

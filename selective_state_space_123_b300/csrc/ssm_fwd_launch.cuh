@@ -23,7 +23,7 @@ cudaError_t launch_fwd_one(const FwdParams& p, const FwdMaps& m, dim3 grid, int 
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_val[dev] = smem;
     }
-    kern<<<grid, 32 * (warps + 1), smem, st>>>(p, m.u, m.dr, m.z, m.bc);
+    kern<<<grid, 32 * (warps + 1), smem, st>>>(p, m.u, m.dr, m.z, m.bc, m.ya);
     return cudaGetLastError();
 }
 

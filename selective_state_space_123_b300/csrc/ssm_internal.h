@@ -14,6 +14,7 @@ namespace ssm {
 // entries zeroed) and the prepared B/C tile.
 struct FwdMaps {
     CUtensorMap u, dr, z, bc;
+    CUtensorMap ya;   // the bidirectional scan's left-to-right pass: the other direction's output
 };
 
 // Forward kernel launch for padded state size NP (4, 8, 16, 32, 64), NT
@@ -78,9 +79,9 @@ cudaError_t launch_bwd_np32(int NT, int tin, int tout, bool tma, const BwdParams
 cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams& p,
                             const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 // the same over packed sequences (p.cu_seqlens, p.nseq): padded state size 16,
-// two threads per channel, 16-byte token rows (TMA tiles)
-cudaError_t launch_bwd_varlen_np16(int tin, int tout, const BwdParams& p, const BwdMaps& m,
-                                   const BwdLaunch& lc, cudaStream_t st);
+// two or four threads per channel, 16-byte token rows (TMA tiles)
+cudaError_t launch_bwd_varlen_np16(int NT, int tin, int tout, const BwdParams& p,
+                                   const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);

@@ -132,3 +132,16 @@ def test_varlen_bwd_unsupported_shape(ssm):
     x = make_inputs(1, 16, 8, 100, seed=670, in_dtype="bf16", dy=True)
     with pytest.raises(ssm.SSMError):
         _run(ssm, x, [0, 50, 100])
+
+
+@pytest.mark.parametrize("nt", ["2", "4"])
+def test_varlen_bwd_lanes_per_channel(ssm, nt, monkeypatch):
+    """Two and four lanes per channel (32-token super-blocks: restarts in
+    four lanes' runs of the suffix sum)."""
+    monkeypatch.setenv("SSM_BWD_NT", nt)
+    Bt, D, N, L = 1, 50, 16, 320
+    x = make_inputs(Bt, D, N, L, seed=680 + int(nt), in_dtype="bf16", dy=True)
+    ns = len(CUTS) - 1
+    _run(ssm, x, CUTS, _state(ns, Bt, D, N, 690), _state(ns, Bt, D, N, 691))
+    xf = make_inputs(Bt, D, N, L, seed=685 + int(nt), in_dtype="f32", dy=True)
+    _run(ssm, xf, CUTS, _state(ns, Bt, D, N, 692), _state(ns, Bt, D, N, 693))

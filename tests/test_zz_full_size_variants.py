@@ -111,3 +111,58 @@ def test_bidir_full_size_sampled(ssm):
         assert_close(hL_r[[b]][:, ds].cpu().numpy(), hro, TOL["bf16"], "hL_r b=%d" % b)
     del a, r, y, hL, hL_r
     torch.cuda.empty_cache()
+
+
+def test_packed_backward_long_row(ssm):
+    """The packed backward over the packed workload's row (65,536 tokens cut
+    by the bench's length recipe) on 256 channels: every output against the
+    oracle (dB and dC are sums over all channels, so no channel sampling)."""
+    from scan_inputs import make_inputs
+    w = bench.WORKLOADS["packed_mamba1p4b_fwdbwd"]
+    L = w["L"]
+    cu = packed_seqlens(L, seed=w["seed"])
+    x = make_inputs(1, 256, 16, L, seed=w["seed"], in_dtype="bf16", dy=True)
+    nseq = len(cu) - 1
+    rng = np.random.default_rng(71)
+    h0 = rng.standard_normal((nseq, 1, 256, 16)).astype(np.float32)
+    dhL = rng.standard_normal((nseq, 1, 256, 16)).astype(np.float32)
+    t, f32 = torch.bfloat16, torch.float32
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    g = ssm.ssm_scan_bwd_varlen(to_dev(x.u, t), cu_d, to_dev(x.delta_raw, t), to_dev(x.A, f32),
+                                to_dev(x.Bm, t), to_dev(x.Cm, t), to_dev(x.dy, t), to_dev(x.Dv, f32),
+                                to_dev(x.z, t), to_dev(x.delta_bias, f32), to_dev(h0, f32),
+                                to_dev(dhL, f32), out_dtype=f32)
+    torch.cuda.synchronize()
+    o = oracle.scan_bwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, cu, x.Dv, x.z,
+                               x.delta_bias, h0, dhL)
+    for k in o:
+        assert_close(g[k].float().cpu().numpy(), o[k], TOL["bf16"], k)
+
+
+def test_bidir_backward_long_rows(ssm):
+    """The bidirectional backward at the Mamba-1.4B sequence length (4,096
+    tokens) on 128 channels, both directions' parameters, every output
+    against the oracle."""
+    from scan_inputs import make_inputs
+    Bt, D, N, L = 1, 128, 16, 4096
+    xf = make_inputs(Bt, D, N, L, seed=72, in_dtype="bf16", dy=True, h0=True)
+    xr = make_inputs(Bt, D, N, L, seed=73, in_dtype="bf16", h0=True)
+    rng = np.random.default_rng(74)
+    dhL = rng.standard_normal((Bt, D, N)).astype(np.float32)
+    dhL_r = rng.standard_normal((Bt, D, N)).astype(np.float32)
+    t, f32 = torch.bfloat16, torch.float32
+    dev = lambda x: dict(delta_raw=to_dev(x.delta_raw, t), A=to_dev(x.A, f32), B=to_dev(x.Bm, t),
+                         C=to_dev(x.Cm, t), D=to_dev(x.Dv, f32),
+                         delta_bias=to_dev(x.delta_bias, f32), h0=to_dev(x.h0, f32))
+    host = lambda x: dict(delta_raw=x.delta_raw, A=x.A, Bm=x.Bm, Cm=x.Cm, Dv=x.Dv,
+                          delta_bias=x.delta_bias, h0=x.h0)
+    shared, gf, gr = ssm.ssm_scan_bwd_bidir(to_dev(xf.u, t), to_dev(xf.z, t), dev(xf), dev(xr),
+                                            to_dev(xf.dy, t), to_dev(dhL, f32), to_dev(dhL_r, f32),
+                                            out_dtype=f32)
+    torch.cuda.synchronize()
+    so, of, orr = oracle.scan_bwd_bidir(xf.u, xf.z, host(xf), host(xr), xf.dy, dhL, dhL_r)
+    for k in so:
+        assert_close(shared[k].cpu().numpy(), so[k], TOL["bf16"], k)
+    for tag, gg, oo in (("fwd", gf, of), ("rev", gr, orr)):
+        for k in oo:
+            assert_close(gg[k].cpu().numpy(), oo[k], TOL["bf16"], tag + "." + k)
