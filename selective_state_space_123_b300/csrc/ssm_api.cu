@@ -255,10 +255,11 @@ FwdPlan plan_fwd(const ssm_shape& s, int sm_count, bool segments = true) {
     return pl;
 }
 
-// The bidirectional scan runs both directions in one segment each (the
-// two-pass split of a long sequence is not built for the right-to-left pass).
+// The bidirectional scan: both directions share the plan, including the
+// two-pass split of a long row with few channels (each direction runs its own
+// summaries and carry, the right-to-left one from the last segment down).
 FwdPlan plan_fwd_bidir(const ssm_shape& s, int sm_count) {
-    FwdPlan pl = plan_fwd(s, sm_count, false);
+    FwdPlan pl = plan_fwd(s, sm_count, true);
     // the left-to-right pass's stage holds an fp32 tile of the other
     // direction's output besides u, delta_raw, z and B/C
     {
@@ -722,7 +723,7 @@ int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
     p.Bt = Bt; p.D = Dm; p.L = L; p.N = (int)N;
     p.u = u; p.z = z;
     p.seg_chunks = pl.seg_chunks;
-    p.nseg = 1;
+    p.nseg = pl.nseg;
     p.stages = pl.stages;
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
@@ -733,11 +734,47 @@ int ssm_scan_fwd_bidir(const ssm_shape* shape, const void* u, const void* z,
     pf.dr = delta_raw; pf.A = A; pf.Dv = D; pf.bias = delta_bias; pf.h0 = h0;
     pf.bc = bc; pf.y = y; pf.hL = hL; pf.yadd = yrev;
     pf.stages = pl.stages_ltr;
-    const dim3 grid((unsigned)((Dm + pl.CH - 1) / pl.CH), (unsigned)Bt, 1);
-    if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, SSM_F32, 1, pr, mr, grid, pl.W, pl.smem, st) !=
-            cudaSuccess ||
-        launch_fwd_bidir_np16(pl.NT, s.in_dtype, s.out_dtype, 2, pf, mf, grid, pl.W, pl.smem_ltr,
-                              st) != cudaSuccess)
+    const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
+    const unsigned nseg = (unsigned)pl.nseg;
+    if (nseg > 1) {
+        // segmented plan, right to left first: summaries of segments 1 ..
+        // nseg-1 (each from a zero state at its right end), the carry from the
+        // last segment down, then every segment from its initial state
+        pr.hin = reinterpret_cast<float*>(ws + pl.off_hin);
+        pr.hloc = reinterpret_cast<float*>(ws + pl.off_hloc);
+        pr.sumd = reinterpret_cast<float*>(ws + pl.off_sumd);
+        FwdParams pr1 = pr;
+        pr1.hin = nullptr;
+        pr1.seg0 = 1;
+        if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, SSM_F32, 1, true, pr1, mr, dim3(gx, (unsigned)Bt, nseg - 1),
+                                  pl.W, pl.smem, st) != cudaSuccess ||
+            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A_r, h0_r, pr.hloc, pr.sumd, pr.hin, st,
+                         true) != cudaSuccess)
+            return cuda_fail();
+    }
+    if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, SSM_F32, 1, false, pr, mr, dim3(gx, (unsigned)Bt, nseg),
+                              pl.W, pl.smem, st) != cudaSuccess)
+        return cuda_fail();
+    if (nseg > 1) {
+        // left to right: the plain forward's summaries (with its tail search) and carry
+        pf.hin = pr.hin;
+        pf.hloc = pr.hloc;
+        pf.sumd = pr.sumd;
+        FwdParams pf1 = pf;
+        pf1.hin = nullptr;
+        pf1.stages = pl.stages;
+        int* tstart = reinterpret_cast<int*>(ws + pl.off_tstart);
+        if (launch_tail(s.in_dtype, pf, pl.CH, gx, tstart, pf.sumd, st) != cudaSuccess)
+            return cuda_fail();
+        pf1.tstart = tstart;
+        if (launch_fwd(pl, s.in_dtype, s.out_dtype, true, false, false, pf1, mf,
+                       dim3(gx, (unsigned)Bt, nseg - 1), st) != cudaSuccess ||
+            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, pf.hloc, pf.sumd, pf.hin, st) !=
+                cudaSuccess)
+            return cuda_fail();
+    }
+    if (launch_fwd_bidir_np16(pl.NT, s.in_dtype, s.out_dtype, 2, false, pf, mf, dim3(gx, (unsigned)Bt, nseg),
+                              pl.W, pl.smem_ltr, st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
 }

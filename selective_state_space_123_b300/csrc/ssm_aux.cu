@@ -63,9 +63,11 @@ cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const 
 }
 
 // --------------------------------------------------------------- carry ---
+// reverse: the right-to-left scan of the bidirectional form, whose state
+// runs from the last segment to the first (h0 enters the last segment).
 __global__ void carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* __restrict__ A,
                              const float* __restrict__ h0, const float* __restrict__ hloc,
-                             const float* __restrict__ sumd, float* __restrict__ hin) {
+                             const float* __restrict__ sumd, float* __restrict__ hin, bool reverse) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (b, d, n)
     if (i >= Bt * D * NP) return;
     const int n = (int)(i % NP);
@@ -74,9 +76,10 @@ __global__ void carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg, con
     const int64_t seg_stride = Bt * D;
     const float a = n < N ? A[d * N + n] : 0.0f;
     float h = (h0 && n < N) ? h0[row * N + n] : 0.0f;
-    for (int s = 0; s < nseg; ++s) {
+    for (int j = 0; j < nseg; ++j) {
+        const int s = reverse ? nseg - 1 - j : j;
         hin[(s * seg_stride + row) * NP + n] = h;
-        if (s + 1 < nseg) {
+        if (j + 1 < nseg) {
             const float sd = sumd[s * seg_stride + row];
             h = (sd >= kTailSat ? 0.0f : ex2(a * sd) * h) + hloc[(s * seg_stride + row) * NP + n];
         }
@@ -233,10 +236,10 @@ cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int
 
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool reverse) {
     const int64_t total = Bt * D * NP;
     carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Bt, D, N, NP, nseg, A, h0, hloc,
-                                                                  sumd, hin);
+                                                                  sumd, hin, reverse);
     return cudaGetLastError();
 }
 

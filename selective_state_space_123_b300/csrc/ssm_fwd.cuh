@@ -280,7 +280,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int lane = tid & 31;
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CH;
-    const int seg = blockIdx.z;
+    const int seg = (int)blockIdx.z + p.seg0;
     const int64_t L = p.L;
     const int64_t nchunks = (L + kT - 1) / kT;
     const int64_t k_seg = (int64_t)seg * p.seg_chunks;
@@ -692,8 +692,9 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if (g == 0 && (seg_restart || k_begin == k_seg))
                 p.sumd[(int64_t)seg * p.Bt * p.D + row] = seg_restart ? kTailSat : (float)tot;
         }
-    } else if (k_end == nchunks && p.hL && ch_ok) {
-        // the last sequence's final state (packed: the one holding token L-1)
+    } else if ((DIR == 1 ? k_seg == 0 : k_end == nchunks) && p.hL && ch_ok) {
+        // the last sequence's final state (packed: the one holding token L-1;
+        // right to left: the state after token 0, in the first segment)
         const int64_t sf = VARLEN ? (int64_t)min(max(sp - 1, 0), p.nseq - 1) : 0;
         float* hfin = p.hL + (sf * p.Bt * p.D + row) * N;
 #pragma unroll

@@ -37,12 +37,13 @@ cudaError_t launch_fwd_conv_np16(int NT, int tin, int tout, bool summary, const 
 cudaError_t launch_fwd_varlen_np16(int NT, int tin, int tout, bool summary, bool conv,
                                    const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                                    size_t smem, cudaStream_t st);
-// The bidirectional scan's two passes, padded state size 16, TMA tiles, one
-// segment: dir 1 = right to left (fp32 gated output into p.y), dir 2 = left
-// to right adding p.yadd.
-cudaError_t launch_fwd_bidir_np16(int NT, int tin, int tout, int dir, const FwdParams& p,
-                                  const FwdMaps& m, dim3 grid, int warps, size_t smem,
-                                  cudaStream_t st);
+// The bidirectional scan's two passes, padded state size 16, TMA tiles:
+// dir 1 = right to left (fp32 gated output into p.y), dir 2 = left to right
+// adding p.yadd; summary = the right-to-left segment summaries (pass 1 of the
+// segmented plan; the left-to-right one is the plain forward's).
+cudaError_t launch_fwd_bidir_np16(int NT, int tin, int tout, int dir, bool summary,
+                                  const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
+                                  size_t smem, cudaStream_t st);
 cudaError_t launch_fwd_np32(int NT, int tin, int tout, bool summary, bool tma_raw,
                             const FwdParams& p, const FwdMaps& m, dim3 grid, int warps,
                             size_t smem, cudaStream_t st);
@@ -92,7 +93,7 @@ cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int
                         cudaStream_t st);
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,
-                         cudaStream_t st);
+                         cudaStream_t st, bool reverse = false);
 // Packed sequences: checks cu_seqlens (0 = c_0 <= c_1 <= ... <= c_nseq = L,
 // else SSM_ERR_SEQLENS in the status word) and writes the final state of
 // every empty sequence (its h0, or zero).  After prep_bc, which clears the

@@ -54,6 +54,7 @@ struct FwdParams {
     // kernel turns them into per-segment initial states, pass 2 writes y.
     int64_t seg_chunks;
     int nseg;
+    int seg0;               // segment of blockIdx.z = 0 (the right-to-left summary pass: 1)
     float* hin;             // (nseg, Bt, D, NP) initial state of each segment (pass 2)
     float* hloc;            // (nseg, Bt, D, NP) end state from a zero start (pass 1)
     float* sumd;            // (nseg, Bt, D) sum of delta/ln2 over the segment (pass 1)

@@ -88,8 +88,9 @@ def _plan_lines(shape, kind):
 def test_launch_counts_follow_the_plan():
     """The bench's launch claims for the packed and bidirectional workloads
     rest on the plan: 4 segments for the packed row (preparation, sequence
-    check, tail search, summary, carry, scan), one segment per direction for
-    the bidirectional scan even on a long row."""
+    check, tail search, summary, carry, scan); one segment per direction for
+    the bidirectional workload's shape (preparation twice, two passes), while
+    a few-channel long row is split in both directions."""
     from tests.buildlib import ensure_built
     ensure_built()
     w = bench.WORKLOADS["packed_mamba1p4b_fwd"]
@@ -97,5 +98,7 @@ def test_launch_counts_follow_the_plan():
     assert lines and "nseg=4 " in lines[-1] and w["launches"] == 6
     w = bench.WORKLOADS["bidir_mamba1p4b_fwd"]
     assert w["launches"] == 4
-    lines = _plan_lines((1, 1536, 16, 1 << 20), 2)
+    lines = _plan_lines((w["Bt"], w["D"], w["N"], w["L"]), 2)
     assert lines and "nseg=1 " in lines[-1]
+    lines = _plan_lines((1, 1536, 16, 1 << 20), 2)
+    assert lines and "nseg=1 " not in lines[-1]

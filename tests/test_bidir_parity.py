@@ -84,11 +84,36 @@ def test_bidir_lanes_per_channel(ssm, nt, monkeypatch):
     _run(ssm, xf, xr)
 
 
-def test_bidir_long_sequence(ssm):
-    """A long row is not split into segments (one pass per direction)."""
+def test_bidir_long_sequence(ssm, monkeypatch):
+    """A long row in one segment per direction."""
+    monkeypatch.setenv("SSM_FWD_NSEG", "1")
     xf, xr = _dirs(1, 24, 16, 64 * 40, 114, "f32")
     _run(ssm, xf, xr)
     xf, xr = _dirs(1, 40, 16, 64 * 100, 116, "bf16")
+    _run(ssm, xf, xr)
+
+
+@pytest.mark.parametrize("nseg", ["2", "3", "7"])
+def test_bidir_segmented(ssm, nseg, monkeypatch):
+    """The two-pass split of a row in both directions: the right-to-left
+    summaries run from each segment's right end and its carry from the last
+    segment down; initial states of both directions, a ragged last chunk,
+    fp32 and bf16."""
+    monkeypatch.setenv("SSM_FWD_NSEG", nseg)
+    xf, xr = _dirs(1, 40, 16, 64 * 29 + 8, 130, "bf16", h0=True)
+    _run(ssm, xf, xr)
+    xf, xr = _dirs(2, 24, 16, 64 * 30, 132, "f32", h0=True)
+    _run(ssm, xf, xr)
+
+
+@pytest.mark.parametrize("shift", [-1.0, 3.0])
+def test_bidir_segmented_long_segments(ssm, shift, monkeypatch):
+    """Two segments of 5,120 tokens with smaller and larger delta (long memory
+    across the segment boundary in both directions; decay to zero)."""
+    monkeypatch.setenv("SSM_FWD_NSEG", "2")
+    xf, xr = _dirs(1, 40, 16, 64 * 160, 134, "bf16", h0=True)
+    for x in (xf, xr):
+        x.delta_bias = (x.delta_bias + np.float32(shift)).astype(np.float32)
     _run(ssm, xf, xr)
 
 
