@@ -296,8 +296,10 @@ struct BwdPlan {
 };
 
 int bwd_tbuf_floats(int NT, int NP) {
-    const int CW = 32 / NT;
-    return 8 * (CW * NP + 4);
+    if (NT == 2) return NP == 8 ? BwdLayout<2, 8>::TBUF : NP == 16 ? BwdLayout<2, 16>::TBUF
+                                                                  : BwdLayout<2, 32>::TBUF;
+    return NP == 16 ? BwdLayout<4, 16>::TBUF : NP == 32 ? BwdLayout<4, 32>::TBUF
+                                                        : BwdLayout<4, 64>::TBUF;
 }
 
 BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {

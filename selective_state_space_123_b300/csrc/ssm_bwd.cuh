@@ -76,21 +76,23 @@ __device__ __forceinline__ void flush_red(const float* red, int W, float* out, i
 }
 
 // Cross-channel sum of one group of 8 tokens through the warp's transpose
-// buffer tb[token][channel][state] (rows padded by 16 bytes): lane tasks are
-// (token, group of 4 states); each sums the CW channels' float4s and writes
-// the 4 sums to the warp's chunk buffer redw[n][t].
+// buffer (token rows of CW channels x NP states, laid out as BwdLayout says):
+// lane tasks are (token, group of 4 states); each sums the CW channels'
+// float4s and writes the 4 sums to the warp's chunk buffer redw[n][t].
 template <int NP, int CW>
 __device__ __forceinline__ void transpose_reduce(const float* tb, float* redw, int t_first, int lane) {
-    constexpr int TROW = BwdLayout<32 / CW, NP>::TROW;
+    using Lay = BwdLayout<32 / CW, NP>;
+    constexpr int NT = 32 / CW;
     constexpr int TASKS = 8 * NP / 4;
     for (int task = lane; task < TASKS; task += 32) {
         const int t = task / (NP / 4);
         const int q = task % (NP / 4);
-        const float* src = tb + t * TROW + q * 4;
+        const int g = q / Lay::KC, kc = q % Lay::KC;    // the lane within a channel and its chunk
+        const float* src = tb + t * Lay::TROW;
         f2 s01 = pk(0.0f, 0.0f), s23 = pk(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < CW; ++c) {
-            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + c * NP);
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + Lay::chunk(c * NT + g, kc));
             s01 = add2(s01, v.x);
             s23 = add2(s23, v.y);
         }
@@ -265,15 +267,17 @@ __device__ __forceinline__ void allreduce_nt(float (&v)[V]) {
         for (int q = 0; q < V; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
 }
 
-// Store the G partials of one token into the transpose buffer slot.
-template <int G>
-__device__ __forceinline__ void put_tr(float* slot, const f2 (&v)[G / 2]) {
+// Store this lane's G partials of one token into the token's row of the
+// transpose buffer.
+template <int NT, int NP>
+__device__ __forceinline__ void put_tr(float* row, int lane, const f2 (&v)[NP / NT / 2]) {
+    using Lay = BwdLayout<NT, NP>;
 #pragma unroll
-    for (int j = 0; j < G / 4; ++j) {
+    for (int j = 0; j < Lay::KC; ++j) {
         float a, bb, cc, dd;
         upk(v[2 * j], a, bb);
         upk(v[2 * j + 1], cc, dd);
-        *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(a, bb, cc, dd);
+        *reinterpret_cast<float4*>(row + Lay::chunk(lane, j)) = make_float4(a, bb, cc, dd);
     }
 }
 
@@ -540,7 +544,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             gh[jj] = mul2(gqp, h[jj]);               // g_t h_t: dC partial
                         }
                     }
-                    put_tr<G>(tb + q * Lay::TROW + cw * NP + g * G, gh);
+                    put_tr<NT, NP>(tb + q * Lay::TROW, lane, gh);
                     float lo, hi;
                     upk(accy, lo, hi);
                     yp[q] = lo + hi;
@@ -842,7 +846,7 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
                         }
                     }
-                    put_tr<G>(tb + q * Lay::TROW + cw * NP + g * G, ld);
+                    put_tr<NT, NP>(tb + q * Lay::TROW, lane, ld);
                     float lo, hi;
                     upk(accb, lo, hi);
                     bp[q] = lo + hi;

@@ -84,15 +84,25 @@ struct FwdParams {
 };
 
 // Backward-kernel layout per (NT, NP): per compute warp a transpose buffer
-// of 8 tokens x CW channels x NP states (token rows padded by 16 bytes) for
-// the cross-channel sums of dB and dC.
+// of 8 tokens x CW channels x NP states for the cross-channel sums of dB and
+// dC.  In a token row, lane L's G states are KC = G/4 16-byte chunks; chunk k
+// sits at slot 32k + (L ^ s(k)), so that the lanes of one quarter warp write
+// eight distinct bank groups, and rows are padded so that the reads of one
+// quarter warp (the same 4 states of up to 32/NP tokens' channels) hit
+// disjoint banks too.
 template <int NT, int NP>
 struct BwdLayout {
     static constexpr int CW = 32 / NT;             // channels per compute warp
     static constexpr int G = NP / NT;              // states per lane
     static constexpr int SB = 8 * NT;              // tokens per super-block
-    static constexpr int TROW = CW * NP + 4;       // floats per token row of the transpose buffer
+    static constexpr int KC = G / 4;               // 16-byte chunks per lane and token
+    static constexpr int TPAD = NP == 8 ? 8 : NP == 16 ? (NT == 2 ? 8 : 16) : 4;
+    static constexpr int TROW = CW * NP + TPAD;    // floats per token row of the transpose buffer
     static constexpr int TBUF = 8 * TROW;          // floats per warp
+    // float offset of lane L's chunk k inside a token row
+    static __host__ __device__ constexpr int chunk(int L, int k) {
+        return 4 * (KC == 1 ? L : 32 * k + (L ^ (KC == 2 ? 4 * k : 2 * k)));
+    }
     static constexpr int kMaxWarps = 7;            // compute warps per CTA at most
 };
 
