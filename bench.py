@@ -147,7 +147,9 @@ def job_rate(world, updates_per_rank, ms_per_step):
     return world * updates_per_rank / (ms_per_step * 1e-3)
 
 
-def recorded_traffic(kind, workload):
+def recorded_traffic(kind, workload, seqlen=None):
+    if seqlen is not None and seqlen != WORKLOADS.get(workload, {}).get("L"):
+        return None     # the record is for the workload's own sequence length
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kind + ":" + workload]
     except Exception:
@@ -847,7 +849,7 @@ def run_ours(args):
         "algorithmic_bytes": wl.bytes,
         "exps": wl.exps,
         "traffic": recorded_traffic({"fwd": "fwd_kernel", "fwdbwd": "fwdbwd", "step": "step_dec16_kernel"}[wl.mode],
-                                    w["name"]),
+                                    w["name"], w["L"]),
         "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum of the forward and the two "
                          "backward sweeps of one step" if wl.mode == "fwdbwd" else
                          "dram__bytes_read.sum + dram__bytes_write.sum of the two passes (right to "
@@ -1004,10 +1006,17 @@ def main(argv=None, target=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end measurement (profiling runs)")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="override the workload's sequence length (small profiler captures)")
     ap.add_argument("--workload", default="mamba1p4b_fwd", choices=sorted(WORKLOADS) + ["peaks"],
                     help="'peaks': the register-only MUFU / FP32 / update-mix rate probes")
     args = ap.parse_args(argv)
     select_workload(args.workload)
+    if args.seqlen:
+        # a shorter (or longer) sequence of the same layer, for profiler captures
+        # that must stay small; the JSON line's config names the length used
+        WORKLOAD["L"] = args.seqlen
+        WORKLOAD["title"] += " (sequence length set by --seqlen)"
     if args.warmup < 3:
         args.warmup = 3
     if target is None:

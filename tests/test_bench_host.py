@@ -37,6 +37,8 @@ def test_recorded_traffic_is_keyed_to_the_sources():
         else:
             assert got is None, key
     assert bench.recorded_traffic("fwd_kernel", "no_such_workload") is None
+    # a run whose sequence length was overridden (--seqlen) gets no record
+    assert bench.recorded_traffic("fwd_kernel", "mamba1p4b_fwd", 1024) is None
 
 
 def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
