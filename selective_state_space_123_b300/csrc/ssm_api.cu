@@ -285,14 +285,26 @@ FwdPlan plan_fwd_bidir(const ssm_shape& s, int sm_count) {
 // Backward plan: the two sweeps need the prepared B/C (state size padded to
 // at least 8), one fp32 number per (batch, channel, token), the final state
 // and the state at the end of every 64-token chunk.  Channel tiles of W
-// compute warps, one CTA per SM, chosen like the forward's.
+// compute warps, one CTA per SM, chosen like the forward's.  Long sequences
+// with too few channel tiles to fill the GPU are cut into segments: the
+// forward's summary pass and carry give each segment its initial state, the
+// adjoint summary and a right-to-left carry the adjoint entering it from the
+// right, and a carry after the forward sweep adds the dA terms of the
+// tangent crossing segment boundaries.
 struct BwdPlan {
     int NP = 16, NT = 2, W = 4, CH = 32;
-    int stages_f = 2, stages_r = 2;
-    size_t smem_f = 0, smem_r = 0;
+    int stages_f = 2, stages_r = 2, stages_l = 2;
+    size_t smem_f = 0, smem_r = 0, smem_l = 0;
     bool tma_raw = false;
     bool ok = false;        // a tile shape fits the shared memory
+    int nseg = 1;
+    int64_t seg_chunks = 0;
+    int fwd_tiles = 0;      // channel tiles of the forward summary pass (segments)
     size_t off_bc = 0, off_phi = 0, off_hfin = 0, off_hck = 0, off_hprev = 0, bytes = 0;
+    // segments: forward summary (initial states, end states from zero, sums
+    // of delta2, tail-search starts), adjoint summary and carry, tangent sums
+    size_t off_hin = 0, off_hloc = 0, off_sumd = 0, off_tstart = 0, off_lamloc = 0,
+           off_lamin = 0, off_sumdr = 0, off_kstop = 0, off_gp = 0, off_mend = 0;
 };
 
 int bwd_tbuf_floats(int NT, int NP) {
@@ -302,15 +314,19 @@ int bwd_tbuf_floats(int NT, int NP) {
                                                         : BwdLayout<4, 64>::TBUF;
 }
 
-BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
+BwdPlan plan_bwd(const ssm_shape& s, int sm_count, bool segments = true) {
     BwdPlan pl;
     pl.NP = padded_state(s.dstate);
     if (pl.NP < 8) pl.NP = 8;
     const int eb = dtype_bytes(s.in_dtype);
     pl.tma_raw = (s.seqlen * eb) % 16 == 0;
+    const int64_t nchunks = (s.seqlen + kT - 1) / kT;
+    // segments are built for 9..16 states and 16-byte token rows
+    const bool seg_ok = segments && pl.NP == 16 && pl.tma_raw && nchunks >= 16;
     const int nts_all[2] = {2, 4};
     int want_nt = env_int("SSM_BWD_NT", 0);
     int want_w = env_int("SSM_BWD_W", 0);
+    const int want_seg = env_int("SSM_BWD_NSEG", 0);
     double best = -1.0;
     // a second search without the overrides when none of them fits
     for (int attempt = 0; attempt < 2 && best < 0.0; ++attempt) {
@@ -329,17 +345,41 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
             const size_t stf = 4 * raw + bcb, str = 4 * raw + rawf + bcb;
             if (2 * str + fixed > (size_t)kMaxSmemPerCta) continue;
             const int64_t tiles = (s.dim + CH - 1) / CH;
+            const int64_t ctas = s.batch * tiles;
             const double work = (double)CH * (NT == 4 ? 1.15 : 1.0);
-            const double cost = bwd_launch_cost(s.batch * tiles, sm_count, W, work);
+            // segments (when the channel tiles leave SMs idle): the sweeps over
+            // seg_chunks chunks each, ~4 % more work in the forward sweep, and
+            // the two summary passes over all segments but one at about a
+            // quarter of the sweeps' cost per chunk
+            int seg_lo = 1, seg_hi = 1;
+            if (seg_ok && want_seg > 0) seg_lo = seg_hi = want_seg;
+            else if (seg_ok && ctas < sm_count) seg_hi = 64;
+            const int64_t nch = nchunks > 0 ? nchunks : 1;   // L = 0: no chunk at all
+            for (int nseg0 = seg_lo; nseg0 <= seg_hi; ++nseg0) {
+            int64_t nseg = nseg0 > nch ? nch : nseg0;
+            if (nseg < 1) nseg = 1;
+            const int64_t seg_chunks = (nch + nseg - 1) / nseg;
+            nseg = (nch + seg_chunks - 1) / seg_chunks;
+            const double frac = (double)seg_chunks / (double)nch;
+            double cost = bwd_launch_cost(ctas * nseg, sm_count, W, work * frac);
+            if (nseg > 1)
+                cost = 1.04 * cost + 0.25 * bwd_launch_cost(ctas * (nseg - 1), sm_count, W, work * frac);
             if (best < 0.0 || cost < best * 0.999) {
                 best = cost;
                 pl.NT = NT; pl.W = W; pl.CH = CH;
+                pl.nseg = (int)nseg;
+                pl.seg_chunks = seg_chunks;
                 int sf = (int)(((size_t)kMaxSmemPerCta - fixed) / stf);
                 int sr = (int)(((size_t)kMaxSmemPerCta - fixed) / str);
                 pl.stages_f = sf > 4 ? 4 : sf;
                 pl.stages_r = sr > 4 ? 4 : sr;
                 pl.smem_f = (size_t)pl.stages_f * stf + fixed;
                 pl.smem_r = (size_t)pl.stages_r * str + fixed;
+                // the adjoint summary: the forward sweep's tiles, no buffers
+                int sl = (int)(((size_t)kMaxSmemPerCta - 1024) / stf);
+                pl.stages_l = sl > 4 ? 4 : sl;
+                pl.smem_l = (size_t)pl.stages_l * stf + 1024;
+            }
             }
         }
     }
@@ -358,10 +398,31 @@ BwdPlan plan_bwd(const ssm_shape& s, int sm_count) {
     // h-dependent term of ddelta from it directly)
     pl.off_hprev = off;
     if (s.in_dtype == SSM_F32) off += align256((size_t)s.batch * s.dim * s.seqlen * pl.NP * 4);
+    if (pl.nseg > 1) {
+        const size_t st = (size_t)pl.nseg * s.batch * s.dim * pl.NP * 4;
+        const size_t sd = (size_t)pl.nseg * s.batch * s.dim * 4;
+        // the forward summary pass on the tiles of the forward's own segmented plan
+        const FwdPlan fp = plan_fwd(s, sm_count, true);
+        pl.fwd_tiles = (int)((s.dim + fp.CH - 1) / fp.CH);
+        const int64_t bwd_tiles = (s.dim + pl.CH - 1) / pl.CH;
+        pl.off_hin = off;    off += align256(st);
+        pl.off_hloc = off;   off += align256(st);
+        pl.off_sumd = off;   off += align256(sd);
+        pl.off_tstart = off; off += align256((size_t)pl.nseg * s.batch * pl.fwd_tiles * 4);
+        pl.off_lamloc = off; off += align256(st);
+        pl.off_lamin = off;  off += align256(st);
+        pl.off_sumdr = off;  off += align256(sd);
+        pl.off_kstop = off;  off += align256((size_t)pl.nseg * s.batch * bwd_tiles * 4);
+        pl.off_gp = off;     off += align256(st);
+        pl.off_mend = off;   off += align256(st);
+    } else {
+        pl.seg_chunks = nchunks;
+    }
     pl.bytes = off;
     if (env_int("SSM_DEBUG_PLAN", 0))
-        std::fprintf(stderr, "ssm bwd plan: NP=%d NT=%d W=%d CH=%d stages=%d/%d smem=%zu/%zu\n",
-                     pl.NP, pl.NT, pl.W, pl.CH, pl.stages_f, pl.stages_r, pl.smem_f, pl.smem_r);
+        std::fprintf(stderr, "ssm bwd plan: NP=%d NT=%d W=%d CH=%d stages=%d/%d/%d smem=%zu/%zu/%zu nseg=%d x %lld\n",
+                     pl.NP, pl.NT, pl.W, pl.CH, pl.stages_f, pl.stages_r, pl.stages_l, pl.smem_f,
+                     pl.smem_r, pl.smem_l, pl.nseg, (long long)pl.seg_chunks);
     return pl;
 }
 
@@ -838,7 +899,8 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const BwdPlan pl = plan_bwd(s, device_sm_count());
+    const int sms = device_sm_count();
+    const BwdPlan pl = plan_bwd(s, sms, !varlen);
     if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
     // packed sequences: built for 9..16 states and 16-byte token rows
     if (varlen && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
@@ -924,6 +986,79 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         lc.smem_f = pl.smem_f;
         lc.smem_r = pl.smem_r;
         if (launch_bwd_varlen_np16(pl.NT, s.in_dtype, s.out_dtype, p, maps, lc, st) != cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
+    if (pl.nseg > 1) {
+        // segmented plan: initial states (the forward's tail search, summary
+        // pass and carry, on its own tiles), the adjoint entering every
+        // segment (adjoint summary, right-to-left carry), the forward sweep,
+        // the tangent's dA terms across segments, the reverse sweep
+        FwdPlan fp = plan_fwd(s, sms, true);
+        fp.nseg = pl.nseg;
+        fp.seg_chunks = pl.seg_chunks;
+        FwdMaps fm;
+        std::memset(&fm, 0, sizeof(fm));
+        fm.bc = maps.bc;
+        const uint32_t box_t = 128 / eb;
+        if (!make_map(&fm.u, u, tdt, eb, L, Bt * Dm, box_t, fp.CH, true) ||
+            !make_map(&fm.dr, delta_raw, tdt, eb, L, Bt * Dm, box_t, fp.CH, true) ||
+            (z && !make_map(&fm.z, z, tdt, eb, L, Bt * Dm, box_t, fp.CH, true)))
+            return cuda_fail();
+        FwdParams pf;
+        std::memset(&pf, 0, sizeof(pf));
+        pf.Bt = Bt; pf.D = Dm; pf.L = L; pf.N = (int)N;
+        pf.u = u; pf.dr = delta_raw; pf.z = z; pf.A = A; pf.Dv = D; pf.bias = delta_bias;
+        pf.h0 = h0; pf.bc = bc;
+        pf.seg_chunks = pl.seg_chunks;
+        pf.nseg = pl.nseg;
+        pf.stages = fp.stages;
+        pf.status = status;
+        pf.timeout_ns = kDefaultTimeoutNs;
+        pf.hin = reinterpret_cast<float*>(ws + pl.off_hin);
+        pf.hloc = reinterpret_cast<float*>(ws + pl.off_hloc);
+        pf.sumd = reinterpret_cast<float*>(ws + pl.off_sumd);
+        int* tstart = reinterpret_cast<int*>(ws + pl.off_tstart);
+        const unsigned gxf = (unsigned)pl.fwd_tiles;
+        FwdParams pf1 = pf;
+        pf1.hin = nullptr;
+        pf1.tstart = tstart;
+        if (launch_tail(s.in_dtype, pf, fp.CH, gxf, tstart, pf.sumd, st) != cudaSuccess ||
+            launch_fwd(fp, s.in_dtype, s.out_dtype, true, false, false, pf1, fm,
+                       dim3(gxf, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess ||
+            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, pf.hloc, pf.sumd, pf.hin, st) !=
+                cudaSuccess)
+            return cuda_fail();
+
+        p.seg_chunks = pl.seg_chunks;
+        p.nseg = pl.nseg;
+        p.hin = pf.hin;
+        p.lam_loc = reinterpret_cast<float*>(ws + pl.off_lamloc);
+        float* lam_in = reinterpret_cast<float*>(ws + pl.off_lamin);
+        p.lam_in = lam_in;
+        p.sumd = reinterpret_cast<float*>(ws + pl.off_sumdr);
+        p.gp = reinterpret_cast<float*>(ws + pl.off_gp);
+        p.mend = reinterpret_cast<float*>(ws + pl.off_mend);
+        BwdLaunch lc;
+        lc.grid = dim3(gx, (unsigned)Bt, (unsigned)pl.nseg);
+        lc.warps = pl.W;
+        lc.stages_f = pl.stages_f;
+        lc.stages_r = pl.stages_r;
+        lc.stages_l = pl.stages_l;
+        lc.smem_f = pl.smem_f;
+        lc.smem_r = pl.smem_r;
+        lc.smem_l = pl.smem_l;
+        int* kstop = reinterpret_cast<int*>(ws + pl.off_kstop);
+        if (launch_head(s.in_dtype, p, pl.CH, gx, kstop, p.sumd, st) != cudaSuccess)
+            return cuda_fail();
+        p.kstop = kstop;
+        if (launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 0, p, maps, lc, st) != cudaSuccess ||
+            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, dhL, p.lam_loc, p.sumd, lam_in, st,
+                         true) != cudaSuccess ||
+            launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 1, p, maps, lc, st) != cudaSuccess ||
+            launch_tangent_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, pf.sumd, p.mend, p.gp, dA, st) !=
+                cudaSuccess ||
+            launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 2, p, maps, lc, st) != cudaSuccess)
             return cuda_fail();
         return SSM_OK;
     }

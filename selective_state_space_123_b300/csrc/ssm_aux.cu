@@ -2,9 +2,11 @@
 //   * prep_bc:   B, C (batch, N, L) -> fp32 (batch, L, 2*NP) with ln2 folded
 //                into B (the scan then uses delta/ln2 throughout);
 //   * tail:      where each segment's summary pass may start (segmented plan);
+//   * head:      where the segmented backward's adjoint summary may stop;
 //   * carry:     per-segment initial states of the segmented forward,
 //                h_in[s+1] = 2^(A * sum_delta2[s]) * h_in[s] + h_loc[s];
 //   * varlen_prep: checks packed-sequence starts, final states of empty ones;
+//   * tangent carry: the segmented backward's dA terms across segments;
 //   * expired_wait: the failure-detection self test (a wait nothing ends).
 #include "ssm_common.cuh"
 #include "ssm_kernels.cuh"
@@ -224,6 +226,103 @@ __global__ void __launch_bounds__(1024) tail_kernel(const FwdParams p, int CH, i
         tstart[((int64_t)seg * p.Bt + b) * gridDim.x + tile] = (int)c_begin + cmin;
 }
 
+// The mirror for the backward's adjoint summary: the adjoint a segment
+// passes to its left neighbour, a_{t0} lambda_{t0}, weighs token t's g_t C_t
+// by the decay from t0 through t, 2^(A_n * S'_t) with S'_t = sum of delta2
+// over tokens t0 .. t; once the slowest state's decay is below 2^-kTailLog2
+// the later tokens do not matter.  The search walks delta forward from each
+// segment's start (one warp per channel) and writes per (segment, batch
+// row, channel tile) the chunk after the last one any channel of the tile
+// needs, and per saturated channel kTailSat into sumd (the carry then drops
+// the adjoint entering the segment from the right).  Segments 1 .. nseg-1
+// (the last one may end with a partial chunk); L * sizeof(TIN) % 16 == 0.
+template <typename TIN>
+__global__ void __launch_bounds__(1024) head_kernel(const BwdParams p, int CH, int* __restrict__ kstop,
+                                                    float* __restrict__ sumd) {
+    constexpr bool ACCURATE = sizeof(TIN) == 4;
+    constexpr int VEC = 16 / (int)sizeof(TIN);        // tokens per 16-byte load
+    constexpr int LOADS = 4;                            // loads per lane per step
+    constexpr int STEP = LOADS * 32 * VEC;              // tokens per warp step
+    const int tile = blockIdx.x;
+    const int64_t b = blockIdx.y;
+    const int seg = blockIdx.z + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t nchunks = (p.L + kT - 1) / kT;
+    const int64_t c_begin = (int64_t)seg * p.seg_chunks;
+    const int64_t c_end = min(nchunks, c_begin + p.seg_chunks);
+    const int64_t s0 = c_begin * kT, s1 = min(p.L, c_end * kT);
+    __shared__ int cmax;
+    if (threadIdx.x == 0) cmax = 0;
+    __syncthreads();
+    const TIN* dr = static_cast<const TIN*>(p.dr);
+    const int whole = (int)(c_end - c_begin);           // chunk counts from the segment's start
+    int my_max = 0;
+    for (int c = warp; c < CH; c += nwarps) {
+        const int64_t d = (int64_t)tile * CH + c;
+        if (d >= p.D) break;
+        if (*reinterpret_cast<volatile int*>(&cmax) == whole) break;   // the tile needs its whole segment
+        const int64_t row = b * p.D + d;
+        float amax = -INFINITY;
+        for (int n = 0; n < p.N; ++n) amax = fmaxf(amax, p.A[d * p.N + n]);
+        const float bias2 = p.bias ? p.bias[d] * kLog2e : 0.0f;
+        const TIN* rp = dr + row * p.L;
+        double tot = 0.0;
+        int64_t t1 = s1;
+        bool sat = false;
+        for (int64_t lo = s0; lo < s1; lo += STEP) {
+            const int64_t hi = lo + STEP < s1 ? lo + STEP : s1;
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < LOADS; ++j) {
+                const int64_t t = lo + (int64_t)(j * 32 + lane) * VEC;
+                if (t < hi) {
+                    float v[VEC];
+                    if constexpr (sizeof(TIN) == 2) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(rp + t);
+                        v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+                        v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+                    } else {
+                        const float4 w = *reinterpret_cast<const float4*>(rp + t);
+                        v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+                    }
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q)
+                        if (t + q < hi) part += softplus2<ACCURATE>(fmaf(v[q], kLog2e, bias2));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            tot += (double)part;
+            if (amax < 0.0f && (double)amax * tot <= -(double)kTailLog2) {
+                t1 = hi;
+                sat = true;
+                break;
+            }
+        }
+        const int need = (int)((t1 - s0 + kT - 1) / kT);
+        if (need > my_max) my_max = need;
+        if (lane == 0) {
+            if (sat) sumd[(int64_t)seg * p.Bt * p.D + row] = kTailSat;
+            if (need == whole) atomicMax(&cmax, whole);
+        }
+    }
+    if (lane == 0) atomicMax(&cmax, my_max);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        kstop[((int64_t)seg * p.Bt + b) * gridDim.x + tile] = (int)c_begin + cmax;
+}
+
+cudaError_t launch_head(int tin, const BwdParams& p, int CH, unsigned tiles, int* kstop, float* sumd,
+                        cudaStream_t st) {
+    const dim3 grid(tiles, (unsigned)p.Bt, (unsigned)(p.nseg - 1));
+    if (tin == SSM_BF16)
+        head_kernel<__nv_bfloat16><<<grid, 1024, 0, st>>>(p, CH, kstop, sumd);
+    else
+        head_kernel<float><<<grid, 1024, 0, st>>>(p, CH, kstop, sumd);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int* tstart, float* sumd,
                         cudaStream_t st) {
     const dim3 grid(tiles, (unsigned)p.Bt, (unsigned)(p.nseg - 1));
@@ -240,6 +339,51 @@ cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const f
     const int64_t total = Bt * D * NP;
     carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Bt, D, N, NP, nseg, A, h0, hloc,
                                                                   sumd, hin, reverse);
+    return cudaGetLastError();
+}
+
+
+// ------------------------------------------------------ tangent carry ---
+// Segmented backward: the forward sweep runs segment s with the tangent
+// m = dh/dA (in units of 1/ln2) from zero, so the tangent of the whole
+// sequence there is m_loc + P * m_in[s], with P the decay since the
+// segment's start and m_in[s] = m_end[s-1] + 2^(A sumd[s-1]) m_in[s-1],
+// m_in[0] = 0 (sumd = the forward summary's sum of delta/ln2, kTailSat where
+// the decay is below fp32 resolution).  The missing dA terms are
+// sum_s m_in[s] * gp[s] (gp = sum_t g_t C_t P_t, plus dhL P_L in the last
+// segment), summed over the batch rows: one thread per (channel, state),
+// added after the sweep's own atomics on the same stream.
+__global__ void tangent_carry_kernel(int64_t Bt, int64_t D, int N, int NP, int nseg,
+                                     const float* __restrict__ A, const float* __restrict__ sumd,
+                                     const float* __restrict__ mend, const float* __restrict__ gp,
+                                     float* __restrict__ dA) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (d, n)
+    if (i >= D * N) return;
+    const int64_t d = i / N;
+    const int n = (int)(i % N);
+    const float a = A[i];
+    const int64_t seg_stride = Bt * D;
+    float acc = 0.0f;
+    for (int64_t b = 0; b < Bt; ++b) {
+        const int64_t row = b * D + d;
+        float m = 0.0f;
+        for (int s = 1; s < nseg; ++s) {
+            const int64_t prev = (int64_t)(s - 1) * seg_stride + row;
+            const float sd = sumd[prev];
+            m = fmaf(sd >= kTailSat ? 0.0f : ex2(a * sd), m, mend[prev * NP + n]);
+            acc = fmaf(m, gp[((int64_t)s * seg_stride + row) * NP + n], acc);
+        }
+    }
+    dA[i] += kLn2 * acc;
+}
+
+cudaError_t launch_tangent_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
+                                 const float* sumd, const float* mend, const float* gp, float* dA,
+                                 cudaStream_t st) {
+    const int64_t total = D * N;
+    if (total == 0 || nseg < 2) return cudaSuccess;
+    tangent_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Bt, D, N, NP, nseg, A, sumd,
+                                                                          mend, gp, dA);
     return cudaGetLastError();
 }
 

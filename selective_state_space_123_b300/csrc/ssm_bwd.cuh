@@ -108,9 +108,9 @@ __device__ __forceinline__ void transpose_reduce(const float* tb, float* redw, i
 }
 
 // Issue the loads of one stage (producer warp).  Raw tiles at slots 0..3
-// (u, delta_raw, z, dy) of RAW bytes each, then (reverse sweep) the fp32
-// per-token tile of RAWF bytes, then the B/C tile.
-template <typename TIN, int NP, bool REV, bool TMA_RAW>
+// (u, delta_raw, z, dy) of RAW bytes each, then (PHI: the reverse sweep) the
+// fp32 per-token tile of RAWF bytes, then the B/C tile.
+template <typename TIN, int NP, bool PHI, bool TMA_RAW>
 __device__ __forceinline__ void bwd_load_stage(
     uint8_t* st, uint64_t* bar, const BwdParams& p, const CUtensorMap* tm_u,
     const CUtensorMap* tm_dr, const CUtensorMap* tm_z, const CUtensorMap* tm_dy,
@@ -124,10 +124,10 @@ __device__ __forceinline__ void bwd_load_stage(
     const int64_t L = p.L;
     const int32_t t0 = (int32_t)(k * kT);
     uint8_t* phi_dst = st + 4 * RAW;
-    uint8_t* bc_dst = st + 4 * RAW + (REV ? RAWF : 0);
+    uint8_t* bc_dst = st + 4 * RAW + (PHI ? RAWF : 0);
     if (TMA_RAW) {
         if (lane == 0) {
-            const uint32_t bytes = (has_z ? 4 : 3) * RAW + (REV ? RAWF : 0) + BCB;
+            const uint32_t bytes = (has_z ? 4 : 3) * RAW + (PHI ? RAWF : 0) + BCB;
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx) {
@@ -137,7 +137,7 @@ __device__ __forceinline__ void bwd_load_stage(
                 if (has_z) tma_load_2d(st + 2 * RAW + bx * CH * 128, tm_z, bar, x, (int32_t)row0);
                 tma_load_2d(st + 3 * RAW + bx * CH * 128, tm_dy, bar, x, (int32_t)row0);
             }
-            if (REV) {
+            if (PHI) {
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx)
                     tma_load_2d(phi_dst + bx * CH * 128, tm_phi, bar, t0 + bx * 32, (int32_t)row0);
@@ -149,7 +149,7 @@ __device__ __forceinline__ void bwd_load_stage(
         fill_raw_tile_r<TIN>(st + RAW, CH, p.dr, row0, rows_valid, L, t0, lane);
         if (has_z) fill_raw_tile_r<TIN>(st + 2 * RAW, CH, p.z, row0, rows_valid, L, t0, lane);
         fill_raw_tile_r<TIN>(st + 3 * RAW, CH, p.dy, row0, rows_valid, L, t0, lane);
-        if (REV) fill_raw_tile_r<float>(phi_dst, CH, p.phi, row0, rows_valid, L, t0, lane);
+        if (PHI) fill_raw_tile_r<float>(phi_dst, CH, p.phi, row0, rows_valid, L, t0, lane);
         __syncwarp();
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, BCB);
@@ -158,13 +158,14 @@ __device__ __forceinline__ void bwd_load_stage(
     }
 }
 
-// Producer warp: stream the chunks (forward or reverse order) through the
-// ring, and add each finished chunk's cross-channel sums (the W warps'
-// slices of the double-buffered chunk buffer) to `out` with vector atomics:
-// the flush of chunk i-1 follows the loads of chunk i, so the compute warps
-// never wait for it and never meet at a CTA barrier.  Gives up (status set)
-// if a bounded wait expires.
-template <typename TIN, int NP, bool REV, bool TMA_RAW>
+// Producer warp: stream the chunks k_begin .. k_end-1 (forward or reverse
+// order) through the ring, and add each finished chunk's cross-channel sums
+// (the W warps' slices of the double-buffered chunk buffer) to `out` with
+// vector atomics: the flush of chunk i-1 follows the loads of chunk i, so the
+// compute warps never wait for it and never meet at a CTA barrier (out null:
+// no sums, nothing to flush).  Gives up (status set) if a bounded wait
+// expires.
+template <typename TIN, int NP, bool REV, bool TMA_RAW, bool PHI = REV>
 __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAGE,
                                              uint64_t* full_bar, uint64_t* empty_bar,
                                              uint64_t* rfull, uint64_t* rempty, const float* red,
@@ -173,7 +174,8 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
                                              const CUtensorMap* tm_dr, const CUtensorMap* tm_z,
                                              const CUtensorMap* tm_dy, const CUtensorMap* tm_phi,
                                              const CUtensorMap* tm_bc, int64_t b, int64_t d0,
-                                             bool has_z, int lane, int CH) {
+                                             bool has_z, int lane, int CH, int64_t k_begin,
+                                             int64_t k_end) {
     if (lane == 0) {
         prefetch_tmap(tm_bc);
         if (TMA_RAW) {
@@ -181,11 +183,11 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
             prefetch_tmap(tm_dr);
             if (has_z) prefetch_tmap(tm_z);
             prefetch_tmap(tm_dy);
-            if (REV) prefetch_tmap(tm_phi);
+            if (PHI) prefetch_tmap(tm_phi);
         }
     }
     const int64_t L = p.L;
-    const int64_t nchunks = (L + kT - 1) / kT;
+    const int64_t nloc = k_end - k_begin;
     const int64_t row0 = b * p.D + d0;
     const int64_t rows_valid = (int64_t)min((int64_t)CH, p.D - d0);
     const int N = p.N;
@@ -197,15 +199,15 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
         if (lane == 0) ok = mbar_wait(&rfull[buf], (uint32_t)((i >> 1) & 1), p.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return false;
-        const int64_t k = REV ? nchunks - 1 - i : i;
+        const int64_t k = REV ? k_end - 1 - i : k_begin + i;
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
         flush_red<NP>(red + (size_t)buf * W * NP * kT, W, out, b, N, L, k * kT, nvalid, scale, lane, 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rempty[buf]);
         return true;
     };
-    for (int64_t i = 0; i < nchunks; ++i) {
-        const int64_t k = REV ? nchunks - 1 - i : i;
+    for (int64_t i = 0; i < nloc; ++i) {
+        const int64_t k = REV ? k_end - 1 - i : k_begin + i;
         const int s = (int)(i % STAGES);
         if (i >= STAGES) {
             bool ok = true;
@@ -217,15 +219,15 @@ __device__ __forceinline__ void bwd_producer(uint8_t* smem, int STAGES, int STAG
                 return;
             }
         }
-        bwd_load_stage<TIN, NP, REV, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr, tm_z,
+        bwd_load_stage<TIN, NP, PHI, TMA_RAW>(smem + s * STAGE, &full_bar[s], p, tm_u, tm_dr, tm_z,
                                               tm_dy, tm_phi, tm_bc, b, row0, rows_valid, k, has_z,
                                               lane, CH);
-        if (i >= 1 && !flush(i - 1)) {
+        if (out && i >= 1 && !flush(i - 1)) {
             if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
             return;
         }
     }
-    if (nchunks >= 1 && !flush(nchunks - 1)) {
+    if (out && nloc >= 1 && !flush(nloc - 1)) {
         if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
     }
 }
@@ -309,7 +311,14 @@ __device__ __forceinline__ uint32_t start_bits(const int* cu, int nseq, int64_t 
 // the ending sequence's dhL term enters dA, its psi = sum_n A dhL h_end is
 // added to phi of its last token (so the reverse sweep's suffix sum restarts
 // from zero there), and h, m start again from the new sequence's h0 and 0.
-template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false>
+// SEG: the sequence is cut into p.nseg segments (grid z), each run from its
+// initial state p.hin[seg] with the tangent m from zero; besides adding its
+// local dA terms, a segment records the tangent at its end (p.mend) and
+// GP = sum_t g_t C_t P_t (p.gp), P_t = the decay from the segment's start
+// through token t (plus dhL P_L in the last segment), from which a carry
+// adds the dA terms of the tangent flowing in from earlier segments.
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false,
+          bool SEG = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -322,6 +331,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     constexpr int BCB = bc_tile_bytes<NP>();
     constexpr bool ACCURATE = EB == 4;
     static_assert(G % 4 == 0 && G <= 16, "states per thread");
+    static_assert(!(SEG && VARLEN), "segments of packed sequences are not built");
 
     const int W = (int)(blockDim.x / 32) - 1;
     const int CH = W * CW;
@@ -346,6 +356,13 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t L = p.L;
     const int64_t nchunks = (L + kT - 1) / kT;
     const bool has_z = p.z != nullptr;
+    // this CTA's chunks: its segment's (all of them without segments)
+    const int seg = (int)blockIdx.z;
+    const int nseg = p.nseg > 1 ? p.nseg : 1;
+    const int64_t seg_chunks = p.nseg > 1 ? p.seg_chunks : nchunks;
+    const int64_t k_begin = (int64_t)seg * seg_chunks;
+    const int64_t k_end = min(nchunks, k_begin + seg_chunks);
+    const bool last_seg = seg == nseg - 1;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -363,7 +380,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (warp == W) {
         bwd_producer<TIN, NP, false, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, rfull, rempty,
                                               red, W, p.dC, 1.0f, p, &tm_u, &tm_dr, &tm_z, &tm_dy,
-                                              nullptr, &tm_bc, b, d0, has_z, lane, CH);
+                                              nullptr, &tm_bc, b, d0, has_z, lane, CH, k_begin, k_end);
         return;
     }
 
@@ -380,20 +397,34 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t seq_stride = p.Bt * p.D * (int64_t)N;
     const int s_first = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, 0) : 0;
     f2 Ap[G / 2], h[G / 2], m[G / 2], dAc[G / 2];
+    f2 hl[ACCURATE ? G / 2 : 1];                     // fp32 inputs: low parts of the compensated state
+    f2 Pd[SEG ? G / 2 : 1], GP[SEG ? G / 2 : 1];   // SEG: decay since the segment start, sum g C P
 #pragma unroll
     for (int j = 0; j < G / 2; ++j) {
         const int n0 = g * G + 2 * j, n1 = n0 + 1;
         Ap[j] = pk((ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f,
                    (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f);
         float h0v = 0.0f, h1v = 0.0f;
-        if (ch_ok && p.h0) {
+        if (SEG && seg > 0) {
+            // the segment's initial state (padded states are zero there)
+            if (ch_ok) {
+                const float* hs = p.hin + ((int64_t)seg * p.Bt * p.D + row) * NP;
+                h0v = hs[n0];
+                h1v = hs[n1];
+            }
+        } else if (ch_ok && p.h0) {
             const float* hs = p.h0 + (int64_t)s_first * seq_stride;
             if (n0 < N) h0v = hs[row * N + n0];
             if (n1 < N) h1v = hs[row * N + n1];
         }
         h[j] = pk(h0v, h1v);
+        if constexpr (ACCURATE) hl[j] = pk(0.0f, 0.0f);
         m[j] = pk(0.0f, 0.0f);
         dAc[j] = pk(0.0f, 0.0f);
+        if constexpr (SEG) {
+            Pd[j] = pk(1.0f, 1.0f);
+            GP[j] = pk(0.0f, 0.0f);
+        }
     }
     const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
     const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
@@ -407,21 +438,27 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     // suffix sum with it.  With fp32 inputs the state before every token is
     // stored as well (the reverse sweep forms the h-dependent term of ddelta
     // from it directly).
+    // the full state of pair j (hi + lo for fp32 inputs)
+    auto full = [&](int j) -> f2 {
+        if constexpr (ACCURATE) return add2(h[j], hl[j]);
+        else return h[j];
+    };
     auto store_anchor = [&](int64_t a) {
         float4* hc = reinterpret_cast<float4*>(p.hck + (row * nchunks + a) * NP + g * G);
 #pragma unroll
         for (int j = 0; j < G / 4; ++j) {
             float x0, x1, x2, x3;
-            upk(h[2 * j], x0, x1);
-            upk(h[2 * j + 1], x2, x3);
+            upk(full(2 * j), x0, x1);
+            upk(full(2 * j + 1), x2, x3);
             hc[j] = make_float4(x0, x1, x2, x3);
         }
     };
-    for (int64_t k = 0; k < nchunks; ++k) {
-        const int s = (int)(k % STAGES);
+    for (int64_t kl = 0; kl < k_end - k_begin; ++kl) {
+        const int64_t k = k_begin + kl;        // the chunk; kl its place in this CTA's ring
+        const int s = (int)(kl % STAGES);
         if (!dead) {
             const bool ok = __all_sync(
-                0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((k / STAGES) & 1), p.timeout_ns));
+                0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((kl / STAGES) & 1), p.timeout_ns));
             if (!ok) {
                 if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
                 dead = true;
@@ -430,11 +467,11 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const uint8_t* st = smem + s * STAGE;
         const float* bct = reinterpret_cast<const float*>(st + 4 * RAW);
         const int nvalid = (int)min((int64_t)kT, L - k * kT);
-        // this chunk's cross-channel sums go to chunk buffer (k & 1), free once
+        // this chunk's cross-channel sums go to chunk buffer (kl & 1), free once
         // the producer has added up the chunk processed two before
-        const int rb = (int)(k & 1);
-        if (!dead && k >= 2) {
-            const bool okr = __all_sync(0xffffffffu, mbar_wait(&rempty[rb], (uint32_t)(((k >> 1) - 1) & 1), p.timeout_ns));
+        const int rb = (int)(kl & 1);
+        if (!dead && kl >= 2) {
+            const bool okr = __all_sync(0xffffffffu, mbar_wait(&rempty[rb], (uint32_t)(((kl >> 1) - 1) & 1), p.timeout_ns));
             if (!okr) {
                 if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
                 dead = true;
@@ -469,9 +506,10 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     const f2 dhp = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
                     dAc[jj] = fma2(dhp, m[jj], dAc[jj]);          // dhL[se] . dh/dA
                     float x0, x1;
-                    upk(mul2(mul2(Ap[jj], dhp), h[jj]), x0, x1);  // A dhL[se] h_end
+                    upk(mul2(mul2(Ap[jj], dhp), full(jj)), x0, x1);  // A dhL[se] h_end
                     psi += x0 + x1;
                     h[jj] = pk((hs && n0 < N) ? hs[n0] : 0.0f, (hs && n0 + 1 < N) ? hs[n0 + 1] : 0.0f);
+                    if constexpr (ACCURATE) hl[jj] = pk(0.0f, 0.0f);
                     m[jj] = pk(0.0f, 0.0f);
                 }
 #pragma unroll
@@ -515,8 +553,8 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
                         for (int jj = 0; jj < G / 4; ++jj) {
                             float x0, x1, x2, x3;
-                            upk(h[2 * jj], x0, x1);
-                            upk(h[2 * jj + 1], x2, x3);
+                            upk(full(2 * jj), x0, x1);
+                            upk(full(2 * jj + 1), x2, x3);
                             hp[jj] = make_float4(x0, x1, x2, x3);
                         }
                     }
@@ -533,15 +571,40 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             const int jj = 2 * q4 + e;
                             const f2 Bj = e ? Bq.y : Bq.x;
                             const f2 Cj = e ? Cq.y : Cq.x;
-                            const f2 arg = mul2(d2p, Ap[jj]);
-                            const f2 a = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
-                            const f2 qv = mul2(a, h[jj]);            // a_t h_{t-1}
-                            h[jj] = fma2(dup, Bj, qv);
+                            f2 a, qv, hn;   // the decay, a_t h_{t-1} and h_t
+                            if constexpr (ACCURATE) {
+                                // compensated state (see comp_update): qv and
+                                // h_t from the full state hi + lo
+                                float x0, x1, i0, i1, h0, h1, l0, l1;
+                                upk(mul2(d2p, Ap[jj]), x0, x1);
+                                upk(mul2(dup, Bj), i0, i1);
+                                upk(h[jj], h0, h1);
+                                upk(hl[jj], l0, l1);
+                                const float e0 = exp2m1_accurate(x0), e1 = exp2m1_accurate(x1);
+                                const float p0 = h0 + l0, p1 = h1 + l1;
+                                qv = pk(fmaf(e0, p0, p0), fmaf(e1, p1, p1));
+                                a = pk(1.0f + e0, 1.0f + e1);
+                                comp_update_e(e0, i0, h0, l0);
+                                comp_update_e(e1, i1, h1, l1);
+                                h[jj] = pk(h0, h1);
+                                hl[jj] = pk(l0, l1);
+                                hn = pk(h0 + l0, h1 + l1);
+                            } else {
+                                a = ex2x2(mul2(d2p, Ap[jj]));
+                                qv = mul2(a, h[jj]);
+                                h[jj] = fma2(dup, Bj, qv);
+                                hn = h[jj];
+                            }
                             m[jj] = fma2(a, m[jj], mul2(d2p, qv));   // dh/dA / ln2
-                            accy = fma2(Cj, h[jj], accy);
+                            accy = fma2(Cj, hn, accy);
                             accp = fma2(Ap[jj], mul2(Cj, qv), accp);
-                            dAc[jj] = fma2(mul2(gqp, Cj), m[jj], dAc[jj]);
-                            gh[jj] = mul2(gqp, h[jj]);               // g_t h_t: dC partial
+                            const f2 gC = mul2(gqp, Cj);
+                            dAc[jj] = fma2(gC, m[jj], dAc[jj]);
+                            if constexpr (SEG) {
+                                Pd[jj] = mul2(a, Pd[jj]);
+                                GP[jj] = fma2(gC, Pd[jj], GP[jj]);
+                            }
+                            gh[jj] = mul2(gqp, hn);                  // g_t h_t: dC partial
                         }
                     }
                     put_tr<NT, NP>(tb + q * Lay::TROW, lane, gh);
@@ -597,22 +660,37 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     }
 
     if (ch_ok && !dead) {
-        // the last sequence's final-state gradient (packed: the one holding token L-1)
+        // the last sequence's final-state gradient (packed: the one holding
+        // token L-1); with segments only the last segment holds it
         const int s_last = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, L - 1) : 0;
-        const float* dhl = p.dhL ? p.dhL + (int64_t)s_last * seq_stride + row * N : nullptr;
+        const float* dhl = (p.dhL && last_seg) ? p.dhL + (int64_t)s_last * seq_stride + row * N : nullptr;
+        const int64_t segrow = ((int64_t)seg * p.Bt * p.D + row) * NP;
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) {
             const int n0 = g * G + 2 * j;
             float hl0, hl1, m0, m1, a0, a1;
-            upk(h[j], hl0, hl1);
+            upk(full(j), hl0, hl1);
             upk(m[j], m0, m1);
             upk(dAc[j], a0, a1);
-            p.hfin[row * NP + n0] = hl0;
-            p.hfin[row * NP + n0 + 1] = hl1;
+            if (last_seg) {
+                p.hfin[row * NP + n0] = hl0;
+                p.hfin[row * NP + n0 + 1] = hl1;
+            }
             const float g0 = (dhl && n0 < N) ? dhl[n0] : 0.0f;
             const float g1 = (dhl && n0 + 1 < N) ? dhl[n0 + 1] : 0.0f;
             if (n0 < N) atomicAdd(p.dA + d * N + n0, kLn2 * fmaf(g0, m0, a0));
             if (n0 + 1 < N) atomicAdd(p.dA + d * N + n0 + 1, kLn2 * fmaf(g1, m1, a1));
+            if constexpr (SEG) {
+                // the carry's inputs: the tangent at this segment's end, and
+                // sum g C P (+ dhL P_L) against the tangent flowing in
+                float p0, p1, q0, q1;
+                upk(Pd[j], p0, p1);
+                upk(GP[j], q0, q1);
+                p.mend[segrow + n0] = m0;
+                p.mend[segrow + n0 + 1] = m1;
+                p.gp[segrow + n0] = fmaf(g0, p0, q0);
+                p.gp[segrow + n0 + 1] = fmaf(g1, p1, q1);
+            }
         }
     }
 }
@@ -622,6 +700,11 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 // the next token is replaced by that sequence's dhL (after the next
 // sequence's dh0 = a lambda has been written), and the suffix sum restarts
 // from zero there (the ending sequence's psi is already in phi of that token).
+// Segments (p.nseg > 1, grid z): a segment other than the last starts from
+// the adjoint flowing in at its right end, p.lam_in[seg] = a_{t1} lambda_{t1}
+// (t1 = the next segment's first token; the decay "after" the segment's
+// last token is then 1), and its suffix sum from sum_n A lam_in h_{t1-1},
+// with h_{t1-1} the forward sweep's state at the end of its last chunk.
 template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
@@ -661,6 +744,13 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t L = p.L;
     const int64_t nchunks = (L + kT - 1) / kT;
     const bool has_z = p.z != nullptr;
+    // this CTA's chunks: its segment's (all of them without segments)
+    const int seg = (int)blockIdx.z;
+    const int nseg = p.nseg > 1 ? p.nseg : 1;
+    const int64_t seg_chunks = p.nseg > 1 ? p.seg_chunks : nchunks;
+    const int64_t k_begin = (int64_t)seg * seg_chunks;
+    const int64_t k_end = min(nchunks, k_begin + seg_chunks);
+    const bool last_seg = seg == nseg - 1;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -678,7 +768,7 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     if (warp == W) {
         bwd_producer<TIN, NP, true, TMA_RAW>(smem, STAGES, STAGE, full_bar, empty_bar, rfull, rempty,
                                               red, W, p.dB, kLn2, p, &tm_u, &tm_dr, &tm_z, &tm_dy,
-                                              &tm_phi, &tm_bc, b, d0, has_z, lane, CH);
+                                              &tm_phi, &tm_bc, b, d0, has_z, lane, CH, k_begin, k_end);
         return;
     }
 
@@ -697,6 +787,10 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const int64_t seq_stride = p.Bt * p.D * (int64_t)N;
     const int s_last = VARLEN ? seq_of_token(p.cu_seqlens, p.nseq, L - 1) : 0;
     const float* dhl_last = p.dhL ? p.dhL + (int64_t)s_last * seq_stride : nullptr;
+    // the state after this CTA's last token: the final state, or the forward
+    // sweep's state at the end of the segment's last chunk
+    const float* hend = last_seg ? p.hfin + row * NP : p.hck + (row * nchunks + (k_end - 1)) * NP;
+    const float* lin = last_seg ? nullptr : p.lam_in + ((int64_t)seg * p.Bt * p.D + row) * NP;
     f2 Ap[G / 2], lam[G / 2], anext[G / 2];
     float psi = 0.0f;
 #pragma unroll
@@ -706,13 +800,16 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         const float a1 = (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f;
         Ap[j] = pk(a0, a1);
         float l0 = 0.0f, l1 = 0.0f;
-        if (ch_ok && dhl_last) {
+        if (ch_ok && lin) {
+            l0 = lin[n0];
+            l1 = lin[n1];
+        } else if (ch_ok && dhl_last) {
             if (n0 < N) l0 = dhl_last[row * N + n0];
             if (n1 < N) l1 = dhl_last[row * N + n1];
         }
         lam[j] = pk(l0, l1);
         anext[j] = pk(1.0f, 1.0f);
-        if (ch_ok) psi += a0 * l0 * p.hfin[row * NP + n0] + a1 * l1 * p.hfin[row * NP + n1];
+        if (ch_ok) psi += a0 * l0 * hend[n0] + a1 * l1 * hend[n1];
     }
 #pragma unroll
     for (int o = 1; o < NT; o <<= 1) psi += __shfl_xor_sync(0xffffffffu, psi, o);
@@ -749,8 +846,8 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         return part;
     };
 
-    for (int64_t i = 0; i < nchunks; ++i) {
-        const int64_t k = nchunks - 1 - i;
+    for (int64_t i = 0; i < k_end - k_begin; ++i) {
+        const int64_t k = k_end - 1 - i;       // the chunk; i its place in this CTA's ring
         const int s = (int)(i % STAGES);
         if (!dead) {
             const bool ok = __all_sync(
@@ -972,7 +1069,7 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if (p.dD) atomicAdd(p.dD + d, dD_acc);
             if (p.dbias) atomicAdd(p.dbias + d, db_acc);
         }
-        if (p.dh0) {
+        if (p.dh0 && seg == 0) {
             // packed: dh0 of the sequence holding token 0
             float* d0p = p.dh0 + (VARLEN ? (int64_t)seq_of_token(p.cu_seqlens, p.nseq, 0) * seq_stride : 0);
 #pragma unroll
@@ -984,6 +1081,172 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 if (n0 + 1 < N) d0p[row * N + n0 + 1] = v1;
             }
         }
+    }
+}
+
+
+// ============================================ adjoint summary (segments) ===
+// For segment seg = blockIdx.z + 1 (segments 1 .. nseg-1): the reverse
+// recurrence lambda_t = g_t C_t + a_{t+1} lambda_{t+1} from zero at the
+// segment's right end down to its first token t0, giving
+// p.lam_loc[seg] = a_{t0} lambda_{t0} (what the segment passes to its left
+// neighbour from a zero start), and p.sumd[seg], the segment's sum of
+// delta/ln2 (its total decay is 2^(A sumd)).  A carry over the segments, from
+// the last one down, then gives every segment the adjoint flowing in at its
+// right end.  Same tiles and ring as the reverse sweep, without the per-token
+// tile; nothing but the recurrence per state.  With a head search (p.kstop)
+// the summary starts at the chunk where the decay from the segment's start
+// has fallen below fp32 resolution for every channel of the tile; the sum
+// of delta2 is then the search's (saturation marks) unless the whole segment
+// ran.
+template <int NP, int NT, typename TIN, bool TMA_RAW>
+__global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
+bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
+               const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_bc) {
+    using Lay = BwdLayout<NT, NP>;
+    constexpr int G = Lay::G;
+    constexpr int CW = Lay::CW;
+    constexpr int SB = Lay::SB;
+    constexpr int EB = (int)sizeof(TIN);
+    constexpr int BCB = bc_tile_bytes<NP>();
+    constexpr bool ACCURATE = EB == 4;
+    static_assert(G % 4 == 0 && G <= 16, "states per thread");
+
+    const int W = (int)(blockDim.x / 32) - 1;
+    const int CH = W * CW;
+    const int RAW = CH * kT * EB;
+    const int STAGE = 4 * RAW + BCB;
+    const int STAGES = p.stages;
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = align_smem_1024(smem_dyn);
+    __shared__ __align__(8) uint64_t full_bar[kFwdMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kFwdMaxStages];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int64_t L = p.L;
+    const int64_t nchunks = (L + kT - 1) / kT;
+    const bool has_z = p.z != nullptr;
+    const int seg = (int)blockIdx.z + 1;
+    const int64_t k_begin = (int64_t)seg * p.seg_chunks;
+    const int64_t k_seg_end = min(nchunks, k_begin + p.seg_chunks);
+    const int64_t k_end = p.kstop ? min(k_seg_end, (int64_t)p.kstop[((int64_t)seg * p.Bt + b) * gridDim.x + blockIdx.x])
+                                  : k_seg_end;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], W);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        bwd_producer<TIN, NP, true, TMA_RAW, false>(smem, STAGES, STAGE, full_bar, empty_bar, nullptr,
+                                                     nullptr, nullptr, W, nullptr, 0.0f, p, &tm_u,
+                                                     &tm_dr, &tm_z, &tm_dy, nullptr, &tm_bc, b, d0,
+                                                     has_z, lane, CH, k_begin, k_end);
+        return;
+    }
+
+    const int cw = lane / NT;
+    const int g = lane % NT;
+    const int c = warp * CW + cw;
+    const int64_t d = d0 + c;
+    const bool ch_ok = d < p.D;
+    const int64_t row = b * p.D + d;
+    const int N = p.N;
+    f2 Ap[G / 2], lam[G / 2], anext[G / 2];
+#pragma unroll
+    for (int j = 0; j < G / 2; ++j) {
+        const int n0 = g * G + 2 * j, n1 = n0 + 1;
+        Ap[j] = pk((ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f,
+                   (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f);
+        lam[j] = pk(0.0f, 0.0f);
+        anext[j] = pk(1.0f, 1.0f);
+    }
+    const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
+    const int src_base = lane & ~(NT - 1);
+    double sum_d2 = 0.0;   // this lane's own tokens
+    bool dead = false;
+
+    for (int64_t i = 0; i < k_end - k_begin; ++i) {
+        const int64_t k = k_end - 1 - i;
+        const int s = (int)(i % STAGES);
+        if (!dead) {
+            const bool ok = __all_sync(
+                0xffffffffu, mbar_wait(&full_bar[s], (uint32_t)((i / STAGES) & 1), p.timeout_ns));
+            if (!ok) {
+                if (lane == 0) set_status(p.status, SSM_ERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        const uint8_t* st = smem + s * STAGE;
+        const float* bct = reinterpret_cast<const float*>(st + 4 * RAW);
+        const int nvalid = (int)min((int64_t)kT, L - k * kT);
+#pragma unroll 1
+        for (int sb = kT / SB - 1; sb >= 0; --sb) {
+            if (dead) break;
+            if (sb * SB >= nvalid) continue;
+            const int tbk = sb * SB + g * 8;
+            float d2[8], du[8], gq[8];
+            token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            float s8 = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) s8 += d2[q];
+            sum_d2 += (double)s8;
+#pragma unroll 1
+            for (int j = NT - 1; j >= 0; --j) {
+                const int src = src_base + j;
+                float D2[8], GQ[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    D2[q] = NT == 1 ? d2[q] : __shfl_sync(0xffffffffu, d2[q], src);
+                    GQ[q] = NT == 1 ? gq[q] : __shfl_sync(0xffffffffu, gq[q], src);
+                }
+                const int t_grp = sb * SB + j * 8;
+#pragma unroll
+                for (int q = 7; q >= 0; --q) {
+                    const float* crow = bct + (t_grp + q) * (2 * NP) + NP + g * G;
+                    const f2 d2p = pk(D2[q], D2[q]), gqp = pk(GQ[q], GQ[q]);
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(crow + 4 * q4);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int jj = 2 * q4 + e;
+                            const f2 Cj = e ? Cq.y : Cq.x;
+                            lam[jj] = fma2(gqp, Cj, mul2(anext[jj], lam[jj]));
+                            const f2 arg = mul2(d2p, Ap[jj]);
+                            anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && !dead) mbar_arrive(&empty_bar[s]);
+    }
+
+#pragma unroll
+    for (int o = 1; o < NT; o <<= 1) sum_d2 += __shfl_xor_sync(0xffffffffu, sum_d2, o);
+    if (ch_ok && !dead) {
+        const int64_t segrow = (int64_t)seg * p.Bt * p.D + row;
+#pragma unroll
+        for (int j = 0; j < G / 2; ++j) {
+            const int n0 = g * G + 2 * j;
+            float v0, v1;
+            upk(mul2(anext[j], lam[j]), v0, v1);
+            p.lam_loc[segrow * NP + n0] = v0;
+            p.lam_loc[segrow * NP + n0 + 1] = v1;
+        }
+        if (g == 0 && k_end == k_seg_end) p.sumd[segrow] = (float)sum_d2;
     }
 }
 

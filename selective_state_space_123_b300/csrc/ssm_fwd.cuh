@@ -154,8 +154,7 @@ struct NoRestart {
 // over the ~1/(delta |A|) tokens the state remembers.  For e < -1/2 (the
 // state forgets within a few tokens, nothing accumulates) the plain form
 // (1 + e) h + xin is used, 1 + e being exact there.
-__device__ __forceinline__ void comp_update(float x, float xin, float& hi, float& lo) {
-    const float e = exp2m1_accurate(x);
+__device__ __forceinline__ void comp_update_e(float e, float xin, float& hi, float& lo) {
     const float a = 1.0f + e;
     const float plain = fmaf(a, hi, xin);
     const float inc = fmaf(e, hi, xin);
@@ -165,6 +164,10 @@ __device__ __forceinline__ void comp_update(float x, float xin, float& hi, float
     const bool fast = e < -0.5f;
     lo = fmaf(e, lo, lo) + (fast ? 0.0f : err);
     hi = fast ? plain : s;
+}
+// the same from x = delta2 * A
+__device__ __forceinline__ void comp_update(float x, float xin, float& hi, float& lo) {
+    comp_update_e(exp2m1_accurate(x), xin, hi, lo);
 }
 
 // The recurrence over one super-block of SB tokens for one lane's G states.

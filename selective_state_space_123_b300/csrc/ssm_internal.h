@@ -63,10 +63,12 @@ struct BwdMaps {
 // Launch shape of one backward call: grid, compute warps per CTA, ring
 // depths and dynamic shared memory of the two sweeps.
 struct BwdLaunch {
-    dim3 grid;
+    dim3 grid;               // z = segments (1 without the segmented plan)
     int warps;
     int stages_f, stages_r;
     size_t smem_f, smem_r;
+    int stages_l = 2;        // segmented plan: the adjoint summary's ring and shared memory
+    size_t smem_l = 0;
 };
 
 // Backward (forward sweep, then reverse sweep) for padded state size NP
@@ -84,12 +86,29 @@ cudaError_t launch_bwd_np64(int NT, int tin, int tout, bool tma, const BwdParams
 cudaError_t launch_bwd_varlen_np16(int NT, int tin, int tout, const BwdParams& p,
                                    const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 
+// The segmented backward for padded state size 16, 16-byte token rows and
+// two or four threads per channel: part 0 = the adjoint summary of segments
+// 1 .. nseg-1 (grid z = nseg - 1), part 1 = the forward sweep with the
+// tangent sums, part 2 = the reverse sweep (both grid z = nseg).
+cudaError_t launch_bwd_seg_np16(int NT, int tin, int tout, int part, const BwdParams& p,
+                                const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
+// The dA terms of the tangent flowing into each segment from the ones before
+// (see ssm_aux.cu); after the forward sweep of the segmented backward.
+cudaError_t launch_tangent_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
+                                 const float* sumd, const float* mend, const float* gp, float* dA,
+                                 cudaStream_t st);
+
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st);
 // Tail search of the segmented plan (see ssm_aux.cu): per (segment, batch
 // row, channel tile) the first chunk pass 1 needs; per saturated channel a
 // marker in sumd.  Segments 0 .. nseg-2.
 cudaError_t launch_tail(int tin, const FwdParams& p, int CH, unsigned tiles, int* tstart, float* sumd,
+                        cudaStream_t st);
+// Head search of the segmented backward (see ssm_aux.cu): per (segment,
+// batch row, channel tile) the chunk after the last one the adjoint summary
+// needs; per saturated channel a marker in sumd.  Segments 1 .. nseg-1.
+cudaError_t launch_head(int tin, const BwdParams& p, int CH, unsigned tiles, int* kstop, float* sumd,
                         cudaStream_t st);
 cudaError_t launch_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,
                          const float* h0, const float* hloc, const float* sumd, float* hin,

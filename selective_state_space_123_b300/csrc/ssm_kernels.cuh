@@ -135,6 +135,18 @@ struct BwdParams {
     float* dbias;           // nullable, accumulated (zeroed by the host)
     float* dh0;             // nullable
     int stages;             // depth of the shared-memory ring (<= kFwdMaxStages)
+    // segmented plan (nseg > 1, grid z = segment; 0 or 1: whole rows): the
+    // sequence is cut into nseg segments of seg_chunks chunks
+    int64_t seg_chunks;
+    int nseg;
+    const float* hin;       // (nseg, Bt, D, NP) state before each segment (the forward's carry)
+    const float* lam_in;    // (nseg, Bt, D, NP) a_{t1} lambda_{t1} entering each segment from the right
+    float* lam_loc;         // (nseg, Bt, D, NP) the same from a zero start (adjoint summary)
+    float* sumd;            // (nseg, Bt, D) sum of delta/ln2 over a segment (adjoint summary)
+    const int* kstop;       // (nseg, Bt, tiles) nullable: chunk after the last one the adjoint
+                            // summary needs (head search; sumd then holds its saturation marks)
+    float* gp;              // (nseg, Bt, D, NP) sum_t g_t C_t P_t, P_t = decay since the segment start
+    float* mend;            // (nseg, Bt, D, NP) dA tangent / ln2 at the segment end from a zero start
     // conv prologue (the kernel instantiated with CONV): u is computed from
     // the branch input x (passed as `u`) by a causal depthwise convolution of
     // width conv_k <= 4 and SiLU; conv_w (D, conv_k), conv_b (D) nullable

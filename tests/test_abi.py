@@ -264,13 +264,32 @@ def test_workspace_query_edge_shapes(pkg, for_backward):
         for ti in (0, 1):
             n = pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, ti, ti), for_backward)
             assert n >= 256, sh
-    for forced in ("1", "2", "3", "7", "1000"):
-        os.environ["SSM_FWD_NSEG"] = forced
-        try:
-            for sh in [(1, 8, 16, 0), (1, 8, 16, 1), (2, 40, 16, 64 * 29 + 13)]:
-                assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, 1, 1), for_backward) >= 256
-        finally:
-            del os.environ["SSM_FWD_NSEG"]
+    for var in ("SSM_FWD_NSEG", "SSM_BWD_NSEG"):
+        for forced in ("1", "2", "3", "7", "1000"):
+            os.environ[var] = forced
+            try:
+                for sh in [(1, 8, 16, 0), (1, 8, 16, 1), (2, 40, 16, 64 * 29 + 13)]:
+                    for ti in (0, 1):
+                        n = pkg.ssm_scan_workspace_bytes(pkg.make_shape(*sh, ti, ti), for_backward)
+                        assert n >= 256, (var, forced, sh)
+            finally:
+                del os.environ[var]
+
+
+def test_backward_segments_enlarge_the_workspace(pkg, monkeypatch):
+    """A segmented backward plan (forced, or the planner's for a few-channel
+    long sequence) adds its per-segment buffers after the whole-row ones."""
+    sh = pkg.make_shape(1, 48, 16, 64 * 40, 1, 1)
+    monkeypatch.setenv("SSM_BWD_NSEG", "1")
+    whole = pkg.ssm_scan_workspace_bytes(sh, True)
+    monkeypatch.setenv("SSM_BWD_NSEG", "4")
+    seg4 = pkg.ssm_scan_workspace_bytes(sh, True)
+    # initial states, end states, adjoint sums and inputs, tangent sums:
+    # 6 arrays of (nseg, batch, dim, 16) fp32 at least
+    assert seg4 >= whole + 6 * 4 * 48 * 16 * 4
+    monkeypatch.delenv("SSM_BWD_NSEG")
+    assert pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 1536, 16, 1 << 20, 1, 1), True) > \
+        pkg.ssm_scan_workspace_bytes(pkg.make_shape(1, 1536, 16, 1 << 20, 1, 1), False)
 
 
 def test_plan_overrides_that_do_not_fit_fall_back(pkg, monkeypatch):
