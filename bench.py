@@ -12,6 +12,7 @@ fp32 arithmetic, bf16 y, fp32 final state.  Other workloads:
   mamba2p8b_fwd     forward, batch 2, D 5120, N 16, L 8192
   mamba2p8b_fwdbwd  forward then backward (all gradients), same shape
   million_fwd       forward, batch 1, D 1536, N 16, L 1,048,576
+  million_fwdbwd    forward then backward (all gradients), same shape (both segmented)
   decode_step       one recurrent step, batch 256, D 5120, N 16, state in place
 Inputs are synthetic (seeded, drawn on the device) and resident in HBM before
 the timed region; every workload's inputs exceed L2 (126 MB) except where the
@@ -54,6 +55,12 @@ WORKLOADS = {
                              title="Mamba-2.8B layer forward + backward"),
     "million_fwd": dict(mode="fwd", Bt=1, D=1536, N=16, L=1 << 20, seed=4,
                         title="million-length forward"),
+    # forward (B/C preparation, tail search, summary pass, carry, scan) +
+    # segmented backward (B/C preparation, tail search, forward summary,
+    # carry, head search, adjoint summary, carry, forward sweep, tangent
+    # carry, reverse sweep)
+    "million_fwdbwd": dict(mode="fwdbwd", Bt=1, D=1536, N=16, L=1 << 20, seed=4, launches=15,
+                           title="million-length forward + backward"),
     "decode_step": dict(mode="step", Bt=256, D=5120, N=16, L=1, seed=4,
                         title="single-token decode step"),
     "mamba1p4b_conv_fwd": dict(mode="fwd", conv=4, Bt=4, D=4096, N=16, L=4096, seed=2,

@@ -2,8 +2,9 @@
 the launch configuration the bench times: the conv prologue (Mamba-1.4B shape,
 width 4), packed sequences (Mamba-1.4B channels, one 65,536-token row of 17
 sequences, four segments) and the bidirectional scan (Mamba-1.4B shape, two
-parameter sets).  Sampled channels of every batch row are compared with the
-oracle (channels are independent).  The smaller parity cases of each variant
+parameter sets), and the backward of the packed row, of the bidirectional
+scan and of the million-token sequence (segmented plan).  Sampled channels
+of every batch row are compared with the oracle (channels are independent).  The smaller parity cases of each variant
 live in test_conv_parity.py, test_varlen_parity.py and test_bidir_parity.py;
 this file is collected after them.
 """
@@ -166,3 +167,31 @@ def test_bidir_backward_long_rows(ssm):
     for tag, gg, oo in (("fwd", gf, of), ("rev", gr, orr)):
         for k in oo:
             assert_close(gg[k].cpu().numpy(), oo[k], TOL["bf16"], tag + "." + k)
+
+
+def test_million_length_backward_sampled(ssm):
+    """The reverse mode of the million-token sequence (batch 1, D 1536, N 16,
+    L 2^20; the planner's segmented plan) against the oracle on sampled
+    channels: every token's du, ddelta_raw and dz, and dA, dD, ddelta_bias and
+    dh0 of those channels.  (dB and dC sum over all 1,536 channels; the
+    segmented plan's dB and dC are compared in full at smaller sizes.)"""
+    w = bench.WORKLOADS["million_fwd"]
+    Bt, D, N, L = w["Bt"], w["D"], w["N"], w["L"]
+    a = device_inputs(Bt, D, N, L, seed=w["seed"], in_dtype="bf16", dy=True)
+    g = ssm.ssm_scan_bwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["dy"], a["Dv"],
+                         a["z"], a["delta_bias"], None, None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ds = np.array([0, 517, 1103, D - 1])
+    bi = [0]
+    host = lambda t: rows_to_host(t, bi, ds)
+    o = oracle.scan_bwd(host(a["u"]), host(a["delta_raw"]), a["A"][ds].cpu().numpy(),
+                        a["Bm"].float().cpu().numpy(), a["Cm"].float().cpu().numpy(),
+                        host(a["dy"]), a["Dv"][ds].cpu().numpy(), host(a["z"]),
+                        a["delta_bias"][ds].cpu().numpy(), None, None)
+    tol = TOL["bf16"]
+    for k in ("du", "ddelta_raw", "dz", "dh0"):
+        assert_close(g[k][bi][:, ds].cpu().numpy(), o[k], tol, "million backward " + k)
+    for k in ("dA", "dD", "ddelta_bias"):
+        assert_close(g[k][ds].cpu().numpy(), o[k], tol, "million backward " + k)
+    del a, g
+    torch.cuda.empty_cache()
