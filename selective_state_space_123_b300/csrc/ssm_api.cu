@@ -900,7 +900,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int sms = device_sm_count();
-    const BwdPlan pl = plan_bwd(s, sms, !varlen);
+    const BwdPlan pl = plan_bwd(s, sms);
     if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
     // packed sequences: built for 9..16 states and 16-byte token rows
     if (varlen && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
@@ -977,7 +977,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
-    if (varlen) {
+    if (varlen && pl.nseg == 1) {
         BwdLaunch lc;
         lc.grid = dim3(gx, (unsigned)Bt);
         lc.warps = pl.W;
@@ -1010,6 +1010,8 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         pf.Bt = Bt; pf.D = Dm; pf.L = L; pf.N = (int)N;
         pf.u = u; pf.dr = delta_raw; pf.z = z; pf.A = A; pf.Dv = D; pf.bias = delta_bias;
         pf.h0 = h0; pf.bc = bc;
+        pf.cu_seqlens = cu_seqlens;
+        pf.nseq = varlen ? nseq : 0;
         pf.seg_chunks = pl.seg_chunks;
         pf.nseg = pl.nseg;
         pf.stages = fp.stages;
@@ -1024,7 +1026,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         pf1.hin = nullptr;
         pf1.tstart = tstart;
         if (launch_tail(s.in_dtype, pf, fp.CH, gxf, tstart, pf.sumd, st) != cudaSuccess ||
-            launch_fwd(fp, s.in_dtype, s.out_dtype, true, false, false, pf1, fm,
+            launch_fwd(fp, s.in_dtype, s.out_dtype, true, false, varlen, pf1, fm,
                        dim3(gxf, (unsigned)Bt, (unsigned)(pl.nseg - 1)), st) != cudaSuccess ||
             launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, h0, pf.hloc, pf.sumd, pf.hin, st) !=
                 cudaSuccess)
@@ -1052,13 +1054,19 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         if (launch_head(s.in_dtype, p, pl.CH, gx, kstop, p.sumd, st) != cudaSuccess)
             return cuda_fail();
         p.kstop = kstop;
-        if (launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 0, p, maps, lc, st) != cudaSuccess ||
-            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, dhL, p.lam_loc, p.sumd, lam_in, st,
+        // (the last segment's adjoint summary starts from the final-state
+        // gradient itself, so the carry starts from zero)
+        auto seg_part = [&](int part) {
+            return varlen ? launch_bwd_seg_varlen_np16(pl.NT, s.in_dtype, s.out_dtype, part, p, maps, lc, st)
+                          : launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, part, p, maps, lc, st);
+        };
+        if (seg_part(0) != cudaSuccess ||
+            launch_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, nullptr, p.lam_loc, p.sumd, lam_in, st,
                          true) != cudaSuccess ||
-            launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 1, p, maps, lc, st) != cudaSuccess ||
+            seg_part(1) != cudaSuccess ||
             launch_tangent_carry(Bt, Dm, (int)N, pl.NP, pl.nseg, A, pf.sumd, p.mend, p.gp, dA, st) !=
                 cudaSuccess ||
-            launch_bwd_seg_np16(pl.NT, s.in_dtype, s.out_dtype, 2, p, maps, lc, st) != cudaSuccess)
+            seg_part(2) != cudaSuccess)
             return cuda_fail();
         return SSM_OK;
     }

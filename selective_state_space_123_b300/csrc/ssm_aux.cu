@@ -252,6 +252,27 @@ __global__ void __launch_bounds__(1024) head_kernel(const BwdParams p, int CH, i
     const int64_t c_begin = (int64_t)seg * p.seg_chunks;
     const int64_t c_end = min(nchunks, c_begin + p.seg_chunks);
     const int64_t s0 = c_begin * kT, s1 = min(p.L, c_end * kT);
+    if (p.cu_seqlens) {
+        // packed sequences: a segment in which a sequence ends (a start in
+        // (s0, s1]) needs only the tokens up to its first end, and passes on
+        // nothing from its right; the condition is the same for the whole block
+        int lo = 0, hi = p.nseq;   // first start after s0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)p.cu_seqlens[mid] <= s0) lo = mid + 1;
+            else hi = mid;
+        }
+        const int64_t c = lo < p.nseq ? (int64_t)p.cu_seqlens[lo] : p.L;
+        if (c <= s1 && c < p.L) {
+            for (int i = threadIdx.x; i < CH; i += blockDim.x) {
+                const int64_t d = (int64_t)tile * CH + i;
+                if (d < p.D) sumd[(int64_t)seg * p.Bt * p.D + b * p.D + d] = kTailSat;
+            }
+            if (threadIdx.x == 0)
+                kstop[((int64_t)seg * p.Bt + b) * gridDim.x + tile] = (int)((c - 1) / kT + 1);
+            return;
+        }
+    }
     __shared__ int cmax;
     if (threadIdx.x == 0) cmax = 0;
     __syncthreads();

@@ -316,7 +316,11 @@ __device__ __forceinline__ uint32_t start_bits(const int* cu, int nseq, int64_t 
 // local dA terms, a segment records the tangent at its end (p.mend) and
 // GP = sum_t g_t C_t P_t (p.gp), P_t = the decay from the segment's start
 // through token t (plus dhL P_L in the last segment), from which a carry
-// adds the dA terms of the tangent flowing in from earlier segments.
+// adds the dA terms of the tangent flowing in from earlier segments.  With
+// packed sequences a start inside the segment adds dhL[ending] P to GP and
+// sets P to 0 (the tangent from outside ends there); psi of a sequence that
+// ends with the segment's last token is added by this segment, not by the
+// next one, which would race with this segment's store of that token.
 template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false,
           bool SEG = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
@@ -331,7 +335,6 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     constexpr int BCB = bc_tile_bytes<NP>();
     constexpr bool ACCURATE = EB == 4;
     static_assert(G % 4 == 0 && G <= 16, "states per thread");
-    static_assert(!(SEG && VARLEN), "segments of packed sequences are not built");
 
     const int W = (int)(blockDim.x / 32) - 1;
     const int CH = W * CW;
@@ -505,6 +508,10 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     const int n0 = g * G + 2 * jj;
                     const f2 dhp = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
                     dAc[jj] = fma2(dhp, m[jj], dAc[jj]);          // dhL[se] . dh/dA
+                    if constexpr (SEG) {
+                        GP[jj] = fma2(dhp, Pd[jj], GP[jj]);       // ... of the tangent from outside
+                        Pd[jj] = pk(0.0f, 0.0f);
+                    }
                     float x0, x1;
                     upk(mul2(mul2(Ap[jj], dhp), full(jj)), x0, x1);  // A dhL[se] h_end
                     psi += x0 + x1;
@@ -542,7 +549,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                             if (g == j) psi_add[q - 1] += psi;
                         } else if (j > 0) {
                             if (g == j - 1) psi_add[7] += psi;
-                        } else if (g == NT - 1 && ch_ok) {
+                        } else if (g == NT - 1 && ch_ok && !(SEG && t_sb == k_begin * kT)) {
                             atomicAdd(p.phi + row * L + t_sb - 1, psi);
                         }
                     }
@@ -628,6 +635,30 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 __syncwarp();   // the transpose buffer is reused by the next group
             }
 
+            if constexpr (VARLEN && SEG) {
+                // a sequence ending with this segment's last token (the next
+                // segment starts one): its psi goes to phi of that token here
+                const int64_t tn = k_end * kT;
+                if (!last_seg && k == k_end - 1 && t_sb + SB == tn && tn < L) {
+                    const int lb = seq_lower_bound(p.cu_seqlens, p.nseq, tn);
+                    if (lb < p.nseq && (int64_t)p.cu_seqlens[lb] == tn) {
+                        const int se = seq_of_token(p.cu_seqlens, p.nseq, tn - 1);
+                        const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+                        float psi = 0.0f;
+#pragma unroll
+                        for (int jj = 0; jj < G / 2; ++jj) {
+                            const int n0 = g * G + 2 * jj;
+                            const f2 dhp = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                            float x0, x1;
+                            upk(mul2(mul2(Ap[jj], dhp), full(jj)), x0, x1);
+                            psi += x0 + x1;
+                        }
+#pragma unroll
+                        for (int o = 1; o < NT; o <<= 1) psi += __shfl_xor_sync(0xffffffffu, psi, o);
+                        if (g == NT - 1) psi_add[7] += psi;
+                    }
+                }
+            }
             // this lane's tokens: dz and phi
             float uv[8], gy[8], zv[8];
             load_raw8r<TIN>(st, CH, c, tbk, uv);
@@ -1090,16 +1121,19 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 // recurrence lambda_t = g_t C_t + a_{t+1} lambda_{t+1} from zero at the
 // segment's right end down to its first token t0, giving
 // p.lam_loc[seg] = a_{t0} lambda_{t0} (what the segment passes to its left
-// neighbour from a zero start), and p.sumd[seg], the segment's sum of
-// delta/ln2 (its total decay is 2^(A sumd)).  A carry over the segments, from
+// neighbour from a zero start; the last segment starts from the final-state
+// gradient dhL instead), and p.sumd[seg], the segment's sum of delta/ln2
+// (its total decay is 2^(A sumd)).  A carry over the segments, from
 // the last one down, then gives every segment the adjoint flowing in at its
 // right end.  Same tiles and ring as the reverse sweep, without the per-token
 // tile; nothing but the recurrence per state.  With a head search (p.kstop)
 // the summary starts at the chunk where the decay from the segment's start
 // has fallen below fp32 resolution for every channel of the tile; the sum
 // of delta2 is then the search's (saturation marks) unless the whole segment
-// ran.
-template <int NP, int NT, typename TIN, bool TMA_RAW>
+// ran.  VARLEN: at the last token of a packed sequence the adjoint restarts
+// from that sequence's dhL (as in the reverse sweep); a segment in which a
+// sequence ends passes on nothing from its right (the search marks it).
+template <int NP, int NT, typename TIN, bool TMA_RAW, bool VARLEN = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -1162,19 +1196,31 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const bool ch_ok = d < p.D;
     const int64_t row = b * p.D + d;
     const int N = p.N;
+    const int64_t seq_stride = p.Bt * p.D * (int64_t)N;
+    // the last segment: dhL of the sequence holding token L-1
+    const bool last_seg = seg == p.nseg - 1;
+    const int s_last = (VARLEN && last_seg) ? seq_of_token(p.cu_seqlens, p.nseq, L - 1) : 0;
+    const float* dhl = (last_seg && p.dhL && ch_ok) ? p.dhL + (int64_t)s_last * seq_stride + row * N : nullptr;
     f2 Ap[G / 2], lam[G / 2], anext[G / 2];
 #pragma unroll
     for (int j = 0; j < G / 2; ++j) {
         const int n0 = g * G + 2 * j, n1 = n0 + 1;
         Ap[j] = pk((ch_ok && n0 < N) ? p.A[d * N + n0] : 0.0f,
                    (ch_ok && n1 < N) ? p.A[d * N + n1] : 0.0f);
-        lam[j] = pk(0.0f, 0.0f);
+        lam[j] = pk((dhl && n0 < N) ? dhl[n0] : 0.0f, (dhl && n1 < N) ? dhl[n1] : 0.0f);
         anext[j] = pk(1.0f, 1.0f);
     }
     const float bias2 = (p.bias && ch_ok) ? p.bias[d] * kLog2e : 0.0f;
     const int src_base = lane & ~(NT - 1);
     double sum_d2 = 0.0;   // this lane's own tokens
     bool dead = false;
+    // packed: a sequence ends inside the segment (a start in (s0, s1])
+    bool cut = false;
+    if constexpr (VARLEN) {
+        const int64_t s0 = k_begin * kT, s1 = min(L, k_seg_end * kT);
+        const int lb = seq_lower_bound(p.cu_seqlens, p.nseq, s0 + 1);
+        cut = lb < p.nseq && (int64_t)p.cu_seqlens[lb] <= s1 && (int64_t)p.cu_seqlens[lb] < L;
+    }
 
     for (int64_t i = 0; i < k_end - k_begin; ++i) {
         const int64_t k = k_end - 1 - i;
@@ -1201,6 +1247,8 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
             for (int q = 0; q < 8; ++q) s8 += d2[q];
             sum_d2 += (double)s8;
+            const int64_t t_sb = k * kT + sb * SB;
+            const uint32_t emask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 1) : 0u;
 #pragma unroll 1
             for (int j = NT - 1; j >= 0; --j) {
                 const int src = src_base + j;
@@ -1213,6 +1261,17 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 const int t_grp = sb * SB + j * 8;
 #pragma unroll
                 for (int q = 7; q >= 0; --q) {
+                    if (VARLEN && ((emask >> (j * 8 + q)) & 1u)) {
+                        // token t ends sequence se: the adjoint restarts from dhL[se]
+                        const int se = seq_of_token(p.cu_seqlens, p.nseq, t_sb + j * 8 + q);
+                        const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+#pragma unroll
+                        for (int jj = 0; jj < G / 2; ++jj) {
+                            const int n0 = g * G + 2 * jj;
+                            lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                            anext[jj] = pk(1.0f, 1.0f);
+                        }
+                    }
                     const float* crow = bct + (t_grp + q) * (2 * NP) + NP + g * G;
                     const f2 d2p = pk(D2[q], D2[q]), gqp = pk(GQ[q], GQ[q]);
 #pragma unroll
@@ -1246,7 +1305,7 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             p.lam_loc[segrow * NP + n0] = v0;
             p.lam_loc[segrow * NP + n0 + 1] = v1;
         }
-        if (g == 0 && k_end == k_seg_end) p.sumd[segrow] = (float)sum_d2;
+        if (g == 0 && k_end == k_seg_end && !cut) p.sumd[segrow] = (float)sum_d2;
     }
 }
 

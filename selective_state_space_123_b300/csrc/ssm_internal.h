@@ -92,6 +92,9 @@ cudaError_t launch_bwd_varlen_np16(int NT, int tin, int tout, const BwdParams& p
 // tangent sums, part 2 = the reverse sweep (both grid z = nseg).
 cudaError_t launch_bwd_seg_np16(int NT, int tin, int tout, int part, const BwdParams& p,
                                 const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
+// the same over packed sequences (p.cu_seqlens, p.nseq)
+cudaError_t launch_bwd_seg_varlen_np16(int NT, int tin, int tout, int part, const BwdParams& p,
+                                       const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st);
 // The dA terms of the tangent flowing into each segment from the ones before
 // (see ssm_aux.cu); after the forward sweep of the segmented backward.
 cudaError_t launch_tangent_carry(int64_t Bt, int64_t D, int N, int NP, int nseg, const float* A,

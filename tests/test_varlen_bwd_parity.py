@@ -145,3 +145,44 @@ def test_varlen_bwd_lanes_per_channel(ssm, nt, monkeypatch):
     _run(ssm, x, CUTS, _state(ns, Bt, D, N, 690), _state(ns, Bt, D, N, 691))
     xf = make_inputs(Bt, D, N, L, seed=685 + int(nt), in_dtype="f32", dy=True)
     _run(ssm, xf, CUTS, _state(ns, Bt, D, N, 692), _state(ns, Bt, D, N, 693))
+
+
+# segment boundaries of the forced segmented plans below: 12 chunks in 3
+# segments start at tokens 256 and 512; in 4 segments at 192, 384 and 576
+SEG_CUTS = [0, 100, 192, 256, 300, 383, 384, 511, 512, 512, 600, 700, 768]
+
+
+@pytest.mark.parametrize("nseg", ["3", "4"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_varlen_bwd_segments(ssm, nseg, dtype, monkeypatch):
+    """The segmented plan over packed sequences: starts on segment
+    boundaries (a sequence ending with a segment's last token), inside
+    segments, an empty sequence on a boundary, and sequences spanning two
+    segments; h0 and dhL per sequence."""
+    monkeypatch.setenv("SSM_BWD_NSEG", nseg)
+    Bt, D, N, L = 2, 40, 16, 768
+    x = make_inputs(Bt, D, N, L, seed=700 + int(nseg), in_dtype=dtype, dy=True)
+    ns = len(SEG_CUTS) - 1
+    _run(ssm, x, SEG_CUTS, _state(ns, Bt, D, N, 701), _state(ns, Bt, D, N, 702))
+
+
+def test_varlen_bwd_segments_long_sequences(ssm, monkeypatch):
+    """Few sequences, each spanning several segments (the carries pass the
+    state, the adjoint and the dA tangent across boundaries inside a
+    sequence), and a last sequence that starts inside the last segment."""
+    monkeypatch.setenv("SSM_BWD_NSEG", "6")
+    Bt, D, N, L = 1, 32, 16, 64 * 30
+    cuts = [0, 64 * 11 + 5, 64 * 27 + 30, L]
+    x = make_inputs(Bt, D, N, L, seed=710, in_dtype="bf16", dy=True)
+    ns = len(cuts) - 1
+    _run(ssm, x, cuts, _state(ns, Bt, D, N, 711), _state(ns, Bt, D, N, 712))
+
+
+def test_varlen_bwd_packed_recipe_planner_segments(ssm):
+    """The packed workload's length mix over a long row with few channels:
+    the planner cuts it into segments by itself."""
+    L = 64 * 256
+    cu = packed_seqlens(L, seed=720, lo=16, hi=4096)
+    x = make_inputs(1, 48, 16, L, seed=721, in_dtype="bf16", dy=True)
+    ns = len(cu) - 1
+    _run(ssm, x, cu, _state(ns, 1, 48, 16, 722), _state(ns, 1, 48, 16, 723))
