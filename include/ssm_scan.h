@@ -235,7 +235,14 @@ SSM_API int ssm_scan_bwd_bidir(const ssm_shape* shape, const void* u, const void
  *   ddelta_raw is the derivative with respect to delta_raw (before softplus).
  * workspace : >= ssm_scan_workspace_bytes(shape, 1) bytes.  The backward
  * reruns the forward recurrence itself (with the derivative of the state
- * with respect to A beside it); nothing from ssm_scan_fwd is needed. */
+ * with respect to A beside it); nothing from ssm_scan_fwd is needed.  Long
+ * sequences with too few channels to fill the GPU ("Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces", section "Key points":
+ * sequences up to a million tokens) are cut into segments run side by side,
+ * each given its initial state, the adjoint entering from its right and the
+ * dA tangent crossing its boundaries by summary passes and carries over the
+ * segments (workspace sized for them); the results are the same reverse
+ * mode. */
 SSM_API int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw,
                  const float* A, const void* B, const void* C, const float* D,
                  const void* z, const float* delta_bias, const float* h0,
