@@ -615,7 +615,7 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 if (NT > 1) {
 #pragma unroll
                     for (int q = 0; q < SB; q += 4)
-                        *reinterpret_cast<float4*>(yb + g * SB + q) =
+                        *reinterpret_cast<float4*>(yb + Lay::xoff(cw, g * SB + q)) =
                             make_float4(yp[q], yp[q + 1], yp[q + 2], yp[q + 3]);
                     __syncwarp();
                 }
@@ -628,8 +628,8 @@ fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     }
 #pragma unroll
                     for (int gg = 0; gg < (NT > 1 ? NT : 0); ++gg) {
-                        const float4 a = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8);
-                        const float4 bq = *reinterpret_cast<const float4*>(yb + gg * SB + g * TPL + 8 * k8 + 4);
+                        const float4 a = *reinterpret_cast<const float4*>(yb + Lay::xoff(cw, gg * SB + g * TPL + 8 * k8));
+                        const float4 bq = *reinterpret_cast<const float4*>(yb + Lay::xoff(cw, gg * SB + g * TPL + 8 * k8 + 4));
                         if (gg == 0) {
                             yt[0] = a.x; yt[1] = a.y; yt[2] = a.z; yt[3] = a.w;
                             yt[4] = bq.x; yt[5] = bq.y; yt[6] = bq.z; yt[7] = bq.w;

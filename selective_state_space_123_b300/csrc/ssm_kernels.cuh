@@ -13,15 +13,24 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
 // Forward-kernel layout per NT (threads per channel).  Per compute warp an
 // exchange buffer holds, per channel, the NT partial read-outs of one
-// super-block; rows are padded by 16 bytes so the lanes' 16-byte accesses
-// spread over all banks.
+// super-block.  With two lanes per channel a row is 40 floats (10 16-byte
+// chunks, 8 used) and chunk f of channel cw sits at slot f ^ (cw & 3): the
+// eight lanes of a quarter warp then reach eight distinct bank groups both
+// when they store their partials (chunks 4g .. 4g+3) and when they read
+// the partials of their own tokens (chunks 4gg + 2g + h); other NT pad the
+// rows by 16 bytes.
 template <int NT>
 struct FwdLayout {
     static constexpr int CW = 32 / NT;             // channels per compute warp
     static constexpr int TPL = 8;                  // tokens each lane finishes per super-block
     static constexpr int SB = TPL * NT;            // tokens per super-block
-    static constexpr int YROW = NT * SB + 4;       // floats per channel row (partial read-outs)
+    static constexpr int YROW = NT * SB + (NT == 2 ? 8 : 4);   // floats per channel row
     static constexpr int XY_FLOATS = CW * YROW;
+    // float offset in channel cw's row of the partial read-out at position f
+    // (f = lane-in-channel * SB + token, a multiple of 4 for a chunk start)
+    static __host__ __device__ constexpr int xoff(int cw, int f) {
+        return NT == 2 ? (((f >> 2) ^ (cw & 3)) << 2) + (f & 3) : f;
+    }
     static constexpr int kMaxWarps = 7;    // compute warps per CTA at most (+ the producer: 256 threads)
     static constexpr int kMinBlocks = 1;   // launch bound: up to 255 registers, no spills
 };
