@@ -60,6 +60,8 @@ def bind(lib):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_conv_silu.argtypes = [I, I, I, I, P, P, P, P]
     lib.oracle_conv_silu.restype = None
+    lib.oracle_conv_silu_bwd.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+    lib.oracle_conv_silu_bwd.restype = None
     lib.oracle_silu.argtypes = [ctypes.c_double]
     lib.oracle_silu.restype = ctypes.c_double
     lib.oracle_scan_fwd.argtypes = [I, I, I, I] + [P] * 11
@@ -115,6 +117,36 @@ def scan_fwd_conv(x, conv_w, conv_b, delta_raw, A, Bm, Cm, Dv=None, z=None, delt
                   h0=None):
     """The scan fed by the block's conv prologue: scan_fwd(conv_silu(x), ...)."""
     return scan_fwd(conv_silu(x, conv_w, conv_b), delta_raw, A, Bm, Cm, Dv, z, delta_bias, h0)
+
+
+def conv_silu_bwd(x, conv_w, conv_b, du):
+    """Reverse mode of conv_silu given du = dLoss/du: returns (dx, dconv_w,
+    dconv_b) (dconv_b None when conv_b is None)."""
+    x, conv_w, du = _f64(x), _f64(conv_w), _f64(du)
+    conv_b = _f64(conv_b)
+    Bt, D, L = x.shape
+    K = conv_w.shape[1]
+    assert conv_w.shape == (D, K) and du.shape == (Bt, D, L)
+    dx = np.empty((Bt, D, L), np.float64)
+    dw = np.empty((D, K), np.float64)
+    db = np.empty((D,), np.float64) if conv_b is not None else None
+    _load().oracle_conv_silu_bwd(Bt, D, L, K, _ptr(x), _ptr(conv_w), _ptr(conv_b), _ptr(du),
+                                 _ptr(dx), _ptr(dw), _ptr(db))
+    return dx, dw, db
+
+
+def scan_bwd_conv(x, conv_w, conv_b, delta_raw, A, Bm, Cm, dy, Dv=None, z=None,
+                  delta_bias=None, h0=None, dhL=None):
+    """Reverse mode of scan_fwd_conv: scan_bwd on u = conv_silu(x), then the
+    prologue's reverse mode on its du.  Returns scan_bwd's dict with du
+    replaced by dx, plus dconv_w and dconv_b."""
+    u = conv_silu(x, conv_w, conv_b)
+    out = scan_bwd(u, delta_raw, A, Bm, Cm, dy, Dv, z, delta_bias, h0, dhL)
+    dx, dw, db = conv_silu_bwd(x, conv_w, conv_b, out.pop("du"))
+    out["dx"] = dx
+    out["dconv_w"] = dw
+    out["dconv_b"] = db
+    return out
 
 
 def scan_fwd_varlen(u, delta_raw, A, Bm, Cm, cu_seqlens, Dv=None, z=None, delta_bias=None,

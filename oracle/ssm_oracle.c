@@ -69,6 +69,52 @@ void oracle_conv_silu(int64_t Bt, int64_t D, int64_t L, int64_t K, const double*
         }
 }
 
+/* Reverse mode of oracle_conv_silu ("Mamba Architecture Explained", section
+ * "The Architecture in Practice": the branch's Conv1D and SiLU before the
+ * selective SSM), given du = dLoss/du.  With pre[t] = conv_b + sum_k
+ * conv_w[k] x[t-(K-1)+k] (x before token 0 is 0) and u = silu(pre):
+ *   dpre[t]      = du[t] silu'(pre[t]),  silu'(p) = s (1 + p (1 - s)), s = 1 / (1 + e^-p)
+ *   dx[t]        = sum_k conv_w[k] dpre[t+(K-1)-k]      (terms past the end absent)
+ *   dconv_w[d,k] = sum_{b,t} dpre[t] x[t-(K-1)+k]
+ *   dconv_b[d]   = sum_{b,t} dpre[t]
+ * dconv_b nullable. */
+void oracle_conv_silu_bwd(int64_t Bt, int64_t D, int64_t L, int64_t K, const double* x,
+                          const double* conv_w, const double* conv_b, const double* du,
+                          double* dx, double* dconv_w, double* dconv_b) {
+    double* dpre = (double*)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    for (int64_t d = 0; d < D; ++d) {
+        for (int64_t k = 0; k < K; ++k) dconv_w[d * K + k] = 0.0;
+        if (dconv_b) dconv_b[d] = 0.0;
+    }
+    for (int64_t b = 0; b < Bt; ++b)
+        for (int64_t d = 0; d < D; ++d) {
+            const int64_t row = (b * D + d) * L;
+            for (int64_t t = 0; t < L; ++t) {
+                double p = conv_b ? conv_b[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t tt = t - (K - 1) + k;
+                    if (tt >= 0) p += conv_w[d * K + k] * x[row + tt];
+                }
+                const double sg = 1.0 / (1.0 + exp(-p));
+                dpre[t] = du[row + t] * sg * (1.0 + p * (1.0 - sg));
+            }
+            for (int64_t t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t tt = t + (K - 1) - k;
+                    if (tt < L) acc += conv_w[d * K + k] * dpre[tt];
+                }
+                dx[row + t] = acc;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t tt = t - (K - 1) + k;
+                    if (tt >= 0) dconv_w[d * K + k] += dpre[t] * x[row + tt];
+                }
+                if (dconv_b) dconv_b[d] += dpre[t];
+            }
+        }
+    free(dpre);
+}
+
 void oracle_scan_fwd(int64_t Bt, int64_t D, int64_t N, int64_t L,
                      const double* u, const double* delta_raw, const double* A,
                      const double* Bm, const double* Cm,

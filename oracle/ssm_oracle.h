@@ -52,6 +52,10 @@ double oracle_silu(double z);
  * x at t < 0 being 0.  x, u: (Bt, D, L); conv_w: (D, K); conv_b: (D), nullable. */
 void oracle_conv_silu(int64_t Bt, int64_t D, int64_t L, int64_t K, const double* x,
                       const double* conv_w, const double* conv_b /* nullable */, double* u);
+/* Reverse mode of oracle_conv_silu given du (see ssm_oracle.c); dconv_b nullable. */
+void oracle_conv_silu_bwd(int64_t Bt, int64_t D, int64_t L, int64_t K, const double* x,
+                          const double* conv_w, const double* conv_b, const double* du,
+                          double* dx, double* dconv_w, double* dconv_b);
 
 /* Forward selective scan over the whole sequence, sequential in t. */
 void oracle_scan_fwd(int64_t Bt, int64_t D, int64_t N, int64_t L,

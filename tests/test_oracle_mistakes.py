@@ -36,8 +36,9 @@ C_MISTAKES = [
     ("softplus without log1p", "    return log1p(exp(x));\n}", "    return exp(x);\n}"),
     ("h0 ignored", "for (int64_t n = 0; n < N; ++n) h[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;",
      "for (int64_t n = 0; n < N; ++n) h[n] = 0.0;"),
-    ("conv window one token late", "const int64_t tt = t - (K - 1) + k;",
-     "const int64_t tt = t - K + k;"),
+    ("conv window one token late",
+     "const int64_t tt = t - (K - 1) + k;\n                    if (tt >= 0) s += ",
+     "const int64_t tt = t - K + k;\n                    if (tt >= 0) s += "),
     ("conv taps reversed", "if (tt >= 0) s += conv_w[d * K + k] * x[row + tt];",
      "if (tt >= 0) s += conv_w[d * K + (K - 1 - k)] * x[row + tt];"),
     ("dA sign", "dA[d * N + n] += lam[n] * delta * a * hprev;",
@@ -46,6 +47,14 @@ C_MISTAKES = [
      "dB[(b * N + n) * L + t] += g * Cv * delta * u[row + t];"),
     ("dz formula", "dz[row + t] = dy[row + t] * ys[t] * s * (1.0 + zt * (1.0 - s));",
      "dz[row + t] = dy[row + t] * ys[t] * s * (1.0 + zt * s);"),
+    ("conv backward: silu' without its second term",
+     "dpre[t] = du[row + t] * sg * (1.0 + p * (1.0 - sg));", "dpre[t] = du[row + t] * sg;"),
+    ("conv backward: dx taps not mirrored", "const int64_t tt = t + (K - 1) - k;",
+     "const int64_t tt = t + k;"),
+    ("conv backward: dconv_w against the unshifted input",
+     "if (tt >= 0) dconv_w[d * K + k] += dpre[t] * x[row + tt];",
+     "if (tt >= 0) dconv_w[d * K + k] += dpre[t] * x[row + t];"),
+    ("conv backward: dconv_b dropped", "if (dconv_b) dconv_b[d] += dpre[t];", ""),
     ("dh0 without the last decay", "lam[n] *= a; /* becomes a_t lambda_t, the carry into t-1 */",
      "if (t > 0) lam[n] *= a;"),
 ]
@@ -75,13 +84,17 @@ PY_MISTAKES = [
      "\"dz\": gf.pop(\"dz\") + 0.0 * gr.pop(\"dz\")"),
     ("bidirectional backward: the other direction's dhL", "    gr = one(rev, True, dhL_r)\n",
      "    gr = one(rev, True, dhL)\n"),
+    ("conv backward: the scan's du not passed through the prologue",
+     "    dx, dw, db = conv_silu_bwd(x, conv_w, conv_b, out.pop(\"du\"))\n",
+     "    dx, dw, db = conv_silu_bwd(x, conv_w, conv_b, 0.0 * out.pop(\"du\") + 1.0)\n"),
     ("right-to-left output not gated",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        f(z),",
      "        y, h = scan_fwd(f(u), f(d[\"delta_raw\"]), d[\"A\"], f(d[\"Bm\"]), f(d[\"Cm\"]), d.get(\"Dv\"),\n                        None if flip else f(z),"),
 ]
 
 PUBLIC = ("softplus", "silu", "conv_silu", "scan_fwd_conv", "scan_fwd_varlen", "scan_bwd_varlen",
-          "scan_fwd_bidir", "scan_bwd_bidir", "scan_fwd", "scan_step", "scan_bwd")
+          "scan_fwd_bidir", "scan_bwd_bidir", "scan_fwd", "scan_step", "scan_bwd", "conv_silu_bwd",
+          "scan_bwd_conv")
 
 
 def _pin_calls():

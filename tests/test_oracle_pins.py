@@ -604,3 +604,64 @@ def test_bidirectional_backward_adjoint_identity():
     rhs = np.sum(shared["du"] * vu) + np.sum(shared["dz"] * vz)
     rhs += sum(np.sum(gf[names[k]] * vf[k]) for k in f) + sum(np.sum(gr[names[k]] * vr[k]) for k in r)
     assert lhs == pytest.approx(rhs, rel=1e-7)
+
+
+# ----- reverse mode of the conv prologue
+
+def _conv_loss(x, cw, cb, dy, dhL, xin=None, w=None, b=None):
+    y, hL = oracle.scan_fwd_conv(x.u if xin is None else xin, cw if w is None else w,
+                                 cb if b is None else b, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z,
+                                 x.delta_bias, x.h0)
+    return float(np.sum(dy * y) + np.sum(dhL * hL))
+
+
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_conv_backward_matches_central_finite_differences(K):
+    """dx, dconv_w and dconv_b of scan_bwd_conv against central differences of
+    sum(dy * y) + sum(dhL * hL), y and hL from scan_fwd_conv (the tensor in
+    the u slot is the branch input x)."""
+    x = make_inputs(2, 2, 3, 7, seed=30 + K, in_dtype="f32", h0=True, dy=True)
+    rng = _rng(31 + K)
+    cw = rng.standard_normal((2, K)) * 0.7
+    cb = rng.standard_normal(2) * 0.3
+    dhL = rng.standard_normal(x.h0.shape)
+    dy = x.dy.astype(np.float64)
+    g = oracle.scan_bwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, dy, x.Dv, x.z,
+                             x.delta_bias, x.h0, dhL)
+    eps = 1e-6
+    for name, base, gname in (("xin", x.u.astype(np.float64), "dx"), ("w", cw, "dconv_w"),
+                              ("b", cb, "dconv_b")):
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            p = base.copy(); p[idx] += eps
+            m = base.copy(); m[idx] -= eps
+            fd[idx] = (_conv_loss(x, cw, cb, dy, dhL, **{name: p}) -
+                       _conv_loss(x, cw, cb, dy, dhL, **{name: m})) / (2 * eps)
+        np.testing.assert_allclose(g[gname], fd, rtol=2e-6, atol=2e-8, err_msg=gname)
+
+
+def test_conv_backward_width_one_is_the_silu_derivative():
+    """K = 1, weight 1, no bias: u = silu(x), so dx = du silu'(x) with
+    silu'(x) = s + x s (1 - s), s the logistic function, and dconv_w =
+    sum du silu'(x) x."""
+    rng = _rng(40)
+    x = rng.standard_normal((2, 3, 11))
+    du = rng.standard_normal((2, 3, 11))
+    dx, dw, db = oracle.conv_silu_bwd(x, np.ones((3, 1)), None, du)
+    s = expit(x)
+    ref = du * (s + x * s * (1.0 - s))
+    np.testing.assert_allclose(dx, ref, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dw[:, 0], np.sum(ref * x, axis=(0, 2)), rtol=1e-12)
+    assert db is None
+
+
+def test_conv_backward_rest_is_the_scan_backward_on_u():
+    """Every output besides dx, dconv_w, dconv_b is scan_bwd's on u = conv_silu(x)."""
+    x = make_inputs(1, 3, 4, 20, seed=41, in_dtype="f32", h0=True, dy=True)
+    cw = _rng(42).standard_normal((3, 4)) * 0.5
+    g = oracle.scan_bwd_conv(x.u, cw, None, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, x.Dv, x.z,
+                             x.delta_bias, x.h0)
+    u = oracle.conv_silu(x.u, cw, None)
+    r = oracle.scan_bwd(u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, x.Dv, x.z, x.delta_bias, x.h0)
+    for k in ("ddelta_raw", "dA", "dB", "dC", "dD", "dz", "ddelta_bias", "dh0"):
+        np.testing.assert_array_equal(g[k], r[k], err_msg=k)
