@@ -94,7 +94,8 @@ enum {
 
 /* Bytes of device workspace the call needs for this shape on the current
  * device: for_backward = 0 for ssm_scan_fwd (and its _conv and _varlen forms),
- * 1 for ssm_scan_bwd, 2 for ssm_scan_fwd_bidir, 3 for ssm_scan_bwd_bidir.  Always at
+ * 1 for ssm_scan_bwd (and _varlen), 2 for ssm_scan_fwd_bidir, 3 for
+ * ssm_scan_bwd_bidir, 4 for ssm_scan_bwd_conv.  Always at
  * least 256 (the status word lives at offset 0).  Returns 0 for an invalid
  * shape. */
 SSM_API size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward);
@@ -272,6 +273,29 @@ SSM_API int ssm_scan_bwd_varlen(const ssm_shape* shape, const void* u, const int
                  const float* D, const void* z, const float* delta_bias, const float* h0,
                  const void* dy, const float* dhL, void* du, void* ddelta_raw, float* dA,
                  float* dB, float* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                 void* workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/* Reverse mode of ssm_scan_fwd_conv: the scan's reverse mode with u formed
+ * from the branch input x inside both sweeps ("Mamba Architecture
+ * Explained", section "The Architecture in Practice": the branch's Conv1D
+ * and SiLU before the selective SSM), then the prologue's own reverse mode.
+ * With pre[t] = conv_b[d] + sum_{k<conv_k} conv_w[d,k] x[t-(conv_k-1)+k]
+ * (x before token 0 is 0) and u = silu(pre), from the scan's du:
+ *   dx[t] = sum_k conv_w[d,k] dpre[t+(conv_k-1)-k],  dpre = du silu'(pre)
+ *   dconv_w[d,k] = sum_{b,t} dpre[t] x[t-(conv_k-1)+k],  dconv_b[d] = sum_{b,t} dpre[t]
+ *   x, conv_w, conv_b, conv_k : as for ssm_scan_fwd_conv (conv_b nullable).
+ *   dx : out_dtype (batch, dim, seqlen), required (replaces du).
+ *   dconv_w : fp32 (dim, conv_k), required;  dconv_b : fp32 (dim), nullable.
+ *   Everything else as ssm_scan_bwd.  workspace >= ssm_scan_workspace_bytes(
+ *   shape, 4) bytes (it also holds the scan's du, in out_dtype).  Built for
+ *   9 to 16 states and rows of seqlen * element size a multiple of 16 bytes;
+ *   other shapes return SSM_ERR_UNSUPPORTED before anything is enqueued. */
+SSM_API int ssm_scan_bwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,
+                 const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* delta_bias, const float* h0, const void* dy, const float* dhL,
+                 void* dx, void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                 void* dz, float* ddelta_bias, float* dh0, float* dconv_w, float* dconv_b,
                  void* workspace, size_t ws_bytes, ssm_stream_t stream);
 
 /* One recurrent (decode) step for a single token per sequence, with the

@@ -43,7 +43,7 @@ SSM_ERR_SEQLENS = -9
 # Every symbol include/ssm_scan.h declares.
 EXPORTS = ("ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_scan_fwd_conv", "ssm_scan_fwd_varlen",
            "ssm_scan_fwd_bidir", "ssm_scan_bwd", "ssm_scan_bwd_varlen", "ssm_scan_bwd_bidir",
-           "ssm_scan_step",
+           "ssm_scan_bwd_conv", "ssm_scan_step",
            "ssm_get_status", "ssm_strerror", "ssm_debug_expired_wait", "ssm_scan_fwd_noalloc")
 
 
@@ -74,6 +74,9 @@ lib.ssm_scan_bwd_varlen.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, ctypes.c
 lib.ssm_scan_bwd_varlen.restype = ctypes.c_int
 lib.ssm_scan_bwd_bidir.argtypes = [ctypes.POINTER(ssm_shape)] + [_P] * 36 + [ctypes.c_size_t, _P]
 lib.ssm_scan_bwd_bidir.restype = ctypes.c_int
+lib.ssm_scan_bwd_conv.argtypes = ([ctypes.POINTER(ssm_shape), _P, _P, _P, ctypes.c_int] + [_P] * 22
+                                  + [ctypes.c_size_t, _P])
+lib.ssm_scan_bwd_conv.restype = ctypes.c_int
 lib.ssm_scan_step.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32] + [_P] * 12
 lib.ssm_scan_step.restype = ctypes.c_int
 lib.ssm_get_status.argtypes = [_P, _P]
@@ -440,6 +443,59 @@ def ssm_scan_bwd(u, delta_raw, A, B, C, dy, D=None, z=None, delta_bias=None, h0=
                           workspace.numel(), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SSMError(rc, "ssm_scan_bwd")
+    return g
+
+
+def ssm_scan_bwd_conv(x, conv_w, conv_b, delta_raw, A, B, C, dy, D=None, z=None,
+                      delta_bias=None, h0=None, dhL=None, *, out_dtype: Optional[torch.dtype] = None,
+                      workspace=None, stream=None) -> dict:
+    """Reverse mode of ssm_scan_fwd_conv: x is the branch input, conv_w (D, K)
+    fp32 with K <= 4, conv_b (D,) fp32 or None.  Returns the dict of
+    ssm_scan_bwd with du replaced by dx (out_dtype) and dconv_w (D, K),
+    dconv_b (D,) fp32 (None without conv_b)."""
+    Bt, Dm, L = x.shape
+    N = A.shape[1]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssm_scan_bwd_conv runs on CUDA tensors only")
+    if conv_w.dim() != 2 or conv_w.shape[0] != Dm:
+        raise ValueError("conv_w must be (D, K)")
+    K = conv_w.shape[1]
+    tin = x.dtype
+    out_dtype = tin if out_dtype is None else out_dtype
+    for t, n, s in ((x, "x", (Bt, Dm, L)), (delta_raw, "delta_raw", (Bt, Dm, L)),
+                    (z, "z", (Bt, Dm, L)), (dy, "dy", (Bt, Dm, L)), (B, "B", (Bt, N, L)),
+                    (C, "C", (Bt, N, L))):
+        _check(t, n, s, tin, dev)
+    _check(conv_w, "conv_w", (Dm, K), torch.float32, dev)
+    _check(conv_b, "conv_b", (Dm,), torch.float32, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    _check(h0, "h0", (Bt, Dm, N), torch.float32, dev)
+    _check(dhL, "dhL", (Bt, Dm, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {
+        "dx": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev),
+        "ddelta_raw": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev),
+        "dz": torch.empty((Bt, Dm, L), dtype=out_dtype, device=dev) if z is not None else None,
+        "dA": torch.empty((Dm, N), **f32), "dB": torch.empty((Bt, N, L), **f32),
+        "dC": torch.empty((Bt, N, L), **f32), "dD": torch.empty((Dm,), **f32),
+        "ddelta_bias": torch.empty((Dm,), **f32), "dh0": torch.empty((Bt, Dm, N), **f32),
+        "dconv_w": torch.empty((Dm, K), **f32),
+        "dconv_b": torch.empty((Dm,), **f32) if conv_b is not None else None,
+    }
+    shape = make_shape(Bt, Dm, N, L, _dt(tin), _dt(out_dtype))
+    workspace = _workspace(shape, 4, dev, workspace)
+    rc = lib.ssm_scan_bwd_conv(ctypes.byref(shape), _ptr(x), _ptr(conv_w), _ptr(conv_b), K,
+                               _ptr(delta_raw), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                               _ptr(delta_bias), _ptr(h0), _ptr(dy), _ptr(dhL), _ptr(g["dx"]),
+                               _ptr(g["ddelta_raw"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                               _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+                               _ptr(g["dconv_w"]), _ptr(g["dconv_b"]), _ptr(workspace),
+                               workspace.numel(), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SSMError(rc, "ssm_scan_bwd_conv")
     return g
 
 

@@ -572,9 +572,20 @@ const char* ssm_strerror(int code) {
     }
 }
 
+// The backward fed by the conv prologue: the whole-row plan, then the
+// sweeps' fp32 du (which the prologue's reverse mode reads) and, for bf16
+// outputs, their fp32 ddelta_raw and dz (which the same pass rounds once).
+static size_t conv_bwd_du_offset(const BwdPlan& pl) { return align256(pl.bytes); }
+static size_t conv_bwd_bytes(const ssm_shape& s, int sm_count) {
+    const BwdPlan pl = plan_bwd(s, sm_count, false);
+    const size_t row = align256((size_t)s.batch * s.dim * s.seqlen * 4);
+    return conv_bwd_du_offset(pl) + row * (s.out_dtype == SSM_BF16 ? 3 : 1);
+}
+
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
     if (shape_check(shape) != SSM_OK) return 0;
-    const size_t bytes = for_backward == 3 ? bidir_bwd_layout(*shape, device_sm_count()).bytes
+    const size_t bytes = for_backward == 4 ? conv_bwd_bytes(*shape, device_sm_count())
+                         : for_backward == 3 ? bidir_bwd_layout(*shape, device_sm_count()).bytes
                          : for_backward == 2 ? plan_fwd_bidir(*shape, device_sm_count()).bytes
                          : for_backward ? plan_bwd(*shape, device_sm_count()).bytes
                                         : plan_fwd(*shape, device_sm_count()).bytes;
@@ -857,14 +868,26 @@ int ssm_scan_fwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu
                          stream);
 }
 
-// The backward, over whole rows or over packed sequences (cu_seqlens non-null).
+// The conv prologue's part of a backward call: u is then the branch input x,
+// and dx, dconv_w, dconv_b replace du.
+struct ConvBwd {
+    const float* w;
+    const float* b;
+    int k;
+    void* dx;
+    float* dw;
+    float* db;
+};
+
+// The backward, over whole rows or over packed sequences (cu_seqlens non-null),
+// or fed by the conv prologue (conv non-null; whole rows).
 static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,
                          int nseq, const void* delta_raw, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias,
                          const float* h0, const void* dy, const float* dhL, void* du,
                          void* ddelta_raw, float* dA, float* dB, float* dC, float* dD, void* dz,
                          float* ddelta_bias, float* dh0, void* workspace, size_t ws_bytes,
-                         ssm_stream_t stream) {
+                         ssm_stream_t stream, const ConvBwd* conv = nullptr) {
     const int sc = shape_check(shape);
     if (sc != SSM_OK) return sc;
     const ssm_shape s = *shape;
@@ -874,6 +897,19 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     if (varlen && ((uintptr_t)cu_seqlens % 4) != 0) return SSM_ERR_ALIGN;
     if (Dm > 0 && !A) return SSM_ERR_NULL;
     if (Dm > 0 && !dA) return SSM_ERR_NULL;
+    if (conv) {
+        if (!conv->w || !conv->dw) return SSM_ERR_NULL;
+        if (conv->k < 1 || conv->k > 4) return SSM_ERR_SHAPE;
+        const void* cp[] = {conv->w, conv->b, conv->dx, conv->dw, conv->db};
+        for (const void* q : cp)
+            if (q && !aligned16(q)) return SSM_ERR_ALIGN;
+        // the prologue's parameter gradients are sums: they start at zero
+        cudaStream_t st0 = static_cast<cudaStream_t>(stream);
+        if (Dm > 0 && (cudaMemsetAsync(conv->dw, 0, (size_t)(Dm * conv->k) * 4, st0) != cudaSuccess ||
+                       (conv->db && cudaMemsetAsync(conv->db, 0, (size_t)Dm * 4, st0) != cudaSuccess)))
+            return cuda_fail();
+        if (L > 0 && Bt > 0 && Dm > 0 && !conv->dx) return SSM_ERR_NULL;
+    }
     if (Bt == 0 || Dm == 0) {
         // nothing flows; gradients of the per-channel parameters are zero
         cudaStream_t st0 = static_cast<cudaStream_t>(stream);
@@ -892,7 +928,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         return SSM_OK;
     }
     if (!workspace) return SSM_ERR_WORKSPACE;
-    if (L > 0 && (!u || !delta_raw || !B || !C || !dy || !du || !ddelta_raw || !dB || !dC))
+    if (L > 0 && (!u || !delta_raw || !B || !C || !dy || (!du && !conv) || !ddelta_raw || !dB || !dC))
         return SSM_ERR_NULL;
     const void* ptrs[] = {u, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL, du, ddelta_raw,
                           dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace};
@@ -900,8 +936,28 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         if (q && !aligned16(q)) return SSM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int sms = device_sm_count();
-    const BwdPlan pl = plan_bwd(s, sms);
+    const BwdPlan pl = plan_bwd(s, sms, conv == nullptr);
     if (!pl.ok) return SSM_ERR_SHAPE;   // no channel tile fits the shared memory
+    // conv prologue: built for 9..16 states and 16-byte token rows; the
+    // sweeps' du goes to the workspace, after the plan's buffers
+    if (conv && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
+    if (conv && ws_bytes < conv_bwd_bytes(s, sms)) return SSM_ERR_WORKSPACE;
+    // fp32 copies of ddelta_raw and dz before rounding (bf16 outputs)
+    float* ddr32 = nullptr;
+    float* dz32 = nullptr;
+    void* ddr_user = ddelta_raw;
+    void* dz_user = dz;
+    if (conv) {
+        uint8_t* base = static_cast<uint8_t*>(workspace) + conv_bwd_du_offset(pl);
+        const size_t row = align256((size_t)Bt * Dm * L * 4);
+        du = base;
+        if (s.out_dtype == SSM_BF16) {
+            ddr32 = reinterpret_cast<float*>(base + row);
+            dz32 = dz ? reinterpret_cast<float*>(base + 2 * row) : nullptr;
+            ddelta_raw = ddr32;
+            dz = dz32;
+        }
+    }
     // packed sequences: built for 9..16 states and 16-byte token rows
     if (varlen && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
@@ -976,6 +1032,11 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     p.cu_seqlens = cu_seqlens; p.nseq = varlen ? nseq : 0;
     p.status = status;
     p.timeout_ns = kDefaultTimeoutNs;
+    if (conv) {
+        p.conv_w = conv->w;
+        p.conv_b = conv->b;
+        p.conv_k = conv->k;
+    }
     const unsigned gx = (unsigned)((Dm + pl.CH - 1) / pl.CH);
     if (varlen && pl.nseg == 1) {
         BwdLaunch lc;
@@ -1070,6 +1131,22 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
             return cuda_fail();
         return SSM_OK;
     }
+    if (conv) {
+        // the sweeps with u formed from x, then the prologue's reverse mode
+        BwdLaunch lc;
+        lc.grid = dim3(gx, (unsigned)Bt);
+        lc.warps = pl.W;
+        lc.stages_f = pl.stages_f;
+        lc.stages_r = pl.stages_r;
+        lc.smem_f = pl.smem_f;
+        lc.smem_r = pl.smem_r;
+        if (launch_bwd_conv_np16(pl.NT, s.in_dtype, p, maps, lc, st) != cudaSuccess ||
+            launch_conv_bwd(s.in_dtype, s.out_dtype, Bt, Dm, L, conv->k, u, conv->w, conv->b,
+                            static_cast<const float*>(du), conv->dx, conv->dw, conv->db, ddr32,
+                            ddr_user, dz32, dz_user, st) != cudaSuccess)
+            return cuda_fail();
+        return SSM_OK;
+    }
     if (launch_bwd(pl, s.in_dtype, s.out_dtype, p, maps, dim3(gx, (unsigned)Bt), st) != cudaSuccess)
         return cuda_fail();
     return SSM_OK;
@@ -1084,6 +1161,19 @@ int ssm_scan_bwd(const ssm_shape* shape, const void* u, const void* delta_raw, c
     return scan_bwd_impl(shape, u, nullptr, 0, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL,
                          du, ddelta_raw, dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace,
                          ws_bytes, stream);
+}
+
+int ssm_scan_bwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,
+                      const float* conv_b, int conv_k, const void* delta_raw, const float* A,
+                      const void* B, const void* C, const float* D, const void* z,
+                      const float* delta_bias, const float* h0, const void* dy, const float* dhL,
+                      void* dx, void* ddelta_raw, float* dA, float* dB, float* dC, float* dD,
+                      void* dz, float* ddelta_bias, float* dh0, float* dconv_w, float* dconv_b,
+                      void* workspace, size_t ws_bytes, ssm_stream_t stream) {
+    const ConvBwd cv{conv_w, conv_b, conv_k, dx, dconv_w, dconv_b};
+    return scan_bwd_impl(shape, x, nullptr, 0, delta_raw, A, B, C, D, z, delta_bias, h0, dy, dhL,
+                         nullptr, ddelta_raw, dA, dB, dC, dD, dz, ddelta_bias, dh0, workspace,
+                         ws_bytes, stream, &cv);
 }
 
 int ssm_scan_bwd_varlen(const ssm_shape* shape, const void* u, const int32_t* cu_seqlens,

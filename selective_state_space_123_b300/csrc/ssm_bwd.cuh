@@ -260,6 +260,87 @@ __device__ __forceinline__ void token_prep(const uint8_t* st, int CH, int c, int
     }
 }
 
+// token_prep with u given (the conv prologue forms it from the branch input).
+template <typename TIN, bool ACCURATE>
+__device__ __forceinline__ void token_prep_u(const uint8_t* st, int CH, int c, int tb, int nvalid,
+                                             bool has_z, bool ch_ok, float bias2, const float (&uv)[8],
+                                             float (&d2)[8], float (&du)[8], float (&gq)[8]) {
+    const int RAW = CH * kT * (int)sizeof(TIN);
+    float dv[8], gy[8];
+    load_raw8r<TIN>(st + RAW, CH, c, tb, dv);
+    load_raw8r<TIN>(st + 3 * RAW, CH, c, tb, gy);
+    float zv[8];
+    if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tb, zv);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        d2[q] = softplus2<ACCURATE>(fmaf(dv[q], kLog2e, bias2));
+        du[q] = d2[q] * uv[q];
+        gq[q] = has_z ? gy[q] * zv[q] * rcp(1.0f + ex2(-kLog2e * zv[q])) : gy[q];
+        if (tb + q >= nvalid || !ch_ok) {
+            d2[q] = 0.0f;
+            du[q] = 0.0f;
+            gq[q] = 0.0f;
+        }
+    }
+}
+
+// The conv prologue of the backward: the tile's slot 0 holds the branch
+// input x, and this lane's 8 tokens [tb, tb + 8) of the chunk starting at
+// token t_chunk get u = silu(conv_b + sum_k w_k x[t - 3 + k]) (weights
+// right-aligned to width 4).  The 3 inputs before tb come from the tile, or
+// at tb = 0 from global memory (xrow; zeros before token 0): the reverse
+// sweep meets the chunks last to first, so no halo is carried over.
+template <typename TIN>
+__device__ __forceinline__ void conv_u8(const uint8_t* st, int CH, int c, int tb, int64_t t_chunk,
+                                        const TIN* xrow, const float (&cw4)[4], float cb,
+                                        float (&u)[8]) {
+    float xv[8];
+    load_raw8r<TIN>(st, CH, c, tb, xv);
+    float xw[11];
+    if (tb >= 8) {
+        float pv[8];
+        load_raw8r<TIN>(st, CH, c, tb - 8, pv);
+        xw[0] = pv[5];
+        xw[1] = pv[6];
+        xw[2] = pv[7];
+    } else {
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int64_t t = t_chunk + tb - 3 + q;
+            xw[q] = (xrow && t >= 0) ? Elem<TIN>::to_f(xrow[t]) : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) xw[3 + q] = xv[q];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float a = fmaf(cw4[0], xw[q], cb);
+        a = fmaf(cw4[1], xw[q + 1], a);
+        a = fmaf(cw4[2], xw[q + 2], a);
+        a = fmaf(cw4[3], xw[q + 3], a);
+        u[q] = a * rcp(1.0f + ex2(-kLog2e * a));
+    }
+}
+
+// Load the conv weights of channel d right-aligned to width 4 (leading zeros
+// for a narrower kernel), its bias, and the row of x for the halo loads.
+template <typename TIN>
+__device__ __forceinline__ void conv_setup(const BwdParams& p, bool ch_ok, int64_t d, int64_t row,
+                                           float (&cw4)[4], float& cb, const TIN*& xrow) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cw4[q] = 0.0f;
+    cb = 0.0f;
+    xrow = nullptr;
+    if (!ch_ok) return;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {   // static indices: the weights stay in registers
+        const int kk = q - (4 - p.conv_k);
+        if (kk >= 0) cw4[q] = p.conv_w[d * p.conv_k + kk];
+    }
+    cb = p.conv_b ? p.conv_b[d] : 0.0f;
+    xrow = static_cast<const TIN*>(p.u) + row * p.L;
+}
+
 // Sum over the NT lanes of a channel (every lane gets the sum).
 template <int NT, int V>
 __device__ __forceinline__ void allreduce_nt(float (&v)[V]) {
@@ -322,7 +403,7 @@ __device__ __forceinline__ uint32_t start_bits(const int* cu, int nseq, int64_t 
 // ends with the segment's last token is added by this segment, not by the
 // next one, which would race with this segment's store of that token.
 template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false,
-          bool SEG = false>
+          bool SEG = false, bool CONV = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -433,6 +514,10 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const float Dd = (p.Dv && ch_ok) ? p.Dv[d] : 0.0f;
     const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
     const bool vec_phi = (L % 4) == 0;
+    // CONV: the tile's slot 0 holds the branch input x (u formed per token)
+    float cw4[4], cbias;
+    const TIN* xrow;
+    if constexpr (CONV) conv_setup<TIN>(p, ch_ok, d, row, cw4, cbias, xrow);
     const int src_base = lane & ~(NT - 1);
 
     // A warp whose bounded wait expires records the error and stops working.
@@ -486,8 +571,13 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         for (int sb = 0; sb < kT / SB; ++sb) {
             if (dead || sb * SB >= nvalid) break;
             const int tbk = sb * SB + g * 8;   // this lane's 8 tokens
-            float d2[8], du[8], gq[8];
-            token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            float d2[8], du[8], gq[8], uo[8];
+            if constexpr (CONV) {
+                conv_u8<TIN>(st, CH, c, tbk, k * kT, xrow, cw4, cbias, uo);
+                token_prep_u<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, uo, d2, du, gq);
+            } else {
+                token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            }
             // packed: tokens of this super-block that start a sequence, and
             // psi of an ending sequence to add to phi of its last own token
             const int64_t t_sb = k * kT + sb * SB;
@@ -661,7 +751,12 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             // this lane's tokens: dz and phi
             float uv[8], gy[8], zv[8];
-            load_raw8r<TIN>(st, CH, c, tbk, uv);
+            if constexpr (CONV) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) uv[q] = uo[q];
+            } else {
+                load_raw8r<TIN>(st, CH, c, tbk, uv);
+            }
             load_raw8r<TIN>(st + 3 * RAW, CH, c, tbk, gy);
             if (has_z) load_raw8r<TIN>(st + 2 * RAW, CH, c, tbk, zv);
             float dzv[8], phv[8];
@@ -736,7 +831,8 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
 // (t1 = the next segment's first token; the decay "after" the segment's
 // last token is then 1), and its suffix sum from sum_n A lam_in h_{t1-1},
 // with h_{t1-1} the forward sweep's state at the end of its last chunk.
-template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false>
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA_RAW, bool VARLEN = false,
+          bool CONV = false>
 __global__ void __launch_bounds__(32 * (BwdLayout<NT, NP>::kMaxWarps + 1), 1)
 bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                const __grid_constant__ CUtensorMap tm_dr, const __grid_constant__ CUtensorMap tm_z,
@@ -850,6 +946,9 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
     const bool vec_out = ((L * (int64_t)sizeof(TOUT)) % 16) == 0;
     const int src_base = lane & ~(NT - 1);
     float dD_acc = 0.0f, db_acc = 0.0f;
+    float cw4[4], cbias;   // CONV: see the forward sweep
+    const TIN* xrow;
+    if constexpr (CONV) conv_setup<TIN>(p, ch_ok, d, row, cw4, cbias, xrow);
     bool dead = false;   // see the forward sweep
     // Re-anchor: the suffix sum equals sum_n A a_t lambda_t h_{t-1} at the
     // first token t of a chunk, with h_{t-1} the state the forward sweep
@@ -909,8 +1008,13 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             if (dead) break;
             if (sb * SB >= nvalid) continue;
             const int tbk = sb * SB + g * 8;
-            float d2[8], du[8], gq[8];
-            token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            float d2[8], du[8], gq[8], uo[8];
+            if constexpr (CONV) {
+                conv_u8<TIN>(st, CH, c, tbk, k * kT, xrow, cw4, cbias, uo);
+                token_prep_u<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, uo, d2, du, gq);
+            } else {
+                token_prep<TIN, ACCURATE>(st, CH, c, tbk, nvalid, has_z, ch_ok, bias2, d2, du, gq);
+            }
             // packed: tokens of this super-block that end a sequence
             const int64_t t_sb = k * kT + sb * SB;
             const uint32_t emask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 1) : 0u;
@@ -1022,7 +1126,12 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             const int RAWB = RAW;
             float phv[8], uv[8], dv[8];
             load_raw8r<float>(phit, CH, c, tbk, phv);
-            load_raw8r<TIN>(st, CH, c, tbk, uv);
+            if constexpr (CONV) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) uv[q] = uo[q];
+            } else {
+                load_raw8r<TIN>(st, CH, c, tbk, uv);
+            }
             load_raw8r<TIN>(st + RAWB, CH, c, tbk, dv);
             float suf[8];
             float run = 0.0f;

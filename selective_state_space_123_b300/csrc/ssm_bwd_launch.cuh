@@ -8,10 +8,10 @@
 
 namespace ssm {
 
-template <int NP, int NT, typename TIN, typename TOUT, bool TMA, bool VARLEN = false>
+template <int NP, int NT, typename TIN, typename TOUT, bool TMA, bool VARLEN = false, bool CONV = false>
 cudaError_t launch_bwd_one(const BwdParams& p, const BwdMaps& m, const BwdLaunch& lc, cudaStream_t st) {
-    auto kf = bwd_fwd_kernel<NP, NT, TIN, TOUT, TMA, VARLEN>;
-    auto kr = bwd_rev_kernel<NP, NT, TIN, TOUT, TMA, VARLEN>;
+    auto kf = bwd_fwd_kernel<NP, NT, TIN, TOUT, TMA, VARLEN, false, CONV>;
+    auto kr = bwd_rev_kernel<NP, NT, TIN, TOUT, TMA, VARLEN, CONV>;
     // raise the kernels' dynamic shared-memory limits when a launch needs more
     // than any earlier one on this device
     static size_t attr_f[64] = {}, attr_r[64] = {};
