@@ -13,6 +13,7 @@ fp32 arithmetic, bf16 y, fp32 final state.  Other workloads:
   mamba2p8b_fwdbwd  forward then backward (all gradients), same shape
   million_fwd       forward, batch 1, D 1536, N 16, L 1,048,576
   million_fwdbwd    forward then backward (all gradients), same shape (both segmented)
+  mamba1p4b_conv_fwdbwd  the conv-prologue forward and its backward (dx, conv weight grads)
   decode_step       one recurrent step, batch 256, D 5120, N 16, state in place
 Inputs are synthetic (seeded, drawn on the device) and resident in HBM before
 the timed region; every workload's inputs exceed L2 (126 MB) except where the
@@ -71,6 +72,13 @@ WORKLOADS = {
     # sequence check, tail search, summary pass, carry, scan = 6 launches
     # two directions, each with its own delta/A/B/C/D/bias (B/C preparation
     # twice, right-to-left pass, left-to-right pass = 4 launches)
+    # conv forward (B/C preparation, scan) + conv backward (B/C preparation,
+    # forward sweep, reverse sweep, prologue's reverse mode)
+    "mamba1p4b_conv_fwdbwd": dict(mode="fwdbwd", conv=4, Bt=4, D=4096, N=16, L=4096, seed=2,
+                                  launches=6,
+                                  title="Mamba-1.4B layer forward + backward from the conv branch "
+                                        "input (width-4 causal conv + SiLU fused, and its "
+                                        "reverse mode)"),
     "bidir_mamba1p4b_fwd": dict(mode="fwd", bidir=True, Bt=4, D=4096, N=16, L=4096, seed=6,
                                 launches=4,
                                 title="Mamba-1.4B layer bidirectional scan (left-to-right + "
@@ -316,8 +324,11 @@ def _oracle_worker(args):
         if mode == "fwdbwd":
             oracle.scan_bwd_varlen(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, cu, x.Dv, x.z,
                                    x.delta_bias)
-    elif mode == "fwd" and conv_k:
+    elif conv_k:
         oracle.scan_fwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
+        if mode == "fwdbwd":
+            oracle.scan_bwd_conv(x.u, cw, cb, x.delta_raw, x.A, x.Bm, x.Cm, x.dy, x.Dv, x.z,
+                                 x.delta_bias)
     elif mode == "fwd":
         oracle.scan_fwd(x.u, x.delta_raw, x.A, x.Bm, x.Cm, x.Dv, x.z, x.delta_bias, x.h0)
     elif mode == "fwdbwd":
@@ -373,7 +384,7 @@ class OracleTimer:
         busy = max(r[1] for r in res)
         what = {"fwd": "forward", "fwdbwd": "forward + backward", "step": "decode step"}[w["mode"]]
         if self.conv_k:
-            what = "conv prologue + forward"
+            what = "conv prologue + " + what
         if self.varlen:
             what = "packed-sequence " + what
         if self.bidir:
@@ -440,7 +451,8 @@ class Workload:
             self.y = torch.empty(Bt, D, L, dtype=bf, device="cuda")
             self.hL = torch.empty(Bt, D, N, dtype=torch.float32, device="cuda")
             shape = ssm.make_shape(Bt, D, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
-            nb = ssm.ssm_scan_workspace_bytes(shape, self.mode == "fwdbwd")
+            nb = ssm.ssm_scan_workspace_bytes(
+                shape, (4 if self.conv_k else 1) if self.mode == "fwdbwd" else 0)
             nb = max(nb, ssm.ssm_scan_workspace_bytes(shape, False))
             self.ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
             self.bytes = fwd_bytes(Bt, D, N, L)
@@ -556,6 +568,11 @@ class Workload:
             ssm.ssm_scan_fwd_conv(a["u"], self.conv_w, self.conv_b, a["delta_raw"], a["A"], a["Bm"],
                                   a["Cm"], a["Dv"], a["z"], a["delta_bias"], None,
                                   out_dtype=torch.bfloat16, y=self.y, hL=self.hL, workspace=self.ws)
+            if self.mode == "fwdbwd":
+                self.grads = ssm.ssm_scan_bwd_conv(a["u"], self.conv_w, self.conv_b, a["delta_raw"],
+                                                   a["A"], a["Bm"], a["Cm"], a["dy"], a["Dv"], a["z"],
+                                                   a["delta_bias"], None, None,
+                                                   out_dtype=torch.bfloat16, workspace=self.ws)
             return
         ssm.ssm_scan_fwd(a["u"], a["delta_raw"], a["A"], a["Bm"], a["Cm"], a["Dv"], a["z"],
                          a["delta_bias"], None, out_dtype=torch.bfloat16, y=self.y, hL=self.hL,
