@@ -370,21 +370,64 @@ __device__ __forceinline__ int seq_of_token(const int* cu, int nseq, int64_t t) 
     return max(seq_lower_bound(cu, nseq, t + 1) - 1, 0);
 }
 
-// Bits i (0 <= i < SB) of the super-block starting at token t_sb for which
-// token t_sb + i + shift starts a sequence (shift 0: the token starts one;
-// shift 1: the token is the last of one), counting starts in (0, L) only.
-template <int SB>
-__device__ __forceinline__ uint32_t start_bits(const int* cu, int nseq, int64_t L, int64_t t_sb,
-                                               int shift) {
-    uint32_t m = 0;
-    const int64_t lo = t_sb + shift, hi = t_sb + shift + SB;
-    for (int j = seq_lower_bound(cu, nseq, lo); j < nseq; ++j) {
-        const int64_t c = cu[j];
-        if (c >= hi || c >= L) break;
-        if (c > 0) m |= 1u << (int)(c - lo);
+// A compile-time flag passed to a generic lambda: the token loops of the
+// packed sweeps are instantiated twice, with the per-token start test for
+// the 8-token groups that hold a start and without it for all others.
+template <bool V>
+struct Flag {
+    static constexpr bool value = V;
+};
+
+// The sequence starts in (0, L) met by a sweep, super-block by super-block,
+// walked incrementally instead of searched for in every super-block: one
+// compare per super-block, a load of cu only where a start is passed.
+// bits(lo) returns bit i (0 <= i < SB) set when token lo + i is a start; lo
+// must not decrease between calls (StartsUp) or increase (StartsDown).  The
+// index stays in [-1, nseq] and moves at most nseq times in all, also on
+// unsorted input, and every bit set lies inside the window.
+struct StartsUp {
+    const int* cu;
+    int nseq, j;
+    int64_t L, c;
+    __device__ __forceinline__ void init(const int* cu_, int nseq_, int64_t L_, int64_t t) {
+        cu = cu_; nseq = nseq_; L = L_;
+        j = seq_lower_bound(cu, nseq, t);
+        c = j < nseq ? (int64_t)cu[j] : INT64_MAX;
     }
-    return m;
-}
+    __device__ __forceinline__ void step() { ++j; c = j < nseq ? (int64_t)cu[j] : INT64_MAX; }
+    template <int SB>
+    __device__ __forceinline__ uint32_t bits(int64_t lo) {
+        while (c < lo) step();
+        uint32_t m = 0;
+        while (c < lo + SB) {
+            if (c > 0 && c < L) m |= 1u << (int)(c - lo);
+            step();
+        }
+        return m;
+    }
+};
+struct StartsDown {
+    const int* cu;
+    int nseq, j;
+    int64_t L, c;
+    // t: above every window of the sweep
+    __device__ __forceinline__ void init(const int* cu_, int nseq_, int64_t L_, int64_t t) {
+        cu = cu_; nseq = nseq_; L = L_;
+        j = seq_lower_bound(cu, nseq, t) - 1;
+        c = j >= 0 ? (int64_t)cu[j] : INT64_MIN;
+    }
+    __device__ __forceinline__ void step() { --j; c = j >= 0 ? (int64_t)cu[j] : INT64_MIN; }
+    template <int SB>
+    __device__ __forceinline__ uint32_t bits(int64_t lo) {
+        while (c >= lo + SB) step();
+        uint32_t m = 0;
+        while (c >= lo) {
+            if (c > 0 && c < L) m |= 1u << (int)(c - lo);
+            step();
+        }
+        return m;
+    }
+};
 
 // ===================================================== forward sweep ===
 // blockDim.x = 32 * (W + 1): W compute warps and one producer warp (the last).
@@ -541,6 +584,8 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             hc[j] = make_float4(x0, x1, x2, x3);
         }
     };
+    StartsUp starts;
+    if constexpr (VARLEN) starts.init(p.cu_seqlens, p.nseq, L, k_begin * kT);
     for (int64_t kl = 0; kl < k_end - k_begin; ++kl) {
         const int64_t k = k_begin + kl;        // the chunk; kl its place in this CTA's ring
         const int s = (int)(kl % STAGES);
@@ -581,7 +626,7 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             // packed: tokens of this super-block that start a sequence, and
             // psi of an ending sequence to add to phi of its last own token
             const int64_t t_sb = k * kT + sb * SB;
-            const uint32_t rmask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 0) : 0u;
+            const uint32_t rmask = VARLEN ? starts.template bits<SB>(t_sb) : 0u;
             float psi_add[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) psi_add[q] = 0.0f;
@@ -627,90 +672,94 @@ bwd_fwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
                 const int t_grp = sb * SB + j * 8;
                 float yp[8], pp[8];
+                auto tokens = [&](auto starts_here) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (VARLEN && ((rmask >> (j * 8 + q)) & 1u)) {
-                        const float psi = restart(t_sb + j * 8 + q);
-                        // psi belongs to the token before: an own token of
-                        // this super-block, or one of the previous super-block
-                        // that its owner (the channel's last lane, the thread
-                        // that stored it) adds to in place
-                        if (q > 0) {
-                            if (g == j) psi_add[q - 1] += psi;
-                        } else if (j > 0) {
-                            if (g == j - 1) psi_add[7] += psi;
-                        } else if (g == NT - 1 && ch_ok && !(SEG && t_sb == k_begin * kT)) {
-                            atomicAdd(p.phi + row * L + t_sb - 1, psi);
-                        }
-                    }
-                    if (ACCURATE && ch_ok && t_grp + q < nvalid) {
-                        // h_{t-1} as this token's update uses it (after a restart)
-                        float4* hp = reinterpret_cast<float4*>(
-                            p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
-#pragma unroll
-                        for (int jj = 0; jj < G / 4; ++jj) {
-                            float x0, x1, x2, x3;
-                            upk(full(2 * jj), x0, x1);
-                            upk(full(2 * jj + 1), x2, x3);
-                            hp[jj] = make_float4(x0, x1, x2, x3);
-                        }
-                    }
-                    const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
-                    const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
-                    f2 accy = pk(0.0f, 0.0f), accp = pk(0.0f, 0.0f);
-                    f2 gh[G / 2];
-#pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
-                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int jj = 2 * q4 + e;
-                            const f2 Bj = e ? Bq.y : Bq.x;
-                            const f2 Cj = e ? Cq.y : Cq.x;
-                            f2 a, qv, hn;   // the decay, a_t h_{t-1} and h_t
-                            if constexpr (ACCURATE) {
-                                // compensated state (see comp_update): qv and
-                                // h_t from the full state hi + lo
-                                float x0, x1, i0, i1, h0, h1, l0, l1;
-                                upk(mul2(d2p, Ap[jj]), x0, x1);
-                                upk(mul2(dup, Bj), i0, i1);
-                                upk(h[jj], h0, h1);
-                                upk(hl[jj], l0, l1);
-                                const float e0 = exp2m1_accurate(x0), e1 = exp2m1_accurate(x1);
-                                const float p0 = h0 + l0, p1 = h1 + l1;
-                                qv = pk(fmaf(e0, p0, p0), fmaf(e1, p1, p1));
-                                a = pk(1.0f + e0, 1.0f + e1);
-                                comp_update_e(e0, i0, h0, l0);
-                                comp_update_e(e1, i1, h1, l1);
-                                h[jj] = pk(h0, h1);
-                                hl[jj] = pk(l0, l1);
-                                hn = pk(h0 + l0, h1 + l1);
-                            } else {
-                                a = ex2x2(mul2(d2p, Ap[jj]));
-                                qv = mul2(a, h[jj]);
-                                h[jj] = fma2(dup, Bj, qv);
-                                hn = h[jj];
+                    for (int q = 0; q < 8; ++q) {
+                        if (decltype(starts_here)::value && ((rmask >> (j * 8 + q)) & 1u)) {
+                            const float psi = restart(t_sb + j * 8 + q);
+                            // psi belongs to the token before: an own token of
+                            // this super-block, or one of the previous super-block
+                            // that its owner (the channel's last lane, the thread
+                            // that stored it) adds to in place
+                            if (q > 0) {
+                                if (g == j) psi_add[q - 1] += psi;
+                            } else if (j > 0) {
+                                if (g == j - 1) psi_add[7] += psi;
+                            } else if (g == NT - 1 && ch_ok && !(SEG && t_sb == k_begin * kT)) {
+                                atomicAdd(p.phi + row * L + t_sb - 1, psi);
                             }
-                            m[jj] = fma2(a, m[jj], mul2(d2p, qv));   // dh/dA / ln2
-                            accy = fma2(Cj, hn, accy);
-                            accp = fma2(Ap[jj], mul2(Cj, qv), accp);
-                            const f2 gC = mul2(gqp, Cj);
-                            dAc[jj] = fma2(gC, m[jj], dAc[jj]);
-                            if constexpr (SEG) {
-                                Pd[jj] = mul2(a, Pd[jj]);
-                                GP[jj] = fma2(gC, Pd[jj], GP[jj]);
-                            }
-                            gh[jj] = mul2(gqp, hn);                  // g_t h_t: dC partial
                         }
+                        if (ACCURATE && ch_ok && t_grp + q < nvalid) {
+                            // h_{t-1} as this token's update uses it (after a restart)
+                            float4* hp = reinterpret_cast<float4*>(
+                                p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
+#pragma unroll
+                            for (int jj = 0; jj < G / 4; ++jj) {
+                                float x0, x1, x2, x3;
+                                upk(full(2 * jj), x0, x1);
+                                upk(full(2 * jj + 1), x2, x3);
+                                hp[jj] = make_float4(x0, x1, x2, x3);
+                            }
+                        }
+                        const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
+                        const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
+                        f2 accy = pk(0.0f, 0.0f), accp = pk(0.0f, 0.0f);
+                        f2 gh[G / 2];
+#pragma unroll
+                        for (int q4 = 0; q4 < G / 4; ++q4) {
+                            const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+                            const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int jj = 2 * q4 + e;
+                                const f2 Bj = e ? Bq.y : Bq.x;
+                                const f2 Cj = e ? Cq.y : Cq.x;
+                                f2 a, qv, hn;   // the decay, a_t h_{t-1} and h_t
+                                if constexpr (ACCURATE) {
+                                    // compensated state (see comp_update): qv and
+                                    // h_t from the full state hi + lo
+                                    float x0, x1, i0, i1, h0, h1, l0, l1;
+                                    upk(mul2(d2p, Ap[jj]), x0, x1);
+                                    upk(mul2(dup, Bj), i0, i1);
+                                    upk(h[jj], h0, h1);
+                                    upk(hl[jj], l0, l1);
+                                    const float e0 = exp2m1_accurate(x0), e1 = exp2m1_accurate(x1);
+                                    const float p0 = h0 + l0, p1 = h1 + l1;
+                                    qv = pk(fmaf(e0, p0, p0), fmaf(e1, p1, p1));
+                                    a = pk(1.0f + e0, 1.0f + e1);
+                                    comp_update_e(e0, i0, h0, l0);
+                                    comp_update_e(e1, i1, h1, l1);
+                                    h[jj] = pk(h0, h1);
+                                    hl[jj] = pk(l0, l1);
+                                    hn = pk(h0 + l0, h1 + l1);
+                                } else {
+                                    a = ex2x2(mul2(d2p, Ap[jj]));
+                                    qv = mul2(a, h[jj]);
+                                    h[jj] = fma2(dup, Bj, qv);
+                                    hn = h[jj];
+                                }
+                                m[jj] = fma2(a, m[jj], mul2(d2p, qv));   // dh/dA / ln2
+                                accy = fma2(Cj, hn, accy);
+                                accp = fma2(Ap[jj], mul2(Cj, qv), accp);
+                                const f2 gC = mul2(gqp, Cj);
+                                dAc[jj] = fma2(gC, m[jj], dAc[jj]);
+                                if constexpr (SEG) {
+                                    Pd[jj] = mul2(a, Pd[jj]);
+                                    GP[jj] = fma2(gC, Pd[jj], GP[jj]);
+                                }
+                                gh[jj] = mul2(gqp, hn);                  // g_t h_t: dC partial
+                            }
+                        }
+                        put_tr<NT, NP>(tb + q * Lay::TROW, lane, gh);
+                        float lo, hi;
+                        upk(accy, lo, hi);
+                        yp[q] = lo + hi;
+                        upk(accp, lo, hi);
+                        pp[q] = lo + hi;
                     }
-                    put_tr<NT, NP>(tb + q * Lay::TROW, lane, gh);
-                    float lo, hi;
-                    upk(accy, lo, hi);
-                    yp[q] = lo + hi;
-                    upk(accp, lo, hi);
-                    pp[q] = lo + hi;
-                }
+                };
+                if (VARLEN && ((rmask >> (j * 8)) & 0xffu)) tokens(Flag<VARLEN>{});
+                else tokens(Flag<false>{});
                 __syncwarp();
                 transpose_reduce<NP, CW>(tb, redw, t_grp, lane);
                 allreduce_nt<NT, 8>(yp);
@@ -976,6 +1025,8 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         return part;
     };
 
+    StartsDown starts;
+    if constexpr (VARLEN) starts.init(p.cu_seqlens, p.nseq, L, k_end * kT + 1);
     for (int64_t i = 0; i < k_end - k_begin; ++i) {
         const int64_t k = k_end - 1 - i;       // the chunk; i its place in this CTA's ring
         const int s = (int)(i % STAGES);
@@ -1017,7 +1068,7 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             // packed: tokens of this super-block that end a sequence
             const int64_t t_sb = k * kT + sb * SB;
-            const uint32_t emask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 1) : 0u;
+            const uint32_t emask = VARLEN ? starts.template bits<SB>(t_sb + 1) : 0u;
 
             float sb_own[8], sab_own[8];       // sum_n lambda B', sum_n A a_{t+1} lambda_{t+1} B'
             float qd_own[8];                   // fp32 inputs: Q of the own tokens, formed directly
@@ -1033,78 +1084,82 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                 }
                 const int t_grp = sb * SB + j * 8;
                 float bp[8], abp[8], qd[8];
+                auto tokens = [&](auto ends_here) {
 #pragma unroll
-                for (int q = 7; q >= 0; --q) {
-                    if (VARLEN && ((emask >> (j * 8 + q)) & 1u)) {
-                        // token t ends sequence se, t + 1 starts sn: write
-                        // dh0[sn] = a_{t+1} lambda_{t+1}, then carry dhL[se]
-                        const int64_t t = t_sb + j * 8 + q;
-                        const int sn = seq_of_token(p.cu_seqlens, p.nseq, t + 1);
-                        const int se = seq_of_token(p.cu_seqlens, p.nseq, t);
-                        const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
-                        float* d0p = (p.dh0 && ch_ok) ? p.dh0 + (int64_t)sn * seq_stride + row * N : nullptr;
+                    for (int q = 7; q >= 0; --q) {
+                        if (decltype(ends_here)::value && ((emask >> (j * 8 + q)) & 1u)) {
+                            // token t ends sequence se, t + 1 starts sn: write
+                            // dh0[sn] = a_{t+1} lambda_{t+1}, then carry dhL[se]
+                            const int64_t t = t_sb + j * 8 + q;
+                            const int sn = seq_of_token(p.cu_seqlens, p.nseq, t + 1);
+                            const int se = seq_of_token(p.cu_seqlens, p.nseq, t);
+                            const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+                            float* d0p = (p.dh0 && ch_ok) ? p.dh0 + (int64_t)sn * seq_stride + row * N : nullptr;
 #pragma unroll
-                        for (int jj = 0; jj < G / 2; ++jj) {
-                            const int n0 = g * G + 2 * jj;
-                            if (d0p) {
-                                float v0, v1;
-                                upk(mul2(anext[jj], lam[jj]), v0, v1);
-                                if (n0 < N) d0p[n0] = v0;
-                                if (n0 + 1 < N) d0p[n0 + 1] = v1;
-                            }
-                            lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
-                            anext[jj] = pk(1.0f, 1.0f);
-                        }
-                    }
-                    const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
-                    const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
-                    f2 accb = pk(0.0f, 0.0f), accab = pk(0.0f, 0.0f);
-                    f2 ld[G / 2];
-#pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
-                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int jj = 2 * q4 + e;
-                            const f2 Bj = e ? Bq.y : Bq.x;
-                            const f2 Cj = e ? Cq.y : Cq.x;
-                            const f2 al = mul2(anext[jj], lam[jj]);   // a_{t+1} lambda_{t+1}
-                            lam[jj] = fma2(gqp, Cj, al);
-                            accb = fma2(lam[jj], Bj, accb);
-                            accab = fma2(Ap[jj], mul2(al, Bj), accab);
-                            ld[jj] = mul2(lam[jj], dup);              // dB partial / ln2
-                            const f2 arg = mul2(d2p, Ap[jj]);
-                            anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
-                        }
-                    }
-                    put_tr<NT, NP>(tb + q * Lay::TROW, lane, ld);
-                    float lo, hi;
-                    upk(accb, lo, hi);
-                    bp[q] = lo + hi;
-                    upk(accab, lo, hi);
-                    abp[q] = lo + hi;
-                    if constexpr (ACCURATE) {
-                        // Q_t = sum_n A a_t lambda_t h_{t-1} from the stored state
-                        float qacc = 0.0f;
-                        if (ch_ok && t_grp + q < nvalid) {
-                            const float4* hp = reinterpret_cast<const float4*>(
-                                p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
-#pragma unroll
-                            for (int jj = 0; jj < G / 4; ++jj) {
-                                const float4 hv = hp[jj];
-                                float l0, l1, l2, l3;
-                                upk(mul2(mul2(Ap[2 * jj], anext[2 * jj]), lam[2 * jj]), l0, l1);
-                                upk(mul2(mul2(Ap[2 * jj + 1], anext[2 * jj + 1]), lam[2 * jj + 1]), l2, l3);
-                                qacc = fmaf(l0, hv.x, qacc);
-                                qacc = fmaf(l1, hv.y, qacc);
-                                qacc = fmaf(l2, hv.z, qacc);
-                                qacc = fmaf(l3, hv.w, qacc);
+                            for (int jj = 0; jj < G / 2; ++jj) {
+                                const int n0 = g * G + 2 * jj;
+                                if (d0p) {
+                                    float v0, v1;
+                                    upk(mul2(anext[jj], lam[jj]), v0, v1);
+                                    if (n0 < N) d0p[n0] = v0;
+                                    if (n0 + 1 < N) d0p[n0 + 1] = v1;
+                                }
+                                lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                                anext[jj] = pk(1.0f, 1.0f);
                             }
                         }
-                        qd[q] = qacc;
+                        const float* bcrow = bct + (t_grp + q) * (2 * NP) + g * G;
+                        const f2 d2p = pk(D2[q], D2[q]), dup = pk(DU[q], DU[q]), gqp = pk(GQ[q], GQ[q]);
+                        f2 accb = pk(0.0f, 0.0f), accab = pk(0.0f, 0.0f);
+                        f2 ld[G / 2];
+#pragma unroll
+                        for (int q4 = 0; q4 < G / 4; ++q4) {
+                            const ulonglong2 Bq = *reinterpret_cast<const ulonglong2*>(bcrow + 4 * q4);
+                            const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(bcrow + NP + 4 * q4);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int jj = 2 * q4 + e;
+                                const f2 Bj = e ? Bq.y : Bq.x;
+                                const f2 Cj = e ? Cq.y : Cq.x;
+                                const f2 al = mul2(anext[jj], lam[jj]);   // a_{t+1} lambda_{t+1}
+                                lam[jj] = fma2(gqp, Cj, al);
+                                accb = fma2(lam[jj], Bj, accb);
+                                accab = fma2(Ap[jj], mul2(al, Bj), accab);
+                                ld[jj] = mul2(lam[jj], dup);              // dB partial / ln2
+                                const f2 arg = mul2(d2p, Ap[jj]);
+                                anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
+                            }
+                        }
+                        put_tr<NT, NP>(tb + q * Lay::TROW, lane, ld);
+                        float lo, hi;
+                        upk(accb, lo, hi);
+                        bp[q] = lo + hi;
+                        upk(accab, lo, hi);
+                        abp[q] = lo + hi;
+                        if constexpr (ACCURATE) {
+                            // Q_t = sum_n A a_t lambda_t h_{t-1} from the stored state
+                            float qacc = 0.0f;
+                            if (ch_ok && t_grp + q < nvalid) {
+                                const float4* hp = reinterpret_cast<const float4*>(
+                                    p.hprev + (row * L + k * kT + t_grp + q) * NP + g * G);
+#pragma unroll
+                                for (int jj = 0; jj < G / 4; ++jj) {
+                                    const float4 hv = hp[jj];
+                                    float l0, l1, l2, l3;
+                                    upk(mul2(mul2(Ap[2 * jj], anext[2 * jj]), lam[2 * jj]), l0, l1);
+                                    upk(mul2(mul2(Ap[2 * jj + 1], anext[2 * jj + 1]), lam[2 * jj + 1]), l2, l3);
+                                    qacc = fmaf(l0, hv.x, qacc);
+                                    qacc = fmaf(l1, hv.y, qacc);
+                                    qacc = fmaf(l2, hv.z, qacc);
+                                    qacc = fmaf(l3, hv.w, qacc);
+                                }
+                            }
+                            qd[q] = qacc;
+                        }
                     }
-                }
+                };
+                if (VARLEN && ((emask >> (j * 8)) & 0xffu)) tokens(Flag<VARLEN>{});
+                else tokens(Flag<false>{});
                 __syncwarp();
                 transpose_reduce<NP, CW>(tb, redw, t_grp, lane);
                 allreduce_nt<NT, 8>(bp);
@@ -1331,6 +1386,8 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
         cut = lb < p.nseq && (int64_t)p.cu_seqlens[lb] <= s1 && (int64_t)p.cu_seqlens[lb] < L;
     }
 
+    StartsDown starts;
+    if constexpr (VARLEN) starts.init(p.cu_seqlens, p.nseq, L, k_end * kT + 1);
     for (int64_t i = 0; i < k_end - k_begin; ++i) {
         const int64_t k = k_end - 1 - i;
         const int s = (int)(i % STAGES);
@@ -1357,7 +1414,7 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             for (int q = 0; q < 8; ++q) s8 += d2[q];
             sum_d2 += (double)s8;
             const int64_t t_sb = k * kT + sb * SB;
-            const uint32_t emask = VARLEN ? start_bits<SB>(p.cu_seqlens, p.nseq, L, t_sb, 1) : 0u;
+            const uint32_t emask = VARLEN ? starts.template bits<SB>(t_sb + 1) : 0u;
 #pragma unroll 1
             for (int j = NT - 1; j >= 0; --j) {
                 const int src = src_base + j;
@@ -1368,34 +1425,38 @@ bwd_lam_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
                     GQ[q] = NT == 1 ? gq[q] : __shfl_sync(0xffffffffu, gq[q], src);
                 }
                 const int t_grp = sb * SB + j * 8;
+                auto tokens = [&](auto ends_here) {
 #pragma unroll
-                for (int q = 7; q >= 0; --q) {
-                    if (VARLEN && ((emask >> (j * 8 + q)) & 1u)) {
-                        // token t ends sequence se: the adjoint restarts from dhL[se]
-                        const int se = seq_of_token(p.cu_seqlens, p.nseq, t_sb + j * 8 + q);
-                        const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
+                    for (int q = 7; q >= 0; --q) {
+                        if (decltype(ends_here)::value && ((emask >> (j * 8 + q)) & 1u)) {
+                            // token t ends sequence se: the adjoint restarts from dhL[se]
+                            const int se = seq_of_token(p.cu_seqlens, p.nseq, t_sb + j * 8 + q);
+                            const float* dh = (p.dhL && ch_ok) ? p.dhL + (int64_t)se * seq_stride + row * N : nullptr;
 #pragma unroll
-                        for (int jj = 0; jj < G / 2; ++jj) {
-                            const int n0 = g * G + 2 * jj;
-                            lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
-                            anext[jj] = pk(1.0f, 1.0f);
+                            for (int jj = 0; jj < G / 2; ++jj) {
+                                const int n0 = g * G + 2 * jj;
+                                lam[jj] = pk((dh && n0 < N) ? dh[n0] : 0.0f, (dh && n0 + 1 < N) ? dh[n0 + 1] : 0.0f);
+                                anext[jj] = pk(1.0f, 1.0f);
+                            }
+                        }
+                        const float* crow = bct + (t_grp + q) * (2 * NP) + NP + g * G;
+                        const f2 d2p = pk(D2[q], D2[q]), gqp = pk(GQ[q], GQ[q]);
+#pragma unroll
+                        for (int q4 = 0; q4 < G / 4; ++q4) {
+                            const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(crow + 4 * q4);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int jj = 2 * q4 + e;
+                                const f2 Cj = e ? Cq.y : Cq.x;
+                                lam[jj] = fma2(gqp, Cj, mul2(anext[jj], lam[jj]));
+                                const f2 arg = mul2(d2p, Ap[jj]);
+                                anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
+                            }
                         }
                     }
-                    const float* crow = bct + (t_grp + q) * (2 * NP) + NP + g * G;
-                    const f2 d2p = pk(D2[q], D2[q]), gqp = pk(GQ[q], GQ[q]);
-#pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2*>(crow + 4 * q4);
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int jj = 2 * q4 + e;
-                            const f2 Cj = e ? Cq.y : Cq.x;
-                            lam[jj] = fma2(gqp, Cj, mul2(anext[jj], lam[jj]));
-                            const f2 arg = mul2(d2p, Ap[jj]);
-                            anext[jj] = ACCURATE ? exp2_accurate_x2(arg) : ex2x2(arg);
-                        }
-                    }
-                }
+                };
+                if (VARLEN && ((emask >> (j * 8)) & 0xffu)) tokens(Flag<VARLEN>{});
+                else tokens(Flag<false>{});
             }
         }
         __syncwarp();
