@@ -287,7 +287,8 @@ SSM_API int ssm_scan_bwd_varlen(const ssm_shape* shape, const void* u, const int
  *   dx : out_dtype (batch, dim, seqlen), required (replaces du).
  *   dconv_w : fp32 (dim, conv_k), required;  dconv_b : fp32 (dim), nullable.
  *   Everything else as ssm_scan_bwd.  workspace >= ssm_scan_workspace_bytes(
- *   shape, 4) bytes (it also holds the scan's du, in out_dtype).  Built for
+ *   shape, 4) bytes (it also holds the scan's du in fp32, so that dx is
+ *   rounded once).  Built for
  *   9 to 16 states and rows of seqlen * element size a multiple of 16 bytes;
  *   other shapes return SSM_ERR_UNSUPPORTED before anything is enqueued. */
 SSM_API int ssm_scan_bwd_conv(const ssm_shape* shape, const void* x, const float* conv_w,

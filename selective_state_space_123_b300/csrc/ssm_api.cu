@@ -573,13 +573,11 @@ const char* ssm_strerror(int code) {
 }
 
 // The backward fed by the conv prologue: the whole-row plan, then the
-// sweeps' fp32 du (which the prologue's reverse mode reads) and, for bf16
-// outputs, their fp32 ddelta_raw and dz (which the same pass rounds once).
+// sweeps' fp32 du, which the prologue's reverse mode reads.
 static size_t conv_bwd_du_offset(const BwdPlan& pl) { return align256(pl.bytes); }
 static size_t conv_bwd_bytes(const ssm_shape& s, int sm_count) {
     const BwdPlan pl = plan_bwd(s, sm_count, false);
-    const size_t row = align256((size_t)s.batch * s.dim * s.seqlen * 4);
-    return conv_bwd_du_offset(pl) + row * (s.out_dtype == SSM_BF16 ? 3 : 1);
+    return conv_bwd_du_offset(pl) + align256((size_t)s.batch * s.dim * s.seqlen * 4);
 }
 
 size_t ssm_scan_workspace_bytes(const ssm_shape* shape, int for_backward) {
@@ -942,22 +940,7 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
     // sweeps' du goes to the workspace, after the plan's buffers
     if (conv && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (conv && ws_bytes < conv_bwd_bytes(s, sms)) return SSM_ERR_WORKSPACE;
-    // fp32 copies of ddelta_raw and dz before rounding (bf16 outputs)
-    float* ddr32 = nullptr;
-    float* dz32 = nullptr;
-    void* ddr_user = ddelta_raw;
-    void* dz_user = dz;
-    if (conv) {
-        uint8_t* base = static_cast<uint8_t*>(workspace) + conv_bwd_du_offset(pl);
-        const size_t row = align256((size_t)Bt * Dm * L * 4);
-        du = base;
-        if (s.out_dtype == SSM_BF16) {
-            ddr32 = reinterpret_cast<float*>(base + row);
-            dz32 = dz ? reinterpret_cast<float*>(base + 2 * row) : nullptr;
-            ddelta_raw = ddr32;
-            dz = dz32;
-        }
-    }
+    if (conv) du = static_cast<uint8_t*>(workspace) + conv_bwd_du_offset(pl);
     // packed sequences: built for 9..16 states and 16-byte token rows
     if (varlen && L > 0 && (pl.NP != 16 || !pl.tma_raw)) return SSM_ERR_UNSUPPORTED;
     if (ws_bytes < pl.bytes) return SSM_ERR_WORKSPACE;
@@ -1140,10 +1123,10 @@ static int scan_bwd_impl(const ssm_shape* shape, const void* u, const int32_t* c
         lc.stages_r = pl.stages_r;
         lc.smem_f = pl.smem_f;
         lc.smem_r = pl.smem_r;
-        if (launch_bwd_conv_np16(pl.NT, s.in_dtype, p, maps, lc, st) != cudaSuccess ||
+        if (launch_bwd_conv_np16(pl.NT, s.in_dtype, s.out_dtype, p, maps, lc, st) != cudaSuccess ||
             launch_conv_bwd(s.in_dtype, s.out_dtype, Bt, Dm, L, conv->k, u, conv->w, conv->b,
-                            static_cast<const float*>(du), conv->dx, conv->dw, conv->db, ddr32,
-                            ddr_user, dz32, dz_user, st) != cudaSuccess)
+                            static_cast<const float*>(du), conv->dx, conv->dw, conv->db, st) !=
+                cudaSuccess)
             return cuda_fail();
         return SSM_OK;
     }

@@ -1242,7 +1242,10 @@ bwd_rev_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tm_u,
             }
             if (ch_ok) {
                 const int64_t off = row * L + k * kT + tbk;
-                store_out8<TOUT>(p.du, off, duv, nvalid - tbk, vec_out);
+                // CONV: du is an intermediate (the prologue's reverse mode
+                // reads it), kept in fp32 so that dx is rounded once
+                if constexpr (CONV) store_out8<float>(p.du, off, duv, nvalid - tbk, (L % 4) == 0);
+                else store_out8<TOUT>(p.du, off, duv, nvalid - tbk, vec_out);
                 store_out8<TOUT>(p.ddr, off, ddv, nvalid - tbk, vec_out);
             }
         }

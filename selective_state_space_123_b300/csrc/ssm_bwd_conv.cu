@@ -8,12 +8,19 @@ namespace ssm {
 
 namespace {
 
-// the sweeps write fp32 gradients (the prologue's pass rounds them once)
+// the sweeps write ddelta_raw and dz in the output type and du in fp32 (the
+// prologue's pass reads it and rounds dx once)
+template <int NT, typename TIN>
+cudaError_t conv_tin(int tout, const BwdParams& p, const BwdMaps& m, const BwdLaunch& lc,
+                     cudaStream_t st) {
+    return tout == SSM_BF16 ? launch_bwd_one<16, NT, TIN, __nv_bfloat16, true, false, true>(p, m, lc, st)
+                            : launch_bwd_one<16, NT, TIN, float, true, false, true>(p, m, lc, st);
+}
 template <int NT>
-cudaError_t conv_nt(int tin, const BwdParams& p, const BwdMaps& m, const BwdLaunch& lc,
+cudaError_t conv_nt(int tin, int tout, const BwdParams& p, const BwdMaps& m, const BwdLaunch& lc,
                     cudaStream_t st) {
-    return tin == SSM_BF16 ? launch_bwd_one<16, NT, __nv_bfloat16, float, true, false, true>(p, m, lc, st)
-                           : launch_bwd_one<16, NT, float, float, true, false, true>(p, m, lc, st);
+    return tin == SSM_BF16 ? conv_tin<NT, __nv_bfloat16>(tout, p, m, lc, st)
+                           : conv_tin<NT, float>(tout, p, m, lc, st);
 }
 
 // The prologue's reverse mode over one tile of kConvTile tokens of one
@@ -23,13 +30,14 @@ cudaError_t conv_nt(int tin, const BwdParams& p, const BwdMaps& m, const BwdLaun
 //   dpre[t] = du[t] silu'(pre[t]),  silu'(p) = s (1 + p (1 - s)), s = 1 / (1 + e^-p)
 //   dx[t] = sum_k w[k] dpre[t+(K-1)-k] (terms past the end absent)
 //   dconv_w[d,k] += sum_t dpre[t] x[t-(K-1)+k],  dconv_b[d] += sum_t dpre[t]
-// x of the tile and the 3 tokens on each side, and dpre of the tile and the
-// 3 tokens after it, go through shared memory; the weight and bias sums are
-// reduced over the block and added once per tile.  The sweeps' gradients are
-// fp32; with bf16 outputs the same pass also writes ddelta_raw and dz in the
-// output type (cv_src -> cv_dst, nullable).  Rows of L % 8 != 0 (fp32 inputs
-// with L % 8 = 4) and a group of 8 tokens that crosses a row's end take
-// scalar accesses.
+// Each thread keeps the x and dpre windows of its 8 tokens in registers;
+// only the 3 x before them (from the previous thread) and the 3 dpre after
+// them (from the next thread) go through shared memory, and the tile's
+// first and last threads take those from global memory.  The weight and
+// bias sums are reduced over the block and added once per tile.  du is the
+// sweeps' fp32 output, so dx is rounded once.  Rows of L % 8 != 0 (fp32
+// inputs with L % 8 = 4) and a group of 8 tokens that crosses a row's end
+// take scalar accesses.
 template <typename T> __device__ __forceinline__ T out_as(float v);
 template <> __device__ __forceinline__ float out_as<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 out_as<__nv_bfloat16>(float v) {
@@ -69,15 +77,12 @@ template <typename TIN, typename TOUT>
 __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(
     int64_t D, int64_t L, int K, const TIN* __restrict__ x, const float* __restrict__ conv_w,
     const float* __restrict__ conv_b, const float* __restrict__ du, TOUT* __restrict__ dx,
-    float* __restrict__ dconv_w, float* __restrict__ dconv_b, const float* __restrict__ cv_src0,
-    TOUT* __restrict__ cv_dst0, const float* __restrict__ cv_src1, TOUT* __restrict__ cv_dst1) {
-    // x[t0-3 .. t0+TILE+3) and dpre[t0 .. t0+TILE+3), element i at P(i) =
-    // i + i/32: a thread's 8 tokens are 8 floats apart from its neighbour's,
-    // and the padding puts the 32 lanes' elements in 32 different banks
-    __shared__ float xs[kConvTile + 6 + (kConvTile + 6) / 32 + 1];
-    __shared__ float dps[kConvTile + 3 + (kConvTile + 3) / 32 + 1];
+    float* __restrict__ dconv_w, float* __restrict__ dconv_b) {
+    // the 3 last x and the 3 first dpre of every thread's tokens (stride 3:
+    // the 32 lanes of a warp hit 32 different banks)
+    __shared__ float x_tail[kConvThreads * 3];
+    __shared__ float dp_head[kConvThreads * 3];
     __shared__ float red[kConvThreads / 32][5];
-    auto P = [](int i) { return i + (i >> 5); };
     const int64_t row = blockIdx.x;                    // (batch, channel) row
     const int64_t d = row % D;
     const int64_t t0 = (int64_t)blockIdx.y * kConvTile;
@@ -88,139 +93,144 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(
     const bool full = (L % 8) == 0 && tt + kConvPer <= L;
     const TIN* xr = x + row * L;
     const float* dur = du + row * L;
-    float w[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // the taps aligned to a 4-token window ending at the token: tap m of
+    // wa multiplies x[t-3+m] (zero for m < 4-K), tap m of wb multiplies
+    // dpre[t+m] (zero for m >= K)
+    float wa[4], wb[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-        if (k < K) w[k] = conv_w[d * K + k];
+    for (int m = 0; m < 4; ++m) {
+        wa[m] = m >= 4 - K ? conv_w[d * K + m - (4 - K)] : 0.0f;
+        wb[m] = m < K ? conv_w[d * K + K - 1 - m] : 0.0f;
+    }
     const float cb = conv_b ? conv_b[d] : 0.0f;
-    // x of the own tokens, and the halos (thread 0: the 3 before the tile;
-    // the last thread: the 3 after it)
-    float xv[8];
+    // xw[3 + q] = x of own token q, xw[0..2] = the 3 tokens before (zero
+    // before token 0 and past the row's end)
+    float xw[kConvPer + 3], g[kConvPer];
     if (full) {
-        load8<TIN>(xr + tt, xv);
+        float v[8];
+        load8<TIN>(xr + tt, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xw[3 + q] = v[q];
+        load8<float>(dur + tt, g);
     } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) xv[q] = tt + q < L ? Elem<TIN>::to_f(xr[tt + q]) : 0.0f;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) xs[P(3 + tid * kConvPer + q)] = xv[q];
-    if (tid < 3) {
-        const int64_t t = t0 - 3 + tid;
-        xs[P(tid)] = t >= 0 ? Elem<TIN>::to_f(xr[t]) : 0.0f;
-        const int64_t ta = t0 + kConvTile + tid;
-        xs[P(3 + kConvTile + tid)] = ta < L ? Elem<TIN>::to_f(xr[ta]) : 0.0f;
-    }
-    __syncthreads();
-    // dpre of the own tokens (and of the 3 tokens after the tile)
-    auto dpre_at = [&](int i, float g) -> float {   // i = token index in the tile
-        float pre = cb;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (k < K) pre = fmaf(w[k], xs[P(i + 3 - (K - 1) + k)], pre);
-        const float s = 1.0f / (1.0f + expf(-pre));
-        return g * s * fmaf(pre, 1.0f - s, 1.0f);
-    };
-    float gv[8];
-    if (full) {
-        load8<float>(dur + tt, gv);
-    } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) gv[q] = tt + q < L ? dur[tt + q] : 0.0f;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) dps[P(tid * kConvPer + q)] = dpre_at(tid * kConvPer + q, gv[q]);
-    if (tid < 3) {
-        const int64_t ta = t0 + kConvTile + tid;
-        dps[P(kConvTile + tid)] = ta < L ? dpre_at(kConvTile + tid, dur[ta]) : 0.0f;
-    }
-    __syncthreads();
-    float pw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, pb = 0.0f;
-    if (tt < L) {
-        float o[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int i = tid * kConvPer + q;
-            float acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < K) acc = fmaf(w[k], dps[P(i + (K - 1) - k)], acc);
-            o[q] = acc;
-            if (tt + q < L) {
-                const float dp = dps[P(i)];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (k < K) pw[k] = fmaf(dp, xs[P(i + 3 - (K - 1) + k)], pw[k]);
-                pb += dp;
-            }
-        }
-        TOUT* dxr = dx + row * L;
-        if (full) {
-            store8<TOUT>(dxr + tt, o);
-        } else {
-            for (int q = 0; q < 8; ++q)
-                if (tt + q < L) dxr[tt + q] = out_as<TOUT>(o[q]);
-        }
-        const float* srcs[2] = {cv_src0, cv_src1};
-        TOUT* dsts[2] = {cv_dst0, cv_dst1};
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (!srcs[j]) continue;
-            float v[8];
-            if (full) {
-                load8<float>(srcs[j] + row * L + tt, v);
-                store8<TOUT>(dsts[j] + row * L + tt, v);
-            } else {
-                for (int q = 0; q < 8; ++q)
-                    if (tt + q < L) dsts[j][row * L + tt + q] = out_as<TOUT>(srcs[j][row * L + tt + q]);
-            }
+            xw[3 + q] = tt + q < L ? Elem<TIN>::to_f(xr[tt + q]) : 0.0f;
+            g[q] = tt + q < L ? dur[tt + q] : 0.0f;
         }
     }
-    // block sums: warp shuffles, then the warps' partials
+#pragma unroll
+    for (int j = 0; j < 3; ++j) x_tail[tid * 3 + j] = xw[8 + j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int64_t t = tt - 3 + j;
+        xw[j] = tid > 0 ? x_tail[(tid - 1) * 3 + j] : (t >= 0 ? Elem<TIN>::to_f(xr[t]) : 0.0f);
+    }
+    // dpre = du silu'(pre) from the 4-token window before each token
+    auto dpre = [&](const float (&w4)[4], float gv) -> float {
+        float pre = cb;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) pre = fmaf(wa[m], w4[m], pre);
+        const float sg = rcp(1.0f + ex2(-kLog2e * pre));
+        return gv * sg * fmaf(pre, 1.0f - sg, 1.0f);
+    };
+    // dpw[q] = dpre of own token q, dpw[8..10] = of the 3 tokens after
+    float dpw[kConvPer + 3];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float w4[4] = {xw[q], xw[q + 1], xw[q + 2], xw[q + 3]};
+        dpw[q] = dpre(w4, g[q]);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) dp_head[tid * 3 + j] = dpw[j];
+    if (tid == kConvThreads - 1) {
+        // the 3 tokens after the tile, from their own x and du
+        float xe[6], ge[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int64_t t = tt + 8 + j;
+            xe[j] = xw[8 + j];
+            xe[3 + j] = t < L ? Elem<TIN>::to_f(xr[t]) : 0.0f;
+            ge[j] = t < L ? dur[t] : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const float w4[4] = {xe[j], xe[j + 1], xe[j + 2], xe[j + 3]};
+            dpw[8 + j] = dpre(w4, ge[j]);
+        }
+    }
+    __syncthreads();
+    if (tid < kConvThreads - 1) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) dpw[8 + j] = dp_head[(tid + 1) * 3 + j];
+    }
+    // dx, and the weight and bias sums (dpre is zero past the row's end)
+    float o[8], pw[4] = {0.0f, 0.0f, 0.0f, 0.0f}, pb = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            acc = fmaf(wb[m], dpw[q + m], acc);
+            pw[m] = fmaf(dpw[q], xw[q + m], pw[m]);
+        }
+        o[q] = acc;
+        pb += dpw[q];
+    }
+    TOUT* dxr = dx + row * L;
+    if (full) {
+        store8<TOUT>(dxr + tt, o);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (tt + q < L) dxr[tt + q] = out_as<TOUT>(o[q]);
+    }
+    // block sums: warp shuffles, then the warps' partials; tap m of pw is
+    // weight k = m - (4 - K)
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int sh = 16; sh > 0; sh >>= 1) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) pw[k] += __shfl_xor_sync(0xffffffffu, pw[k], o);
-        pb += __shfl_xor_sync(0xffffffffu, pb, o);
+        for (int m = 0; m < 4; ++m) pw[m] += __shfl_xor_sync(0xffffffffu, pw[m], sh);
+        pb += __shfl_xor_sync(0xffffffffu, pb, sh);
     }
     if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) red[warp][k] = pw[k];
+        for (int m = 0; m < 4; ++m) red[warp][m] = pw[m];
         red[warp][4] = pb;
     }
     __syncthreads();
     if (tid < K + 1) {
-        float s = 0.0f;
-        for (int w8 = 0; w8 < kConvThreads / 32; ++w8) s += red[w8][tid == K ? 4 : tid];
-        if (tid < K) atomicAdd(dconv_w + d * K + tid, s);
-        else if (dconv_b) atomicAdd(dconv_b + d, s);
+        const int slot = tid == K ? 4 : tid + 4 - K;
+        float sum = 0.0f;
+        for (int w8 = 0; w8 < kConvThreads / 32; ++w8) sum += red[w8][slot];
+        if (tid < K) atomicAdd(dconv_w + d * K + tid, sum);
+        else if (dconv_b) atomicAdd(dconv_b + d, sum);
     }
 }
 
 template <typename TIN>
 cudaError_t conv_bwd_tin(int tout, int64_t Bt, int64_t D, int64_t L, int K, const void* x,
                          const float* w, const float* b, const float* du, void* dx, float* dw,
-                         float* db, const float* src0, void* dst0, const float* src1, void* dst1,
-                         cudaStream_t st) {
+                         float* db, cudaStream_t st) {
     const dim3 grid((unsigned)(Bt * D), (unsigned)((L + kConvTile - 1) / kConvTile));
     if (tout == SSM_BF16)
         conv_bwd_kernel<TIN, __nv_bfloat16><<<grid, kConvThreads, 0, st>>>(
-            D, L, K, static_cast<const TIN*>(x), w, b, du, static_cast<__nv_bfloat16*>(dx), dw, db,
-            src0, static_cast<__nv_bfloat16*>(dst0), src1, static_cast<__nv_bfloat16*>(dst1));
+            D, L, K, static_cast<const TIN*>(x), w, b, du, static_cast<__nv_bfloat16*>(dx), dw, db);
     else
         conv_bwd_kernel<TIN, float><<<grid, kConvThreads, 0, st>>>(
-            D, L, K, static_cast<const TIN*>(x), w, b, du, static_cast<float*>(dx), dw, db,
-            src0, static_cast<float*>(dst0), src1, static_cast<float*>(dst1));
+            D, L, K, static_cast<const TIN*>(x), w, b, du, static_cast<float*>(dx), dw, db);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_conv_np16(int NT, int tin, const BwdParams& p, const BwdMaps& m,
+cudaError_t launch_bwd_conv_np16(int NT, int tin, int tout, const BwdParams& p, const BwdMaps& m,
                                  const BwdLaunch& lc, cudaStream_t st) {
     switch (NT) {
-        case 2: return conv_nt<2>(tin, p, m, lc, st);
-        case 4: return conv_nt<4>(tin, p, m, lc, st);
+        case 2: return conv_nt<2>(tin, tout, p, m, lc, st);
+        case 4: return conv_nt<4>(tin, tout, p, m, lc, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -228,14 +238,13 @@ cudaError_t launch_bwd_conv_np16(int NT, int tin, const BwdParams& p, const BwdM
 cudaError_t launch_conv_bwd(int tin, int tout, int64_t Bt, int64_t D, int64_t L, int K,
                             const void* x, const float* conv_w, const float* conv_b,
                             const float* du, void* dx, float* dconv_w, float* dconv_b,
-                            const float* ddr32, void* ddr, const float* dz32, void* dz,
                             cudaStream_t st) {
     if (Bt * D == 0 || L == 0) return cudaSuccess;
     return tin == SSM_BF16
                ? conv_bwd_tin<__nv_bfloat16>(tout, Bt, D, L, K, x, conv_w, conv_b, du, dx, dconv_w,
-                                             dconv_b, ddr32, ddr, dz32, dz, st)
+                                             dconv_b, st)
                : conv_bwd_tin<float>(tout, Bt, D, L, K, x, conv_w, conv_b, du, dx, dconv_w, dconv_b,
-                                     ddr32, ddr, dz32, dz, st);
+                                     st);
 }
 
 }  // namespace ssm

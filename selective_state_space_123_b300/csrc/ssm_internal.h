@@ -99,14 +99,13 @@ cudaError_t launch_bwd_seg_varlen_np16(int NT, int tin, int tout, int part, cons
 // the branch input x, p.conv_w/conv_b/conv_k as in FwdParams), padded state
 // size 16, 16-byte token rows, whole rows; and the prologue's reverse mode:
 // dx (tout), dconv_w, dconv_b (both accumulated with atomics; zeroed by the
-// host) from the sweeps' fp32 du; with ddr32 / dz32 non-null the same pass
-// writes those fp32 gradients as tout into ddr / dz.
-cudaError_t launch_bwd_conv_np16(int NT, int tin, const BwdParams& p, const BwdMaps& m,
+// host) from the sweeps' du.  The sweeps write ddelta_raw and dz as tout and
+// du in fp32 (p.du: an fp32 buffer).
+cudaError_t launch_bwd_conv_np16(int NT, int tin, int tout, const BwdParams& p, const BwdMaps& m,
                                  const BwdLaunch& lc, cudaStream_t st);
 cudaError_t launch_conv_bwd(int tin, int tout, int64_t Bt, int64_t D, int64_t L, int K,
                             const void* x, const float* conv_w, const float* conv_b,
                             const float* du, void* dx, float* dconv_w, float* dconv_b,
-                            const float* ddr32, void* ddr, const float* dz32, void* dz,
                             cudaStream_t st);
 // The dA terms of the tangent flowing into each segment from the ones before
 // (see ssm_aux.cu); after the forward sweep of the segmented backward.
