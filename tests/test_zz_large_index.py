@@ -6,7 +6,9 @@ every batch row, always including the last row of the last batch (whose
 offsets lie beyond 2^31), are compared with the oracle (channels are
 independent given the shared B and C).  The forward runs both on whole rows
 (the planner's segmented plan turned off) and with the planner's choice; the
-backward takes the planner's choice (segments over the long row).
+backward takes the planner's choice (segments over the long row).  The
+decode step runs on a state of more than 2^31 fp32 values (its rows, batch x
+channels, stay below 2^31).
 
 Collected after the other parity files and before test_zz_no_alloc.py.
 """
@@ -92,4 +94,30 @@ def test_backward_past_2_31_elements(ssm):
     for k in ("dA", "dD", "ddelta_bias"):
         assert_close(g[k][ds].cpu().numpy(), o[k], tol, "backward past 2^31 " + k)
     del a, g, dhL
+    torch.cuda.empty_cache()
+
+
+def test_decode_step_state_past_2_31_elements(ssm):
+    """One decode step on (27,000, 5,120, 16): the state holds 2.2e9 fp32 values,
+    updated in place; sampled (batch row, channel) pairs against the oracle's step."""
+    Bt, D, N = 27000, 5120, 16
+    assert Bt * D * N > 2 ** 31
+    a = device_inputs(Bt, D, N, 1, seed=4444, in_dtype="bf16", h0=True)
+    step = {k: a[k][:, :, 0].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
+    state = a["h0"]
+    bsel = [0, 13331, Bt - 1]
+    dsel = np.array([0, 2047, D - 1])
+    state0 = state[bsel][:, dsel].cpu().numpy()
+    y = ssm.ssm_scan_step(step["u"], step["delta_raw"], a["A"], step["Bm"], step["Cm"], state,
+                          a["Dv"], step["z"], a["delta_bias"], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    sub = lambda t: t[bsel][:, dsel].float().cpu().numpy()
+    yo, so = oracle.scan_step(sub(step["u"]), sub(step["delta_raw"]), a["A"][dsel].cpu().numpy(),
+                              step["Bm"][bsel].float().cpu().numpy(),
+                              step["Cm"][bsel].float().cpu().numpy(), state0,
+                              a["Dv"][dsel].cpu().numpy(), sub(step["z"]),
+                              a["delta_bias"][dsel].cpu().numpy())
+    assert_close(y[bsel][:, dsel].cpu().numpy(), yo, TOL["bf16"], "decode past 2^31 y")
+    assert_close(state[bsel][:, dsel].cpu().numpy(), so, TOL["bf16"], "decode past 2^31 state")
+    del a, step, state, y
     torch.cuda.empty_cache()
