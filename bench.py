@@ -708,6 +708,117 @@ def pipelined_e2e(ssm, wl, host, dev, outs_host, state_host, ngroups=4):
     return one_step
 
 
+# gradients with one row per batch row (the rest, per channel, are summed
+# over the batch rows and so over the groups)
+PER_ROW_GRADS = ("du", "dx", "ddelta_raw", "dz", "dB", "dC", "dh0")
+
+
+def pipelined_e2e_fwdbwd(ssm, wl, host, dev, ngroups=4):
+    """End-to-end forward + backward through the public API with the host
+    copies overlapped: the batch rows are split into up to `ngroups` groups
+    that alternate between two streams; each group copies its inputs in, runs
+    the forward and the backward of its rows (plain, conv prologue or
+    bidirectional) and copies its outputs and per-row gradients back, so one
+    group's copies overlap another's kernels and the two copy directions run
+    at once.  The per-channel gradients (dA, dD, ddelta_bias, the conv
+    weights') of the groups are added on the device and copied back once.
+    Returns (step, d2h bytes per step, groups, (forward outputs' host
+    buffers, {(part, key): gradient host buffer}))."""
+    import torch
+    bf = torch.bfloat16
+    cur = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    Bt, D, N, L = wl.w["Bt"], wl.w["D"], wl.w["N"], wl.w["L"]
+    ngroups = max(1, min(ngroups, Bt))
+    bounds = [(i * Bt // ngroups, (i + 1) * Bt // ngroups) for i in range(ngroups)]
+    per_row = [k for k in ("u", "delta_raw", "z", "dy", "delta_raw_r", "Bm", "Cm", "Bm_r", "Cm_r")
+               if k in host]
+    shared = [k for k in host if k not in per_row]
+    gb = max(hi - lo for lo, hi in bounds)
+    shape = ssm.make_shape(gb, D, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
+    flag = 3 if wl.bidir else (4 if wl.conv_k else 1)
+    nb = max(ssm.ssm_scan_workspace_bytes(shape, flag),
+             ssm.ssm_scan_workspace_bytes(shape, 2 if wl.bidir else 0))
+    ws = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in streams]
+    fwd_outs = [wl.y, wl.hL] + ([wl.hL_r] if wl.bidir else [])
+    fwd_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in fwd_outs]
+    grad_host = {}   # (part, key) -> pinned host buffer of the whole batch
+
+    def run_group(a, lo, hi, s_, w_):
+        """Forward and backward of rows lo:hi on stream s_; returns the
+        backward's gradient dicts."""
+        y, h1 = wl.y[lo:hi], wl.hL[lo:hi]
+        if wl.bidir:
+            f = dict(delta_raw=a["delta_raw"], A=dev["A"], B=a["Bm"], C=a["Cm"], D=dev["Dv"],
+                     delta_bias=dev["delta_bias"])
+            r = dict(delta_raw=a["delta_raw_r"], A=dev["A_r"], B=a["Bm_r"], C=a["Cm_r"],
+                     D=dev["Dv_r"], delta_bias=dev["delta_bias_r"])
+            ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=bf, y=y, hL=h1,
+                                   hL_r=wl.hL_r[lo:hi], workspace=w_, stream=s_)
+            return ssm.ssm_scan_bwd_bidir(a["u"], a["z"], f, r, a["dy"], out_dtype=bf,
+                                          workspace=w_, stream=s_)
+        if wl.conv_k:
+            ssm.ssm_scan_fwd_conv(a["u"], wl.conv_w, wl.conv_b, a["delta_raw"], dev["A"], a["Bm"],
+                                  a["Cm"], dev["Dv"], a["z"], dev["delta_bias"], None, out_dtype=bf,
+                                  y=y, hL=h1, workspace=w_, stream=s_)
+            return (ssm.ssm_scan_bwd_conv(a["u"], wl.conv_w, wl.conv_b, a["delta_raw"], dev["A"],
+                                          a["Bm"], a["Cm"], a["dy"], dev["Dv"], a["z"],
+                                          dev["delta_bias"], None, None, out_dtype=bf,
+                                          workspace=w_, stream=s_),)
+        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], dev["A"], a["Bm"], a["Cm"], dev["Dv"], a["z"],
+                         dev["delta_bias"], None, out_dtype=bf, y=y, hL=h1, workspace=w_, stream=s_)
+        return (ssm.ssm_scan_bwd(a["u"], a["delta_raw"], dev["A"], a["Bm"], a["Cm"], a["dy"],
+                                 dev["Dv"], a["z"], dev["delta_bias"], None, None, out_dtype=bf,
+                                 workspace=w_, stream=s_),)
+
+    def host_buf(part, k, t, rows):
+        key = (part, k)
+        if key not in grad_host:
+            shp = (Bt,) + tuple(t.shape[1:]) if rows else tuple(t.shape)
+            grad_host[key] = torch.empty(shp, dtype=t.dtype, pin_memory=True)
+        return grad_host[key]
+
+    def one_step():
+        for k in shared:
+            dev[k].copy_(host[k], non_blocking=True)
+        for s_ in streams:
+            s_.wait_stream(cur)
+        partial = []   # per group: {(part, key): per-channel gradient}
+        for gi, (lo, hi) in enumerate(bounds):
+            s_ = streams[gi % 2]
+            with torch.cuda.stream(s_):
+                a = {}
+                for k in per_row:
+                    a[k] = dev[k][lo:hi]
+                    a[k].copy_(host[k][lo:hi], non_blocking=True)
+                grads = run_group(a, lo, hi, s_, ws[gi % 2])
+                for o, oh in zip(fwd_outs, fwd_host):
+                    oh[lo:hi].copy_(o[lo:hi], non_blocking=True)
+                mine = {}
+                for part, g in enumerate(grads):
+                    for k, t in g.items():
+                        if t is None:
+                            continue
+                        if k in PER_ROW_GRADS:
+                            host_buf(part, k, t, True)[lo:hi].copy_(t, non_blocking=True)
+                        else:
+                            mine[(part, k)] = t
+                partial.append(mine)
+        for s_ in streams:
+            cur.wait_stream(s_)
+        for key, t in partial[0].items():
+            tot = t
+            for m in partial[1:]:
+                tot = tot + m[key]
+            host_buf(key[0], key[1], tot, False).copy_(tot, non_blocking=True)
+
+    one_step()
+    torch.cuda.synchronize()
+    d2h = sum(o.numel() * o.element_size() for o in fwd_host) + \
+        sum(t.numel() * t.element_size() for t in grad_host.values())
+    return one_step, d2h, ngroups, (fwd_host, grad_host)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -819,6 +930,11 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
 
         e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
+        if wl.mode == "fwdbwd" and wl.w["Bt"] > 1 and wl.cu is None:
+            e2e_step, d2h, ng, _ = pipelined_e2e_fwdbwd(ssm, wl, host, dev)
+            e2e_how = ("%d groups of batch rows on 2 streams: a group's copies overlap the other "
+                       "groups' forward and backward; per-channel gradients added on the device"
+                       % ng)
         if wl.mode in ("fwd", "step"):
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
