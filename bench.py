@@ -708,101 +708,138 @@ def pipelined_e2e(ssm, wl, host, dev, outs_host, state_host, ngroups=4):
     return one_step
 
 
-# gradients with one row per batch row (the rest, per channel, are summed
-# over the batch rows and so over the groups)
-PER_ROW_GRADS = ("du", "dx", "ddelta_raw", "dz", "dB", "dC", "dh0")
-
-
 def pipelined_e2e_fwdbwd(ssm, wl, host, dev, ngroups=4):
     """End-to-end forward + backward through the public API with the host
-    copies overlapped: the batch rows are split into up to `ngroups` groups
-    that alternate between two streams; each group copies its inputs in, runs
-    the forward and the backward of its rows (plain, conv prologue or
-    bidirectional) and copies its outputs and per-row gradients back, so one
-    group's copies overlap another's kernels and the two copy directions run
-    at once.  The per-channel gradients (dA, dD, ddelta_bias, the conv
-    weights') of the groups are added on the device and copied back once.
-    Returns (step, d2h bytes per step, groups, (forward outputs' host
-    buffers, {(part, key): gradient host buffer}))."""
+    copies overlapped: the batch rows (or, for a single row, the channels)
+    are split into up to `ngroups` groups that alternate between two
+    streams; each group copies its inputs in, runs the forward and the
+    backward of its part (plain, conv prologue, packed sequences or
+    bidirectional) and copies its outputs and gradients back, so one group's
+    copies overlap another's kernels and the two copy directions run at once.
+    Gradients that sum over the split dimension (per channel: dA, dD,
+    ddelta_bias, the conv weights', when the batch rows are split; dB and dC
+    when the channels are) are added over the groups on the device and copied
+    back once.  Each output is copied into one pinned host buffer, group after
+    group.  Returns (step, d2h bytes per step, groups, {key: host buffer})."""
     import torch
     bf = torch.bfloat16
     cur = torch.cuda.current_stream()
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     Bt, D, N, L = wl.w["Bt"], wl.w["D"], wl.w["N"], wl.w["L"]
-    ngroups = max(1, min(ngroups, Bt))
-    bounds = [(i * Bt // ngroups, (i + 1) * Bt // ngroups) for i in range(ngroups)]
-    per_row = [k for k in ("u", "delta_raw", "z", "dy", "delta_raw_r", "Bm", "Cm", "Bm_r", "Cm_r")
-               if k in host]
-    shared = [k for k in host if k not in per_row]
-    gb = max(hi - lo for lo, hi in bounds)
-    shape = ssm.make_shape(gb, D, N, L, ssm.SSM_BF16, ssm.SSM_BF16)
+    by_batch = Bt > 1
+    n = Bt if by_batch else D
+    ngroups = max(1, min(ngroups, n))
+    bounds = [(i * n // ngroups, (i + 1) * n // ngroups) for i in range(ngroups)]
+    varlen = wl.cu is not None
+    nseq = wl.cu.numel() - 1 if varlen else 0
+    row_keys = [k for k in ("u", "delta_raw", "z", "dy", "delta_raw_r") if k in host]
+    b_keys = [k for k in ("Bm", "Cm", "Bm_r", "Cm_r") if k in host]
+    d_keys = [k for k in ("A", "Dv", "delta_bias", "A_r", "Dv_r", "delta_bias_r") if k in host]
+    sliced = row_keys + (b_keys if by_batch else d_keys)
+    shared = [k for k in host if k not in sliced]
+    summed = ("dA", "dD", "ddelta_bias", "dconv_w", "dconv_b") if by_batch else ("dB", "dC")
+
+    def cut(t, lo, hi):   # a (Bt, D, ...) tensor's part
+        return t[lo:hi] if by_batch else t[:, lo:hi]
+
+    def part(k, t, lo, hi):   # an input's part
+        if k in row_keys:
+            return cut(t, lo, hi)
+        return t[lo:hi]
+
+    gsize = max(hi - lo for lo, hi in bounds)
+    shape = ssm.make_shape(gsize if by_batch else Bt, D if by_batch else gsize, N, L,
+                           ssm.SSM_BF16, ssm.SSM_BF16)
     flag = 3 if wl.bidir else (4 if wl.conv_k else 1)
     nb = max(ssm.ssm_scan_workspace_bytes(shape, flag),
              ssm.ssm_scan_workspace_bytes(shape, 2 if wl.bidir else 0))
     ws = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in streams]
-    fwd_outs = [wl.y, wl.hL] + ([wl.hL_r] if wl.bidir else [])
-    fwd_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in fwd_outs]
-    grad_host = {}   # (part, key) -> pinned host buffer of the whole batch
+    hv = ([torch.empty(nseq, Bt, hi - lo, N, dtype=torch.float32, device="cuda")
+           for lo, hi in bounds] if varlen else None)
+    out_host = {}   # key -> flat pinned host buffer of the whole output
 
-    def run_group(a, lo, hi, s_, w_):
-        """Forward and backward of rows lo:hi on stream s_; returns the
-        backward's gradient dicts."""
-        y, h1 = wl.y[lo:hi], wl.hL[lo:hi]
+    def run_group(gi, a, p, lo, hi, s_):
+        """Forward and backward of group gi on stream s_: returns the forward's
+        outputs and the backward's gradient dicts."""
+        w_ = ws[gi % 2]
+        y = cut(wl.y, lo, hi)
         if wl.bidir:
-            f = dict(delta_raw=a["delta_raw"], A=dev["A"], B=a["Bm"], C=a["Cm"], D=dev["Dv"],
-                     delta_bias=dev["delta_bias"])
-            r = dict(delta_raw=a["delta_raw_r"], A=dev["A_r"], B=a["Bm_r"], C=a["Cm_r"],
-                     D=dev["Dv_r"], delta_bias=dev["delta_bias_r"])
-            ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=bf, y=y, hL=h1,
-                                   hL_r=wl.hL_r[lo:hi], workspace=w_, stream=s_)
-            return ssm.ssm_scan_bwd_bidir(a["u"], a["z"], f, r, a["dy"], out_dtype=bf,
-                                          workspace=w_, stream=s_)
+            h1, h2 = cut(wl.hL, lo, hi), cut(wl.hL_r, lo, hi)
+            f = dict(delta_raw=a["delta_raw"], A=p["A"], B=p["Bm"], C=p["Cm"], D=p["Dv"],
+                     delta_bias=p["delta_bias"])
+            r = dict(delta_raw=a["delta_raw_r"], A=p["A_r"], B=p["Bm_r"], C=p["Cm_r"],
+                     D=p["Dv_r"], delta_bias=p["delta_bias_r"])
+            ssm.ssm_scan_fwd_bidir(a["u"], a["z"], f, r, out_dtype=bf, y=y, hL=h1, hL_r=h2,
+                                   workspace=w_, stream=s_)
+            g = ssm.ssm_scan_bwd_bidir(a["u"], a["z"], f, r, a["dy"], out_dtype=bf,
+                                       workspace=w_, stream=s_)
+            return {"y": y, "hL": h1, "hL_r": h2}, g
+        if varlen:
+            h1 = hv[gi]
+            ssm.ssm_scan_fwd_varlen(a["u"], wl.cu, a["delta_raw"], p["A"], p["Bm"], p["Cm"],
+                                    p["Dv"], a["z"], p["delta_bias"], None, out_dtype=bf, y=y,
+                                    hL=h1, workspace=w_, stream=s_)
+            g = ssm.ssm_scan_bwd_varlen(a["u"], wl.cu, a["delta_raw"], p["A"], p["Bm"], p["Cm"],
+                                        a["dy"], p["Dv"], a["z"], p["delta_bias"], out_dtype=bf,
+                                        workspace=w_, stream=s_)
+            return {"y": y, "hL": h1}, (g,)
+        h1 = cut(wl.hL, lo, hi)
         if wl.conv_k:
-            ssm.ssm_scan_fwd_conv(a["u"], wl.conv_w, wl.conv_b, a["delta_raw"], dev["A"], a["Bm"],
-                                  a["Cm"], dev["Dv"], a["z"], dev["delta_bias"], None, out_dtype=bf,
-                                  y=y, hL=h1, workspace=w_, stream=s_)
-            return (ssm.ssm_scan_bwd_conv(a["u"], wl.conv_w, wl.conv_b, a["delta_raw"], dev["A"],
-                                          a["Bm"], a["Cm"], a["dy"], dev["Dv"], a["z"],
-                                          dev["delta_bias"], None, None, out_dtype=bf,
-                                          workspace=w_, stream=s_),)
-        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], dev["A"], a["Bm"], a["Cm"], dev["Dv"], a["z"],
-                         dev["delta_bias"], None, out_dtype=bf, y=y, hL=h1, workspace=w_, stream=s_)
-        return (ssm.ssm_scan_bwd(a["u"], a["delta_raw"], dev["A"], a["Bm"], a["Cm"], a["dy"],
-                                 dev["Dv"], a["z"], dev["delta_bias"], None, None, out_dtype=bf,
-                                 workspace=w_, stream=s_),)
+            cw = wl.conv_w if by_batch else wl.conv_w[lo:hi]
+            cb = wl.conv_b if by_batch else wl.conv_b[lo:hi]
+            ssm.ssm_scan_fwd_conv(a["u"], cw, cb, a["delta_raw"], p["A"], p["Bm"], p["Cm"],
+                                  p["Dv"], a["z"], p["delta_bias"], None, out_dtype=bf, y=y,
+                                  hL=h1, workspace=w_, stream=s_)
+            g = ssm.ssm_scan_bwd_conv(a["u"], cw, cb, a["delta_raw"], p["A"], p["Bm"], p["Cm"],
+                                      a["dy"], p["Dv"], a["z"], p["delta_bias"], None, None,
+                                      out_dtype=bf, workspace=w_, stream=s_)
+            return {"y": y, "hL": h1}, (g,)
+        ssm.ssm_scan_fwd(a["u"], a["delta_raw"], p["A"], p["Bm"], p["Cm"], p["Dv"], a["z"],
+                         p["delta_bias"], None, out_dtype=bf, y=y, hL=h1, workspace=w_, stream=s_)
+        g = ssm.ssm_scan_bwd(a["u"], a["delta_raw"], p["A"], p["Bm"], p["Cm"], a["dy"], p["Dv"],
+                             a["z"], p["delta_bias"], None, None, out_dtype=bf, workspace=w_,
+                             stream=s_)
+        return {"y": y, "hL": h1}, (g,)
 
-    def host_buf(part, k, t, rows):
-        key = (part, k)
-        if key not in grad_host:
-            shp = (Bt,) + tuple(t.shape[1:]) if rows else tuple(t.shape)
-            grad_host[key] = torch.empty(shp, dtype=t.dtype, pin_memory=True)
-        return grad_host[key]
+    sizes, dtypes = {}, {}   # key -> total elements and type, found by the first step
 
     def one_step():
         for k in shared:
             dev[k].copy_(host[k], non_blocking=True)
         for s_ in streams:
             s_.wait_stream(cur)
-        partial = []   # per group: {(part, key): per-channel gradient}
+        offs = {}
+        partial = []   # per group: {key: gradient summed over the groups}
         for gi, (lo, hi) in enumerate(bounds):
             s_ = streams[gi % 2]
             with torch.cuda.stream(s_):
-                a = {}
-                for k in per_row:
-                    a[k] = dev[k][lo:hi]
-                    a[k].copy_(host[k][lo:hi], non_blocking=True)
-                grads = run_group(a, lo, hi, s_, ws[gi % 2])
-                for o, oh in zip(fwd_outs, fwd_host):
-                    oh[lo:hi].copy_(o[lo:hi], non_blocking=True)
+                a, p = {}, dict(dev)
+                for k in sliced:
+                    t = part(k, dev[k], lo, hi)
+                    t.copy_(part(k, host[k], lo, hi), non_blocking=True)
+                    if k in row_keys:
+                        a[k] = t
+                    else:
+                        p[k] = t
+                for k in row_keys:
+                    a.setdefault(k, None)
+                a.setdefault("z", None)
+                outs, grads = run_group(gi, a, p, lo, hi, s_)
+                items = list(outs.items())
+                for pi, g in enumerate(grads):
+                    items += [("%d.%s" % (pi, k), t) for k, t in g.items() if t is not None]
                 mine = {}
-                for part, g in enumerate(grads):
-                    for k, t in g.items():
-                        if t is None:
-                            continue
-                        if k in PER_ROW_GRADS:
-                            host_buf(part, k, t, True)[lo:hi].copy_(t, non_blocking=True)
-                        else:
-                            mine[(part, k)] = t
+                for key, t in items:
+                    if key.split(".")[-1] in summed:
+                        mine[key] = t
+                        continue
+                    if key not in out_host:
+                        sizes[key] = sizes.get(key, 0) + t.numel()
+                        dtypes[key] = t.dtype
+                        continue
+                    off = offs.get(key, 0)
+                    out_host[key][off:off + t.numel()].view_as(t).copy_(t, non_blocking=True)
+                    offs[key] = off + t.numel()
                 partial.append(mine)
         for s_ in streams:
             cur.wait_stream(s_)
@@ -810,13 +847,22 @@ def pipelined_e2e_fwdbwd(ssm, wl, host, dev, ngroups=4):
             tot = t
             for m in partial[1:]:
                 tot = tot + m[key]
-            host_buf(key[0], key[1], tot, False).copy_(tot, non_blocking=True)
+            if key not in out_host:
+                sizes[key] = tot.numel()
+                dtypes[key] = tot.dtype
+                continue
+            out_host[key].view_as(tot).copy_(tot, non_blocking=True)
 
+    # a first step sizes the host buffers (nothing copied back), then the
+    # buffers are allocated and every later step copies into them
     one_step()
     torch.cuda.synchronize()
-    d2h = sum(o.numel() * o.element_size() for o in fwd_host) + \
-        sum(t.numel() * t.element_size() for t in grad_host.values())
-    return one_step, d2h, ngroups, (fwd_host, grad_host)
+    for key, nel in sizes.items():
+        out_host[key] = torch.empty(nel, dtype=dtypes[key], pin_memory=True)
+    one_step()
+    torch.cuda.synchronize()
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    return one_step, d2h, ngroups, out_host
 
 
 def run_ours(args):
@@ -912,29 +958,19 @@ def run_ours(args):
         dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
         if wl.mode == "step":
             state_host = wl.state.cpu().pin_memory()
-        wl.step(dev)
-        outs_dev = wl.results()
-        outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs_dev]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         if wl.mode == "step":
             h2d += state_host.numel() * 4
-        d2h = sum(o.numel() * o.element_size() for o in outs_host)
-
-        def e2e_serial():
-            for k, v in host.items():
-                dev[k].copy_(v, non_blocking=True)
-            if wl.mode == "step":
-                wl.state.copy_(state_host, non_blocking=True)
-            wl.step(dev)
-            for oh, od in zip(outs_host, wl.results()):
-                oh.copy_(od, non_blocking=True)
-
-        e2e_step, e2e_how = e2e_serial, "one stream: copy in, scan, copy out"
-        if wl.mode == "fwdbwd" and wl.w["Bt"] > 1 and wl.cu is None:
+        if wl.mode == "fwdbwd":
+            # (the pipelined step sizes and allocates its own host buffers)
             e2e_step, d2h, ng, _ = pipelined_e2e_fwdbwd(ssm, wl, host, dev)
-            e2e_how = ("%d groups of batch rows on 2 streams: a group's copies overlap the other "
-                       "groups' forward and backward; per-channel gradients added on the device"
-                       % ng)
+            e2e_how = ("%d groups of %s on 2 streams: a group's copies overlap the other groups' "
+                       "forward and backward; gradients summed over the split added on the device"
+                       % (ng, "batch rows" if wl.w["Bt"] > 1 else "channels"))
+        else:
+            wl.step(dev)
+            outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in wl.results()]
+            d2h = sum(o.numel() * o.element_size() for o in outs_host)
         if wl.mode in ("fwd", "step"):
             e2e_step = pipelined_e2e(ssm, wl, host, dev, outs_host, state_host if wl.mode == "step" else None)
             e2e_how = ("4 groups of %s on 2 streams: a group's copies overlap the other groups' "
