@@ -106,6 +106,27 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(
     // xw[3 + q] = x of own token q, xw[0..2] = the 3 tokens before (zero
     // before token 0 and past the row's end)
     float xw[kConvPer + 3], g[kConvPer];
+    // the tile's edges, loaded with the main loads so that a CTA waits for
+    // global memory once: the first thread's 3 x before the tile, the last
+    // thread's 3 x and du after it (zeros outside the row)
+    float xh[3] = {0.0f, 0.0f, 0.0f}, xa[3] = {0.0f, 0.0f, 0.0f}, ga[3] = {0.0f, 0.0f, 0.0f};
+    if (tid == 0) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int64_t t = tt - 3 + j;
+            if (t >= 0) xh[j] = Elem<TIN>::to_f(xr[t]);
+        }
+    }
+    if (tid == kConvThreads - 1) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int64_t t = tt + 8 + j;
+            if (t < L) {
+                xa[j] = Elem<TIN>::to_f(xr[t]);
+                ga[j] = dur[t];
+            }
+        }
+    }
     if (full) {
         float v[8];
         load8<TIN>(xr + tt, v);
@@ -123,10 +144,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(
     for (int j = 0; j < 3; ++j) x_tail[tid * 3 + j] = xw[8 + j];
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        const int64_t t = tt - 3 + j;
-        xw[j] = tid > 0 ? x_tail[(tid - 1) * 3 + j] : (t >= 0 ? Elem<TIN>::to_f(xr[t]) : 0.0f);
-    }
+    for (int j = 0; j < 3; ++j) xw[j] = tid > 0 ? x_tail[(tid - 1) * 3 + j] : xh[j];
     // dpre = du silu'(pre) from the 4-token window before each token
     auto dpre = [&](const float (&w4)[4], float gv) -> float {
         float pre = cb;
@@ -146,18 +164,16 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(
     for (int j = 0; j < 3; ++j) dp_head[tid * 3 + j] = dpw[j];
     if (tid == kConvThreads - 1) {
         // the 3 tokens after the tile, from their own x and du
-        float xe[6], ge[3];
+        float xe[6];
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            const int64_t t = tt + 8 + j;
             xe[j] = xw[8 + j];
-            xe[3 + j] = t < L ? Elem<TIN>::to_f(xr[t]) : 0.0f;
-            ge[j] = t < L ? dur[t] : 0.0f;
+            xe[3 + j] = xa[j];
         }
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const float w4[4] = {xe[j], xe[j + 1], xe[j + 2], xe[j + 3]};
-            dpw[8 + j] = dpre(w4, ge[j]);
+            dpw[8 + j] = dpre(w4, ga[j]);
         }
     }
     __syncthreads();
