@@ -52,8 +52,65 @@ __global__ void prep_bc_kernel(int64_t Bt, int N, int NP, int64_t L, const TIN* 
     }
 }
 
+// The same for bf16 inputs whose rows are 16-byte aligned (L % 8 = 0) and at
+// most 16 states: a CTA of 256 threads takes 64 tokens of one batch row,
+// reads 8 tokens of one (B or C, state) row per 16-byte load, transposes
+// through shared memory (rows padded to 65 floats, so that both the loads'
+// stores and the output's reads hit 32 distinct banks per warp) and writes
+// whole 16-byte chunks of the output rows.
+constexpr int kPrepT = 64;
+constexpr int kPrepPitch = kPrepT + 1;
+__global__ void __launch_bounds__(256) prep_bc16_kernel(int64_t Bt, int N, int64_t L,
+                                                        const __nv_bfloat16* __restrict__ B,
+                                                        const __nv_bfloat16* __restrict__ C,
+                                                        float* __restrict__ out, int* status) {
+    constexpr int NP = 16;
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+    __shared__ float tile[2 * NP * kPrepPitch];   // [B or C][state][token]
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t t0 = (int64_t)blockIdx.x * kPrepT;
+    {
+        // task = (B or C, state, group of 8 tokens): 2 x 16 x 8 = 256 tasks
+        const int c8 = tid & 7;
+        const int n = (tid >> 3) & (NP - 1);
+        const int which = tid >> 7;
+        const int64_t t = t0 + c8 * 8;
+        float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        if (n < N && t < L) {   // L % 8 = 0: the 8 tokens are all in the row
+            const __nv_bfloat16* src = (which ? C : B) + (b * N + n) * L + t;
+            const uint4 w = *reinterpret_cast<const uint4*>(src);
+            v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+            v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+        }
+        const float sc = which ? 1.0f : kLn2;
+        float* row = tile + (which * NP + n) * kPrepPitch + c8 * 8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) row[q] = v[q] * sc;
+    }
+    __syncthreads();
+    // output: 64 token rows x 8 chunks of 4 floats (B' states 0..15, then C)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int idx = tid + 256 * k;
+        const int r = idx >> 3, j4 = idx & 7;
+        const int64_t t = t0 + r;
+        if (t < L) {
+            const float* col = tile + (j4 * 4) * kPrepPitch + r;
+            *reinterpret_cast<float4*>(out + (b * L + t) * (2 * NP) + j4 * 4) =
+                make_float4(col[0], col[kPrepPitch], col[2 * kPrepPitch], col[3 * kPrepPitch]);
+        }
+    }
+}
+
 cudaError_t launch_prep_bc(int tin, int64_t Bt, int N, int NP, int64_t L, const void* B,
                            const void* C, float* out, int* status, cudaStream_t st) {
+    if (tin == SSM_BF16 && NP == 16 && N <= 16 && L % 8 == 0) {
+        dim3 grid16((unsigned)((L + kPrepT - 1) / kPrepT), (unsigned)Bt);
+        prep_bc16_kernel<<<grid16, 256, 0, st>>>(Bt, N, L, static_cast<const __nv_bfloat16*>(B),
+                                                 static_cast<const __nv_bfloat16*>(C), out, status);
+        return cudaGetLastError();
+    }
     dim3 grid((unsigned)((L + 31) / 32), (unsigned)Bt), block(32, 8);
     if (tin == SSM_BF16)
         prep_bc_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
