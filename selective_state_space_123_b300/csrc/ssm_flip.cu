@@ -85,6 +85,63 @@ __global__ void bidir_combine_kernel(int64_t rows, int64_t L, const float* __res
     }
 }
 
+// The same 8 tokens at a time when L % 8 = 0 (then the mirrored group of 8
+// tokens is again 32-byte aligned): 16-byte loads and stores, one index
+// division per 8 tokens.
+__device__ __forceinline__ void ld8f(const float* p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <typename TOUT>
+__device__ __forceinline__ void st8(TOUT* p, const float (&v)[8]);
+template <>
+__device__ __forceinline__ void st8<float>(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void st8<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+template <typename TOUT>
+__global__ void bidir_combine8_kernel(int64_t rows, int64_t L, const float* __restrict__ du1,
+                                      const float* __restrict__ du2, const float* __restrict__ dz1,
+                                      const float* __restrict__ dz2, const float* __restrict__ ddr1,
+                                      const float* __restrict__ ddr2, TOUT* __restrict__ du,
+                                      TOUT* __restrict__ dz, TOUT* __restrict__ ddr,
+                                      TOUT* __restrict__ ddr_r) {
+    const int64_t groups = L / 8;
+    const int64_t total = rows * groups;
+    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < total;
+         gi += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = gi / groups;
+        const int64_t t = (gi - r * groups) * 8;
+        const int64_t i = r * L + t;            // tokens t .. t+7
+        const int64_t j = r * L + (L - 8 - t);  // their mirrors, last to first
+        float a[8], b[8], o[8];
+        ld8f(du1 + i, a);
+        ld8f(du2 + j, b);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[q] = a[q] + b[7 - q];
+        st8<TOUT>(du + i, o);
+        if (dz) {
+            ld8f(dz1 + i, a);
+            ld8f(dz2 + j, b);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = a[q] + b[7 - q];
+            st8<TOUT>(dz + i, o);
+        }
+        ld8f(ddr1 + i, a);
+        st8<TOUT>(ddr + i, a);
+        ld8f(ddr2 + j, b);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[q] = b[7 - q];
+        st8<TOUT>(ddr_r + i, o);
+    }
+}
+
 __global__ void fold_status_kernel(int* outer, const int* inner) {
     const int v = *inner;
     if (v != SSM_OK) atomicCAS(outer, SSM_OK, v);
@@ -120,6 +177,19 @@ cudaError_t launch_bidir_combine(int tout, int64_t rows, int64_t L, const float*
                                  const float* ddr1, const float* ddr2, void* du, void* dz,
                                  void* ddr, void* ddr_r, cudaStream_t st) {
     if (rows <= 0 || L <= 0) return cudaSuccess;
+    if (L % 8 == 0) {
+        const unsigned g8 = grid_for(rows * (L / 8), 256);
+        if (tout == SSM_F32)
+            bidir_combine8_kernel<float><<<g8, 256, 0, st>>>(
+                rows, L, du1, du2, dz1, dz2, ddr1, ddr2, static_cast<float*>(du),
+                static_cast<float*>(dz), static_cast<float*>(ddr), static_cast<float*>(ddr_r));
+        else
+            bidir_combine8_kernel<__nv_bfloat16><<<g8, 256, 0, st>>>(
+                rows, L, du1, du2, dz1, dz2, ddr1, ddr2, static_cast<__nv_bfloat16*>(du),
+                static_cast<__nv_bfloat16*>(dz), static_cast<__nv_bfloat16*>(ddr),
+                static_cast<__nv_bfloat16*>(ddr_r));
+        return cudaGetLastError();
+    }
     const unsigned g = grid_for(rows * L, 256);
     if (tout == SSM_F32)
         bidir_combine_kernel<float><<<g, 256, 0, st>>>(
